@@ -1,0 +1,517 @@
+"""Benchmark of the multi-adapter LoRA hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config decode]
+
+One step = lora_build_segments + lora_apply (the MoE config: build +
+gate/up delta + down delta) over one batch of synthetic inputs, already
+resident in HBM.  To keep L2 (129 MB) from serving the weights, every step
+uses the next of R independent input sets (own adapter table, ids, x, y),
+with R * bytes-per-set above 2x L2.  Steps are issued as one CUDA graph and
+timed with CUDA events on the launching stream, bracketed by a barrier and a
+device synchronize; rank 0 prints one JSON line.
+
+Multi-GPU runs are independent replicas (the path has no exchange step):
+every rank processes its own batches, the elapsed time is the max over ranks
+and the value counts the tokens of all ranks.
+
+--impl reference times the CPU oracle (plain C, fp64) on the host cores on
+the same workload; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-delta tokens/s at 1 GB300; achieved HBM GB/s or TC TFLOPS vs roofline"
+L2_BYTES = 129 * 1024 * 1024
+ENGINE_SRC = os.path.join(ROOT, "segmented_rank_gemm_lora_gb300", "csrc", "engine.cu")
+
+CONFIGS = {
+    "tiny": "M=64 tokens, K=256, N=512, 4 adapters ranks 8/16/16/32, ids uniform in -1..3, scale 2",
+    "decode": "M=32 tokens (one per sequence), K=N=4096, 20 adapters ranks cycling 16/32/64, 10% ids -1, scale 2",
+    "prefill": "16 requests, lengths ~ l^-1.2 on [16,512] (~1900 tokens), one adapter each, K=N=4096, "
+               "16 adapters ranks cycling 16/32/64",
+    "stacked_qkv": "M=1024 (512 decode + prefill runs), 32 adapters r=64, A=(3r,4096), B slices 4096/1024/1024",
+    "stacked_gate_up": "M=1024 (512 decode + prefill runs), 32 adapters r=64, A=(2r,4096), B slices 14336/14336",
+    "stacked_down": "M=1024 (512 decode + prefill runs), 32 adapters r=64, A=(r,14336), B 4096",
+    "moe": "M=512, top-2 of 8 experts, hidden 4096, intermediate 14336, 8 adapters ranks 16/32/64, block_m 64",
+}
+
+
+def make_problem(config: str, seed: int, base: str = "random"):
+    from segmented_rank_gemm_lora_gb300 import synth
+    if config == "tiny":
+        return synth.tiny(seed, y_base=base)
+    if config == "decode":
+        return synth.decode(seed, y_base=base)
+    if config == "prefill":
+        return synth.prefill(seed, y_base=base)
+    if config.startswith("stacked_"):
+        return synth.stacked(config[len("stacked_"):], seed, y_base=base)
+    if config == "moe":
+        return synth.moe(seed)
+    raise ValueError(config)
+
+
+def dense_algorithmic(p):
+    """(bytes, flops) the method must move / do for one batch (true ranks, A and B read once)."""
+    K, N = p.K, p.N
+    active = sorted(set(int(i) for i in p.ids if 0 <= i < p.L))
+    wbytes = sum(2 * (p.A[i].size + p.B[i].size) for i in active)
+    Ma = int(sum(1 for i in p.ids if 0 <= i < p.L))
+    nbytes = wbytes + Ma * (2 * K + 4 * N) + 4 * p.M
+    flops = 0
+    for i in active:
+        m = int((p.ids == i).sum())
+        flops += 2 * m * p.ranks[i] * (p.n_a * K + N)
+    return nbytes, flops
+
+
+def moe_algorithmic(p):
+    """Gate/up + down deltas: A read once per used (adapter, expert) factor, x once per token,
+    caches once per pair (read + write), cache2 read once per pair."""
+    H, I, E, topk = p.H, p.I, p.E, p.topk
+    pairs = [(int(p.ids[q // topk]), int(p.topk_ids.reshape(-1)[q])) for q in range(p.M * topk)]
+    pairs = [(l, e) for l, e in pairs if 0 <= l < p.L]
+    used_l = sorted(set(l for l, _ in pairs))
+    used_le = sorted(set(pairs))
+    wb = 0
+    for l in used_l:
+        wb += 2 * p.A_gu[l].shape[1] * p.A_gu[l].shape[2] * (p.A_gu[l].shape[0] if p.A_gu[l].shape[0] > 1 else 1)
+        wb += 2 * p.B_d[l][0].size * (p.B_d[l].shape[0] if p.B_d[l].shape[0] > 1 else 1)
+    for l, e in used_le:
+        wb += 2 * p.B_gu[l][e if p.B_gu[l].shape[0] > 1 else 0].size
+        wb += 2 * p.A_d[l][e if p.A_d[l].shape[0] > 1 else 0].size
+    tokens = len(set(q // topk for q in range(p.M * topk) if 0 <= p.ids[q // topk] < p.L))
+    P = len(pairs)
+    nbytes = wb + tokens * 2 * H + P * (4 * 2 * I) + P * 2 * I + P * 4 * H + 4 * p.M + 4 * p.M * topk
+    flops = sum(2 * p.ranks[l] * (H + 2 * I) + 2 * p.ranks[l] * (I + H) for l, _ in pairs)
+    return nbytes, flops
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9], f[4]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r[0] > 0.5 * r[1]] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# traffic recorded by ncu for the current engine source (null if stale)
+# ---------------------------------------------------------------------------
+def engine_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("engine.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "segmented_rank_gemm_lora_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    path = os.path.join(ROOT, "profiles", "engine_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+    except ValueError:
+        return None
+    entry = rec.get(config)
+    if not entry or entry.get("engine_sha") != engine_source_sha():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+def oracle_step(p):
+    import oracle
+    if hasattr(p, "A_gu"):
+        oracle.moe_delta(p.ids, p.topk_ids, p.x, p.cache1, p.A_gu, p.B_gu, p.ranks, p.scales, p.E, True)
+        oracle.moe_delta(p.ids, p.topk_ids, p.cache2, p.cache3, p.A_d, p.B_d, p.ranks, p.scales, p.E, False)
+    else:
+        oracle.lora_apply(p.ids, p.x, p.y_base, p.A, p.B, p.ranks, p.scales, p.slice_n, p.n_a)
+
+
+def sample_problem(config: str, p, max_tokens: int):
+    """A bounded sample of the workload: the first max_tokens tokens of the batch."""
+    if hasattr(p, "A_gu") or p.M <= max_tokens:
+        return p, p.M
+    from segmented_rank_gemm_lora_gb300 import synth
+    q = synth.DenseProblem(**{**p.__dict__})
+    q.ids, q.x, q.y_base, q.M = p.ids[:max_tokens], p.x[:max_tokens], p.y_base[:max_tokens], max_tokens
+    return q, max_tokens
+
+
+def cpu_baseline(config: str, budget_s: float = 10.0):
+    import oracle
+    oracle.build()
+    p = make_problem(config, 1000)
+    q, tokens = sample_problem(config, p, 256)
+    t0 = time.perf_counter()
+    oracle_step(q)
+    one = time.perf_counter() - t0
+    reps = max(1, min(50, int(budget_s / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(q)
+    dt = time.perf_counter() - t0
+    unit_tokens = tokens if not hasattr(q, "A_gu") else q.M
+    return {"value": unit_tokens * reps / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d x one %s batch of %d tokens (first %d tokens of the batch), single-threaded C fp64"
+                      % (reps, config, p.M, unit_tokens)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    p = make_problem(args.config, 1000)
+    q, tokens = sample_problem(args.config, p, 256)
+    for _ in range(args.warmup):
+        oracle_step(q)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(q)
+    dt = time.perf_counter() - t0
+    value = tokens * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "%s: %s" % (args.config, CONFIGS[args.config]),
+                       "sample": "first %d tokens of each batch" % tokens},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d steps of %d tokens, single-threaded C fp64" % (args.steps, tokens)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def _to_dev(a, torch, dev):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def build_sets(config, R, torch, lora, dev, first=0):
+    sets = []
+    for j in range(first, first + R):
+        p = make_problem(config, 1000 + j)
+        s = {"p": p}
+        if hasattr(p, "A_gu"):
+            s["gu"] = lora.lora_pack_weights([_to_dev(a, torch, dev) for a in p.A_gu],
+                                             [_to_dev(b, torch, dev) for b in p.B_gu], p.ranks, p.scales, p.H,
+                                             [2 * p.I], 1, E_A=p.A_gu[0].shape[0], E_B=p.B_gu[0].shape[0])
+            s["dn"] = lora.lora_pack_weights([_to_dev(a, torch, dev) for a in p.A_d],
+                                             [_to_dev(b, torch, dev) for b in p.B_d], p.ranks, p.scales, p.I,
+                                             [p.H], 1, E_A=p.A_d[0].shape[0], E_B=p.B_d[0].shape[0])
+            s["ids"] = torch.from_numpy(p.ids).to(dev)
+            s["tk"] = torch.from_numpy(p.topk_ids).to(dev)
+            s["x"] = _to_dev(p.x, torch, dev)
+            s["c1"] = _to_dev(p.cache1, torch, dev)
+            s["c2"] = _to_dev(p.cache2, torch, dev)
+            s["c3"] = _to_dev(p.cache3, torch, dev)
+            s["ws"] = lora.Workspace(p.M, p.L, p.topk, p.E, p.block_m, device=dev)
+            s["alg"] = moe_algorithmic(p)
+            s["tokens"] = p.M
+            s["bytes"] = sum(t.numel() * t.element_size() for t in (s["x"], s["c1"], s["c2"], s["c3"])) + \
+                s["gu"].info().device_bytes + s["dn"].info().device_bytes
+        else:
+            s["table"] = lora.lora_pack_weights([_to_dev(a, torch, dev) for a in p.A],
+                                                [_to_dev(b, torch, dev) for b in p.B], p.ranks, p.scales, p.K,
+                                                p.slice_n, p.n_a)
+            s["ids"] = torch.from_numpy(p.ids).to(dev)
+            s["x"] = _to_dev(p.x, torch, dev)
+            s["y"] = _to_dev(p.y_base, torch, dev)
+            s["ws"] = lora.Workspace(p.M, p.L, device=dev)
+            s["alg"] = dense_algorithmic(p)
+            s["tokens"] = p.M
+            s["bytes"] = s["x"].numel() * 2 + s["y"].numel() * 2 + s["table"].info().device_bytes
+        sets.append(s)
+    torch.cuda.synchronize()
+    return sets
+
+
+def step(s, lora, build=True):
+    if "gu" in s:
+        if build:
+            lora.lora_build_segments(s["ws"], s["ids"], s["tk"])
+        lora.lora_moe_delta(s["gu"], lora.LORA_MOE_GATE_UP, s["ws"], s["x"], s["c1"])
+        lora.lora_moe_delta(s["dn"], lora.LORA_MOE_DOWN, s["ws"], s["c2"], s["c3"])
+        return (1 if build else 0) + 2
+    if build:
+        lora.lora_build_segments(s["ws"], s["ids"])
+    lora.lora_apply(s["table"], s["ws"], s["x"], s["y"])
+    return (1 if build else 0) + 1
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from segmented_rank_gemm_lora_gb300 import lora
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lora.load()
+
+    sets = build_sets(args.config, 1, torch, lora, dev)
+    per_set = sets[0]["bytes"]
+    R = max(4, min(64, int(np.ceil(2.5 * L2_BYTES / max(per_set, 1)))))
+    sets += build_sets(args.config, R - 1, torch, lora, dev, first=1)
+    # warm every set once eagerly (first launches set kernel attributes)
+    for s in sets:
+        step(s, lora)
+    torch.cuda.synchronize()
+    for s in sets:
+        st = lora.lora_get_status(s["ws"])
+        if st != lora.LORA_OK:
+            raise RuntimeError("device status %s" % lora.STATUS[st])
+
+    stream = torch.cuda.Stream(device=dev)
+    K, W = args.steps, args.warmup
+    launches = {"n": 0}
+
+    def steps_fn(n, build=True):
+        def fn():
+            c = 0
+            for i in range(n):
+                c += step(sets[i % R], lora, build)
+            launches["n"] = c
+        return fn
+
+    g_warm = capture(torch, steps_fn(W), stream)
+    g_main = capture(torch, steps_fn(K), stream)
+    gpu_launches = launches["n"]
+    g_apply = capture(torch, steps_fn(K, build=False), stream)
+
+    # ---------------- timed region: K steps ----------------
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    torch.cuda.synchronize()
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g_main.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    ms_max = max_over_ranks(ms, world)
+
+    # ---------------- dominant kernel alone: K applies, same rotation ----------------
+    with torch.cuda.stream(stream):
+        g_apply.replay()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    g_apply.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    apply_ms = a0.elapsed_time(a1) / K
+    if "gu" in sets[0]:
+        apply_ms /= 2.0     # two delta launches per step
+
+    tokens_step = np.mean([sets[i % R]["tokens"] for i in range(K)])
+    value = world * tokens_step * K / (ms_max / 1e3)
+    alg_bytes = np.mean([sets[i % R]["alg"][0] for i in range(K)])
+    alg_flops = np.mean([sets[i % R]["alg"][1] for i in range(K)])
+    if "gu" in sets[0]:
+        alg_bytes /= 2.0
+        alg_flops /= 2.0
+    hbm, tc, src = peaks()
+    achieved = alg_bytes / (apply_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": recorded_traffic(args.config), "kernel": "engine_kernel",
+                "kernel_ms": apply_ms, "algorithmic_bytes": alg_bytes,
+                "tflops": alg_flops / (apply_ms / 1e3) / 1e12, "peak_source": src + " (burst)"}
+
+    # ---------------- end to end through host buffers ----------------
+    e2e = run_e2e(args, sets, torch, lora, dev, stream, world)
+
+    cpu = cpu_baseline(args.config, args.cpu_seconds) if (rank == 0 and world == 1 and args.cpu_seconds > 0) else None
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+                "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "%s: %s" % (args.config, CONFIGS[args.config]),
+                           "step": "build_segments + " + ("gate/up + down deltas" if "gu" in sets[0] else "apply"),
+                           "l2": "inputs larger than L2: %d rotating input sets, %.0f MB each" % (R, per_set / 1e6),
+                           "parallelism": "replicas x%d" % world},
+                "gpu_launches": gpu_launches, "roofline": roofline, "e2e": e2e, "clocks": clk,
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, sets, torch, lora, dev, stream, world):
+    """Same metric through the public API with host-resident inputs: every step copies ids, x and y_base
+    from pinned host memory, builds, applies, and copies the result back."""
+    R = len(sets)
+    host = []
+    for s in sets[:min(R, 8)]:
+        if "gu" in s:
+            host.append({k: s[k].cpu().pin_memory() for k in ("ids", "tk", "x", "c1", "c2", "c3")})
+        else:
+            host.append({k: s[k].cpu().pin_memory() for k in ("ids", "x", "y")})
+    outs = [{k: torch.empty_like(h[k], pin_memory=True) for k in (("c1", "c3") if "c1" in h else ("y",))}
+            for h in host]
+    h2d = d2h = 0
+
+    def one(i):
+        nonlocal h2d, d2h
+        s, h, o = sets[i % len(host)], host[i % len(host)], outs[i % len(host)]
+        h2d = d2h = 0
+        for k in h:
+            s[k].copy_(h[k], non_blocking=True)
+            h2d += h[k].numel() * h[k].element_size()
+        step(s, lora)
+        for k in o:
+            o[k].copy_(s[k], non_blocking=True)
+            d2h += o[k].numel() * o[k].element_size()
+
+    K = args.steps
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            one(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            one(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    tokens = np.mean([sets[i % len(host)]["tokens"] for i in range(K)])
+    return {"value": world * tokens * K / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode", choices=sorted(CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,547 @@
+// Host side of the C ABI declared in include/lora.h.
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+using namespace lora;
+
+namespace {
+
+constexpr int64_t kPartialFloatsPerRow = 16384;   // L2 scratch for rank-sized partials, per row of work
+constexpr int64_t kMaxRows = 65536;               // tokens (or token/expert pairs) per build
+
+std::atomic<int64_t> g_opt_path{0};
+std::atomic<int64_t> g_opt_tc_min_rows{16};
+std::atomic<int64_t> g_opt_timeout_ns{1000000000LL};
+std::atomic<int64_t> g_opt_grid{0};
+std::atomic<int64_t> g_opt_withhold{0};
+
+struct DeviceInfo {
+    int sms = 0;
+    int engine_blocks_per_sm = 0;
+    bool attr_done = false;
+};
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_dev;
+
+lora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lora_status device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.attr_done) {
+        const size_t smem = engine_smem_bytes(0);
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LORA_ERR_CUDA;
+        if (cudaFuncSetAttribute(engine_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.engine_blocks_per_sm, engine_kernel_ptr(),
+                                                          kEngineThreads, smem) != cudaSuccess)
+            return LORA_ERR_CUDA;
+        if (d.engine_blocks_per_sm < 1) return LORA_ERR_UNSUPPORTED;
+        d.attr_done = true;
+    }
+    *out = d;
+    return LORA_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// table
+// ---------------------------------------------------------------------------
+struct lora_table_s {
+    int32_t L = 0, K = 0, N = 0, n_slices = 0, n_a = 0, E_A = 1, E_B = 1;
+    int32_t slice_n[kMaxSlices] = {0}, slice_off[kMaxSlices] = {0}, slice_tile_off[kMaxSlices] = {0};
+    int32_t b_tiles = 0;                // n-tiles per B block
+    std::vector<int32_t> rank, rpad;
+    std::vector<float> scale;
+    std::vector<uint64_t> a_ptr, b_ptr; // host copies of the device pointer tables
+    std::vector<void *> group_mem;      // one allocation per stored rank
+    int64_t device_bytes = 0;
+    uint64_t *d_a_ptr = nullptr, *d_b_ptr = nullptr;
+    int32_t *d_rpad = nullptr;
+    float *d_scale = nullptr;
+    int32_t max_R = 0;
+    uint32_t magic = 0x4c6f5241u;
+};
+
+static bool valid_table(lora_table t) { return t != nullptr && t->magic == 0x4c6f5241u; }
+
+extern "C" int32_t lora_rank_padded(int32_t rank)
+{
+    if (rank < 1 || rank > kMaxRank) return -1;
+    return (int32_t)round_up(rank, 16);
+}
+
+static void free_table(lora_table t)
+{
+    for (void *m : t->group_mem) cudaFree(m);
+    cudaFree(t->d_a_ptr);
+    cudaFree(t->d_b_ptr);
+    cudaFree(t->d_rpad);
+    cudaFree(t->d_scale);
+    t->magic = 0;
+    delete t;
+}
+
+extern "C" lora_status lora_pack_weights(const lora_adapter_desc *adapters, int32_t L, const lora_proj_shape *shape,
+                                         lora_stream_t stream, lora_table *out)
+{
+    if (!adapters || !shape || !out || L < 1) return LORA_ERR_INVALID_ARG;
+    *out = nullptr;
+    const lora_proj_shape &sh = *shape;
+    if (sh.K < 8 || sh.K % 8 != 0) return LORA_ERR_INVALID_ARG;
+    if (sh.n_slices < 1 || sh.n_slices > kMaxSlices) return LORA_ERR_INVALID_ARG;
+    if (!(sh.n_a == 1 || sh.n_a == sh.n_slices)) return LORA_ERR_INVALID_ARG;
+    if (sh.E_A < 1 || sh.E_B < 1) return LORA_ERR_INVALID_ARG;
+    int64_t N = 0;
+    for (int s = 0; s < sh.n_slices; ++s) {
+        if (sh.slice_n[s] < 8 || sh.slice_n[s] % 8 != 0) return LORA_ERR_INVALID_ARG;
+        N += sh.slice_n[s];
+    }
+    if (N > (1 << 30)) return LORA_ERR_UNSUPPORTED;
+    for (int i = 0; i < L; ++i) {
+        if (lora_rank_padded(adapters[i].rank) < 0) return LORA_ERR_INVALID_ARG;
+        if (!adapters[i].A || !adapters[i].B) return LORA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    lora_table t = new (std::nothrow) lora_table_s();
+    if (!t) return LORA_ERR_OOM;
+    t->L = L;
+    t->K = sh.K;
+    t->N = (int32_t)N;
+    t->n_slices = sh.n_slices;
+    t->n_a = sh.n_a;
+    t->E_A = sh.E_A;
+    t->E_B = sh.E_B;
+    int32_t col = 0, tiles = 0;
+    for (int i = 0; i < sh.n_slices; ++i) {
+        t->slice_n[i] = sh.slice_n[i];
+        t->slice_off[i] = col;
+        t->slice_tile_off[i] = tiles;
+        col += sh.slice_n[i];
+        tiles += (int32_t)ceil_div(sh.slice_n[i], kNTile);
+    }
+    t->b_tiles = tiles;
+    t->rank.resize(L);
+    t->rpad.resize(L);
+    t->scale.resize(L);
+    t->a_ptr.assign((size_t)L * sh.E_A, 0);
+    t->b_ptr.assign((size_t)L * sh.E_B, 0);
+    for (int i = 0; i < L; ++i) {
+        t->rank[i] = adapters[i].rank;
+        t->rpad[i] = lora_rank_padded(adapters[i].rank);
+        t->scale[i] = adapters[i].scale;
+        t->max_R = std::max(t->max_R, sh.n_a * t->rpad[i]);
+    }
+
+    // one contiguous allocation per stored rank: all A blocks of that rank, then all B blocks
+    std::vector<int32_t> ranks_present(t->rpad);
+    std::sort(ranks_present.begin(), ranks_present.end());
+    ranks_present.erase(std::unique(ranks_present.begin(), ranks_present.end()), ranks_present.end());
+    lora_status st = LORA_OK;
+    for (int32_t rp : ranks_present) {
+        const int64_t a_block = round_up((int64_t)sh.K * sh.n_a * rp * 2, 256);
+        const int64_t b_block = round_up((int64_t)tiles * kNTile * rp * 2, 256);
+        std::vector<int> members;
+        for (int i = 0; i < L; ++i)
+            if (t->rpad[i] == rp) members.push_back(i);
+        const int64_t bytes = (int64_t)members.size() * (sh.E_A * a_block + sh.E_B * b_block);
+        void *mem = nullptr;
+        if (cudaMalloc(&mem, (size_t)bytes) != cudaSuccess) {
+            cudaGetLastError();
+            st = LORA_ERR_OOM;
+            break;
+        }
+        t->group_mem.push_back(mem);
+        t->device_bytes += bytes;
+        char *base = static_cast<char *>(mem);
+        int64_t off = 0;
+        for (int i : members) {
+            for (int e = 0; e < sh.E_A; ++e) {
+                t->a_ptr[(size_t)i * sh.E_A + e] = reinterpret_cast<uint64_t>(base + off);
+                off += a_block;
+            }
+        }
+        for (int i : members) {
+            for (int e = 0; e < sh.E_B; ++e) {
+                t->b_ptr[(size_t)i * sh.E_B + e] = reinterpret_cast<uint64_t>(base + off);
+                off += b_block;
+            }
+        }
+    }
+    if (st == LORA_OK) {
+        for (int i = 0; i < L && st == LORA_OK; ++i) {
+            const int32_t r = t->rank[i], rp = t->rpad[i];
+            const auto *A = static_cast<const __nv_bfloat16 *>(adapters[i].A);
+            const auto *B = static_cast<const __nv_bfloat16 *>(adapters[i].B);
+            for (int e = 0; e < sh.E_A && st == LORA_OK; ++e)
+                st = cuda_status(launch_pack_a(A + (int64_t)e * sh.n_a * r * sh.K,
+                                               reinterpret_cast<__nv_bfloat16 *>(t->a_ptr[(size_t)i * sh.E_A + e]),
+                                               sh.K, sh.n_a, r, rp, s));
+            for (int e = 0; e < sh.E_B && st == LORA_OK; ++e)
+                st = cuda_status(launch_pack_b(B + (int64_t)e * N * r,
+                                               reinterpret_cast<__nv_bfloat16 *>(t->b_ptr[(size_t)i * sh.E_B + e]),
+                                               r, rp, sh.n_slices, sh.slice_n, s));
+        }
+    }
+    if (st == LORA_OK) {
+        const size_t na = t->a_ptr.size() * 8, nb = t->b_ptr.size() * 8;
+        if (cudaMalloc(&t->d_a_ptr, na) != cudaSuccess || cudaMalloc(&t->d_b_ptr, nb) != cudaSuccess ||
+            cudaMalloc(&t->d_rpad, (size_t)L * 4) != cudaSuccess || cudaMalloc(&t->d_scale, (size_t)L * 4) != cudaSuccess) {
+            cudaGetLastError();
+            st = LORA_ERR_OOM;
+        }
+    }
+    if (st == LORA_OK) {
+        // the host vectors live as long as the table, so async copies from them are safe
+        if (cudaMemcpyAsync(t->d_a_ptr, t->a_ptr.data(), t->a_ptr.size() * 8, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(t->d_b_ptr, t->b_ptr.data(), t->b_ptr.size() * 8, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(t->d_rpad, t->rpad.data(), (size_t)L * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(t->d_scale, t->scale.data(), (size_t)L * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            st = LORA_ERR_CUDA;
+    }
+    if (st != LORA_OK) {
+        cudaStreamSynchronize(s);
+        free_table(t);
+        return st;
+    }
+    *out = t;
+    return LORA_OK;
+}
+
+extern "C" lora_status lora_table_destroy(lora_table table)
+{
+    if (!valid_table(table)) return LORA_ERR_INVALID_ARG;
+    free_table(table);
+    return LORA_OK;
+}
+
+extern "C" lora_status lora_table_info(lora_table t, lora_table_info_t *info)
+{
+    if (!valid_table(t) || !info) return LORA_ERR_INVALID_ARG;
+    info->L = t->L;
+    info->K = t->K;
+    info->N = t->N;
+    info->n_slices = t->n_slices;
+    info->n_a = t->n_a;
+    info->E_A = t->E_A;
+    info->E_B = t->E_B;
+    info->num_rank_groups = (int32_t)t->group_mem.size();
+    info->device_bytes = t->device_bytes;
+    int32_t best = 0, best_rank = -1;
+    for (int i = 0; i < t->L; ++i)
+        if (t->rank[i] > best_rank) best_rank = t->rank[i], best = t->rpad[i];
+    info->stored_rank_of_max = best;
+    return LORA_OK;
+}
+
+extern "C" int32_t lora_table_stored_rank(lora_table t, int32_t adapter)
+{
+    if (!valid_table(t) || adapter < 0 || adapter >= t->L) return -1;
+    return t->rpad[adapter];
+}
+
+// ---------------------------------------------------------------------------
+// workspace
+// ---------------------------------------------------------------------------
+bool lora::ws_layout(int32_t max_M, int32_t L, int32_t topk, int32_t E, int32_t block_m, WsLayout *o)
+{
+    if (max_M < 1 || L < 1 || block_m < 0) return false;
+    if (block_m > 0 && (topk < 1 || E < 1)) return false;
+    if (L + 1 > 16000) return false;
+    if (block_m > 0 && (int64_t)L * E + 1 > 16000) return false;
+    WsLayout w{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = (size_t)round_up((int64_t)(off + bytes), 256);
+        return at;
+    };
+    w.header = take(kHeaderInts * 4);
+    w.perm = take((size_t)max_M * 4);
+    w.seg_capacity = std::max(1, std::min(L, max_M));
+    w.segments = take((size_t)w.seg_capacity * 16);
+    int64_t max_rows = max_M;
+    w.moe_group_capacity = 0;
+    if (block_m > 0) {
+        const int64_t P = (int64_t)max_M * topk;
+        const int64_t P_max = round_up(P + (int64_t)E * (block_m - 1), block_m);
+        if (P_max > (1LL << 30)) return false;
+        w.P_max_cap = (int32_t)P_max;
+        w.B_max_cap = (int32_t)(P_max / block_m);
+        w.sorted_ids = take((size_t)L * P_max * 4);
+        w.expert_ids = take((size_t)L * w.B_max_cap * 4);
+        w.ntpp = take((size_t)L * 4);
+        w.moe_group_capacity = (int32_t)std::max<int64_t>(1, std::min<int64_t>((int64_t)L * E, P));
+        w.moe_groups = take((size_t)w.moe_group_capacity * 16);
+        max_rows = std::max<int64_t>(max_rows, P);
+    } else {
+        w.sorted_ids = w.expert_ids = w.ntpp = w.moe_groups = off;
+    }
+    if (max_rows > kMaxRows) return false;   // keeps every scratch offset inside int32
+    const int64_t groups = std::max<int64_t>(w.seg_capacity, w.moe_group_capacity);
+    w.max_tiles = (int32_t)(ceil_div(max_rows, kBgmvRows) + groups);
+    w.sync = take((size_t)w.max_tiles * 16);
+    w.partial_floats = max_rows * kPartialFloatsPerRow;
+    w.partials = take((size_t)w.partial_floats * 4);
+    w.total = off;
+    *o = w;
+    return true;
+}
+
+extern "C" size_t lora_workspace_bytes(int32_t max_M, int32_t L, int32_t topk, int32_t num_experts, int32_t block_m)
+{
+    WsLayout w;
+    if (!ws_layout(max_M, L, topk, num_experts, block_m, &w)) return 0;
+    return w.total;
+}
+
+static lora_status check_ws(const lora_workspace *ws, WsLayout *w)
+{
+    if (!ws || !ws->d_ptr || (reinterpret_cast<uintptr_t>(ws->d_ptr) & 255u) != 0) return LORA_ERR_INVALID_ARG;
+    if (!ws_layout(ws->max_M, ws->L, ws->topk, ws->num_experts, ws->block_m, w)) return LORA_ERR_INVALID_ARG;
+    if (ws->bytes < w->total) return LORA_ERR_WORKSPACE;
+    return LORA_OK;
+}
+
+extern "C" lora_status lora_workspace_layout(const lora_workspace *ws, lora_workspace_layout_t *out)
+{
+    WsLayout w;
+    if (!out) return LORA_ERR_INVALID_ARG;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    out->header = w.header;
+    out->perm = w.perm;
+    out->segments = w.segments;
+    out->sorted_ids = w.sorted_ids;
+    out->expert_ids = w.expert_ids;
+    out->ntpp = w.ntpp;
+    out->moe_groups = w.moe_groups;
+    out->scratch = w.sync;
+    out->seg_capacity = w.seg_capacity;
+    out->moe_group_capacity = w.moe_group_capacity;
+    return LORA_OK;
+}
+
+template <class T>
+static T *at(const lora_workspace *ws, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<char *>(ws->d_ptr) + off);
+}
+
+extern "C" lora_status lora_build_segments(const lora_workspace *ws, const int32_t *d_ids, int32_t M,
+                                           const int32_t *d_topk_ids, const uint8_t *d_enabled, lora_stream_t stream)
+{
+    WsLayout w;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    if (M < 0 || (M > 0 && !d_ids)) return LORA_ERR_INVALID_ARG;
+    if (M > ws->max_M) return LORA_ERR_WORKSPACE;
+    if (d_topk_ids && ws->block_m <= 0) return LORA_ERR_INVALID_ARG;
+    BuildParams p{};
+    p.ids = d_ids;
+    p.topk_ids = d_topk_ids;
+    p.enabled = d_enabled;
+    p.M = M;
+    p.L = ws->L;
+    p.topk = ws->topk;
+    p.E = ws->num_experts;
+    p.block_m = d_topk_ids ? ws->block_m : 0;
+    p.header = at<int32_t>(ws, w.header);
+    p.perm = at<int32_t>(ws, w.perm);
+    p.segments = at<int4>(ws, w.segments);
+    p.sorted_ids = at<int32_t>(ws, w.sorted_ids);
+    p.expert_ids = at<int32_t>(ws, w.expert_ids);
+    p.ntpp = at<int32_t>(ws, w.ntpp);
+    p.moe_groups = at<int4>(ws, w.moe_groups);
+    p.seg_capacity = w.seg_capacity;
+    p.moe_group_capacity = w.moe_group_capacity;
+    p.sync = at<int32_t>(ws, w.sync);
+    p.sync_ints = w.max_tiles * 4;
+    return cuda_status(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLayout &w, bool moe, int32_t src_div,
+                              const void *x, int64_t ldx, void *y, int64_t ldy, const float *row_weight,
+                              lora_stream_t stream)
+{
+    // scratch needed per row of work at this table's largest A block
+    {
+        const int64_t R = t->max_R;
+        int64_t kc = (32 * 1024 / (2 * R)) / 64 * 64;
+        kc = std::max<int64_t>(64, std::min<int64_t>(1024, kc));
+        if (ceil_div(t->K, kc) * R > kPartialFloatsPerRow) return LORA_ERR_UNSUPPORTED;
+    }
+    DeviceInfo di;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    EngineParams p{};
+    p.a_ptr = t->d_a_ptr;
+    p.b_ptr = t->d_b_ptr;
+    p.rpad = t->d_rpad;
+    p.scale = t->d_scale;
+    p.L = t->L;
+    p.E_A = t->E_A;
+    p.E_B = t->E_B;
+    p.K = t->K;
+    p.n_slices = t->n_slices;
+    p.n_a = t->n_a;
+    for (int s = 0; s < kMaxSlices; ++s) {
+        p.slice_n[s] = t->slice_n[s];
+        p.slice_off[s] = t->slice_off[s];
+        p.slice_tile_off[s] = t->slice_tile_off[s];
+    }
+    int32_t *header = at<int32_t>(ws, w.header);
+    if (moe) {
+        p.groups = at<int4>(ws, w.moe_groups);
+        p.num_groups = header + H_NUM_MOE_GROUPS;
+        p.group_capacity = w.moe_group_capacity;
+        p.num_experts = ws->num_experts;
+        p.rows_capacity = (int64_t)ws->L * w.P_max_cap;
+        p.rows = at<int32_t>(ws, w.sorted_ids);
+    } else {
+        p.groups = at<int4>(ws, w.segments);
+        p.num_groups = header + H_NUM_SEGMENTS;
+        p.group_capacity = w.seg_capacity;
+        p.num_experts = 1;
+        p.rows_capacity = ws->max_M;
+        p.rows = at<int32_t>(ws, w.perm);
+    }
+    p.src_div = src_div;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.ldx = ldx;
+    p.y = static_cast<__nv_bfloat16 *>(y);
+    p.ldy = ldy;
+    p.row_weight = row_weight;
+    p.sync = at<int32_t>(ws, w.sync);
+    p.partials = at<float>(ws, w.partials);
+    p.partial_floats = w.partial_floats;
+    p.max_tiles = w.max_tiles;
+    p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
+    p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
+    p.withhold = g_opt_withhold.load() != 0;
+    int grid = di.sms * di.engine_blocks_per_sm;
+    const int64_t want = g_opt_grid.load();
+    if (want > 0 && want < grid) grid = (int)want;
+    cudaError_t e;
+    launch_engine(p, grid, engine_smem_bytes(0), reinterpret_cast<cudaStream_t>(stream), &e);
+    return cuda_status(e);
+}
+
+extern "C" lora_status lora_apply(lora_table t, const lora_workspace *ws, const void *d_x, int64_t ldx, void *d_y,
+                                  int64_t ldy, lora_stream_t stream)
+{
+    if (!valid_table(t) || !d_x || !d_y) return LORA_ERR_INVALID_ARG;
+    WsLayout w;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    if (ws->L != t->L) return LORA_ERR_INVALID_ARG;
+    if (t->E_A != 1 || t->E_B != 1) return LORA_ERR_INVALID_ARG;
+    if (ldx < t->K || ldy < t->N || ldx % 8 || ldy % 8 || !aligned16(d_x) || !aligned16(d_y)) return LORA_ERR_INVALID_ARG;
+    return run_engine(t, ws, w, false, 1, d_x, ldx, d_y, ldy, nullptr, stream);
+}
+
+extern "C" lora_status lora_moe_delta(lora_table t, int32_t stage, const lora_workspace *ws, const void *d_in,
+                                      int64_t ld_in, void *d_cache, int64_t ld_cache, const float *d_topk_weights,
+                                      lora_stream_t stream)
+{
+    if (!valid_table(t) || !d_in || !d_cache) return LORA_ERR_INVALID_ARG;
+    if (stage != LORA_MOE_GATE_UP && stage != LORA_MOE_DOWN) return LORA_ERR_INVALID_ARG;
+    WsLayout w;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    if (ws->L != t->L || ws->block_m <= 0) return LORA_ERR_INVALID_ARG;
+    if ((t->E_A != 1 && t->E_A != ws->num_experts) || (t->E_B != 1 && t->E_B != ws->num_experts))
+        return LORA_ERR_INVALID_ARG;
+    if (ld_in < t->K || ld_cache < t->N || ld_in % 8 || ld_cache % 8 || !aligned16(d_in) || !aligned16(d_cache))
+        return LORA_ERR_INVALID_ARG;
+    const int32_t src_div = stage == LORA_MOE_GATE_UP ? ws->topk : 1;
+    return run_engine(t, ws, w, true, src_div, d_in, ld_in, d_cache, ld_cache, d_topk_weights, stream);
+}
+
+extern "C" lora_status lora_get_status(const lora_workspace *ws, lora_stream_t stream)
+{
+    WsLayout w;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ERR_CUDA;
+    uint32_t word = 0;
+    uint32_t *dev = reinterpret_cast<uint32_t *>(at<int32_t>(ws, w.header) + H_ERR);
+    if (cudaMemcpy(&word, dev, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LORA_ERR_CUDA;
+    if (word != 0 && cudaMemset(dev, 0, 4) != cudaSuccess) return LORA_ERR_CUDA;
+    if (word & kErrTimeout) return LORA_ERR_TIMEOUT;
+    if (word & kErrWorkspace) return LORA_ERR_WORKSPACE;
+    if (word & kErrBadId) return LORA_ERR_BAD_ADAPTER_ID;
+    if (word & kErrBadExpert) return LORA_ERR_BAD_EXPERT_ID;
+    return LORA_OK;
+}
+
+extern "C" const char *lora_status_string(lora_status s)
+{
+    switch (s) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_INVALID_ARG: return "invalid argument";
+    case LORA_ERR_CUDA: return "CUDA runtime error";
+    case LORA_ERR_OOM: return "out of device memory";
+    case LORA_ERR_BAD_ADAPTER_ID: return "adapter id out of range";
+    case LORA_ERR_BAD_EXPERT_ID: return "expert id out of range";
+    case LORA_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case LORA_ERR_WORKSPACE: return "workspace too small";
+    case LORA_ERR_UNSUPPORTED: return "unsupported shape";
+    }
+    return "unknown status";
+}
+
+extern "C" lora_status lora_set_option(int32_t option, int64_t value)
+{
+    switch (option) {
+    case LORA_OPT_PATH:
+        if (value < 0 || value > 2) return LORA_ERR_INVALID_ARG;
+        g_opt_path = value;
+        return LORA_OK;
+    case LORA_OPT_TC_MIN_ROWS:
+        if (value < 0) return LORA_ERR_INVALID_ARG;
+        g_opt_tc_min_rows = value;
+        return LORA_OK;
+    case LORA_OPT_WAIT_TIMEOUT_NS:
+        if (value < 1000) return LORA_ERR_INVALID_ARG;
+        g_opt_timeout_ns = value;
+        return LORA_OK;
+    case LORA_OPT_GRID_CTAS:
+        if (value < 0) return LORA_ERR_INVALID_ARG;
+        g_opt_grid = value;
+        return LORA_OK;
+    case LORA_OPT_TEST_WITHHOLD_HANDOFF:
+        g_opt_withhold = value != 0;
+        return LORA_OK;
+    }
+    return LORA_ERR_INVALID_ARG;
+}
+
+extern "C" int64_t lora_get_option(int32_t option)
+{
+    switch (option) {
+    case LORA_OPT_PATH: return g_opt_path.load();
+    case LORA_OPT_TC_MIN_ROWS: return g_opt_tc_min_rows.load();
+    case LORA_OPT_WAIT_TIMEOUT_NS: return g_opt_timeout_ns.load();
+    case LORA_OPT_GRID_CTAS: return g_opt_grid.load();
+    case LORA_OPT_TEST_WITHHOLD_HANDOFF: return g_opt_withhold.load();
+    }
+    return -1;
+}

@@ -1,0 +1,214 @@
+// Internal definitions shared by the library's translation units: workspace
+// layout, kernel parameter blocks and small sm_103a PTX wrappers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/lora.h"
+
+namespace lora {
+
+// ---------------------------------------------------------------------------
+// sizes
+// ---------------------------------------------------------------------------
+constexpr int kMaxRank = 64;           // largest true rank
+constexpr int kMaxSlices = 4;
+constexpr int kNTile = 256;            // B is stored in tiles of 256 output rows
+constexpr int kBgmvRows = 16;          // rows of one CUDA-core tile
+constexpr int kEngineThreads = 256;
+constexpr int kHeaderInts = 16;
+
+// device error word bits (sticky, cleared by lora_get_status)
+constexpr uint32_t kErrBadId = 1u << 0;
+constexpr uint32_t kErrBadExpert = 1u << 1;
+constexpr uint32_t kErrTimeout = 1u << 2;
+constexpr uint32_t kErrWorkspace = 1u << 3;
+
+// header slots
+enum HeaderSlot {
+    H_M = 0, H_NUM_SEGMENTS = 1, H_NUM_VALID = 2, H_NUM_MOE_GROUPS = 3, H_TOPK = 4, H_E = 5,
+    H_BLOCK_M = 6, H_P_MAX = 7, H_B_MAX = 8, H_ERR = 12
+};
+
+inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Workspace layout, derived on the host from the lora_workspace fields.
+struct WsLayout {
+    size_t header, perm, segments, sorted_ids, expert_ids, ntpp, moe_groups;
+    size_t sync, partials, total;
+    int32_t seg_capacity, moe_group_capacity, P_max_cap, B_max_cap;
+    int32_t max_tiles;
+    int64_t partial_floats;
+};
+bool ws_layout(int32_t max_M, int32_t L, int32_t topk, int32_t E, int32_t block_m, WsLayout *out);
+
+// ---------------------------------------------------------------------------
+// engine parameters (one launch of the shrink/expand kernel)
+// ---------------------------------------------------------------------------
+struct EngineParams {
+    // weight table
+    const uint64_t *a_ptr;   // [L * E_A] packed A block addresses
+    const uint64_t *b_ptr;   // [L * E_B] packed B block addresses
+    const int32_t *rpad;     // [L] stored rank (multiple of 16)
+    const float *scale;      // [L]
+    int32_t L, E_A, E_B, K, n_slices, n_a;
+    int32_t slice_n[kMaxSlices], slice_off[kMaxSlices], slice_tile_off[kMaxSlices];
+    // work description written by lora_build_segments
+    const int4 *groups;      // (adapter, expert, index into rows, count)
+    const int32_t *num_groups;
+    int32_t group_capacity;
+    int32_t num_experts;     // experts a group may name (1 for dense)
+    int64_t rows_capacity;   // entries of the row list
+    const int32_t *rows;     // row list
+    int32_t src_div;         // shrink input row = rows[i] / src_div
+    // operands
+    const __nv_bfloat16 *x;  int64_t ldx;
+    __nv_bfloat16 *y;        int64_t ldy;
+    const float *row_weight; // optional, indexed by rows[i]
+    // scratch
+    int32_t *sync;           // [max_tiles][4] counters
+    float *partials;
+    int64_t partial_floats;
+    int32_t max_tiles;
+    uint32_t *err;
+    uint64_t timeout_ns;
+    int32_t withhold;        // test hook: do not publish shrink results
+};
+
+void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s, cudaError_t *err);
+size_t engine_smem_bytes(int group_capacity);
+const void *engine_kernel_ptr();
+
+struct BuildParams {
+    const int32_t *ids;
+    const int32_t *topk_ids;      // nullable
+    const uint8_t *enabled;       // nullable
+    int32_t M, L, topk, E, block_m;
+    int32_t *header, *perm;
+    int4 *segments;
+    int32_t *sorted_ids, *expert_ids, *ntpp;
+    int4 *moe_groups;
+    int32_t seg_capacity, moe_group_capacity;
+    int32_t *sync;                // zeroed
+    int32_t sync_ints;
+};
+cudaError_t launch_build(const BuildParams &p, cudaStream_t s);
+
+cudaError_t launch_pack_a(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int32_t K, int32_t n_a, int32_t rank,
+                          int32_t rpad, cudaStream_t s);
+cudaError_t launch_pack_b(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int32_t rank, int32_t rpad,
+                          int32_t n_slices, const int32_t *slice_n, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier with a time limit.  Returns false
+// (and sets the timeout bit) when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns, uint32_t *err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > limit_ns) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Bulk (non-tensor) async copy global -> shared, completing on an mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int atom_add_release_gpu(int32_t *p, int v)
+{
+    int old;
+    asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *p, int v)
+{
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void nanosleep_ns(uint32_t ns)
+{
+    asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+
+// 8 bf16 (one uint4) -> 8 floats
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float f[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+#endif
+
+}  // namespace lora

@@ -144,9 +144,10 @@ def make_dense(name: str, seed: int, ids: np.ndarray, K: int, slice_n: Sequence[
     """Draw one dense problem.
 
     x ~ N(0,1); A_i ~ N(0, 1/K); B_i ~ N(0, 1/r_i); all bf16.
-    y_base: "zero" (delta-only runs), "random" (N(0, K) entries, the
-    distribution of x @ W^T with W ~ N(0,1)), or "none" (caller computes it
-    from W, e.g. with a library GEMM).
+    y_base: "xw" (bf16 of the fp32 product x @ W^T, W ~ N(0,1)), "zero"
+    (delta-only runs), "random" (N(0, K) entries, the distribution of x @ W^T,
+    drawn directly for sizes where the base GEMM is not worth running on the
+    host), or "none".
     """
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     M = int(ids.shape[0])
@@ -157,7 +158,11 @@ def make_dense(name: str, seed: int, ids: np.ndarray, K: int, slice_n: Sequence[
     A = [_normal_bf16(_rng(seed, _K_A, i), (n_a * r, K), 1.0 / np.sqrt(K)) for i, r in enumerate(ranks)]
     B = [_normal_bf16(_rng(seed, _K_B, i), (N, r), 1.0 / np.sqrt(r)) for i, r in enumerate(ranks)]
     W = _normal_bf16(_rng(seed, _K_W), (N, K), 1.0) if with_W else None
-    if y_base == "zero":
+    if y_base == "xw":
+        if W is None:
+            W = _normal_bf16(_rng(seed, _K_W), (N, K), 1.0)
+        yb = f32_to_bf16_bits(bf16_bits_to_f32(x) @ bf16_bits_to_f32(W).T)
+    elif y_base == "zero":
         yb = np.zeros((M, N), np.uint16)
     elif y_base == "random":
         yb = _normal_bf16(_rng(seed, _K_YBASE), (M, N), float(np.sqrt(K)))
@@ -244,6 +249,14 @@ def router_topk(seed: int, M: int, E: int, topk: int):
     return order.astype(np.int32), w.astype(np.float32)
 
 
+def moe_routing(seed: int, M: int, E: int, topk: int, L: int, ids: Optional[np.ndarray] = None):
+    """(ids, topk_ids, topk_weights) of an MoE batch: ids uniform over the L adapters."""
+    if ids is None:
+        ids = _rng(seed, _K_STRUCT).integers(0, L, M).astype(np.int32)
+    topk_ids, topk_w = router_topk(seed, M, E, topk)
+    return np.ascontiguousarray(ids, dtype=np.int32), topk_ids, topk_w
+
+
 def make_moe(seed: int, M: int, H: int, I: int, E: int, topk: int, ranks: Sequence[int], block_m: int = 64,
              ids: Optional[np.ndarray] = None, shared_outer: bool = True, scale: float = 2.0,
              zero_base: bool = False) -> MoEProblem:
@@ -257,10 +270,7 @@ def make_moe(seed: int, M: int, H: int, I: int, E: int, topk: int, ranks: Sequen
     delta-only checks.
     """
     L = len(ranks)
-    if ids is None:
-        ids = _rng(seed, _K_STRUCT).integers(0, L, M).astype(np.int32)
-    ids = np.ascontiguousarray(ids, dtype=np.int32)
-    topk_ids, topk_w = router_topk(seed, M, E, topk)
+    ids, topk_ids, topk_w = moe_routing(seed, M, E, topk, L, ids)
     P = M * topk
     x = _normal_bf16(_rng(seed, _K_X), (M, H), 1.0)
     if zero_base:

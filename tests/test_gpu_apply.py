@@ -1,0 +1,170 @@
+"""lora_apply on the GPU vs the CPU oracle.
+
+Gates: max|y - y_ref| <= 1e-2 max|y_ref| on every config, plus the same gate
+on the delta alone (y_base = 0), because y_base dominates |y|; rows of tokens
+without an adapter bit-identical; integer inputs bit-exact; results invariant
+(bitwise) to token order and repeatable.
+"""
+import numpy as np
+import pytest
+import torch
+
+from segmented_rank_gemm_lora_gb300 import lora, synth
+from gpu_util import check_close, dev_bf16, host_bits, host_f64, oracle_dense, pack_dense, run_dense
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [0]
+
+
+def problems():
+    yield "tiny", lambda base: synth.tiny(0, y_base="xw" if base else "zero")
+    yield "decode", lambda base: synth.decode(1, y_base="random" if base else "zero")
+    yield "prefill", lambda base: synth.prefill(2, y_base="random" if base else "zero")
+    yield "stacked_qkv", lambda base: synth.stacked("qkv", y_base="random" if base else "zero")
+    yield "stacked_gate_up", lambda base: synth.stacked("gate_up", y_base="random" if base else "zero")
+    yield "stacked_down", lambda base: synth.stacked("down", y_base="random" if base else "zero")
+    yield "ragged", lambda base: synth.make_dense("ragged", 9, np.random.default_rng(9).integers(-1, 3, 37)
+                                                  .astype(np.int32), 200, [72, 136], [8, 24, 40],
+                                                  y_base="random" if base else "zero")
+    yield "shared_a", lambda base: synth.make_dense("shared", 10, np.random.default_rng(10).integers(-1, 4, 50)
+                                                    .astype(np.int32), 264, [128, 128], [16, 32, 8, 64], n_a=1,
+                                                    y_base="random" if base else "zero")
+
+
+@pytest.mark.parametrize("name,make", list(problems()), ids=[n for n, _ in problems()])
+def test_apply_matches_oracle(name, make):
+    for base in (True, False):
+        p = make(base)
+        y, table, ws = run_dense(p)
+        assert lora.lora_get_status(ws) == lora.LORA_OK
+        got = host_f64(y)
+        ref = oracle_dense(p)
+        check_close(got, ref, "%s base=%s" % (name, base))
+        none = p.ids < 0
+        assert np.array_equal(host_bits(y)[none], p.y_base[none])
+        table.destroy()
+
+
+def test_canary_columns_and_rows_untouched():
+    p = synth.decode(3, y_base="random")
+    y, table, ws = run_dense(p, x_extra=8, y_extra=24)
+    yb = host_bits(y)
+    assert (yb[:, p.N:] == 0x7FC1).all()
+    check_close(synth.bf16_bits_to_f32(yb[:, :p.N]).astype(np.float64), oracle_dense(p))
+
+
+@pytest.mark.parametrize("slices,n_a", [([96], None), ([64, 32, 32], None), ([48, 48], 1)])
+def test_integer_inputs_are_bit_exact(slices, n_a):
+    ids = np.random.default_rng(4).integers(-1, 5, 90).astype(np.int32)
+    ids[:20] = 2   # one segment large enough to span several row tiles
+    p = synth.make_dense_int(12, ids, 384, slices, [8, 16, 32, 64, 40], n_a=n_a)
+    ref = oracle_dense(p)
+    assert np.abs(ref).max() <= 256 and np.array_equal(ref, np.round(ref))
+    y, _, ws = run_dense(p)
+    assert lora.lora_get_status(ws) == lora.LORA_OK
+    assert np.array_equal(host_f64(y), ref)
+
+
+def test_token_order_invariance_is_bitwise():
+    p = synth.prefill(2, y_base="random")
+    y, table, ws = run_dense(p)
+    perm = np.random.default_rng(1).permutation(p.M)
+    q = synth.DenseProblem(**{**p.__dict__})
+    q.ids, q.x, q.y_base = p.ids[perm], p.x[perm], p.y_base[perm]
+    yq, _, _ = run_dense(q, table=table, ws=ws)
+    assert np.array_equal(host_bits(yq), host_bits(y)[perm])
+
+
+def test_repeatable():
+    p = synth.decode(1, y_base="random")
+    y1, table, ws = run_dense(p)
+    y2, _, _ = run_dense(p, table=table, ws=ws)
+    y3, _, _ = run_dense(p, table=table, ws=ws, build=False)   # second apply on the same segment table
+    assert np.array_equal(host_bits(y1), host_bits(y2))
+    assert np.array_equal(host_bits(y1), host_bits(y3))
+
+
+def test_all_none_and_empty_batches_are_no_ops():
+    p = synth.decode(1, y_base="random")
+    p.ids[:] = -1
+    y, table, ws = run_dense(p)
+    assert lora.lora_get_status(ws) == lora.LORA_OK
+    assert np.array_equal(host_bits(y), p.y_base)
+    ws0 = lora.Workspace(4, p.L)
+    lora.lora_build_segments(ws0, torch.zeros(0, dtype=torch.int32, device="cuda"))
+    x = torch.zeros(1, p.K, dtype=torch.bfloat16, device="cuda")[:0]
+    yy = torch.zeros(1, p.N, dtype=torch.bfloat16, device="cuda")[:0]
+    lora.lora_apply(table, ws0, x, yy)
+    assert lora.lora_get_status(ws0) == lora.LORA_OK
+
+
+def test_bad_ids_leave_rows_and_report():
+    p = synth.decode(6, y_base="random")
+    p.ids[[0, 5]] = [25, -4]
+    y, table, ws = run_dense(p)
+    assert lora.lora_get_status(ws) == lora.LORA_ERR_BAD_ADAPTER_ID
+    yb = host_bits(y)
+    assert np.array_equal(yb[[0, 5]], p.y_base[[0, 5]])
+    q = synth.DenseProblem(**{**p.__dict__})
+    ref = oracle_dense(q)
+    check_close(synth.bf16_bits_to_f32(yb).astype(np.float64), ref)
+
+
+def test_one_workspace_serves_every_projection():
+    ids = synth.ids_stacked(3)
+    ws = lora.Workspace(len(ids), 32)
+    lora.lora_build_segments(ws, torch.from_numpy(ids).cuda())
+    for proj in ("qkv", "gate_up", "down"):
+        p = synth.stacked(proj, y_base="zero")
+        y, table, _ = run_dense(p, ws=ws, build=False)
+        assert lora.lora_get_status(ws) == lora.LORA_OK
+        check_close(host_f64(y), oracle_dense(p), proj)
+        table.destroy()
+
+
+def test_stored_ranks_follow_the_padding_rule():
+    p = synth.make_dense("r", 1, np.zeros(4, np.int32), 64, [64], [16, 20, 8, 33, 64])
+    table = pack_dense(p)
+    assert [table.stored_rank(i) for i in range(5)] == [16, 32, 16, 48, 64]
+    info = table.info()
+    assert info.num_rank_groups == 4 and info.L == 5 and info.N == 64
+
+
+def test_handoff_wait_times_out_cleanly_and_recovers():
+    p = synth.decode(1, y_base="random")
+    table = pack_dense(p)
+    ws = lora.Workspace(p.M, p.L)
+    old = lora.lora_get_option(lora.LORA_OPT_WAIT_TIMEOUT_NS)
+    try:
+        lora.lora_set_option(lora.LORA_OPT_WAIT_TIMEOUT_NS, 2_000_000)
+        lora.lora_set_option(lora.LORA_OPT_TEST_WITHHOLD_HANDOFF, 1)
+        y, _, _ = run_dense(p, table=table, ws=ws)
+        assert lora.lora_get_status(ws) == lora.LORA_ERR_TIMEOUT
+        assert np.array_equal(host_bits(y), p.y_base)      # nothing was added
+    finally:
+        lora.lora_set_option(lora.LORA_OPT_TEST_WITHHOLD_HANDOFF, 0)
+        lora.lora_set_option(lora.LORA_OPT_WAIT_TIMEOUT_NS, old)
+    y, _, _ = run_dense(p, table=table, ws=ws)                   # rebuild resets the scratch
+    assert lora.lora_get_status(ws) == lora.LORA_OK
+    check_close(host_f64(y), oracle_dense(p))
+
+
+def test_graph_capture_replays():
+    p = synth.decode(2, y_base="random")
+    table = pack_dense(p)
+    ws = lora.Workspace(p.M, p.L)
+    ids = torch.from_numpy(p.ids).cuda()
+    x = dev_bf16(p.x)
+    y = dev_bf16(p.y_base)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        lora.lora_build_segments(ws, ids)
+        lora.lora_apply(table, ws, x, y)
+    y.copy_(dev_bf16(p.y_base))
+    g.replay()
+    torch.cuda.synchronize()
+    assert lora.lora_get_status(ws) == lora.LORA_OK
+    check_close(host_f64(y), oracle_dense(p))
