@@ -381,39 +381,61 @@ def run_ours(args, world, rank, local):
             launches["n"] = c
         return fn
 
-    g_warm = capture(torch, steps_fn(W), stream)
-    g_main = capture(torch, steps_fn(K), stream)
-    gpu_launches = launches["n"]
-    g_apply = capture(torch, steps_fn(K, build=False), stream)
+    # K steps are issued as replays of a graph of C = R steps (one rotation over the sets) plus one
+    # graph with the remaining K mod C steps, so exactly K steps run in the timed region.
+    C = R
+    g_chunk = capture(torch, steps_fn(C), stream)
+    launches_chunk = launches["n"]
+    tail = K % C
+    g_tail = capture(torch, steps_fn(tail), stream) if tail else None
+    launches_tail = launches["n"] if tail else 0
+    gpu_launches = (K // C) * launches_chunk + launches_tail
+    g_apply = capture(torch, steps_fn(C, build=False), stream)
 
-    # ---------------- timed region: K steps ----------------
+    def run_steps(n_chunks, with_tail):
+        for _ in range(n_chunks):
+            g_chunk.replay()
+        if with_tail and g_tail is not None:
+            g_tail.replay()
+
+    # ---------------- warm-up (W steps) and a load period so clock samples see a busy GPU ----------------
     clocks = ClockSampler(local)
-    with torch.cuda.stream(stream):
-        g_warm.replay()
-    torch.cuda.synchronize()
     clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(max(1, (W + C - 1) // C)):
+            g_chunk.replay()
+        torch.cuda.synchronize()
+        t_end = time.perf_counter() + args.load_seconds
+        while time.perf_counter() < t_end:
+            run_steps(8, False)
+            torch.cuda.synchronize()
+
+    # ---------------- timed region: exactly K steps ----------------
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    g_main.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        run_steps(K // C, True)
+        e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
     ms_max = max_over_ranks(ms, world)
 
-    # ---------------- dominant kernel alone: K applies, same rotation ----------------
+    # ---------------- dominant kernel alone: the same rotation of applies ----------------
+    reps = max(1, K // C)
     with torch.cuda.stream(stream):
         g_apply.replay()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            g_apply.replay()
+        a1.record(stream)
     torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    g_apply.replay()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    apply_ms = a0.elapsed_time(a1) / K
+    apply_ms = a0.elapsed_time(a1) / (reps * C)
     if "gu" in sets[0]:
         apply_ms /= 2.0     # two delta launches per step
 
@@ -477,7 +499,7 @@ def run_e2e(args, sets, torch, lora, dev, stream, world):
             o[k].copy_(s[k], non_blocking=True)
             d2h += o[k].numel() * o[k].element_size()
 
-    K = args.steps
+    K = min(args.steps, args.e2e_steps)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             one(i)
@@ -492,14 +514,17 @@ def run_e2e(args, sets, torch, lora, dev, stream, world):
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     tokens = np.mean([sets[i % len(host)]["tokens"] for i in range(K)])
     return {"value": world * tokens * K / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h)}
+            "d2h_bytes_per_step": int(d2h), "steps": K,
+            "path": "eager calls through the Python binding, pinned host buffers, non-blocking copies"}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--load-seconds", type=float, default=1.0)
+    ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode", choices=sorted(CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
