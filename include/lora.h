@@ -262,6 +262,16 @@ typedef enum {
 lora_status lora_set_option(int32_t option, int64_t value);
 int64_t lora_get_option(int32_t option);
 
+/*
+ * Phase tracing (off by default).  With a non-NULL device buffer, every later
+ * lora_apply / lora_moe_delta launch writes, per thread block, 8 uint64
+ * %globaltimer stamps (ns): entry, work list ready, first shrink operands
+ * landed, last shrink result published, first hand-off observed, partials
+ * reduced, first expand operands landed, exit.  Blocks past bytes/64 are not
+ * traced.  Pass NULL to switch tracing off.  Process-wide.
+ */
+lora_status lora_set_trace(void *d_trace, size_t bytes);
+
 /* Stored rank for a true rank: rounded up to a multiple of 16 ("vLLM-Ascend
  * dynamic LoRA fused operator", section 4.3: 16 stays 16, 20 becomes 32).
  * Host-only; returns -1 outside 1..64. */

@@ -22,6 +22,8 @@ std::atomic<int64_t> g_opt_tc_min_rows{16};
 std::atomic<int64_t> g_opt_timeout_ns{1000000000LL};
 std::atomic<int64_t> g_opt_grid{0};
 std::atomic<int64_t> g_opt_withhold{0};
+std::atomic<void *> g_trace{nullptr};
+std::atomic<int64_t> g_trace_bytes{0};
 
 struct DeviceInfo {
     int sms = 0;
@@ -435,6 +437,8 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
     p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
     p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
     p.withhold = g_opt_withhold.load() != 0;
+    p.trace = static_cast<uint64_t *>(g_trace.load());
+    p.trace_ctas = p.trace ? (int32_t)(g_trace_bytes.load() / 64) : 0;
     int grid = di.sms * di.engine_blocks_per_sm;
     const int64_t want = g_opt_grid.load();
     if (want > 0 && want < grid) grid = (int)want;
@@ -532,6 +536,14 @@ extern "C" lora_status lora_set_option(int32_t option, int64_t value)
         return LORA_OK;
     }
     return LORA_ERR_INVALID_ARG;
+}
+
+extern "C" lora_status lora_set_trace(void *d_trace, size_t bytes)
+{
+    if (d_trace && (bytes < 64 || (reinterpret_cast<uintptr_t>(d_trace) & 7u))) return LORA_ERR_INVALID_ARG;
+    g_trace_bytes = d_trace ? (int64_t)bytes : 0;
+    g_trace = d_trace;
+    return LORA_OK;
 }
 
 extern "C" int64_t lora_get_option(int32_t option)

@@ -76,6 +76,8 @@ struct EngineParams {
     uint32_t *err;
     uint64_t timeout_ns;
     int32_t withhold;        // test hook: do not publish shrink results
+    uint64_t *trace;         // optional [trace_ctas][8] phase stamps
+    int32_t trace_ctas;
 };
 
 void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s, cudaError_t *err);

@@ -28,7 +28,7 @@ LORA_OPT_PATH, LORA_OPT_TC_MIN_ROWS, LORA_OPT_WAIT_TIMEOUT_NS, LORA_OPT_GRID_CTA
 EXPORTED = ["lora_pack_weights", "lora_table_destroy", "lora_table_info", "lora_table_stored_rank",
             "lora_workspace_bytes", "lora_workspace_layout", "lora_build_segments", "lora_apply",
             "lora_moe_delta", "lora_get_status", "lora_status_string", "lora_set_option", "lora_get_option",
-            "lora_rank_padded"]
+            "lora_rank_padded", "lora_set_trace"]
 
 
 class LoraError(RuntimeError):
@@ -97,6 +97,7 @@ def load(build_if_missing: bool = False):
         "lora_set_option": (_c_i32, [_c_i32, _c_i64]),
         "lora_get_option": (_c_i64, [_c_i32]),
         "lora_rank_padded": (_c_i32, [_c_i32]),
+        "lora_set_trace": (_c_i32, [P, _c_sz]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -291,6 +292,14 @@ def lora_set_option(option: int, value: int):
 
 def lora_get_option(option: int) -> int:
     return int(load().lora_get_option(int(option)))
+
+
+def lora_set_trace(buf: Optional[torch.Tensor]):
+    """Per-block phase stamps of later engine launches into buf (CUDA int64/uint8 tensor), or None to stop."""
+    if buf is None:
+        _check(load().lora_set_trace(None, 0), "lora_set_trace")
+    else:
+        _check(load().lora_set_trace(buf.data_ptr(), buf.numel() * buf.element_size()), "lora_set_trace")
 
 
 def lora_rank_padded(rank: int) -> int:
