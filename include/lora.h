@@ -272,6 +272,34 @@ int64_t lora_get_option(int32_t option);
  */
 lora_status lora_set_trace(void *d_trace, size_t bytes);
 
+/*
+ * One step without any caller-provided device scratch: builds the segment
+ * table of d_lora_id_map (int32 [M], device) and applies the LoRA delta of
+ * `table` to d_y exactly as lora_build_segments + lora_apply would.  The
+ * pages have no counterpart; it exists for callers that cannot allocate
+ * device memory (code running inside another allocator's arena, under a
+ * no-allocation policy on a serving hot path, or in a process that only
+ * receives pre-made buffers), who can still pass their inputs and outputs.
+ *
+ * Every byte of scratch (segment table, hand-off partials and counters) is a
+ * fixed array in this library, about 8.4 MiB, that each GPU which loads the
+ * library holds until the process exits.  Limits: M <= 4096 tokens, and
+ * M * ceil(K / kc) * R <= 2^21 partial floats, where R is the table's largest
+ * A block (n_a * stored rank) and kc = clamp(floor(16384 / R) rounded down to a
+ * multiple of 64, 64, 1024); larger calls return LORA_ERR_WORKSPACE before
+ * launching anything.  Same argument rules as lora_apply (dense tables only).
+ *
+ * The first call on a device looks the array up (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All
+ * calls share the one array and it keeps the last call's contents: the call
+ * clears what must start at zero itself, and calls that overlap on the GPU
+ * (different streams, or different host threads) race on it.  Device-side
+ * conditions (ids out of range are left unchanged as in lora_apply; a wait
+ * that ran out) are not reported by this entry point.
+ */
+lora_status lora_apply_static_scratch(lora_table table, const int32_t *d_lora_id_map, int32_t M, const void *d_x,
+                                      int64_t ldx, void *d_y, int64_t ldy, lora_stream_t stream);
+
 /* Stored rank for a true rank: rounded up to a multiple of 16 ("vLLM-Ascend
  * dynamic LoRA fused operator", section 4.3: 16 stays 16, 20 becomes 32).
  * Host-only; returns -1 outside 1..64. */

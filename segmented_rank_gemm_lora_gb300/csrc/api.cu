@@ -557,3 +557,130 @@ extern "C" int64_t lora_get_option(int32_t option)
     }
     return -1;
 }
+
+// ---------------------------------------------------------------------------
+// lora_apply_static_scratch: the whole step (segment table + fused apply) with
+// every byte of scratch in one fixed device array, for callers that cannot
+// allocate device memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int32_t kStaticMaxM = 4096;                        // tokens per call
+constexpr int32_t kStaticMaxTiles = kStaticMaxM / kBgmvRows + kStaticMaxM;
+constexpr int64_t kStaticPartialFloats = 2 * 1024 * 1024;   // 8 MiB of hand-off partials
+constexpr size_t kStaticHeader = 0;
+constexpr size_t kStaticPerm = 256;
+constexpr size_t kStaticSegments = kStaticPerm + (size_t)kStaticMaxM * 4;
+constexpr size_t kStaticSync = kStaticSegments + (size_t)kStaticMaxM * 16;
+constexpr size_t kStaticPartials = kStaticSync + (size_t)kStaticMaxTiles * 16;
+constexpr size_t kStaticBytes = kStaticPartials + (size_t)kStaticPartialFloats * 4;
+
+// Shared by every call on a device and kept until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
+
+std::mutex g_static_mu;
+std::map<int, unsigned char *> g_static_addr;   // device -> address of g_static_scratch
+
+// Device address of g_static_scratch on the current device (looked up once per device).
+lora_status static_scratch_address(unsigned char **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    auto it = g_static_addr.find(dev);
+    if (it == g_static_addr.end()) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return LORA_ERR_CUDA;
+        }
+        it = g_static_addr.emplace(dev, static_cast<unsigned char *>(ptr)).first;
+    }
+    *out = it->second;
+    return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_ids, int32_t M, const void *d_x,
+                                                 int64_t ldx, void *d_y, int64_t ldy, lora_stream_t stream)
+{
+    if (!valid_table(t) || M < 0 || (M > 0 && (!d_ids || !d_x || !d_y))) return LORA_ERR_INVALID_ARG;
+    if (t->E_A != 1 || t->E_B != 1) return LORA_ERR_INVALID_ARG;
+    if (M > 0 && (ldx < t->K || ldy < t->N || ldx % 8 || ldy % 8 || !aligned16(d_x) || !aligned16(d_y)))
+        return LORA_ERR_INVALID_ARG;
+    if (M > kStaticMaxM) return LORA_ERR_WORKSPACE;
+    // the hand-off partials of M rows at this table's largest A block must fit the fixed array
+    {
+        const int64_t R = t->max_R;
+        int64_t kc = (32 * 1024 / (2 * R)) / 64 * 64;
+        kc = std::max<int64_t>(64, std::min<int64_t>(1024, kc));
+        if ((int64_t)M * ceil_div(t->K, kc) * R > kStaticPartialFloats) return LORA_ERR_WORKSPACE;
+    }
+    unsigned char *base = nullptr;
+    lora_status st = static_scratch_address(&base);
+    if (st != LORA_OK) return st;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != LORA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t *header = reinterpret_cast<int32_t *>(base + kStaticHeader);
+    // this call's device-side status starts clean (the array keeps the last call's contents)
+    if (cudaMemsetAsync(header + H_ERR, 0, 4, s) != cudaSuccess) return LORA_ERR_CUDA;
+
+    BuildParams b{};
+    b.ids = d_ids;
+    b.M = M;
+    b.L = t->L;
+    b.header = header;
+    b.perm = reinterpret_cast<int32_t *>(base + kStaticPerm);
+    b.segments = reinterpret_cast<int4 *>(base + kStaticSegments);
+    b.seg_capacity = kStaticMaxM;
+    b.sync = reinterpret_cast<int32_t *>(base + kStaticSync);   // zeroed by the build kernel
+    b.sync_ints = kStaticMaxTiles * 4;
+    if (launch_build(b, s) != cudaSuccess) return LORA_ERR_CUDA;
+
+    EngineParams p{};
+    p.a_ptr = t->d_a_ptr;
+    p.b_ptr = t->d_b_ptr;
+    p.rpad = t->d_rpad;
+    p.scale = t->d_scale;
+    p.L = t->L;
+    p.E_A = 1;
+    p.E_B = 1;
+    p.K = t->K;
+    p.n_slices = t->n_slices;
+    p.n_a = t->n_a;
+    for (int i = 0; i < kMaxSlices; ++i) {
+        p.slice_n[i] = t->slice_n[i];
+        p.slice_off[i] = t->slice_off[i];
+        p.slice_tile_off[i] = t->slice_tile_off[i];
+    }
+    p.groups = b.segments;
+    p.num_groups = header + H_NUM_SEGMENTS;
+    p.group_capacity = kStaticMaxM;
+    p.num_experts = 1;
+    p.rows_capacity = kStaticMaxM;
+    p.rows = b.perm;
+    p.src_div = 1;
+    p.x = static_cast<const __nv_bfloat16 *>(d_x);
+    p.ldx = ldx;
+    p.y = static_cast<__nv_bfloat16 *>(d_y);
+    p.ldy = ldy;
+    p.row_weight = nullptr;
+    p.sync = b.sync;
+    p.partials = reinterpret_cast<float *>(base + kStaticPartials);
+    p.partial_floats = kStaticPartialFloats;
+    p.max_tiles = kStaticMaxTiles;
+    p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
+    p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
+    p.withhold = 0;
+    p.trace = nullptr;
+    p.trace_ctas = 0;
+    int grid = di.sms * di.engine_blocks_per_sm;
+    const int64_t want = g_opt_grid.load();
+    if (want > 0 && want < grid) grid = (int)want;
+    cudaError_t e;
+    launch_engine(p, grid, engine_smem_bytes(0), s, &e);
+    return cuda_status(e);
+}

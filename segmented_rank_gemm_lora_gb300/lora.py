@@ -28,7 +28,7 @@ LORA_OPT_PATH, LORA_OPT_TC_MIN_ROWS, LORA_OPT_WAIT_TIMEOUT_NS, LORA_OPT_GRID_CTA
 EXPORTED = ["lora_pack_weights", "lora_table_destroy", "lora_table_info", "lora_table_stored_rank",
             "lora_workspace_bytes", "lora_workspace_layout", "lora_build_segments", "lora_apply",
             "lora_moe_delta", "lora_get_status", "lora_status_string", "lora_set_option", "lora_get_option",
-            "lora_rank_padded", "lora_set_trace"]
+            "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch"]
 
 
 class LoraError(RuntimeError):
@@ -98,6 +98,7 @@ def load(build_if_missing: bool = False):
         "lora_get_option": (_c_i64, [_c_i32]),
         "lora_rank_padded": (_c_i32, [_c_i32]),
         "lora_set_trace": (_c_i32, [P, _c_sz]),
+        "lora_apply_static_scratch": (_c_i32, [P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
