@@ -437,6 +437,8 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
     p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
     p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
     p.withhold = g_opt_withhold.load() != 0;
+    p.path = (int32_t)g_opt_path.load();
+    p.tc_min_rows = (int32_t)g_opt_tc_min_rows.load();
     p.trace = static_cast<uint64_t *>(g_trace.load());
     p.trace_ctas = p.trace ? (int32_t)(g_trace_bytes.load() / 64) : 0;
     int grid = di.sms * di.engine_blocks_per_sm;
@@ -675,6 +677,8 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
     p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
     p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
     p.withhold = 0;
+    p.path = (int32_t)g_opt_path.load();
+    p.tc_min_rows = (int32_t)g_opt_tc_min_rows.load();
     p.trace = nullptr;
     p.trace_ctas = 0;
     int grid = di.sms * di.engine_blocks_per_sm;

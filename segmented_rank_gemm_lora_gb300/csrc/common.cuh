@@ -76,6 +76,8 @@ struct EngineParams {
     uint32_t *err;
     uint64_t timeout_ns;
     int32_t withhold;        // test hook: do not publish shrink results
+    int32_t path;            // 0 auto, 1 every group on CUDA cores, 2 every group on tensor cores
+    int32_t tc_min_rows;     // groups with more rows take the tensor-core path
     uint64_t *trace;         // optional [trace_ctas][8] phase stamps
     int32_t trace_ctas;
 };
@@ -162,6 +164,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         }
     }
     return true;
+}
+
+// Retire `bytes` of an mbarrier's expected transactions that will never arrive.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
 // Bulk (non-tensor) async copy global -> shared, completing on an mbarrier.

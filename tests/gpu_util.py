@@ -64,3 +64,20 @@ def check_close(got, ref, what=""):
     scale = float(np.abs(ref).max()) if ref.size else 0.0
     assert err <= TOL * scale, "%s: max err %.4g vs bound %.4g" % (what, err, TOL * scale)
     return err, scale
+
+
+class forced_path:
+    """Context manager: LORA_OPT_PATH = path (0 auto, 1 CUDA-core, 2 tensor-core) inside the block."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        self.old = lora.lora_get_option(lora.LORA_OPT_PATH)
+        lora.lora_set_option(lora.LORA_OPT_PATH, self.path)
+
+    def __exit__(self, *exc):
+        lora.lora_set_option(lora.LORA_OPT_PATH, self.old)
+
+
+PATHS = (0, 1, 2)

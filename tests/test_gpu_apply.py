@@ -10,11 +10,9 @@ import pytest
 import torch
 
 from segmented_rank_gemm_lora_gb300 import lora, synth
-from gpu_util import check_close, dev_bf16, host_bits, host_f64, oracle_dense, pack_dense, run_dense
+from gpu_util import PATHS, check_close, dev_bf16, forced_path, host_bits, host_f64, oracle_dense, pack_dense, run_dense
 
 pytestmark = pytest.mark.gpu
-
-PATHS = [0]
 
 
 def problems():
@@ -34,15 +32,19 @@ def problems():
 
 @pytest.mark.parametrize("name,make", list(problems()), ids=[n for n, _ in problems()])
 def test_apply_matches_oracle(name, make):
+    """Every path (auto, CUDA-core forced, tensor-core forced) against the oracle, full output and delta only."""
     for base in (True, False):
         p = make(base)
-        y, table, ws = run_dense(p)
-        assert lora.lora_get_status(ws) == lora.LORA_OK
-        got = host_f64(y)
         ref = oracle_dense(p)
-        check_close(got, ref, "%s base=%s" % (name, base))
-        none = p.ids < 0
-        assert np.array_equal(host_bits(y)[none], p.y_base[none])
+        table = pack_dense(p)
+        ws = lora.Workspace(max(p.M, 1), p.L)
+        for path in PATHS:
+            with forced_path(path):
+                y, _, _ = run_dense(p, table=table, ws=ws)
+            assert lora.lora_get_status(ws) == lora.LORA_OK
+            check_close(host_f64(y), ref, "%s base=%s path=%d" % (name, base, path))
+            none = p.ids < 0
+            assert np.array_equal(host_bits(y)[none], p.y_base[none])
         table.destroy()
 
 
@@ -61,23 +63,41 @@ def test_integer_inputs_are_bit_exact(slices, n_a):
     p = synth.make_dense_int(12, ids, 384, slices, [8, 16, 32, 64, 40], n_a=n_a)
     ref = oracle_dense(p)
     assert np.abs(ref).max() <= 256 and np.array_equal(ref, np.round(ref))
-    y, _, ws = run_dense(p)
-    assert lora.lora_get_status(ws) == lora.LORA_OK
-    assert np.array_equal(host_f64(y), ref)
+    for path in PATHS:
+        with forced_path(path):
+            y, _, ws = run_dense(p)
+        assert lora.lora_get_status(ws) == lora.LORA_OK
+        assert np.array_equal(host_f64(y), ref), "path %d" % path
 
 
-def test_token_order_invariance_is_bitwise():
+def test_integer_inputs_bit_exact_with_ragged_k_on_tensor_cores():
+    # K = 200 ends on an odd 8-wide K-group: the zero-filled half step must add nothing
+    ids = np.repeat(np.arange(3, dtype=np.int32), [70, 130, 5])
+    p = synth.make_dense_int(13, ids, 200, [136, 72], [16, 48, 8])
+    ref = oracle_dense(p)
+    assert np.abs(ref).max() <= 256
+    for path in (1, 2):
+        with forced_path(path):
+            y, _, ws = run_dense(p)
+        assert lora.lora_get_status(ws) == lora.LORA_OK
+        assert np.array_equal(host_f64(y), ref), "path %d" % path
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_token_order_invariance_is_bitwise(path):
     p = synth.prefill(2, y_base="random")
-    y, table, ws = run_dense(p)
-    perm = np.random.default_rng(1).permutation(p.M)
-    q = synth.DenseProblem(**{**p.__dict__})
-    q.ids, q.x, q.y_base = p.ids[perm], p.x[perm], p.y_base[perm]
-    yq, _, _ = run_dense(q, table=table, ws=ws)
+    with forced_path(path):
+        y, table, ws = run_dense(p)
+        perm = np.random.default_rng(1).permutation(p.M)
+        q = synth.DenseProblem(**{**p.__dict__})
+        q.ids, q.x, q.y_base = p.ids[perm], p.x[perm], p.y_base[perm]
+        yq, _, _ = run_dense(q, table=table, ws=ws)
     assert np.array_equal(host_bits(yq), host_bits(y)[perm])
 
 
-def test_repeatable():
-    p = synth.decode(1, y_base="random")
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_repeatable(name):
+    p = synth.decode(1, y_base="random") if name == "decode" else synth.prefill(2, y_base="random")
     y1, table, ws = run_dense(p)
     y2, _, _ = run_dense(p, table=table, ws=ws)
     y3, _, _ = run_dense(p, table=table, ws=ws, build=False)   # second apply on the same segment table
@@ -132,7 +152,8 @@ def test_stored_ranks_follow_the_padding_rule():
     assert info.num_rank_groups == 4 and info.L == 5 and info.N == 64
 
 
-def test_handoff_wait_times_out_cleanly_and_recovers():
+@pytest.mark.parametrize("path", [1, 2])
+def test_handoff_wait_times_out_cleanly_and_recovers(path):
     p = synth.decode(1, y_base="random")
     table = pack_dense(p)
     ws = lora.Workspace(p.M, p.L)
@@ -140,13 +161,15 @@ def test_handoff_wait_times_out_cleanly_and_recovers():
     try:
         lora.lora_set_option(lora.LORA_OPT_WAIT_TIMEOUT_NS, 2_000_000)
         lora.lora_set_option(lora.LORA_OPT_TEST_WITHHOLD_HANDOFF, 1)
-        y, _, _ = run_dense(p, table=table, ws=ws)
+        with forced_path(path):
+            y, _, _ = run_dense(p, table=table, ws=ws)
         assert lora.lora_get_status(ws) == lora.LORA_ERR_TIMEOUT
         assert np.array_equal(host_bits(y), p.y_base)      # nothing was added
     finally:
         lora.lora_set_option(lora.LORA_OPT_TEST_WITHHOLD_HANDOFF, 0)
         lora.lora_set_option(lora.LORA_OPT_WAIT_TIMEOUT_NS, old)
-    y, _, _ = run_dense(p, table=table, ws=ws)                   # rebuild resets the scratch
+    with forced_path(path):
+        y, _, _ = run_dense(p, table=table, ws=ws)               # rebuild resets the scratch
     assert lora.lora_get_status(ws) == lora.LORA_OK
     check_close(host_f64(y), oracle_dense(p))
 

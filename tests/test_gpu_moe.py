@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from segmented_rank_gemm_lora_gb300 import lora, synth
-from gpu_util import check_close, dev_bf16, host_bits, host_f64
+from gpu_util import PATHS, check_close, dev_bf16, forced_path, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -44,10 +44,12 @@ def refs(p, weights=False):
 @pytest.mark.parametrize("zero_base", [False, True])
 def test_moe_workload_matches_oracle(zero_base):
     p = synth.moe(zero_base=zero_base)
-    c1, c3 = run_moe(p)
     r1, r3 = refs(p)
-    check_close(host_f64(c1), r1, "gate_up")
-    check_close(host_f64(c3), r3, "down")
+    for path in PATHS:
+        with forced_path(path):
+            c1, c3 = run_moe(p)
+        check_close(host_f64(c1), r1, "gate_up path %d" % path)
+        check_close(host_f64(c3), r3, "down path %d" % path)
 
 
 @pytest.mark.parametrize("shared", [True, False])
@@ -56,10 +58,12 @@ def test_moe_small_shapes(shared, weights):
     ids = np.random.default_rng(2).integers(-1, 3, 45).astype(np.int32)
     p = synth.make_moe(5, 45, 264, 200, 6, 3, [8, 24, 64], block_m=16, ids=ids, shared_outer=shared,
                        zero_base=True)
-    c1, c3 = run_moe(p, weights)
     r1, r3 = refs(p, weights)
-    check_close(host_f64(c1), r1, "gate_up")
-    check_close(host_f64(c3), r3, "down")
-    none = np.repeat(ids < 0, p.topk)
-    assert np.array_equal(host_bits(c1)[none], p.cache1[none])
-    assert np.array_equal(host_bits(c3)[none], p.cache3[none])
+    for path in PATHS:
+        with forced_path(path):
+            c1, c3 = run_moe(p, weights)
+        check_close(host_f64(c1), r1, "gate_up path %d" % path)
+        check_close(host_f64(c3), r3, "down path %d" % path)
+        none = np.repeat(ids < 0, p.topk)
+        assert np.array_equal(host_bits(c1)[none], p.cache1[none])
+        assert np.array_equal(host_bits(c3)[none], p.cache3[none])
