@@ -264,10 +264,12 @@ int64_t lora_get_option(int32_t option);
 
 /*
  * Phase tracing (off by default).  With a non-NULL device buffer, every later
- * lora_apply / lora_moe_delta launch writes, per thread block, 8 uint64
- * %globaltimer stamps (ns): entry, work list ready, first shrink operands
- * landed, last shrink result published, first hand-off observed, partials
- * reduced, first expand operands landed, exit.  Blocks past bytes/64 are not
+ * lora_apply / lora_moe_delta launch writes, per thread block, 32 uint64
+ * %globaltimer stamps (ns, 0 = phase not reached): 0 entry, 1 work list
+ * ready, 2 first shrink item started, 3..10 its pipeline stages issued,
+ * 11 its MMAs done, 12 its partial stored, 13 it was published, 14 first
+ * expand item's tile ready, 15 its S in place, 16..23 its first four units
+ * (operands landed, output written), 31 exit.  Blocks past bytes/256 are not
  * traced.  Pass NULL to switch tracing off.  Process-wide.
  */
 lora_status lora_set_trace(void *d_trace, size_t bytes);

@@ -35,6 +35,42 @@ std::map<int, DeviceInfo> g_dev;
 
 lora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+typedef CUresult (*encode_tiled_fn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::mutex g_encode_mu;
+encode_tiled_fn g_encode = nullptr;
+
+// 2-D map over a bf16 [rows][K] matrix with row stride ld: box 64 columns x 128 rows, 128-byte swizzle,
+// reads outside the matrix return zero.
+lora_status encode_rows_map(const void *base, int64_t rows, int32_t K, int64_t ld, CUtensorMap *out)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_encode_mu);
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn) {
+                cudaGetLastError();
+                return LORA_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<encode_tiled_fn>(fn);
+        }
+    }
+    // the kernel only issues boxes that lie inside the rows of x, so the row extent may be rounded up to one box
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)std::max<int64_t>(rows, 128)};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LORA_OK : LORA_ERR_UNSUPPORTED;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 lora_status device_info(DeviceInfo *out)
@@ -379,8 +415,8 @@ extern "C" lora_status lora_build_segments(const lora_workspace *ws, const int32
 }
 
 static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLayout &w, bool moe, int32_t src_div,
-                              const void *x, int64_t ldx, void *y, int64_t ldy, const float *row_weight,
-                              lora_stream_t stream)
+                              const void *x, int64_t ldx, int64_t x_rows, void *y, int64_t ldy,
+                              const float *row_weight, lora_stream_t stream)
 {
     // scratch needed per row of work at this table's largest A block
     {
@@ -393,6 +429,13 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
     EngineParams p{};
+    if (t->K >= 64) {   // narrower inputs always take the cp.async gather
+        st = encode_rows_map(x, x_rows, t->K, ldx, &p.x_map);
+        if (st != LORA_OK) return st;
+        p.x_rows = (int32_t)x_rows;
+    }
+    p.m_ptr = at<int32_t>(ws, w.header) + H_M;
+    p.m_mult = (moe && src_div == 1) ? ws->topk : 1;
     p.a_ptr = t->d_a_ptr;
     p.b_ptr = t->d_b_ptr;
     p.rpad = t->d_rpad;
@@ -440,7 +483,7 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
     p.path = (int32_t)g_opt_path.load();
     p.tc_min_rows = (int32_t)g_opt_tc_min_rows.load();
     p.trace = static_cast<uint64_t *>(g_trace.load());
-    p.trace_ctas = p.trace ? (int32_t)(g_trace_bytes.load() / 64) : 0;
+    p.trace_ctas = p.trace ? (int32_t)(g_trace_bytes.load() / (8 * kTraceSlots)) : 0;
     int grid = di.sms * di.engine_blocks_per_sm;
     const int64_t want = g_opt_grid.load();
     if (want > 0 && want < grid) grid = (int)want;
@@ -459,7 +502,7 @@ extern "C" lora_status lora_apply(lora_table t, const lora_workspace *ws, const 
     if (ws->L != t->L) return LORA_ERR_INVALID_ARG;
     if (t->E_A != 1 || t->E_B != 1) return LORA_ERR_INVALID_ARG;
     if (ldx < t->K || ldy < t->N || ldx % 8 || ldy % 8 || !aligned16(d_x) || !aligned16(d_y)) return LORA_ERR_INVALID_ARG;
-    return run_engine(t, ws, w, false, 1, d_x, ldx, d_y, ldy, nullptr, stream);
+    return run_engine(t, ws, w, false, 1, d_x, ldx, ws->max_M, d_y, ldy, nullptr, stream);
 }
 
 extern "C" lora_status lora_moe_delta(lora_table t, int32_t stage, const lora_workspace *ws, const void *d_in,
@@ -477,7 +520,8 @@ extern "C" lora_status lora_moe_delta(lora_table t, int32_t stage, const lora_wo
     if (ld_in < t->K || ld_cache < t->N || ld_in % 8 || ld_cache % 8 || !aligned16(d_in) || !aligned16(d_cache))
         return LORA_ERR_INVALID_ARG;
     const int32_t src_div = stage == LORA_MOE_GATE_UP ? ws->topk : 1;
-    return run_engine(t, ws, w, true, src_div, d_in, ld_in, d_cache, ld_cache, d_topk_weights, stream);
+    const int64_t in_rows = stage == LORA_MOE_GATE_UP ? (int64_t)ws->max_M : (int64_t)ws->max_M * ws->topk;
+    return run_engine(t, ws, w, true, src_div, d_in, ld_in, in_rows, d_cache, ld_cache, d_topk_weights, stream);
 }
 
 extern "C" lora_status lora_get_status(const lora_workspace *ws, lora_stream_t stream)
@@ -542,7 +586,7 @@ extern "C" lora_status lora_set_option(int32_t option, int64_t value)
 
 extern "C" lora_status lora_set_trace(void *d_trace, size_t bytes)
 {
-    if (d_trace && (bytes < 64 || (reinterpret_cast<uintptr_t>(d_trace) & 7u))) return LORA_ERR_INVALID_ARG;
+    if (d_trace && (bytes < 8 * kTraceSlots || (reinterpret_cast<uintptr_t>(d_trace) & 7u))) return LORA_ERR_INVALID_ARG;
     g_trace_bytes = d_trace ? (int64_t)bytes : 0;
     g_trace = d_trace;
     return LORA_OK;
@@ -643,6 +687,13 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
     if (launch_build(b, s) != cudaSuccess) return LORA_ERR_CUDA;
 
     EngineParams p{};
+    if (M > 0 && t->K >= 64) {
+        st = encode_rows_map(d_x, M, t->K, ldx, &p.x_map);
+        if (st != LORA_OK) return st;
+        p.x_rows = M;
+    }
+    p.m_ptr = header + H_M;
+    p.m_mult = 1;
     p.a_ptr = t->d_a_ptr;
     p.b_ptr = t->d_b_ptr;
     p.rpad = t->d_rpad;

@@ -2,6 +2,7 @@
 // layout, kernel parameter blocks and small sm_103a PTX wrappers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -19,6 +20,7 @@ constexpr int kNTile = 256;            // B is stored in tiles of 256 output row
 constexpr int kBgmvRows = 16;          // rows of one CUDA-core tile
 constexpr int kEngineThreads = 256;
 constexpr int kHeaderInts = 16;
+constexpr int kTraceSlots = 32;        // uint64 phase stamps per thread block (lora_set_trace)
 
 // device error word bits (sticky, cleared by lora_get_status)
 constexpr uint32_t kErrBadId = 1u << 0;
@@ -49,6 +51,12 @@ bool ws_layout(int32_t max_M, int32_t L, int32_t topk, int32_t E, int32_t block_
 // engine parameters (one launch of the shrink/expand kernel)
 // ---------------------------------------------------------------------------
 struct EngineParams {
+    // 2-D tensor map over the shrink input (bf16 [x_rows][K], row stride ldx; box 64 columns x
+    // 128 rows, 128-byte swizzle): the tensor-core path loads runs of 128 consecutive rows through it
+    CUtensorMap x_map;
+    int32_t x_rows;          // rows the map spans; 0 = no map (every load takes the cp.async gather)
+    const int32_t *m_ptr;    // token count of the last build (device)
+    int32_t m_mult;          // rows of x per token (topk for the per-pair MoE input, else 1)
     // weight table
     const uint64_t *a_ptr;   // [L * E_A] packed A block addresses
     const uint64_t *b_ptr;   // [L * E_B] packed B block addresses

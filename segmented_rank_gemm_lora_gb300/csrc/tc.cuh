@@ -29,6 +29,31 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     return d;
 }
 
+// Descriptor of a K-major operand written by TMA with 128-byte swizzle: rows
+// of 128 bytes, 8-row atoms 1024 bytes apart (SBO); the base is 1024-byte
+// aligned and a K=16 step advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// 2-D TMA tile load (box from the tensor map) at (col, row) into dst,
+// completing on an mbarrier.  col * 2 bytes must be a multiple of 16.
+__device__ __forceinline__ void tma_tile2d(void *dst_smem, const void *tmap, int col, int row, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst_smem)),
+        "l"(tmap), "r"(col), "r"(row), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Instruction descriptor for kind::f16: D fp32, A and B bf16, both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
