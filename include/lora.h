@@ -242,9 +242,13 @@ const char *lora_status_string(lora_status status);
 
 /*
  * Process-wide tuning knobs (not thread-safe against concurrent calls).
- *   LORA_OPT_PATH            : 0 auto, 1 every segment on the CUDA-core path,
- *                              2 every segment on the tensor-core path.
- *   LORA_OPT_TC_MIN_ROWS     : segments with more rows take the tensor-core path.
+ *   LORA_OPT_PATH            : 0 auto (groups of at most 4 rows on the CUDA-core
+ *                              path, up to LORA_OPT_TC_MIN_ROWS rows on narrow
+ *                              tensor-core tiles, the rest on 128-row tensor-core
+ *                              tiles), 1 every group on the CUDA-core path,
+ *                              2 every group on 128-row tensor-core tiles,
+ *                              3 every group on narrow (16-row) tensor-core tiles.
+ *   LORA_OPT_TC_MIN_ROWS     : groups with more rows take 128-row tensor-core tiles.
  *   LORA_OPT_WAIT_TIMEOUT_NS : limit of every in-kernel wait (default 1 s).
  *   LORA_OPT_GRID_CTAS       : persistent grid size (0 = one wave over all SMs).
  *   LORA_OPT_TEST_WITHHOLD_HANDOFF : test hook; nonzero makes the next launches
@@ -265,10 +269,13 @@ int64_t lora_get_option(int32_t option);
 /*
  * Phase tracing (off by default).  With a non-NULL device buffer, every later
  * lora_apply / lora_moe_delta launch writes, per thread block, 32 uint64
- * %globaltimer stamps (ns, 0 = phase not reached): 0 entry, 1 work list
- * ready, 2 first shrink item started, 3..10 its pipeline stages issued,
- * 11 its MMAs done, 12 its partial stored, 13 it was published, 14 first
- * expand item's tile ready, 15 its S in place, 16..23 its first four units
+ * %globaltimer stamps (ns, 0 = phase not reached): 0 entry, 24 group
+ * records loaded, 25 launch plan made, 1 work list ready, 2 first shrink item
+ * started, 3..10 its pipeline stages issued (CUDA cores: 3 = operands
+ * landed, 30 = partial computed), 11 its MMAs done, 12 its partial stored,
+ * 13 it was published, 29 shrink items done, 26 first finish item started,
+ * 27 its tile's partials all in, 28 its S stored, 14 first expand item's
+ * tile ready, 15 its S in place, 16..23 the first four expand units
  * (operands landed, output written), 31 exit.  Blocks past bytes/256 are not
  * traced.  Pass NULL to switch tracing off.  Process-wide.
  */
@@ -286,9 +293,10 @@ lora_status lora_set_trace(void *d_trace, size_t bytes);
  * Every byte of scratch (segment table, hand-off partials and counters) is a
  * fixed array in this library, about 8.4 MiB, that each GPU which loads the
  * library holds until the process exits.  Limits: M <= 4096 tokens, and
- * M * ceil(K / kc) * R <= 2^21 partial floats, where R is the table's largest
- * A block (n_a * stored rank) and kc = clamp(floor(16384 / R) rounded down to a
- * multiple of 64, 64, 1024); larger calls return LORA_ERR_WORKSPACE before
+ * R * (M * (ceil(K / kc) + 1) + 64 * min(M, L)) <= 2^21 partial floats, where
+ * R is the table's largest A block (n_a * stored rank) and kc = clamp(floor(
+ * 20480 / R) rounded down to a multiple of 64, 64, 512), the smallest K-chunk
+ * the engine falls back to; larger calls return LORA_ERR_WORKSPACE before
  * launching anything.  Same argument rules as lora_apply (dense tables only).
  *
  * The first call on a device looks the array up (cudaGetSymbolAddress) with

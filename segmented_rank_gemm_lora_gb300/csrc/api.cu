@@ -418,12 +418,13 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
                               const void *x, int64_t ldx, int64_t x_rows, void *y, int64_t ldy,
                               const float *row_weight, lora_stream_t stream)
 {
-    // scratch needed per row of work at this table's largest A block
+    // scratch needed per row of work at this table's largest A block, at the largest K-chunk of a
+    // 16-row CUDA-core tile (x rows <= 16 KB, A chunk <= 40 KB), plus the row's finished S
     {
         const int64_t R = t->max_R;
-        int64_t kc = (32 * 1024 / (2 * R)) / 64 * 64;
-        kc = std::max<int64_t>(64, std::min<int64_t>(1024, kc));
-        if (ceil_div(t->K, kc) * R > kPartialFloatsPerRow) return LORA_ERR_UNSUPPORTED;
+        int64_t kc = (20480 / R) / 64 * 64;
+        kc = std::max<int64_t>(64, std::min<int64_t>(512, kc));
+        if ((ceil_div(t->K, kc) + 1) * R > kPartialFloatsPerRow) return LORA_ERR_UNSUPPORTED;
     }
     DeviceInfo di;
     lora_status st = device_info(&di);
@@ -562,7 +563,7 @@ extern "C" lora_status lora_set_option(int32_t option, int64_t value)
 {
     switch (option) {
     case LORA_OPT_PATH:
-        if (value < 0 || value > 2) return LORA_ERR_INVALID_ARG;
+        if (value < 0 || value > 3) return LORA_ERR_INVALID_ARG;
         g_opt_path = value;
         return LORA_OK;
     case LORA_OPT_TC_MIN_ROWS:
@@ -656,12 +657,15 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
     if (M > 0 && (ldx < t->K || ldy < t->N || ldx % 8 || ldy % 8 || !aligned16(d_x) || !aligned16(d_y)))
         return LORA_ERR_INVALID_ARG;
     if (M > kStaticMaxM) return LORA_ERR_WORKSPACE;
-    // the hand-off partials of M rows at this table's largest A block must fit the fixed array
+    // the hand-off scratch of M rows at this table's largest A block must fit the fixed array even at
+    // the largest K-chunks the engine picks when scratch is short (16-row tiles: x rows <= 16 KB,
+    // A chunk <= 40 KB), plus the finished S of every tile
     {
         const int64_t R = t->max_R;
-        int64_t kc = (32 * 1024 / (2 * R)) / 64 * 64;
-        kc = std::max<int64_t>(64, std::min<int64_t>(1024, kc));
-        if ((int64_t)M * ceil_div(t->K, kc) * R > kStaticPartialFloats) return LORA_ERR_WORKSPACE;
+        int64_t kc = (20480 / R) / 64 * 64;
+        kc = std::max<int64_t>(64, std::min<int64_t>(512, kc));
+        const int64_t need = R * ((int64_t)M * (ceil_div(t->K, kc) + 1) + 64 * std::min<int64_t>(M, t->L));
+        if (need > kStaticPartialFloats) return LORA_ERR_WORKSPACE;
     }
     unsigned char *base = nullptr;
     lora_status st = static_scratch_address(&base);

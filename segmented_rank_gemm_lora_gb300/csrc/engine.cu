@@ -12,24 +12,27 @@
 // Each group (an adapter segment, or an (adapter, expert) group of the MoE
 // variant) takes one of two paths:
 //   * CUDA-core path (at most LORA_OPT_TC_MIN_ROWS rows, decode-sized):
-//     tiles of up to 16 rows; shrink item = (tile, K-chunk of about 32 KB of
-//     A), fp32 partial by FMA; the expand item sums the published partials in
-//     K order itself.
-//   * tensor-core path (more rows, prefill-sized): tiles of up to 128 rows;
-//     shrink item = (tile, 512-wide K-chunk) on tcgen05 with the accumulator
-//     in tensor memory; the last shrink item of a tile sums the partials in K
-//     order and writes S in bf16; the expand runs D = S B^T on tcgen05 with a
-//     double-buffered accumulator and adds scale * D in the epilogue.
-// An expand item is a run of output-column units of one slice of one tile;
-// its units stream through a three-stage ring of {B rows, output rows}
-// buffers, and items are sized so each CTA gets about two of them.
-// Shrink items publish their fp32 partials to L2 and bump the tile's counter
-// with release semantics; expand items put their first operands in flight
-// and then wait (bounded) for the tile.  CTA b takes shrink items b, b+grid,
-// ... before any expand item, and the whole grid is co-resident, so every
-// wait ends.  Operand chunks are contiguous runs of the packed table or whole
-// input/output rows and move by bulk async copies on mbarriers; the
-// tensor-core gathers of token rows use 16-byte cp.async.  The summation
+//     tiles of up to 16 rows, fp32 dot products by FMA;
+//   * tensor-core path (more rows, prefill-sized): tiles of up to 128 rows on
+//     tcgen05 with the accumulators in tensor memory.
+// Three kinds of work item, in this order on every CTA:
+//   1. shrink items (tile, K-chunk): fp32 partial X_tile A_chunk^T to L2
+//      scratch, then a release bump of the tile's counter;
+//   2. finish items (16 rows of a tile): once every chunk of the tile is in,
+//      sum the partials in K order into S (bf16 in the MMA operand layout on
+//      the tensor-core path, fp32 otherwise) and bump a second counter;
+//   3. expand items (a run of output-column units of one slice of one tile):
+//      y = y_base + scale * S B^T.  Small CUDA-core tiles skip step 2: their
+//      expand items sum the few partials they need themselves.
+// Shrink items never wait on other CTAs, finish items wait only on shrink
+// items and expand items only on the other two, and the whole grid is
+// co-resident, so every wait ends.  The chunk sizes are picked per launch from
+// the total bytes so that each SM gets about one shrink item and two to three
+// expand units.  Expand units stream through a three-stage ring that runs
+// across item boundaries; the first units are put in flight while the shrink
+// work is still running.  Operands move as bulk async copies (whole rows of
+// x and y, contiguous runs of the packed table) or 2-D TMA tiles on
+// mbarriers; tensor-core results leave as bulk row stores.  The summation
 // order never depends on timing or on which rows share a tile, so the same
 // inputs always give the same bits.
 #include "common.cuh"
@@ -38,86 +41,126 @@
 namespace lora {
 
 constexpr int kT = kEngineThreads;
-constexpr int kGroupCap = 2048;                     // groups per launch held in shared memory
-constexpr int kGroupCache = 512;                    // group records cached in shared memory
-constexpr int kRankCache = 1024;                    // stored ranks cached in shared memory
-// CUDA-core path
-constexpr int kChunkBytes = 32 * 1024;              // target bytes of one A chunk / one B unit
-constexpr int kMaxKc = 1024;                        // K elements of a chunk at the smallest R
-constexpr int kMaxBgUnit = 512;                     // output columns of one CUDA-core expand unit, at most
-// tensor-core path
-constexpr int kTcRows = 128;                        // MMA M: rows of one tile
-constexpr int kTcKc = 512;                          // K elements of one shrink item
-constexpr int kTcStageK = 64;                       // K elements of one shrink pipeline stage
-constexpr int kTcCols = 128;                        // output columns of one expand unit (MMA N)
-constexpr int kTcMaxDepth = 4;                      // shrink pipeline stages
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemExpandCol = 256;            // shrink accumulator: [0, R); expand: [256, 384), [384, 512)
-// shared-memory pool: the shrink work uses [0, 96K); the expand ring grows down from the top
-constexpr int kShrinkBytes = 96 * 1024;
-constexpr int kExpandBytes = 72 * 1024;
-constexpr int kPool = kShrinkBytes + kExpandBytes;
-constexpr int kBgA = 0, kBgX = 32 * 1024, kBgRed = 64 * 1024;   // CUDA-core shrink carve-up
-constexpr int kSOff = 0;                            // an expand item's S: fp32 [16][64] or bf16 [rp/8][128][8]
-constexpr int kEsBytes = 48 * 1024;                 // one expand stage: B rows at 0, output rows after them
+constexpr int kGroupCap = 2048;                 // groups per launch held in shared memory
+constexpr int kGroupCache = 256;                // group records and sizes cached in shared memory
+constexpr int kRankCache = 1024;                // stored ranks cached in shared memory
+// shared-memory pool: S at [0, 16K), three expand stages of 50 KB above it (stage 0 on top)
+constexpr int kStageBytes = 50 * 1024;
 constexpr int kEsDepth = 3;
-constexpr int kEsYbg = 32 * 1024, kEsYtc = 16 * 1024;
-constexpr int kItemsPerCta = 2;                     // expand items per CTA the work list aims for
-// trace slots (lora_set_trace): first shrink item, first expand item, first units
+constexpr int kSBytes = 16 * 1024;
+constexpr int kPool = kSBytes + kEsDepth * kStageBytes;
+constexpr int kBgShrinkBytes = kPool - 2 * kStageBytes;   // narrow shrink leaves stages 0 and 1 alone
+constexpr int kTcShrinkBytes = kPool - kStageBytes;       // tensor-core shrink leaves stage 0 alone
+// narrow tiles (at most 16 rows): the tokens are the MMA N dimension, the weights the M dimension
+constexpr int kNtRows = kBgmvRows;              // MMA N: token rows of a narrow tile
+constexpr int kNtABytes = 40 * 1024;            // A chunk staging at 0: [kc/8][R][8]
+constexpr int kNtXOff = kNtABytes;              // x rows after it: [kc/8][16][8]
+constexpr int kNtXBytes = 24 * 1024;
+constexpr int kNtMaxUnit = 1024;                // output columns of one narrow expand unit, at most
+// vector tiles (at most kFmaMaxRows rows by default): fp32 FMA on the CUDA cores
+constexpr int kFmaMaxRows = 4;
+constexpr int kFmaXBytes = 16 * 1024;           // x rows, row-major [rows][kc], at kNtXOff
+constexpr int kFmaRedOff = kNtXOff + kFmaXBytes; // cross-warp sums of the shrink: [3][4][R] fp32 at most
+constexpr int64_t kDirectLoads = 128 * 1024;    // partial loads of a tile's expand items below which they sum them
+constexpr int kBgUnitsPerItem = 2;              // CUDA-core expand units per item (one S per item)
+// tensor-core path
+constexpr int kTcRows = 128;                    // MMA M: rows of one tile
+constexpr int kTcKc = 512;                      // K elements of one shrink item (at least)
+constexpr int kTcStageK = 64;                   // K elements of one shrink pipeline stage
+constexpr int kTcCols = 128;                    // output columns of one expand unit (MMA N)
+constexpr int kTcMaxDepth = 4;                  // shrink pipeline stages
+constexpr int kFinRows = 16;                    // rows of one finish item
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemExpandCol = 256;        // shrink accumulator: [0, R); expand: [256, 384), [384, 512)
+constexpr int kTcYOff = 16 * 1024;              // tensor-core stage: B [rp/8][128][8] at 0, y rows after
+constexpr int kTcYStride = kTcCols * 2 + 16;    // padded rows: a warp (one row per lane) hits every bank group
+constexpr int kItemsPerCta = 2;                 // tensor-core expand items per CTA the plan aims for
+static_assert(kTcYOff + kTcRows * kTcYStride <= kStageBytes, "tensor-core expand stage");
+static_assert(kNtXOff + kNtXBytes <= kBgShrinkBytes, "narrow shrink staging");
+static_assert(kFmaRedOff + 3 * 4 * 32 * 4 <= kBgShrinkBytes, "vector shrink staging");
+static_assert(kSBytes >= (kMaxRank / 8) * kTcRows * 16, "S area");
+static_assert(sizeof(EngineParams) % 4 == 0, "parameter mirror");
+
+// trace slots (lora_set_trace)
 enum {
-    TS_ENTRY = 0, TS_WORKLIST = 1, TS_SH_START = 2, TS_SH_STAGE = 3 /* 8 slots: stage s MMAs issued */,
-    TS_SH_MMA_DONE = 11, TS_SH_STORED = 12, TS_SH_PUBLISHED = 13, TS_EX_READY = 14, TS_EX_S = 15,
-    TS_EX_UNIT = 16 /* 4 units x (landed, epilogue done) */, TS_EXIT = 31
+    TS_ENTRY = 0, TS_WORKLIST = 1, TS_SH_START = 2, TS_SH_STAGE = 3 /* 8 slots */, TS_SH_MMA_DONE = 11,
+    TS_SH_STORED = 12, TS_SH_PUBLISHED = 13, TS_EX_READY = 14, TS_EX_S = 15,
+    TS_EX_UNIT = 16 /* 4 units x (landed, written) */, TS_PRO_LOADED = 24, TS_PRO_PLANNED = 25,
+    TS_FIN_START = 26, TS_FIN_READY = 27, TS_FIN_DONE = 28, TS_PREFETCHED = 29, TS_SH_COMPUTED = 30,
+    TS_EXIT = 31
 };
 
-__device__ __forceinline__ int kc_for(int R)
-{
-    int kc = (kChunkBytes / (2 * R)) / 64 * 64;
-    return kc < 64 ? 64 : (kc > kMaxKc ? kMaxKc : kc);
-}
-// CUDA-core expand unit: about 32 KB of B, a multiple of the 256-row B tile, at most 512 columns
-__device__ __forceinline__ int bg_unit_for(int rp)
-{
-    int w = (kChunkBytes / (2 * rp)) / kNTile * kNTile;
-    return w < kNTile ? kNTile : (w > kMaxBgUnit ? kMaxBgUnit : w);
-}
-__device__ __forceinline__ int es_off(int st) { return kPool - (st + 1) * kEsBytes; }
+__device__ __forceinline__ int es_off(int st) { return kPool - (st + 1) * kStageBytes; }
+
+// One expand unit sitting in a stage; written by the thread that issued its copies.
+struct UnitRec {
+    int n0, nw, nrows, kgs, tw, yoff, ystride, kind;   // kind: 0 vector, 1 narrow, 2 wide
+    float scale;
+};
+
+struct Plan {
+    int ta;      // target A bytes of one CUDA-core shrink item
+    int tb;      // target B bytes of one CUDA-core expand unit
+    int ue;      // tensor-core expand units per item
+    int kctc;    // K elements of one tensor-core shrink item
+};
+
+struct GroupDims {
+    int a, e, rows_off, count, rp, R;
+    bool tc, fma, fin;   // wide tensor-core tiles; vector (CUDA-core) tiles; otherwise narrow tensor-core tiles
+    int tile_rows, rows1, tiles, kc, n_kc, uw, ue, ipt, fins;
+    int64_t scratch;   // floats of hand-off scratch: partials, then S of each tile when finished
+};
+
+struct ExpandItem {
+    int g, tile, s, u0, nu, r0, nrows, sa, tg;
+    GroupDims d;
+};
+
+// Issue side of the expand ring: the next unit of this CTA's expand items to
+// put in flight (unit k of item `item`).
+struct IssState {
+    int item, k;
+    ExpandItem it;
+};
 
 struct __align__(1024) EngineSmem {
     __align__(1024) unsigned char pool[kPool];
     uint64_t bar_shrink;                 // CUDA-core shrink copies
     uint64_t bar_es[kEsDepth];           // expand stage copies
     uint64_t bar_s;                      // tensor-core expand: S copy
-    uint64_t bar_stage[kTcMaxDepth];     // tensor-core shrink stage: A chunk landed
-    uint64_t bar_mma[kTcMaxDepth];       // tensor-core shrink stage: consumed by the MMAs
+    uint64_t bar_stage[kTcMaxDepth];     // tensor-core shrink stage landed
+    uint64_t bar_mma[kTcMaxDepth];       // tensor-core shrink stage consumed by the MMAs
     uint64_t bar_mmae[2];                // tensor-core expand MMAs done, per accumulator buffer
+    EngineParams pc;                     // the launch parameters, mirrored (helpers read them from here)
     uint32_t tmem_base;
-    int32_t G, flag, fin, ue;
+    int32_t G, flag, x_total;
+    int32_t ta, tb, ue, kctc;            // launch plan (see plan_launch)
+    UnitRec unit[kEsDepth];
+    IssState iss;
+    int32_t row_dst[kEsDepth][kTcRows];
+    float row_w[kEsDepth][kTcRows];
     int32_t row_src[kTcRows];
-    int32_t row_dst[kTcRows];
-    float row_w[kTcRows];
     int32_t sh_pre[kGroupCap + 1];       // shrink items before group g
+    int32_t fin_pre[kGroupCap + 1];      // finish items before group g
     int32_t ex_pre[kGroupCap + 1];       // expand items before group g
     int32_t tile_pre[kGroupCap + 1];     // tiles before group g
     int32_t part_pre[kGroupCap + 1];     // scratch floats before group g
     int4 grp[kGroupCache];               // (adapter, expert, rows_off, count) of the first groups
+    int4 gdim[kGroupCache];              // their packed sizes under the launch plan (pack_dims)
     int32_t rp_cache[kRankCache];        // stored rank of the first adapters
 };
 
+static_assert(sizeof(EngineSmem) <= 227 * 1024, "shared memory per CTA");
 size_t engine_smem_bytes(int) { return sizeof(EngineSmem); }
 
-struct GroupDims {
-    int a, e, rows_off, count;
-    int rp, R;
-    bool tc;
-    int tile_rows, kc, n_kc, tiles;
-    int uw;        // output columns of one expand unit
-    int units;     // expand units of one tile over all slices
-    int ipt;       // expand items of one tile (needs the launch-wide units per item; 0 before it is known)
-    int scratch;   // floats of hand-off scratch: partials (+ bf16 S of each tile on the tensor-core path)
-};
 
-__device__ __forceinline__ GroupDims group_dims(const EngineParams &p, const EngineSmem &sm, int g, int ue)
+
+__device__ __forceinline__ int floor_pow2(int v) { return v <= 0 ? 0 : 1 << (31 - __clz(v)); }
+__device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
+
+// Sizes of group g under plan pl, from scratch.
+__device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, const EngineSmem &sm, int g, const Plan &pl)
 {
     GroupDims d;
     const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
@@ -128,20 +171,84 @@ __device__ __forceinline__ GroupDims group_dims(const EngineParams &p, const Eng
     d.rp = d.a < kRankCache ? sm.rp_cache[d.a] : p.rpad[d.a];
     d.R = p.n_a * d.rp;
     d.tc = p.path == 2 || (p.path == 0 && d.count > p.tc_min_rows);
+    d.fma = !d.tc && (p.path == 1 || (p.path == 0 && d.count <= kFmaMaxRows));
     d.tile_rows = d.tc ? kTcRows : kBgmvRows;
-    d.kc = d.tc ? kTcKc : kc_for(d.R);
-    d.n_kc = (p.K + d.kc - 1) / d.kc;
     d.tiles = (d.count + d.tile_rows - 1) / d.tile_rows;
-    d.uw = d.tc ? kTcCols : bg_unit_for(d.rp);
-    int units = 0, items = 0;
+    d.rows1 = min(d.count, d.tile_rows);
+    const int kmax = (p.K + 63) & ~63;
+    if (d.tc) {
+        d.kc = min(pl.kctc, kmax);
+        d.uw = kTcCols;
+        d.ue = pl.ue;
+    } else {
+        // the x rows ([kc/8][16][8], or [rows][kc] for vector tiles) and the A chunk must fit their staging
+        const int xcap = d.fma ? kFmaXBytes / 2 / d.rows1 : kNtXBytes / (16 * kNtRows / 8);
+        const int cap = max(64, min(xcap, kNtABytes / 2 / d.R) & ~63);
+        const int want = max(64, (pl.ta / (2 * d.R) + 63) & ~63);
+        d.kc = min(min(cap, kmax), want);
+        // one unit's B rows and y rows must fit a stage; widths are powers of two from 128
+        const int ucap = min(kNtMaxUnit, floor_pow2(kStageBytes / 2 / (d.rp + d.rows1)));
+        d.uw = min(max(kTcCols, floor_pow2(pl.tb / (2 * d.rp))), ucap);
+        d.ue = kBgUnitsPerItem;
+    }
+    d.n_kc = (p.K + d.kc - 1) / d.kc;
+    int ipt = 0;
+    #pragma unroll 1
     for (int s = 0; s < p.n_slices; ++s) {
         const int us = (p.slice_n[s] + d.uw - 1) / d.uw;
-        units += us;
-        if (ue > 0) items += (us + ue - 1) / ue;
+        ipt += (us + d.ue - 1) / d.ue;
     }
-    d.units = units;
-    d.ipt = items;
-    d.scratch = d.n_kc * d.count * d.R + (d.tc ? d.tiles * (kTcRows / 2) * d.R : 0);
+    d.ipt = ipt;
+    d.fin = d.tc || (int64_t)d.rows1 * d.rp * d.n_kc * ipt > kDirectLoads;
+    d.fins = !d.fin ? 0 : (d.tc ? (d.count + kFinRows - 1) / kFinRows : d.tiles);
+    d.scratch = (int64_t)d.n_kc * d.count * d.R +
+                (!d.fin ? 0 : d.tc ? (int64_t)d.tiles * (kTcRows / 2) * d.R : (int64_t)d.count * d.R);
+    return d;
+}
+
+// The same for groups past the shared-memory cache (rare: out of line).
+__device__ __noinline__ GroupDims group_dims_full(const EngineParams &p, const EngineSmem &sm, int g, const Plan &pl)
+{
+    return group_dims_calc(p, sm, g, pl);
+}
+
+// Packed sizes of a cached group, written by the plan: (kc, flags, ipt, n_kc), flags = log2(uw) |
+// log2(ue) << 5 | fin << 10 | tc << 11 | fma << 12.
+__device__ __forceinline__ int4 pack_dims(const GroupDims &d)
+{
+    return make_int4(d.kc,
+                     ceil_log2(d.uw) | (ceil_log2(d.ue) << 5) | ((int)d.fin << 10) | ((int)d.tc << 11) |
+                         ((int)d.fma << 12),
+                     d.ipt,
+                     d.n_kc);
+}
+
+// Sizes of group g under the launch plan: unpacked from shared memory for the first groups.
+__device__ __forceinline__ GroupDims group_dims(const EngineParams &p, const EngineSmem &sm, int g, const Plan &pl)
+{
+    if (g >= kGroupCache) return group_dims_full(p, sm, g, pl);
+    GroupDims d;
+    const int4 gr = sm.grp[g];
+    const int4 gd = sm.gdim[g];
+    d.a = gr.x;
+    d.e = gr.y;
+    d.rows_off = gr.z;
+    d.count = gr.w;
+    d.rp = d.a < kRankCache ? sm.rp_cache[d.a] : p.rpad[d.a];
+    d.R = p.n_a * d.rp;
+    d.kc = gd.x;
+    d.uw = 1 << (gd.y & 31);
+    d.ue = 1 << ((gd.y >> 5) & 31);
+    d.fin = (gd.y >> 10) & 1;
+    d.tc = (gd.y >> 11) & 1;
+    d.fma = (gd.y >> 12) & 1;
+    d.ipt = gd.z;
+    d.n_kc = gd.w;
+    d.tile_rows = d.tc ? kTcRows : kBgmvRows;
+    d.tiles = (d.count + d.tile_rows - 1) >> (d.tc ? 7 : 4);
+    d.rows1 = min(d.count, d.tile_rows);
+    d.fins = !d.fin ? 0 : (d.tc ? (d.count + kFinRows - 1) >> 4 : d.tiles);
+    d.scratch = 0;   // only the plan needs it
     return d;
 }
 
@@ -149,7 +256,7 @@ __device__ __forceinline__ int find_group(const int32_t *pre, int G, int item)
 {
     int lo = 0, hi = G;   // pre[lo] <= item < pre[hi]
     while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
+        const int mid = (lo + hi) >> 1;
         if (pre[mid] <= item) lo = mid; else hi = mid;
     }
     return lo;
@@ -171,7 +278,7 @@ __device__ __forceinline__ void release_add(int32_t *ctr, int v)
 }
 
 // Thread 0 waits (bounded) until *ctr >= target (acquire); returns false on timeout.
-__device__ __forceinline__ bool wait_counter(const int32_t *ctr, int target, const EngineParams &p)
+__device__ __noinline__ bool wait_counter(const int32_t *ctr, int target, const EngineParams &p)
 {
     if (ld_acquire_gpu(ctr) >= target) return true;
     const uint64_t t0 = globaltimer();
@@ -185,7 +292,7 @@ __device__ __forceinline__ bool wait_counter(const int32_t *ctr, int target, con
     return true;
 }
 
-// Phase stamps for lora_set_trace (slot k of this block, kTraceSlots per block).
+// Phase stamps for lora_set_trace (slot k of this block).
 __device__ __forceinline__ void stamp(const EngineParams &p, int k)
 {
     if (p.trace != nullptr && threadIdx.x == 0 && (int)blockIdx.x < p.trace_ctas)
@@ -202,64 +309,222 @@ enum { PH_SHRINK = 0, PH_ES = 1 /* 3 bits */, PH_S = 4, PH_STAGE = 5 /* 4 bits *
        PH_MMAE = 13 /* 2 bits */ };
 
 // ===========================================================================
-// CUDA-core path
+// shrink items, narrow tiles
 // ===========================================================================
-// Shrink partial for up to ROWS rows: thread (ks, j) accumulates row j of the
-// A chunk against every row over K-groups ks, ks + nks, ... and leaves its
-// sums in red[ks][i][j].
-template <int ROWS>
-__device__ __forceinline__ void bg_shrink_rows(EngineSmem &sm, int R, int kw, int xstride, int nrows)
+struct BgShrink {
+    int r0, nrows, k0, kw;
+};
+
+// Put the item's A chunk ([kw/8][R][8], one run of the packed table) in
+// flight on bar_shrink and gather its x rows with 16-byte cp.async into the
+// K-major MMA layout [kc/8][16][8].  An odd K-group count leaves one K-group
+// of both operands zero so the MMAs can run whole K=16 steps.
+__device__ __forceinline__ BgShrink nt_shrink_issue(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+                                                    int tile, int chunk)
 {
+    BgShrink b;
     const int tid = threadIdx.x;
-    const int nks = kT / R;
-    const int j = tid % R, ks = tid / R;
-    if (ks >= nks) return;
-    const uint4 *A = reinterpret_cast<const uint4 *>(sm.pool + kBgA);
-    const uint4 *X = reinterpret_cast<const uint4 *>(sm.pool + kBgX);
-    float *red = reinterpret_cast<float *>(sm.pool + kBgRed);
-    float acc[ROWS];
+    b.r0 = tile * kNtRows;
+    b.nrows = min(kNtRows, d.count - b.r0);
+    b.k0 = chunk * d.kc;
+    b.kw = min(d.kc, p.K - b.k0);
+    const int kgs = b.kw / 8, kgp = (kgs + 1) & ~1;
+    if (tid == 0) {
+        const __nv_bfloat16 *ablk =
+            reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)]);
+        const uint32_t a_bytes = (uint32_t)kgs * d.R * 16;
+        mbar_arrive_expect_tx(&sm.bar_shrink, a_bytes);
+        bulk_g2s(sm.pool, ablk + (int64_t)(b.k0 / 8) * d.R * 8, a_bytes, &sm.bar_shrink);
+    }
+    if (kgs < kgp) {
+        uint4 *z = reinterpret_cast<uint4 *>(sm.pool + kgs * d.R * 16);
+        for (int i = tid; i < d.R; i += kT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+        tc::fence_proxy_async_smem();
+    }
+    unsigned char *X = sm.pool + kNtXOff;
+    for (int idx = tid; idx < b.nrows * kgp; idx += kT) {
+        const int i = idx / kgp, c = idx - i * kgp;
+        const int src = p.rows[d.rows_off + b.r0 + i] / p.src_div;
+        const bool valid = c < kgs;
+        tc::cp_async16(X + (c * kNtRows + i) * 16, valid ? (const void *)(p.x + (int64_t)src * p.ldx + b.k0 + c * 8)
+                                                         : (const void *)p.x, valid);
+    }
+    tc::cp_async_commit();
+    return b;
+}
+
+// Wait for the operands, run D[R][16] = A_chunk X_rows^T on tcgen05 (tokens
+// as N; rows of D past R and columns past the tile's rows are never read) and
+// store the fp32 partial of every row to the tile's scratch slot.
+__device__ __forceinline__ bool nt_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+                                              const BgShrink &b, int g, int chunk, Phases &ph, bool first)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    tc::cp_async_wait<0>();
+    tc::fence_proxy_async_smem();
+    if (!cta_wait(&sm.bar_shrink, ph.get(PH_SHRINK), p)) return false;
+    ph.flip(PH_SHRINK);
+    if (first) stamp(p, TS_SH_STAGE);
+    const int R = d.R;
+    const int steps = ((b.kw / 8) + 1) / 2;
+    if (tid == 0) {
+        tc::fence_after_sync();
+        const uint32_t a0 = smem_u32(sm.pool), x0 = smem_u32(sm.pool + kNtXOff);
+        const uint32_t idesc = tc::idesc_bf16(kTcRows, kNtRows);
+        for (int st = 0; st < steps; ++st) {
+            const uint64_t bd = tc::smem_desc(x0 + st * 2 * kNtRows * 16, kNtRows * 16, 128);
+            tc::mma_bf16(sm.tmem_base, tc::smem_desc(a0 + st * 2 * R * 16, R * 16, 128), bd, idesc, st > 0);
+            if (R > kTcRows)
+                tc::mma_bf16(sm.tmem_base + kNtRows, tc::smem_desc(a0 + st * 2 * R * 16 + kTcRows * 16, R * 16, 128),
+                             bd, idesc, st > 0);
+        }
+        tc::mma_commit(&sm.bar_mma[0]);
+    }
+    if (!cta_wait(&sm.bar_mma[0], ph.get(PH_MMA + 0), p)) return false;
+    ph.flip(PH_MMA + 0);
+    tc::fence_after_sync();
+    if (first) stamp(p, TS_SH_COMPUTED);
+    // tensor memory -> partial: warp w reads A rows 128 (w / 4) + 32 (w % 4) + lane, one column per token
+    const int h = warp >> 2;
+    if (h == 0 || R > kTcRows) {
+        const int j = h * kTcRows + (warp & 3) * 32 + lane;
+        float v[16];
+        tc::tmem_ld16(sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + h * kNtRows, v);
+        float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * b.r0 * R + (int64_t)chunk * b.nrows * R;
+        if (j < R) {
 #pragma unroll
-    for (int i = 0; i < ROWS; ++i) acc[i] = 0.f;
-    const int kgs = kw / 8;
-    for (int kg = ks; kg < kgs; kg += nks) {
-        float af[8];
-        bf16x8_to_f32(A[kg * R + j], af);
-#pragma unroll
-        for (int i = 0; i < ROWS; ++i) {
-            if (i < nrows) {
-                float xf[8];
-                bf16x8_to_f32(X[i * xstride + kg], xf);
-                float s = acc[i];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) s = fmaf(xf[u], af[u], s);
-                acc[i] = s;
-            }
+            for (int t = 0; t < kNtRows; ++t)
+                if (t < b.nrows) dst[t * R + j] = v[t];
         }
     }
-#pragma unroll
-    for (int i = 0; i < ROWS; ++i)
-        if (i < nrows) red[(ks * kBgmvRows + i) * R + j] = acc[i];
+    tc::fence_before_sync();
+    __syncthreads();
+    return true;
 }
 
+// ===========================================================================
+// shrink items, vector tiles (CUDA cores)
+// ===========================================================================
+// Put the item's A chunk and its x rows (one bulk copy per row, row-major
+// [rows][kc] at kNtXOff) in flight on bar_shrink.
+__device__ __forceinline__ BgShrink fma_shrink_issue(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+                                                     int tile, int chunk)
+{
+    BgShrink b;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    b.r0 = tile * kNtRows;
+    b.nrows = min(kNtRows, d.count - b.r0);
+    b.k0 = chunk * d.kc;
+    b.kw = min(d.kc, p.K - b.k0);
+    const uint32_t x_bytes = (uint32_t)b.kw * 2;
+    if (tid == 0) {
+        const __nv_bfloat16 *ablk =
+            reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)]);
+        const uint32_t a_bytes = (uint32_t)(b.kw / 8) * d.R * 16;
+        mbar_arrive_expect_tx(&sm.bar_shrink, a_bytes + b.nrows * x_bytes);
+        bulk_g2s(sm.pool, ablk + (int64_t)(b.k0 / 8) * d.R * 8, a_bytes, &sm.bar_shrink);
+    }
+    if (warp == 1 && lane < b.nrows) {
+        const int src = p.rows[d.rows_off + b.r0 + lane] / p.src_div;
+        bulk_g2s(sm.pool + kNtXOff + (size_t)lane * d.kc * 2, p.x + (int64_t)src * p.ldx + b.k0, x_bytes,
+                 &sm.bar_shrink);
+    }
+    return b;
+}
+
+// Wait for the copies, form the fp32 partial of every row against the A
+// chunk by FMA and store it to the tile's scratch slot.  Thread (j, ks) takes
+// row j of A and K-groups ks, ks + nks, ...; the eight lanes of each
+// quarter-warp read eight consecutive rows of A (no bank conflicts) and the
+// sums of a row meet in a fixed order: a shuffle tree over the ks inside a
+// warp, then, for small R, over warps through shared memory.  Rows go four at
+// a time.
+__device__ __forceinline__ bool fma_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+                                               const BgShrink &b, int g, int chunk, Phases &ph, bool first)
+{
+    if (!cta_wait(&sm.bar_shrink, ph.get(PH_SHRINK), p)) return false;
+    ph.flip(PH_SHRINK);
+    if (first) stamp(p, TS_SH_STAGE);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = d.R;
+    int nks = 1;
+    while (nks * 2 * R <= kT) nks *= 2;
+    const int kq = min(nks, 4), jw = 32 / kq;            // ks values per warp, rows of A per warp
+    const int jblocks = (R + jw - 1) / jw;
+    const int j = (warp % jblocks) * jw + (lane % jw);
+    const int ksb = warp / jblocks;                      // block of kq ks values
+    const int ks = ksb * kq + lane / jw;
+    const bool act = warp < jblocks * (nks / kq) && j < R;
+    const uint4 *A = reinterpret_cast<const uint4 *>(sm.pool);
+    const uint4 *X = reinterpret_cast<const uint4 *>(sm.pool + kNtXOff);
+    float *red = reinterpret_cast<float *>(sm.pool + kFmaRedOff);   // [ksb - 1][4][R]
+    const int xs = d.kc / 8;
+    const int kgs = b.kw / 8;
+    float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * b.r0 * R + (int64_t)chunk * b.nrows * R;
+    for (int i0 = 0; i0 < b.nrows; i0 += 4) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+        if (act) {
+#pragma unroll 2
+            for (int kg = ks; kg < kgs; kg += nks) {
+                float af[8];
+                bf16x8_to_f32(A[kg * R + j], af);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i0 + i < b.nrows) {
+                        float xf[8];
+                        bf16x8_to_f32(X[(i0 + i) * xs + kg], xf);
+                        float s0 = acc[i], s1 = acc2[i];
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            s0 = fmaf(xf[u], af[u], s0);
+                            s1 = fmaf(xf[u + 1], af[u + 1], s1);
+                        }
+                        acc[i] = s0;
+                        acc2[i] = s1;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[i] += acc2[i];
+            for (int o = jw; o < 32; o <<= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+        }
+        const int nksb = nks / kq;
+        if (nksb > 1) {   // warps of ks blocks 1.. hand their sums to block 0
+            if (act && ksb > 0 && lane < jw) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) red[((ksb - 1) * 4 + i) * R + j] = acc[i];
+            }
+            __syncthreads();
+            if (act && ksb == 0 && lane < jw) {
+                for (int q = 0; q < nksb - 1; ++q) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] += red[(q * 4 + i) * R + j];
+                }
+            }
+            __syncthreads();
+        }
+        if (act && ksb == 0 && lane < jw) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i0 + i < b.nrows) dst[(i0 + i) * R + j] = acc[i];
+        }
+    }
+    if (first) stamp(p, TS_SH_COMPUTED);
+    __syncthreads();
+    return true;
+}
 
 // ===========================================================================
-// tensor-core path
+// shrink items, tensor-core path
 // ===========================================================================
 __device__ __forceinline__ int tc_stage_bytes(int R) { return kTcRows * kTcStageK * 2 + R * kTcStageK * 2; }
-__device__ __forceinline__ int tc_depth(int R)
-{
-    const int d = kShrinkBytes / tc_stage_bytes(R);
-    return d > kTcMaxDepth ? kTcMaxDepth : d;
-}
 
-// Scratch layout of a tensor-core tile: [n_kc][nrows][R] fp32 partials for
-// every tile of the group, then one bf16 S [R/8][128][8] per tile.
-__device__ __forceinline__ const __nv_bfloat16 *tc_S(const EngineParams &p, const EngineSmem &sm, const GroupDims &d,
-                                                     int g, int tile)
-{
-    return reinterpret_cast<const __nv_bfloat16 *>(p.partials + sm.part_pre[g] + (int64_t)d.n_kc * d.count * d.R +
-                                                   (int64_t)tile * (kTcRows / 2) * d.R);
-}
+struct TcShrink {
+    int r0, nrows, k0, kw, nst, depth;
+    bool run;
+};
 
 // Put one shrink pipeline stage in flight: 128 token rows x 64 K in the
 // 128-byte swizzled K-major layout, and the matching A chunk (one bulk copy).
@@ -267,19 +532,19 @@ __device__ __forceinline__ const __nv_bfloat16 *tc_S(const EngineParams &p, cons
 // 128-row box inside x, a single TMA tile load brings them; otherwise every
 // thread gathers 16-byte pieces with cp.async into the same swizzled places
 // (zero for rows past the tile or columns past K).
-__device__ __forceinline__ void tc_issue_stage(const EngineParams &p, EngineSmem &sm, const GroupDims &d, int nrows,
-                                               int k0, int kw, int s, int depth, bool run)
+__device__ __noinline__ void tc_issue_stage(const EngineParams &p, const CUtensorMap *xmap, EngineSmem &sm, int a,
+                                            int e, int R, int nrows, int k0, int kw, int depth, int run, int s)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slot = s % depth;
-    unsigned char *Xs = sm.pool + slot * tc_stage_bytes(d.R);
+    unsigned char *Xs = sm.pool + slot * tc_stage_bytes(R);
     unsigned char *As = Xs + kTcRows * kTcStageK * 2;
     const int kb = k0 + s * kTcStageK;
     const int vkg = min(8, (kw - s * kTcStageK) / 8);       // K-groups of 8 present in this stage
     const int need = ((vkg + 1) / 2) * 2;                   // K-groups the MMAs read (whole K=16 steps)
     if (vkg < need) {   // odd K-group count at the end of K: the last A K-group reads as zero
-        uint4 *z = reinterpret_cast<uint4 *>(As + vkg * d.R * 16);
-        for (int i = tid; i < d.R; i += kT) z[i] = make_uint4(0u, 0u, 0u, 0u);
+        uint4 *z = reinterpret_cast<uint4 *>(As + vkg * R * 16);
+        for (int i = tid; i < R; i += kT) z[i] = make_uint4(0u, 0u, 0u, 0u);
         tc::fence_proxy_async_smem();
     }
     if (!run) {
@@ -298,68 +563,73 @@ __device__ __forceinline__ void tc_issue_stage(const EngineParams &p, EngineSmem
         tc::cp_async_commit();
     }
     if (tid == 0) {
-        const __nv_bfloat16 *ablk =
-            reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)]);
-        const uint32_t bytes = (uint32_t)vkg * d.R * 16;
+        const __nv_bfloat16 *ablk = reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[a * p.E_A + (p.E_A == 1 ? 0 : e)]);
+        const uint32_t bytes = (uint32_t)vkg * R * 16;
         mbar_arrive_expect_tx(&sm.bar_stage[slot], bytes + (run ? kTcRows * kTcStageK * 2 : 0));
-        bulk_g2s(As, ablk + (int64_t)(kb / 8) * d.R * 8, bytes, &sm.bar_stage[slot]);
-        if (run) tc::tma_tile2d(Xs, &p.x_map, kb, sm.row_src[0], &sm.bar_stage[slot]);
+        bulk_g2s(As, ablk + (int64_t)(kb / 8) * R * 8, bytes, &sm.bar_stage[slot]);
+        if (run) tc::tma_tile2d(Xs, xmap, kb, sm.row_src[0], &sm.bar_stage[slot]);
     }
 }
 
-template <int N>
-__device__ __forceinline__ void cp_wait_n() { tc::cp_async_wait<N>(); }
 __device__ __forceinline__ void cp_wait_pending(int pending)
 {
-    if (pending <= 0) cp_wait_n<0>();
-    else if (pending == 1) cp_wait_n<1>();
-    else if (pending == 2) cp_wait_n<2>();
-    else cp_wait_n<3>();
+    if (pending <= 0) tc::cp_async_wait<0>();
+    else if (pending == 1) tc::cp_async_wait<1>();
+    else if (pending == 2) tc::cp_async_wait<2>();
+    else tc::cp_async_wait<3>();
 }
 
-
-// Tensor-core shrink item: partial = X_rows[:, K-chunk] A[:, K-chunk]^T into
-// tensor memory, then out to the tile's scratch slot.  A pipeline stage is
-// refilled one iteration after its MMAs were issued, so the refill rarely
-// waits.  Returns false if a wait ran out.
-__device__ bool tc_shrink_item(const EngineParams &p, EngineSmem &sm, const GroupDims &d, int g, int tile, int chunk,
-                               Phases &ph, bool first)
+// Record the tile's source rows, decide between TMA runs and gathers, and put
+// the first pipeline stages in flight.
+__device__ __forceinline__ TcShrink tc_shrink_issue(const EngineParams &p, const CUtensorMap *xmap, EngineSmem &sm,
+                                                    const GroupDims &d, int tile, int chunk)
 {
-    if (first) stamp(p, TS_SH_START);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r0 = tile * kTcRows;
-    const int nrows = min(kTcRows, d.count - r0);
-    const int k0 = chunk * kTcKc;
-    const int kw = min(kTcKc, p.K - k0);
-    const int nst = (kw + kTcStageK - 1) / kTcStageK;
-    const int depth = min(tc_depth(d.R), nst);
+    TcShrink t;
+    const int tid = threadIdx.x;
+    t.r0 = tile * kTcRows;
+    t.nrows = min(kTcRows, d.count - t.r0);
+    t.k0 = chunk * d.kc;
+    t.kw = min(d.kc, p.K - t.k0);
+    t.nst = (t.kw + kTcStageK - 1) / kTcStageK;
+    t.depth = min(min(kTcMaxDepth, kTcShrinkBytes / tc_stage_bytes(d.R)), t.nst);
     int my_row = 0;
     if (tid < kTcRows) {
-        my_row = tid < nrows ? p.rows[d.rows_off + r0 + tid] / p.src_div : 0;
+        my_row = tid < t.nrows ? p.rows[d.rows_off + t.r0 + tid] / p.src_div : 0;
         sm.row_src[tid] = my_row;
     }
     __syncthreads();
     // one TMA tile per stage when the rows are one run of consecutive rows and the 128-row box stays inside x
-    const int x_total = *p.m_ptr * p.m_mult;
-    const bool consecutive = tid >= nrows || my_row == sm.row_src[0] + tid;
-    const bool run = __syncthreads_and(consecutive ? 1 : 0) != 0 && p.x_rows > 0 && sm.row_src[0] + kTcRows <= x_total;
-    for (int s = 0; s < depth; ++s) tc_issue_stage(p, sm, d, nrows, k0, kw, s, depth, run);
+    const int x_total = sm.x_total;
+    const bool consecutive = tid >= t.nrows || my_row == sm.row_src[0] + tid;
+    t.run = __syncthreads_and(consecutive ? 1 : 0) != 0 && p.x_rows > 0 && sm.row_src[0] + kTcRows <= x_total;
+    for (int s = 0; s < t.depth; ++s) tc_issue_stage(p, xmap, sm, d.a, d.e, d.R, t.nrows, t.k0, t.kw, t.depth, t.run, s);
+    return t;
+}
 
+// The MMA loop of a tensor-core shrink item (partial = X_rows[:, K-chunk]
+// A[:, K-chunk]^T into tensor memory), then the partial out to the tile's
+// scratch slot.  A stage is refilled one iteration after its MMAs were
+// issued.  Returns false if a wait ran out.
+__device__ __forceinline__ bool tc_shrink_run(const EngineParams &p, const CUtensorMap *xmap, EngineSmem &sm,
+                                              const GroupDims &d, const TcShrink &t, int g,
+                              int chunk, Phases &ph, bool first)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t idesc = tc::idesc_bf16(kTcRows, d.R);
     uint32_t pending = 0;   // slots whose MMA commit has not been waited for
     bool ok = true;
-    for (int s = 0; s < nst && ok; ++s) {
-        const int slot = s % depth;
-        if (s >= 1 && s - 1 + depth < nst) {   // refill the previous stage's slot
-            const int ps = (s - 1) % depth;
+    for (int s = 0; s < t.nst && ok; ++s) {
+        const int slot = s % t.depth;
+        if (s >= 1 && s - 1 + t.depth < t.nst) {   // refill the previous stage's slot
+            const int ps = (s - 1) % t.depth;
             ok = cta_wait(&sm.bar_mma[ps], ph.get(PH_MMA + ps), p);
             ph.flip(PH_MMA + ps);
             pending &= ~(1u << ps);
             if (!ok) break;
-            tc_issue_stage(p, sm, d, nrows, k0, kw, s - 1 + depth, depth, run);
+            tc_issue_stage(p, xmap, sm, d.a, d.e, d.R, t.nrows, t.k0, t.kw, t.depth, t.run, s - 1 + t.depth);
         }
-        if (!run) {
-            cp_wait_pending(min(nst, s + depth) - (s + 1));
+        if (!t.run) {
+            cp_wait_pending(min(t.nst, s + t.depth) - (s + 1));
             tc::fence_proxy_async_smem();
         }
         __syncthreads();
@@ -370,7 +640,7 @@ __device__ bool tc_shrink_item(const EngineParams &p, EngineSmem &sm, const Grou
                 tc::fence_after_sync();
                 const unsigned char *Xs = sm.pool + slot * tc_stage_bytes(d.R);
                 const unsigned char *As = Xs + kTcRows * kTcStageK * 2;
-                const int vkg = min(8, (kw - s * kTcStageK) / 8);
+                const int vkg = min(8, (t.kw - s * kTcStageK) / 8);
                 const int steps = (vkg + 1) / 2;
                 for (int j = 0; j < steps; ++j) {
                     const uint64_t ad = tc::smem_desc_sw128(smem_u32(Xs) + j * 32);
@@ -394,25 +664,23 @@ __device__ bool tc_shrink_item(const EngineParams &p, EngineSmem &sm, const Grou
             ok = ok && done;
         }
     }
-    cp_wait_n<0>();
+    tc::cp_async_wait<0>();
     if (!ok) return false;
     tc::fence_after_sync();
     if (first) stamp(p, TS_SH_MMA_DONE);
 
-    // tensor memory -> this tile's partial slot: warp w (w < 4) owns rows 32w .. 32w + 31
-    if (warp < 4) {
-        const int row = warp * 32 + lane;
-        float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * r0 * d.R + (int64_t)chunk * nrows * d.R +
-                     (int64_t)row * d.R;
-        for (int c0 = 0; c0 < d.R; c0 += 16) {
-            float v[16];
-            tc::tmem_ld16(sm.tmem_base + ((uint32_t)(warp * 32) << 16) + c0, v);
-            if (row < nrows) {
+    // tensor memory -> the partial slot: warp w reads rows 32 (w % 4) + lane, 16-column blocks w / 4, w / 4 + 2, ...
+    const int row = (warp & 3) * 32 + lane;
+    float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * t.r0 * d.R + (int64_t)chunk * t.nrows * d.R +
+                 (int64_t)row * d.R;
+    for (int c0 = (warp >> 2) * 16; c0 < d.R; c0 += 32) {
+        float v[16];
+        tc::tmem_ld16(sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + c0, v);
+        if (row < t.nrows) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<float4 *>(dst + c0 + 4 * q) =
-                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<float4 *>(dst + c0 + 4 * q) =
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
     }
     tc::fence_before_sync();
@@ -421,77 +689,100 @@ __device__ bool tc_shrink_item(const EngineParams &p, EngineSmem &sm, const Grou
     return true;
 }
 
-// Last shrink item of a tensor-core tile: S = sum over K-chunks (ascending) of
-// the partials, rounded once to bf16, stored [R/8][128][8] (rows past the tile
-// are zero).
-__device__ void tc_finish_tile(const EngineParams &p, const EngineSmem &sm, const GroupDims &d, int g, int tile)
+// ===========================================================================
+// finish items
+// ===========================================================================
+// Scratch of a group: [tiles][n_kc][rows of the tile][R] fp32 partials, then
+// the finished S: per tile bf16 [R/8][128][8] (tensor cores), or fp32
+// [rows][R] of the whole group (CUDA cores).
+__device__ __forceinline__ float *fin_area(const EngineParams &p, const EngineSmem &sm, const GroupDims &d, int g,
+                                           int tile)
 {
-    const int r0 = tile * kTcRows;
-    const int nrows = min(kTcRows, d.count - r0);
-    const float *part = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * r0 * d.R;
-    const int64_t stride = (int64_t)nrows * d.R;
-    uint4 *S = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(tc_S(p, sm, d, g, tile)));
-    const int kgs = d.R / 8;
-    for (int u = threadIdx.x; u < kTcRows * kgs; u += kT) {
-        const int i = u % kTcRows, kg = u / kTcRows;
-        float acc[8];
+    return p.partials + sm.part_pre[g] + (int64_t)d.n_kc * d.count * d.R +
+           (int64_t)tile * (d.tc ? kTcRows / 2 : kBgmvRows) * d.R;
+}
+
+// Rows [16 sl, 16 sl + 16) of a tile: S = sum over K-chunks (ascending) of the
+// partials, rounded once to bf16 on the tensor-core path.
+__device__ __forceinline__ bool finish_item(const EngineParams &p, EngineSmem &sm, const Plan &pl, int G, int f, bool first)
+{
+    if (first) stamp(p, TS_FIN_START);
+    const int tid = threadIdx.x;
+    const int g = find_group(sm.fin_pre, G, f);
+    const GroupDims d = group_dims(p, sm, g, pl);
+    const int local = f - sm.fin_pre[g];
+    const int tile = d.tc ? local / (kTcRows / kFinRows) : local;
+    const int sl = d.tc ? local % (kTcRows / kFinRows) : 0;
+    const int r0 = tile * d.tile_rows;
+    const int nrows = min(d.tile_rows, d.count - r0);
+    const int tg = sm.tile_pre[g] + tile;
+    if (tid == 0) sm.flag = wait_counter(&p.sync[tg * 4 + 0], d.n_kc, p) ? 1 : 0;
+    __syncthreads();
+    if (sm.flag == 0) return false;
+    if (first) stamp(p, TS_FIN_READY);
+    const int R = d.R, c4s = R / 4;
+    const float *part = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * r0 * R;
+    const int64_t stride = (int64_t)nrows * R;
+    float *fa = fin_area(p, sm, d, g, tile);
+    #pragma unroll 1
+    for (int u = tid; u < kFinRows * c4s; u += kT) {
+        const int row = sl * kFinRows + u / c4s, c = (u % c4s) * 4;
+        if (row >= nrows) continue;
+        const float *src = part + (int64_t)row * R + c;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 < d.n_kc; q0 += 8) {
+            float4 v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        if (i < nrows) {
-            const float *src = part + (int64_t)i * d.R + kg * 8;
-            for (int c0 = 0; c0 < d.n_kc; c0 += 4) {
-                float4 v[4][2];
+            for (int q = 0; q < 8; ++q)
+                if (q0 + q < d.n_kc) v[q] = __ldcg(reinterpret_cast<const float4 *>(src + (q0 + q) * stride));
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (c0 + c < d.n_kc) {
-                        v[c][0] = __ldcg(reinterpret_cast<const float4 *>(src + (c0 + c) * stride));
-                        v[c][1] = __ldcg(reinterpret_cast<const float4 *>(src + (c0 + c) * stride + 4));
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (c0 + c < d.n_kc) {
-                        acc[0] += v[c][0].x; acc[1] += v[c][0].y; acc[2] += v[c][0].z; acc[3] += v[c][0].w;
-                        acc[4] += v[c][1].x; acc[5] += v[c][1].y; acc[6] += v[c][1].z; acc[7] += v[c][1].w;
-                    }
+            for (int q = 0; q < 8; ++q) {
+                if (q0 + q < d.n_kc) {
+                    acc.x += v[q].x; acc.y += v[q].y; acc.z += v[q].z; acc.w += v[q].w;
                 }
             }
         }
-        __align__(16) __nv_bfloat16 o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = __float2bfloat16_rn(acc[e]);
-        S[kg * kTcRows + i] = *reinterpret_cast<const uint4 *>(o);
+        if (d.tc) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t *>(&lo);
+            w.y = *reinterpret_cast<uint32_t *>(&hi);
+            __nv_bfloat16 *S = reinterpret_cast<__nv_bfloat16 *>(fa);
+            *reinterpret_cast<uint2 *>(S + ((int64_t)(c / 8) * kTcRows + row) * 8 + (c % 8)) = w;
+        } else {
+            *reinterpret_cast<float4 *>(fa + (int64_t)row * R + c) = acc;
+        }
     }
+    __syncthreads();
+    if (tid == 0) release_add(&p.sync[tg * 4 + 2], 1);
+    if (first) stamp(p, TS_FIN_DONE);
+    return true;
 }
 
-
 // ===========================================================================
-// expand items (both paths)
+// expand items
 // ===========================================================================
-struct ExpandItem {
-    int g, tile, s, u0, nu, r0, nrows, sa, tg;
-    GroupDims d;
-};
 
-__device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const EngineSmem &sm, int G, int item)
+__device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const EngineSmem &sm, const Plan &pl, int G,
+                                                    int item)
 {
     ExpandItem it;
-    const int ue = sm.ue;
     it.g = find_group(sm.ex_pre, G, item);
-    it.d = group_dims(p, sm, it.g, ue);
+    it.d = group_dims(p, sm, it.g, pl);
     const int local = item - sm.ex_pre[it.g];
     it.tile = local / it.d.ipt;
     int q = local % it.d.ipt;
     int s = 0;
+    #pragma unroll 1
     for (; s < p.n_slices; ++s) {
-        const int is = ((p.slice_n[s] + it.d.uw - 1) / it.d.uw + ue - 1) / ue;
+        const int is = ((p.slice_n[s] + it.d.uw - 1) / it.d.uw + it.d.ue - 1) / it.d.ue;
         if (q < is) break;
         q -= is;
     }
     const int us = (p.slice_n[s] + it.d.uw - 1) / it.d.uw;
     it.s = s;
-    it.u0 = q * ue;
-    it.nu = min(ue, us - it.u0);
+    it.u0 = q * it.d.ue;
+    it.nu = min(it.d.ue, us - it.u0);
     it.r0 = it.tile * it.d.tile_rows;
     it.nrows = min(it.d.tile_rows, it.d.count - it.r0);
     it.sa = (p.n_a == 1) ? 0 : s;
@@ -499,129 +790,285 @@ __device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const
     return it;
 }
 
-// Put unit k of an expand item in flight into stage k % 3: its B rows and its
-// output rows.  Unit 0 also records the item's output rows and row weights.
-__device__ __forceinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, const ExpandItem &it, int k)
+// The issue side of the expand ring: the next unit of this CTA's expand
+// items to put in flight.
+// Thread 0 moves the issuer (sm.iss) to the next unit: unit k + 1 of the
+// item, or the first unit of item `item` when start is set or the item is
+// used up (the CTA's items are e0, e0 + grid, ...).
+__device__ __noinline__ void iss_next(const EngineParams &p, EngineSmem &sm, int ta, int tb, int ue, int kctc, int G,
+                                      int n_expand, bool start, int item)
+{
+    if (!start) {
+        if (++sm.iss.k < sm.iss.it.nu) return;
+        item = sm.iss.item + gridDim.x;
+    }
+    sm.iss.item = item;
+    sm.iss.k = 0;
+    if (item < n_expand) {
+        const Plan pl = {ta, tb, ue, kctc};
+        sm.iss.it = decode_expand(p, sm, pl, G, item);
+    }
+}
+
+// Put the issuer's next unit in flight into stage seq % 3: its B rows and its
+// output rows (bulk copies on bar_es), with a record of the unit.  The first
+// unit of an item reads the item's output rows from the row list; later ones
+// take them from the previous unit's stage.
+__device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, int seq)
 {
     const int tid = threadIdx.x;
+    const IssState &is = sm.iss;
+    const ExpandItem &it = is.it;
     const GroupDims &d = it.d;
-    const int st = k % kEsDepth;
+    const int st = seq % kEsDepth;
     unsigned char *base = sm.pool + es_off(st);
-    const int uu = it.u0 + k;
+    const int uu = it.u0 + is.k;
     const int n0 = p.slice_off[it.s] + uu * d.uw;
     const int nw = min(d.uw, p.slice_n[it.s] - uu * d.uw);
-    const int yoff = d.tc ? kEsYtc : kEsYbg;
+    const int ystride = d.tc ? kTcYStride : d.uw * 2;
+    const int yoff = d.tc ? kTcYOff : d.uw * d.rp * 2;
     if (tid < it.nrows) {
         int row;
-        if (k == 0) {
+        float w;
+        if (is.k == 0) {
             row = p.rows[d.rows_off + it.r0 + tid];
-            sm.row_dst[tid] = row;
-            sm.row_w[tid] = p.row_weight ? p.row_weight[row] : 1.0f;
+            w = p.row_weight ? p.row_weight[row] : 1.0f;
         } else {
-            row = sm.row_dst[tid];   // written by this thread when unit 0 was issued
+            const int pst = (seq + kEsDepth - 1) % kEsDepth;   // the previous unit, same item
+            row = sm.row_dst[pst][tid];
+            w = sm.row_w[pst][tid];
         }
-        bulk_g2s(base + yoff + tid * d.uw * 2, p.y + (int64_t)row * p.ldy + n0, (uint32_t)nw * 2, &sm.bar_es[st]);
+        sm.row_dst[st][tid] = row;
+        sm.row_w[st][tid] = w;
+        bulk_g2s(base + yoff + tid * ystride, p.y + (int64_t)row * p.ldy + n0, (uint32_t)nw * 2, &sm.bar_es[st]);
     }
     if (tid == 0) {
         const __nv_bfloat16 *bblk =
             reinterpret_cast<const __nv_bfloat16 *>(p.b_ptr[d.a * p.E_B + (p.E_B == 1 ? 0 : d.e)]);
         const uint32_t y_bytes = (uint32_t)it.nrows * nw * 2;
-        if (d.tc) {
+        const int kgs = d.rp / 8;
+        UnitRec r;
+        r.n0 = n0;
+        r.nw = nw;
+        r.nrows = it.nrows;
+        r.kgs = kgs;
+        r.yoff = yoff;
+        r.ystride = ystride / 2;
+        r.kind = d.tc ? 2 : (d.fma ? 0 : 1);
+        r.scale = p.scale[d.a];
+        if (d.uw == kTcCols) {
             // 128 output columns = one half of a 256-row B tile: rp/8 runs of 128 x 16 bytes
-            const uint32_t kgs = d.rp / 8;
             const int btile = p.slice_tile_off[it.s] + uu / 2, half = uu & 1;
-            mbar_arrive_expect_tx(&sm.bar_es[st], kgs * kTcCols * 16 + y_bytes);
-            for (uint32_t kg = 0; kg < kgs; ++kg)
+            r.tw = kTcCols;
+            mbar_arrive_expect_tx(&sm.bar_es[st], (uint32_t)kgs * kTcCols * 16 + y_bytes);
+            for (int kg = 0; kg < kgs; ++kg)
                 bulk_g2s(base + kg * kTcCols * 16, bblk + ((int64_t)(btile * kgs + kg) * kNTile + half * kTcCols) * 8,
                          kTcCols * 16, &sm.bar_es[st]);
         } else {
+            // whole 256-row B tiles: one contiguous run
             const int tile0 = p.slice_tile_off[it.s] + uu * (d.uw / kNTile);
             const int ntl = (nw + kNTile - 1) / kNTile;
             const uint32_t b_bytes = (uint32_t)ntl * kNTile * d.rp * 2;
+            r.tw = kNTile;
             mbar_arrive_expect_tx(&sm.bar_es[st], b_bytes + y_bytes);
             bulk_g2s(base, bblk + (int64_t)tile0 * kNTile * d.rp, b_bytes, &sm.bar_es[st]);
         }
+        sm.unit[st] = r;
     }
 }
 
-// CUDA-core unit: thread per output column; y = bf16(y_base + scale * w_row * sum_j S[i][j] B[n][j]).
-template <int ROWS>
-__device__ __forceinline__ void bg_unit(const EngineParams &p, const EngineSmem &sm, const ExpandItem &it, int k)
+// Wait until the item's tile has its shrink results, then bring S into
+// shared memory: bf16 [rp/8][128][8] by a bulk copy (tensor cores), fp32
+// [16][64] from the finished S or summed from the partials (CUDA cores).
+// The last consumer of the tile resets its counters for the next launch.
+__device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm, const ExpandItem &it, Phases &ph, bool first)
 {
+    const int tid = threadIdx.x;
     const GroupDims &d = it.d;
-    const int st = k % kEsDepth;
+    if (tid == 0) {
+        const bool ok = d.fin ? wait_counter(&p.sync[it.tg * 4 + 2], d.tc ? (it.nrows + kFinRows - 1) / kFinRows : 1, p)
+                              : wait_counter(&p.sync[it.tg * 4 + 0], d.n_kc, p);
+        if (ok && d.tc) {
+            // S was written by other CTAs through ordinary stores: order them before the async copy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint32_t s_bytes = (uint32_t)(d.rp / 8) * kTcRows * 16;
+            const __nv_bfloat16 *S = reinterpret_cast<const __nv_bfloat16 *>(fin_area(p, sm, d, it.g, it.tile)) +
+                                     (int64_t)it.sa * (d.rp / 8) * kTcRows * 8;
+            mbar_arrive_expect_tx(&sm.bar_s, s_bytes);
+            bulk_g2s(sm.pool, S, s_bytes, &sm.bar_s);
+        }
+        sm.flag = ok ? 1 : 0;
+    }
+    if (first) stamp(p, TS_EX_READY);
+    __syncthreads();
+    bool ready = sm.flag != 0;
+    if (ready && !d.tc) {
+        // vector tile: S fp32 [16][64]; narrow tile: S^T in bf16, K-major for the MMA B operand: [rp/8][16][8]
+        float *Sf = reinterpret_cast<float *>(sm.pool);
+        __nv_bfloat16 *S = reinterpret_cast<__nv_bfloat16 *>(sm.pool);
+        const int rp = d.rp;
+        const int64_t stride = (int64_t)it.nrows * d.R;
+        const float *part = p.partials + sm.part_pre[it.g] + (int64_t)d.n_kc * it.r0 * d.R + it.sa * rp;
+        const float *fin = d.fin ? fin_area(p, sm, d, it.g, it.tile) + it.sa * rp : nullptr;
+        for (int idx = tid; idx < it.nrows * rp; idx += kT) {
+            const int i = idx / rp, jj = idx - i * rp;
+            float acc = 0.f;
+            if (d.fin) {
+                acc = __ldcg(fin + (int64_t)i * d.R + jj);
+            } else {   // sum over K-chunks q (ascending) of the published partials
+                const float *src = part + (int64_t)i * d.R + jj;
+                for (int q0 = 0; q0 < d.n_kc; q0 += 16) {
+                    float v[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) v[u] = (q0 + u < d.n_kc) ? __ldcg(src + (q0 + u) * stride) : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        if (q0 + u < d.n_kc) acc += v[u];
+                }
+            }
+            if (d.fma) Sf[i * kMaxRank + jj] = acc;
+            else S[((jj >> 3) * kNtRows + i) * 8 + (jj & 7)] = __float2bfloat16_rn(acc);
+        }
+        tc::fence_proxy_async_smem();
+    }
+    if (ready && d.tc) {
+        ready = cta_wait(&sm.bar_s, ph.get(PH_S), p);
+        ph.flip(PH_S);
+    }
+    __syncthreads();
+    if (first) stamp(p, TS_EX_S);
+    if (tid == 0 && ready) {
+        const int old = atomicAdd(&p.sync[it.tg * 4 + 1], 1);
+        if (old == d.ipt - 1) {   // last consumer of this tile
+            p.sync[it.tg * 4 + 0] = 0;
+            p.sync[it.tg * 4 + 1] = 0;
+            p.sync[it.tg * 4 + 2] = 0;
+        }
+    }
+    return ready;
+}
+
+// Vector unit in stage st: thread per output column, rows four at a time;
+// y = bf16(y_base + scale * w_row * sum_j S[i][j] B[n][j]) with S fp32 [16][64].
+__device__ __noinline__ void fma_unit(const EngineParams &p, EngineSmem &sm, int st)
+{
+    const UnitRec r = sm.unit[st];
     const unsigned char *base = sm.pool + es_off(st);
     const uint4 *B = reinterpret_cast<const uint4 *>(base);
-    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(base + kEsYbg);
-    const float *S = reinterpret_cast<const float *>(sm.pool + kSOff);
-    const int uu = it.u0 + k;
-    const int n0 = p.slice_off[it.s] + uu * d.uw;
-    const int nw = min(d.uw, p.slice_n[it.s] - uu * d.uw);
-    const float sc = p.scale[d.a];
-    const int kgs = d.rp / 8;
-    const int nrows = it.nrows;
-    for (int nl = threadIdx.x; nl < nw; nl += kT) {
-        float acc[ROWS];
+    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(base + r.yoff);
+    const float *S = reinterpret_cast<const float *>(sm.pool);
+    for (int nl = threadIdx.x; nl < r.nw; nl += kT) {
+        const int tl = nl / r.tw, col = nl % r.tw;
+        for (int i0 = 0; i0 < r.nrows; i0 += 4) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+            for (int kg = 0; kg < r.kgs; ++kg) {
+                float bf[8];
+                bf16x8_to_f32(B[(tl * r.kgs + kg) * r.tw + col], bf);
 #pragma unroll
-        for (int i = 0; i < ROWS; ++i) acc[i] = 0.f;
-        const int tl = nl / kNTile, row = nl % kNTile;
-        for (int kg = 0; kg < kgs; ++kg) {
-            float bfv[8];
-            bf16x8_to_f32(B[(tl * kgs + kg) * kNTile + row], bfv);
-#pragma unroll
-            for (int i = 0; i < ROWS; ++i) {
-                if (i < nrows) {
+                for (int i = 0; i < 4; ++i) {
+                    const float *sr = S + (i0 + i) * kMaxRank + kg * 8;
                     float a = acc[i];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) a = fmaf(S[i * kMaxRank + kg * 8 + u], bfv[u], a);
+                    for (int u = 0; u < 8; ++u) a = fmaf(sr[u], bf[u], a);
                     acc[i] = a;
                 }
             }
-        }
 #pragma unroll
-        for (int i = 0; i < ROWS; ++i) {
-            if (i < nrows) {
-                const float yb = __bfloat162float(ys[i * d.uw + nl]);
-                p.y[(int64_t)sm.row_dst[i] * p.ldy + n0 + nl] = __float2bfloat16_rn(fmaf(sc * sm.row_w[i], acc[i], yb));
+            for (int i = 0; i < 4; ++i) {
+                const int row = i0 + i;
+                if (row < r.nrows) {
+                    const float yb = __bfloat162float(ys[row * r.ystride + nl]);
+                    p.y[(int64_t)sm.row_dst[st][row] * p.ldy + r.n0 + nl] =
+                        __float2bfloat16_rn(fmaf(r.scale * sm.row_w[st][row], acc[i], yb));
+                }
             }
         }
     }
+    __syncthreads();
 }
 
-// Tensor-core unit k: D(k & 1) = S B_k^T (one thread issues, commit on bar_mmae).
-__device__ __forceinline__ void tc_unit_mma(EngineSmem &sm, const ExpandItem &it, int k)
+// Narrow unit in stage st: D^T(buf) = B_unit S^T on tcgen05, the unit's
+// output columns as M (128 per MMA), the tile's tokens as N = 16 (one thread
+// issues, commit on bar_mmae[buf]).
+__device__ __noinline__ void nt_unit_mma(EngineSmem &sm, int st, int buf)
 {
-    const GroupDims &d = it.d;
-    const unsigned char *base = sm.pool + es_off(k % kEsDepth);
-    const uint32_t steps = d.rp / 16;
-    const uint32_t acc = sm.tmem_base + kTmemExpandCol + (k & 1) * kTcCols;
+    const UnitRec r = sm.unit[st];
+    const uint32_t base = smem_u32(sm.pool + es_off(st));
+    const uint32_t s0 = smem_u32(sm.pool);
+    const uint32_t idesc = tc::idesc_bf16(kTcRows, kNtRows);
+    const int nb = (r.nw + kTcCols - 1) / kTcCols;
     tc::fence_after_sync();
-    for (uint32_t j = 0; j < steps; ++j) {
-        const uint64_t ad = tc::smem_desc(smem_u32(sm.pool + kSOff) + j * 2 * kTcRows * 16, kTcRows * 16, 128);
+    for (int bk = 0; bk < nb; ++bk) {
+        // block bk: half (bk & 1) of B tile bk / 2 ([kgs][tw][8] per tile)
+        const uint32_t a0 = base + ((bk >> 1) * r.kgs * r.tw + (bk & 1) * kTcCols) * 16;
+        const uint32_t acc = sm.tmem_base + kTmemExpandCol + buf * kTcCols + bk * kNtRows;
+        for (int j = 0; j < r.kgs / 2; ++j)
+            tc::mma_bf16(acc, tc::smem_desc(a0 + j * 2 * r.tw * 16, r.tw * 16, 128),
+                         tc::smem_desc(s0 + j * 2 * kNtRows * 16, kNtRows * 16, 128), idesc, j > 0 ? 1u : 0u);
+    }
+    tc::mma_commit(&sm.bar_mmae[buf]);
+}
+
+// Narrow epilogue: thread = output column (128-column block (w / 4) + 2i, row
+// 32 (w % 4) + lane of it), one accumulator column per token;
+// y = bf16(y_base + scale * w_row * D), coalesced 2-byte stores per token row.
+__device__ __noinline__ void nt_unit_epilogue(const EngineParams &p, EngineSmem &sm, int st, int buf)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const UnitRec r = sm.unit[st];
+    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(sm.pool + es_off(st) + r.yoff);
+    const int nb = (r.nw + kTcCols - 1) / kTcCols;
+    for (int bk = warp >> 2; bk < nb; bk += 2) {
+        const int n = bk * kTcCols + (warp & 3) * 32 + lane;
+        float v[16];
+        tc::tmem_ld16(sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + kTmemExpandCol + buf * kTcCols +
+                          bk * kNtRows, v);
+        if (n < r.nw) {
+#pragma unroll
+            for (int t = 0; t < kNtRows; ++t) {
+                if (t < r.nrows) {
+                    const float yb = __bfloat162float(ys[t * r.ystride + n]);
+                    p.y[(int64_t)sm.row_dst[st][t] * p.ldy + r.n0 + n] =
+                        __float2bfloat16_rn(fmaf(r.scale * sm.row_w[st][t], v[t], yb));
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+}
+
+// Tensor-core unit in stage st: D(buf) = S B^T (one thread issues, commit on bar_mmae[buf]).
+__device__ __forceinline__ void tc_unit_mma(EngineSmem &sm, int st, int buf)
+{
+    const UnitRec r = sm.unit[st];
+    const unsigned char *base = sm.pool + es_off(st);
+    const uint32_t acc = sm.tmem_base + kTmemExpandCol + buf * kTcCols;
+    tc::fence_after_sync();
+    for (int j = 0; j < r.kgs / 2; ++j) {
+        const uint64_t ad = tc::smem_desc(smem_u32(sm.pool) + j * 2 * kTcRows * 16, kTcRows * 16, 128);
         const uint64_t bd = tc::smem_desc(smem_u32(base) + j * 2 * kTcCols * 16, kTcCols * 16, 128);
         tc::mma_bf16(acc, ad, bd, tc::idesc_bf16(kTcRows, kTcCols), j > 0 ? 1u : 0u);
     }
-    tc::mma_commit(&sm.bar_mmae[k & 1]);
+    tc::mma_commit(&sm.bar_mmae[buf]);
 }
 
-// Tensor-core epilogue of unit k: warp w owns rows 32 (w % 4) + lane and 64
-// columns starting at 64 (w / 4); y = bf16(y_base + scale * w_row * D).
-__device__ __forceinline__ void tc_unit_epilogue(const EngineParams &p, const EngineSmem &sm, const ExpandItem &it,
-                                                 int k)
+// Tensor-core epilogue of the unit in stage st, accumulator buffer buf: warp w
+// owns row 32 (w % 4) + lane and 64 columns from 64 (w / 4); the result
+// bf16(y_base + scale * w_row * D) overwrites the staged y row, which then
+// leaves as one bulk store per row.  On return the stage is free again.
+__device__ __noinline__ void tc_unit_epilogue(const EngineParams &p, EngineSmem &sm, int st, int buf)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const GroupDims &d = it.d;
-    const int uu = it.u0 + k;
-    const int n0 = p.slice_off[it.s] + uu * d.uw;
-    const int nw = min(d.uw, p.slice_n[it.s] - uu * d.uw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const UnitRec r = sm.unit[st];
+    unsigned char *base = sm.pool + es_off(st);
     const int row = (warp & 3) * 32 + lane;
     const int cbase = (warp >> 2) * 64;
-    const bool live = row < it.nrows;
-    const float sc = p.scale[d.a] * (live ? sm.row_w[row] : 0.f);
-    const __nv_bfloat16 *ys =
-        reinterpret_cast<const __nv_bfloat16 *>(sm.pool + es_off(k % kEsDepth) + kEsYtc) + row * kTcCols;
-    __nv_bfloat16 *yg = p.y + (int64_t)(live ? sm.row_dst[row] : 0) * p.ldy + n0;
-    const uint32_t acc = sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + kTmemExpandCol + (k & 1) * kTcCols;
+    const bool live = row < r.nrows;
+    const float sc = r.scale * (live ? sm.row_w[st][row] : 0.f);
+    __nv_bfloat16 *ys = reinterpret_cast<__nv_bfloat16 *>(base + r.yoff + row * kTcYStride);
+    const uint32_t acc = sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + kTmemExpandCol + buf * kTcCols;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int c0 = cbase + h * 32;
@@ -631,147 +1078,172 @@ __device__ __forceinline__ void tc_unit_epilogue(const EngineParams &p, const En
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int c = c0 + 8 * q;
-                if (c < nw) {
+                if (c < r.nw) {
                     float yf[8];
                     bf16x8_to_f32(*reinterpret_cast<const uint4 *>(ys + c), yf);
                     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o[e] = __float2bfloat16_rn(fmaf(sc, v[8 * q + e], yf[e]));
-                    *reinterpret_cast<uint4 *>(yg + c) = *reinterpret_cast<const uint4 *>(o);
+                    *reinterpret_cast<uint4 *>(ys + c) = *reinterpret_cast<const uint4 *>(o);
                 }
             }
         }
     }
-}
-
-// One expand item.  Unit 0 may already be in flight (prefetched during the
-// shrink work).  Returns false if a wait ran out; *inflight tracks the stages
-// whose copies have not been waited for.
-__device__ bool expand_item(const EngineParams &p, EngineSmem &sm, const ExpandItem &it, bool unit0_issued,
-                            Phases &ph, uint32_t &inflight, bool first)
-{
-    const int tid = threadIdx.x;
-    const GroupDims &d = it.d;
-    const int nu = it.nu;
-    for (int k = unit0_issued ? 1 : 0; k < min(nu, kEsDepth); ++k) {
-        issue_unit(p, sm, it, k);
-        inflight |= 1u << (k % kEsDepth);
-    }
-
-    // wait until the tile's shrink results are published
-    if (tid == 0) {
-        const bool ok = d.tc ? wait_counter(&p.sync[it.tg * 4 + 2], 1, p) : wait_counter(&p.sync[it.tg * 4 + 0], d.n_kc, p);
-        if (ok && d.tc) {
-            // S was written by another CTA through ordinary stores: order them before the async copy
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            const uint32_t s_bytes = (uint32_t)(d.rp / 8) * kTcRows * 16;
-            const __nv_bfloat16 *S = tc_S(p, sm, d, it.g, it.tile) + (int64_t)it.sa * (d.rp / 8) * kTcRows * 8;
-            mbar_arrive_expect_tx(&sm.bar_s, s_bytes);
-            bulk_g2s(sm.pool + kSOff, S, s_bytes, &sm.bar_s);
-        }
-        sm.flag = ok ? 1 : 0;
-    }
-    if (first) stamp(p, TS_EX_READY);
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
     __syncthreads();
-    bool ready = sm.flag != 0;
-    if (ready && !d.tc) {
-        // S[i][j] = sum over K-chunks q (ascending) of the published partials; loads first, then the sum
-        float *S = reinterpret_cast<float *>(sm.pool + kSOff);
-        const int64_t stride = (int64_t)it.nrows * d.R;
-        const float *part = p.partials + sm.part_pre[it.g] + (int64_t)d.n_kc * it.r0 * d.R + it.sa * d.rp;
-        for (int idx = tid; idx < it.nrows * d.rp; idx += kT) {
-            const int i = idx / d.rp, jj = idx % d.rp;
-            const float *src = part + (int64_t)i * d.R + jj;
-            float acc = 0.f;
-            for (int q0 = 0; q0 < d.n_kc; q0 += 16) {
-                float v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) v[u] = (q0 + u < d.n_kc) ? __ldcg(src + (q0 + u) * stride) : 0.f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (q0 + u < d.n_kc) acc += v[u];
-            }
-            S[i * kMaxRank + jj] = acc;
-        }
-    }
-    if (ready && d.tc) {
-        ready = cta_wait(&sm.bar_s, ph.get(PH_S), p);
-        ph.flip(PH_S);
+    if (tid < r.nrows) {
+        bulk_s2g(p.y + (int64_t)sm.row_dst[st][tid] * p.ldy + r.n0, base + r.yoff + tid * kTcYStride,
+                 (uint32_t)r.nw * 2);
+        bulk_commit();
+        bulk_wait_read();
     }
     __syncthreads();
-    if (first) stamp(p, TS_EX_S);
-    if (tid == 0 && sm.flag != 0) {
-        const int old = atomicAdd(&p.sync[it.tg * 4 + 1], 1);
-        if (old == d.ipt - 1) {   // last consumer of this tile resets its counters
-            p.sync[it.tg * 4 + 0] = 0;
-            p.sync[it.tg * 4 + 1] = 0;
-            p.sync[it.tg * 4 + 2] = 0;
-        }
-    }
-    if (!ready) return false;
-
-    for (int k = 0; k < nu; ++k) {
-        const int st = k % kEsDepth;
-        if (!cta_wait(&sm.bar_es[st], ph.get(PH_ES + st), p)) return false;
-        ph.flip(PH_ES + st);
-        inflight &= ~(1u << st);
-        if (first && k < 4) stamp(p, TS_EX_UNIT + 2 * k);
-        if (d.tc) {
-            if (tid == 0) tc_unit_mma(sm, it, k);
-            if (k > 0) {   // epilogue of the previous unit overlaps this unit's MMAs
-                const int pb = (k - 1) & 1;
-                if (!cta_wait(&sm.bar_mmae[pb], ph.get(PH_MMAE + pb), p)) return false;
-                ph.flip(PH_MMAE + pb);
-                tc::fence_after_sync();
-                tc_unit_epilogue(p, sm, it, k - 1);
-                tc::fence_before_sync();
-                __syncthreads();   // stage (k - 1) % 3 is free again
-                if (first && k - 1 < 4) stamp(p, TS_EX_UNIT + 2 * (k - 1) + 1);
-                if (k - 1 + kEsDepth < nu) {
-                    issue_unit(p, sm, it, k - 1 + kEsDepth);
-                    inflight |= 1u << ((k - 1) % kEsDepth);
-                }
-            }
-        } else {
-            if (it.nrows <= 2) bg_unit<2>(p, sm, it, k);
-            else if (it.nrows <= 4) bg_unit<4>(p, sm, it, k);
-            else if (it.nrows <= 8) bg_unit<8>(p, sm, it, k);
-            else bg_unit<16>(p, sm, it, k);
-            __syncthreads();       // stage k % 3 is free again
-            if (first && k < 4) stamp(p, TS_EX_UNIT + 2 * k + 1);
-            if (k + kEsDepth < nu) {
-                issue_unit(p, sm, it, k + kEsDepth);
-                inflight |= 1u << st;
-            }
-        }
-    }
-    if (d.tc) {
-        const int pb = (nu - 1) & 1;
-        if (!cta_wait(&sm.bar_mmae[pb], ph.get(PH_MMAE + pb), p)) return false;
-        ph.flip(PH_MMAE + pb);
-        tc::fence_after_sync();
-        tc_unit_epilogue(p, sm, it, nu - 1);
-        tc::fence_before_sync();
-        __syncthreads();
-    }
-    return true;
 }
 
 // ===========================================================================
 // the kernel
 // ===========================================================================
-__global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_constant__ EngineParams p)
+// Warp 0: size the chunks and units for this launch and lay out the work
+// list (per-group prefix counts, packed sizes of the cached groups).
+// Returns false for a workspace that lora_build_segments never filled.
+__device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &sm, int G, bool &any_tc)
+{
+    const int lane = threadIdx.x & 31;
+    const int grid = gridDim.x;
+    int N = 0, tc_units = 0;   // output columns; 128-column units of one tile over all slices
+#pragma unroll 1
+    for (int s = 0; s < p.n_slices; ++s) {
+        N += p.slice_n[s];
+        tc_units += (p.slice_n[s] + kTcCols - 1) >> 7;
+    }
+    // pass 1: validate; CUDA-core A and B bytes (in units of K and N bf16 elements), tensor-core units
+    bool bad = false;
+    long long bga = 0, bgb = 0;
+    int tcu = 0, tci = 0;
+    any_tc = false;
+#pragma unroll 1
+    for (int g = lane; g < G; g += 32) {
+        const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
+        if (gr.x < 0 || gr.x >= p.L || gr.y < 0 || gr.y >= p.num_experts || gr.z < 0 || gr.w < 1 ||
+            (int64_t)gr.z + gr.w > p.rows_capacity) {
+            bad = true;
+            continue;
+        }
+        const int rp = gr.x < kRankCache ? sm.rp_cache[gr.x] : p.rpad[gr.x];
+        const bool tc = p.path == 2 || (p.path == 0 && gr.w > p.tc_min_rows);
+        if (tc) {
+            const int tiles = (gr.w + kTcRows - 1) >> 7;
+            any_tc = true;
+            tcu += tiles * tc_units;
+            tci += tiles * ((p.K + kTcKc - 1) >> 9);
+        } else {
+            const int tiles = (gr.w + kBgmvRows - 1) >> 4;
+            bga += (long long)tiles * p.n_a * rp;
+            bgb += (long long)tiles * rp;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        bga += __shfl_xor_sync(0xffffffffu, bga, o);
+        bgb += __shfl_xor_sync(0xffffffffu, bgb, o);
+        tcu += __shfl_xor_sync(0xffffffffu, tcu, o);
+        tci += __shfl_xor_sync(0xffffffffu, tci, o);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    any_tc = __any_sync(0xffffffffu, any_tc);
+    if (bad) return false;
+    // CUDA-core chunks of about a CTA's share of the A bytes (a quarter more, so that rounding up to
+    // whole chunks rarely needs a second wave); expand units of about 2/5 of a CTA's B share
+    Plan pl;
+    const int spare = max(grid / 4, grid - tci);
+    pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, 1.25f * 2.f * (float)p.K * (float)bga / spare));
+    pl.tb = (int)fminf(268435456.f, fmaxf(4096.f, 2.f * (float)N * (float)bgb / (2.5f * grid)));
+    pl.ue = 1 << ceil_log2(max(1, (tcu + kItemsPerCta * grid - 1) / (kItemsPerCta * grid)));
+    pl.kctc = kTcKc;
+    // pass 2: per-group item counts and their exclusive prefix sums, 32 groups per step; larger chunks
+    // until the hand-off scratch fits the workspace
+#pragma unroll 1
+    for (int iter = 0; iter < 8; ++iter) {
+        int c_sh = 0, c_fin = 0, c_ex = 0, c_tile = 0;
+        long long c_part = 0;
+#pragma unroll 1
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int v_sh = 0, v_fin = 0, v_ex = 0, v_tile = 0;
+            long long v_part = 0;
+            if (g < G) {
+                const GroupDims d = group_dims_calc(p, sm, g, pl);
+                v_sh = d.tiles * d.n_kc;
+                v_fin = d.fins;
+                v_ex = d.tiles * d.ipt;
+                v_tile = d.tiles;
+                v_part = d.scratch;
+                if (g < kGroupCache) sm.gdim[g] = pack_dims(d);
+            }
+            int i_sh = v_sh, i_fin = v_fin, i_ex = v_ex, i_tile = v_tile;
+            long long i_part = v_part;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, i_sh, o), b = __shfl_up_sync(0xffffffffu, i_fin, o);
+                const int c = __shfl_up_sync(0xffffffffu, i_ex, o), e = __shfl_up_sync(0xffffffffu, i_tile, o);
+                const long long f = __shfl_up_sync(0xffffffffu, i_part, o);
+                if (lane >= o) {
+                    i_sh += a; i_fin += b; i_ex += c; i_tile += e; i_part += f;
+                }
+            }
+            if (g < G) {
+                sm.sh_pre[g] = c_sh + i_sh - v_sh;
+                sm.fin_pre[g] = c_fin + i_fin - v_fin;
+                sm.ex_pre[g] = c_ex + i_ex - v_ex;
+                sm.tile_pre[g] = c_tile + i_tile - v_tile;
+                sm.part_pre[g] = (int)min(c_part + i_part - v_part, (long long)INT32_MAX);
+            }
+            c_sh += __shfl_sync(0xffffffffu, i_sh, 31);
+            c_fin += __shfl_sync(0xffffffffu, i_fin, 31);
+            c_ex += __shfl_sync(0xffffffffu, i_ex, 31);
+            c_tile += __shfl_sync(0xffffffffu, i_tile, 31);
+            c_part += __shfl_sync(0xffffffffu, i_part, 31);
+        }
+        if (lane == 0) {
+            sm.sh_pre[G] = c_sh;
+            sm.fin_pre[G] = c_fin;
+            sm.ex_pre[G] = c_ex;
+            sm.tile_pre[G] = c_tile;
+            sm.part_pre[G] = (int)min(c_part, (long long)INT32_MAX);
+            sm.ta = pl.ta;
+            sm.tb = pl.tb;
+            sm.ue = pl.ue;
+            sm.kctc = pl.kctc;
+        }
+        if (c_part <= p.partial_floats || (pl.ta >= (1 << 27) && pl.kctc >= p.K)) break;
+        pl.ta = min(1 << 28, pl.ta * 4);
+        pl.kctc = min(1 << 20, pl.kctc * 4);
+    }
+    __syncwarp();
+    return true;
+}
+
+__global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_constant__ EngineParams pk)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     EngineSmem &sm = *reinterpret_cast<EngineSmem *>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (p.trace != nullptr && tid > 0 && tid < kTraceSlots && (int)blockIdx.x < p.trace_ctas)
-        p.trace[(size_t)blockIdx.x * kTraceSlots + tid] = 0;
-    stamp(p, TS_ENTRY);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int b = blockIdx.x, grid = gridDim.x;
+    if (pk.trace != nullptr && tid > 0 && tid < kTraceSlots && b < pk.trace_ctas)
+        pk.trace[(size_t)b * kTraceSlots + tid] = 0;
+    stamp(pk, TS_ENTRY);
+    {   // mirror the parameters in shared memory: out-of-line helpers read them there
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(&pk);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(&sm.pc);
+        for (int i = tid; i < (int)(sizeof(EngineParams) / 4); i += kT) dst[i] = src[i];
+    }
+    const EngineParams &p = sm.pc;
 
     // ---- prologue: one round trip for the count, the first group records and the stored ranks ----
     if (tid == 0) {
-        sm.G = *p.num_groups;
+        sm.G = *pk.num_groups;
+        sm.x_total = *pk.m_ptr * pk.m_mult;
         sm.flag = 0;
         mbar_init(&sm.bar_shrink, 1);
         for (int i = 0; i < kEsDepth; ++i) mbar_init(&sm.bar_es[i], 1);
@@ -784,218 +1256,176 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         mbar_init(&sm.bar_mmae[1], 1);
         fence_mbar_init();
     }
-    const int gpre = min(p.group_capacity, kGroupCache);
-    for (int g = tid; g < gpre; g += kT) sm.grp[g] = p.groups[g];
-    for (int a = tid; a < min(p.L, kRankCache); a += kT) sm.rp_cache[a] = p.rpad[a];
+    const int gpre = min(pk.group_capacity, kGroupCache);
+    for (int g = tid; g < gpre; g += kT) sm.grp[g] = pk.groups[g];
+    for (int a = tid; a < min(pk.L, kRankCache); a += kT) sm.rp_cache[a] = pk.rpad[a];
     __syncthreads();
+    stamp(p, TS_PRO_LOADED);
     const int G = sm.G;
     if (G <= 0) return;
     if (G > p.group_capacity || G > kGroupCap) {
-        if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
+        if (b == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
         return;
     }
     if (warp == 0) {
-        // pass 1: validate the groups, count expand units -> units per expand item
-        bool bad = false, any_tc = false;
-        int units = 0;
-        for (int g = lane; g < G; g += 32) {
-            const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
-            if (gr.x < 0 || gr.x >= p.L || gr.y < 0 || gr.y >= p.num_experts || gr.z < 0 || gr.w < 1 ||
-                (int64_t)gr.z + gr.w > p.rows_capacity) {
-                bad = true;   // a workspace that lora_build_segments never filled
-            } else {
-                const GroupDims d = group_dims(p, sm, g, 0);
-                units += d.tiles * d.units;
-                any_tc |= d.tc;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
-        bad = __any_sync(0xffffffffu, bad);
-        any_tc = __any_sync(0xffffffffu, any_tc);
-        const int target = kItemsPerCta * (int)gridDim.x;
-        const int ue = max(1, (units + target - 1) / target);
-        // pass 2: per-group item counts and their exclusive prefix sums, 32 groups per step
-        int4 carry = make_int4(0, 0, 0, 0);
-        for (int base = 0; base < G && !bad; base += 32) {
-            const int g = base + lane;
-            int4 v = make_int4(0, 0, 0, 0);
-            if (g < G) {
-                const GroupDims d = group_dims(p, sm, g, ue);
-                v = make_int4(d.tiles * d.n_kc, d.tiles * d.ipt, d.tiles, d.scratch);
-            }
-            int4 incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int4 u = make_int4(__shfl_up_sync(0xffffffffu, incl.x, o), __shfl_up_sync(0xffffffffu, incl.y, o),
-                                         __shfl_up_sync(0xffffffffu, incl.z, o), __shfl_up_sync(0xffffffffu, incl.w, o));
-                if (lane >= o) incl = make_int4(incl.x + u.x, incl.y + u.y, incl.z + u.z, incl.w + u.w);
-            }
-            if (g < G) {
-                sm.sh_pre[g] = carry.x + incl.x - v.x;
-                sm.ex_pre[g] = carry.y + incl.y - v.y;
-                sm.tile_pre[g] = carry.z + incl.z - v.z;
-                sm.part_pre[g] = carry.w + incl.w - v.w;
-            }
-            carry.x += __shfl_sync(0xffffffffu, incl.x, 31);
-            carry.y += __shfl_sync(0xffffffffu, incl.y, 31);
-            carry.z += __shfl_sync(0xffffffffu, incl.z, 31);
-            carry.w += __shfl_sync(0xffffffffu, incl.w, 31);
-        }
-        if (lane == 0) {
-            sm.sh_pre[G] = carry.x;
-            sm.ex_pre[G] = carry.y;
-            sm.tile_pre[G] = carry.z;
-            sm.part_pre[G] = carry.w;
-            sm.ue = ue;
-            sm.flag = bad ? 1 : (any_tc ? 2 : 0);
-        }
+        bool any_tc = false;
+        const bool good = plan_launch(p, sm, G, any_tc);
+        if (tid == 0) sm.flag = good ? (any_tc ? 2 : 0) : 1;
     }
     __syncthreads();
+    stamp(p, TS_PRO_PLANNED);
     if (sm.flag == 1) {
-        if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
+        if (b == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
         return;
     }
     const bool use_tc = sm.flag == 2;
-    const int n_shrink = sm.sh_pre[G], n_expand = sm.ex_pre[G], n_tiles = sm.tile_pre[G], n_part = sm.part_pre[G];
-    if (n_tiles > p.max_tiles || (int64_t)n_part > p.partial_floats) {
-        if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
+    const int n_shrink = sm.sh_pre[G], n_fin = sm.fin_pre[G], n_expand = sm.ex_pre[G];
+    if (sm.tile_pre[G] > p.max_tiles || (int64_t)sm.part_pre[G] > p.partial_floats ||
+        sm.part_pre[G] == INT32_MAX) {
+        if (b == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
         return;
     }
     if (use_tc && (smem_u32(sm.pool) & 1023u) != 0) {   // swizzled TMA tiles need a 1024-byte aligned pool
-        if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
+        if (b == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
         return;
     }
-    if (use_tc) {   // one warp allocates the tensor memory this CTA's MMAs accumulate into
-        if (warp == 0) tc::tmem_alloc(&sm.tmem_base, kTmemCols);
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-    }
-
-    Phases ph = {0u};
-    uint32_t inflight = 0;   // expand stages with copies not yet waited for
-    const int grid = gridDim.x;
-    bool alive = true;
+    // one warp allocates the tensor memory this CTA's MMAs accumulate into
+    if (warp == 0) tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const Plan pl = {sm.ta, sm.tb, sm.ue, sm.kctc};
     stamp(p, TS_WORKLIST);
 
-    // Unit 0 of the first expand item does not depend on any shrink result: it
-    // is put in flight (stage 0 lies in the part of the pool the shrink work
-    // leaves alone) right after the first shrink item's copies.
-    const bool prefetch = (int)blockIdx.x < n_expand;
-    bool unit0_issued = false;
-    if (prefetch && (int)blockIdx.x >= n_shrink) {
-        issue_unit(p, sm, decode_expand(p, sm, G, blockIdx.x), 0);
-        unit0_issued = true;
-        inflight |= 1u;
-    }
+    Phases ph = {0u};
+    uint32_t inflight = 0;   // expand stages whose copies have not been waited for
+    int issued = 0;          // expand units put in flight
+    bool alive = true;
 
-    // ------------------------------------------------------------------
-    // shrink items
-    // ------------------------------------------------------------------
-    for (int item = blockIdx.x; item < n_shrink && alive; item += grid) {
+    // this CTA's items: shrink b, b + grid, ...; then finish and expand items dealt on from where the
+    // previous kind stopped, so CTAs with fewer shrink items take the next kind first
+    const int f0 = ((b - n_shrink) % grid + grid) % grid;
+    const int e0 = ((b - n_shrink - n_fin) % grid + grid) % grid;
+    if (tid == 0) iss_next(p, sm, pl.ta, pl.tb, pl.ue, pl.kctc, G, n_expand, true, e0);
+
+    // expand units that may be in flight while the shrink items run: stage 0 beside a tensor-core
+    // shrink, stages 0 and 1 beside a CUDA-core one
+    int npre = kEsDepth;
+#pragma unroll 1
+    for (int item = b; item < n_shrink; item += grid)
+        npre = min(npre, group_dims(p, sm, find_group(sm.sh_pre, G, item), pl).tc ? 1 : 2);
+    __syncthreads();
+    // put units in flight until `upto` have been issued (units must have left stage (upto - 1) % 3)
+    auto prefetch = [&](int upto) {
+        while (issued < upto && sm.iss.item < n_expand) {
+            inflight |= 1u << (issued % kEsDepth);
+            issue_unit(p, sm, issued++);
+            __syncthreads();
+            if (tid == 0) iss_next(p, sm, pl.ta, pl.tb, pl.ue, pl.kctc, G, n_expand, false, 0);
+            __syncthreads();
+        }
+    };
+
+    // ------------------------------------------------------------------ shrink items
+    for (int item = b; item < n_shrink && alive; item += grid) {
         const int g = find_group(sm.sh_pre, G, item);
-        const GroupDims d = group_dims(p, sm, g, sm.ue);
+        const GroupDims d = group_dims(p, sm, g, pl);
         const int local = item - sm.sh_pre[g];
         const int tile = local / d.n_kc, chunk = local % d.n_kc;
         const int tg = sm.tile_pre[g] + tile;
-        if (d.tc) {
-            if (prefetch && item == (int)blockIdx.x) {
-                issue_unit(p, sm, decode_expand(p, sm, G, blockIdx.x), 0);
-                unit0_issued = true;
-                inflight |= 1u;
-            }
-            if (!tc_shrink_item(p, sm, d, g, tile, chunk, ph, item == (int)blockIdx.x)) {
-                alive = false;
-                break;
-            }
-            // publish; the last K-chunk of the tile turns the partials into S
-            if (tid == 0) {
-                int last = 0;
-                if (!p.withhold) {
-                    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                    last = atom_add_acq_rel_gpu(&p.sync[tg * 4 + 0], 1) == d.n_kc - 1;
-                }
-                sm.fin = last;
-            }
-            __syncthreads();
-            if (sm.fin) {
-                tc_finish_tile(p, sm, d, g, tile);
-                __syncthreads();
-                if (tid == 0) release_add(&p.sync[tg * 4 + 2], 1);
-            }
-            if (item == (int)blockIdx.x) stamp(p, TS_SH_PUBLISHED);
-            continue;
-        }
-        const int r0 = tile * kBgmvRows;
-        const int nrows = min(kBgmvRows, d.count - r0);
-        const int k0 = chunk * d.kc;
-        const int kw = min(d.kc, p.K - k0);
-        const uint32_t a_bytes = (uint32_t)(kw / 8) * d.R * 16;
-        const uint32_t x_bytes = (uint32_t)kw * 2;
-        if (tid == 0) {
-            const __nv_bfloat16 *ablk =
-                reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)]);
-            mbar_arrive_expect_tx(&sm.bar_shrink, a_bytes + nrows * x_bytes);
-            bulk_g2s(sm.pool + kBgA, ablk + (int64_t)(k0 / 8) * d.R * 8, a_bytes, &sm.bar_shrink);
-        }
-        if (warp == 1 && lane < nrows) {
-            const int src = p.rows[d.rows_off + r0 + lane] / p.src_div;
-            bulk_g2s(sm.pool + kBgX + (size_t)lane * d.kc * 2, p.x + (int64_t)src * p.ldx + k0, x_bytes,
-                     &sm.bar_shrink);
-        }
-        if (prefetch && item == (int)blockIdx.x) {
-            issue_unit(p, sm, decode_expand(p, sm, G, blockIdx.x), 0);
-            unit0_issued = true;
-            inflight |= 1u;
-        }
-        const bool ok = cta_wait(&sm.bar_shrink, ph.get(PH_SHRINK), p);
-        ph.flip(PH_SHRINK);
+        const bool first = item == b;
+        if (first) stamp(p, TS_SH_START);
+        TcShrink t;
+        BgShrink bs;
+        if (d.tc) t = tc_shrink_issue(p, &pk.x_map, sm, d, tile, chunk);
+        else if (d.fma) bs = fma_shrink_issue(p, sm, d, tile, chunk);
+        else bs = nt_shrink_issue(p, sm, d, tile, chunk);
+        if (first) prefetch(npre);
+        const bool ok = d.tc ? tc_shrink_run(p, &pk.x_map, sm, d, t, g, chunk, ph, first)
+                             : (d.fma ? fma_shrink_run(p, sm, d, bs, g, chunk, ph, first)
+                                      : nt_shrink_run(p, sm, d, bs, g, chunk, ph, first));
         if (!ok) {
             alive = false;
             break;
         }
-        if (item == (int)blockIdx.x) stamp(p, TS_SH_STAGE);
-
-        // partial dot products: thread (ks, j) covers row j of A, K-groups ks, ks+nks, ...
-        const int R = d.R;
-        const int nks = kT / R;
-        if (nrows <= 2) bg_shrink_rows<2>(sm, R, kw, d.kc / 8, nrows);
-        else if (nrows <= 4) bg_shrink_rows<4>(sm, R, kw, d.kc / 8, nrows);
-        else if (nrows <= 8) bg_shrink_rows<8>(sm, R, kw, d.kc / 8, nrows);
-        else bg_shrink_rows<16>(sm, R, kw, d.kc / 8, nrows);
-        __syncthreads();
-        const float *red = reinterpret_cast<const float *>(sm.pool + kBgRed);
-        float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * r0 * R + (int64_t)chunk * nrows * R;
-        for (int idx = tid; idx < nrows * R; idx += kT) {
-            const int i = idx / R, jj = idx % R;
-            float s = 0.f;
-            for (int q = 0; q < nks; ++q) s += red[(q * kBgmvRows + i) * R + jj];
-            dst[idx] = s;
-        }
-        __syncthreads();
         if (tid == 0 && !p.withhold) release_add(&p.sync[tg * 4 + 0], 1);
-        if (item == (int)blockIdx.x) stamp(p, TS_SH_PUBLISHED);
+        if (first) stamp(p, TS_SH_PUBLISHED);
     }
+    // the shrink staging is free: the rest of the ring may fill while the finish items run
+    if (alive) prefetch(kEsDepth);
+    stamp(p, TS_PREFETCHED);
 
-    // ------------------------------------------------------------------
-    // expand items
-    // ------------------------------------------------------------------
-    for (int item = blockIdx.x; item < n_expand && alive; item += grid) {
-        const ExpandItem it = decode_expand(p, sm, G, item);
-        const bool pre = unit0_issued && item == (int)blockIdx.x;
-        if (!expand_item(p, sm, it, pre, ph, inflight, item == (int)blockIdx.x)) alive = false;
-        __syncthreads();
+    // ------------------------------------------------------------------ finish items
+    for (int f = f0; f < n_fin && alive; f += grid)
+        if (!finish_item(p, sm, pl, G, f, f == f0)) alive = false;
+
+    // ------------------------------------------------------------------ expand items
+    int seq = 0;     // units computed
+    int pend = -1;   // unit whose MMAs are issued and whose epilogue is pending
+    auto drain = [&]() -> bool {   // epilogue of the pending unit, then refill its stage
+        const int q = pend, st = q % kEsDepth, buf = q & 1;
+        if (!cta_wait(&sm.bar_mmae[buf], ph.get(PH_MMAE + buf), p)) return false;
+        ph.flip(PH_MMAE + buf);
+        tc::fence_after_sync();
+        if (sm.unit[st].kind == 2) tc_unit_epilogue(p, sm, st, buf);
+        else nt_unit_epilogue(p, sm, st, buf);
+        if (q < 4) stamp(p, TS_EX_UNIT + 2 * q + 1);
+        pend = -1;
+        prefetch(q + 1 + kEsDepth);
+        return true;
+    };
+    for (int item = e0; item < n_expand && alive; item += grid) {
+        const ExpandItem it = decode_expand(p, sm, pl, G, item);
+        if (pend >= 0 && !drain()) {
+            alive = false;
+            break;
+        }
+        if (!item_ready(p, sm, it, ph, item == e0)) {
+            alive = false;
+            break;
+        }
+        for (int k = 0; k < it.nu; ++k, ++seq) {
+            const int st = seq % kEsDepth;
+            if (!cta_wait(&sm.bar_es[st], ph.get(PH_ES + st), p)) {
+                alive = false;
+                break;
+            }
+            ph.flip(PH_ES + st);
+            inflight &= ~(1u << st);
+            if (seq < 4) stamp(p, TS_EX_UNIT + 2 * seq);
+            if (it.d.fma) {
+                if (pend >= 0 && !drain()) {   // units leave the ring in order
+                    alive = false;
+                    break;
+                }
+                fma_unit(p, sm, st);   // ends with a barrier: stage st is free again
+                if (seq < 4) stamp(p, TS_EX_UNIT + 2 * seq + 1);
+                prefetch(seq + 1 + kEsDepth);
+                continue;
+            }
+            // this unit's MMAs go in while the previous unit's epilogue runs
+            if (tid == 0) {
+                if (it.d.tc) tc_unit_mma(sm, st, seq & 1);
+                else nt_unit_mma(sm, st, seq & 1);
+            }
+            if (pend >= 0 && !drain()) {
+                alive = false;
+                break;
+            }
+            pend = seq;
+        }
     }
-    // a CTA that gave up still lets its own copies land before it leaves
+    if (alive && pend >= 0 && !drain()) alive = false;
+
+    // a CTA that gave up still lets its copies land and its MMAs finish before it leaves
     for (int st = 0; st < kEsDepth; ++st)
         if (inflight & (1u << st)) mbar_wait_bounded(&sm.bar_es[st], ph.get(PH_ES + st), p.timeout_ns, p.err);
+    if (pend >= 0) mbar_wait_bounded(&sm.bar_mmae[pend & 1], ph.get(PH_MMAE + (pend & 1)), p.timeout_ns, p.err);
+    bulk_wait_all();
     stamp(p, TS_EXIT);
-    if (use_tc) {
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 0) tc::tmem_dealloc(sm.tmem_base, kTmemCols);
-    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(sm.tmem_base, kTmemCols);
 }
 
 const void *engine_kernel_ptr() { return reinterpret_cast<const void *>(engine_kernel); }
