@@ -242,13 +242,11 @@ const char *lora_status_string(lora_status status);
 
 /*
  * Process-wide tuning knobs (not thread-safe against concurrent calls).
- *   LORA_OPT_PATH            : 0 auto (groups of at most 4 rows on the CUDA-core
- *                              path, up to LORA_OPT_TC_MIN_ROWS rows on narrow
- *                              tensor-core tiles, the rest on 128-row tensor-core
- *                              tiles), 1 every group on the CUDA-core path,
- *                              2 every group on 128-row tensor-core tiles,
- *                              3 every group on narrow (16-row) tensor-core tiles.
- *   LORA_OPT_TC_MIN_ROWS     : groups with more rows take 128-row tensor-core tiles.
+ *   LORA_OPT_PATH            : 0 auto (groups of at most LORA_OPT_TC_MIN_ROWS
+ *                              rows on small 16-row tiles with warp-level MMAs,
+ *                              the rest on 128-row tcgen05 tiles), 1 every group
+ *                              on small tiles, 2 every group on 128-row tiles.
+ *   LORA_OPT_TC_MIN_ROWS     : groups with more rows take 128-row tcgen05 tiles.
  *   LORA_OPT_WAIT_TIMEOUT_NS : limit of every in-kernel wait (default 1 s).
  *   LORA_OPT_GRID_CTAS       : persistent grid size (0 = one wave over all SMs).
  *   LORA_OPT_TEST_WITHHOLD_HANDOFF : test hook; nonzero makes the next launches
@@ -271,7 +269,7 @@ int64_t lora_get_option(int32_t option);
  * lora_apply / lora_moe_delta launch writes, per thread block, 32 uint64
  * %globaltimer stamps (ns, 0 = phase not reached): 0 entry, 24 group
  * records loaded, 25 launch plan made, 1 work list ready, 2 first shrink item
- * started, 3..10 its pipeline stages issued (CUDA cores: 3 = operands
+ * started, 3..10 its pipeline stages issued (small tiles: 3 = operands
  * landed, 30 = partial computed), 11 its MMAs done, 12 its partial stored,
  * 13 it was published, 29 shrink items done, 26 first finish item started,
  * 27 its tile's partials all in, 28 its S stored, 14 first expand item's

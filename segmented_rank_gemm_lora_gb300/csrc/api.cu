@@ -419,7 +419,7 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
                               const float *row_weight, lora_stream_t stream)
 {
     // scratch needed per row of work at this table's largest A block, at the largest K-chunk of a
-    // 16-row CUDA-core tile (x rows <= 16 KB, A chunk <= 40 KB), plus the row's finished S
+    // 16-row small tile (x rows <= 16 KB, A chunk <= 40 KB), plus the row's finished S
     {
         const int64_t R = t->max_R;
         int64_t kc = (20480 / R) / 64 * 64;
@@ -563,7 +563,7 @@ extern "C" lora_status lora_set_option(int32_t option, int64_t value)
 {
     switch (option) {
     case LORA_OPT_PATH:
-        if (value < 0 || value > 3) return LORA_ERR_INVALID_ARG;
+        if (value < 0 || value > 2) return LORA_ERR_INVALID_ARG;
         g_opt_path = value;
         return LORA_OK;
     case LORA_OPT_TC_MIN_ROWS:

@@ -11,10 +11,12 @@
 // a work list that every CTA derives, identically, from the segment table.
 // Each group (an adapter segment, or an (adapter, expert) group of the MoE
 // variant) takes one of two paths:
-//   * CUDA-core path (at most LORA_OPT_TC_MIN_ROWS rows, decode-sized):
-//     tiles of up to 16 rows, fp32 dot products by FMA;
-//   * tensor-core path (more rows, prefill-sized): tiles of up to 128 rows on
-//     tcgen05 with the accumulators in tensor memory.
+//   * small tiles (at most LORA_OPT_TC_MIN_ROWS rows, decode-sized): up to
+//     16 rows, warp-level m16n8k16 MMAs with the tokens as M.  At these sizes
+//     the per-batch issue-to-commit latency of tcgen05 exceeds the whole
+//     product, while warp-level MMAs finish in registers;
+//   * 128-row tiles (more rows, prefill-sized): tcgen05 with the
+//     accumulators in tensor memory.
 // Three kinds of work item, in this order on every CTA:
 //   1. shrink items (tile, K-chunk): fp32 partial X_tile A_chunk^T to L2
 //      scratch, then a release bump of the tile's counter;
@@ -22,8 +24,8 @@
 //      sum the partials in K order into S (bf16 in the MMA operand layout on
 //      the tensor-core path, fp32 otherwise) and bump a second counter;
 //   3. expand items (a run of output-column units of one slice of one tile):
-//      y = y_base + scale * S B^T.  Small CUDA-core tiles skip step 2: their
-//      expand items sum the few partials they need themselves.
+//      y = y_base + scale * S B^T.  Small tiles with few expand items skip
+//      step 2: their expand items sum the few partials they need themselves.
 // Shrink items never wait on other CTAs, finish items wait only on shrink
 // items and expand items only on the other two, and the whole grid is
 // co-resident, so every wait ends.  The chunk sizes are picked per launch from
@@ -49,20 +51,17 @@ constexpr int kStageBytes = 50 * 1024;
 constexpr int kEsDepth = 3;
 constexpr int kSBytes = 16 * 1024;
 constexpr int kPool = kSBytes + kEsDepth * kStageBytes;
-constexpr int kBgShrinkBytes = kPool - 2 * kStageBytes;   // narrow shrink leaves stages 0 and 1 alone
+constexpr int kBgShrinkBytes = kPool - 2 * kStageBytes;   // small-tile shrink leaves stages 0 and 1 alone
 constexpr int kTcShrinkBytes = kPool - kStageBytes;       // tensor-core shrink leaves stage 0 alone
-// narrow tiles (at most 16 rows): the tokens are the MMA N dimension, the weights the M dimension
-constexpr int kNtRows = kBgmvRows;              // MMA N: token rows of a narrow tile
-constexpr int kNtABytes = 40 * 1024;            // A chunk staging at 0: [kc/8][R][8]
-constexpr int kNtXOff = kNtABytes;              // x rows after it: [kc/8][16][8]
-constexpr int kNtXBytes = 24 * 1024;
-constexpr int kNtMaxUnit = 1024;                // output columns of one narrow expand unit, at most
-// vector tiles (at most kFmaMaxRows rows by default): fp32 FMA on the CUDA cores
-constexpr int kFmaMaxRows = 4;
-constexpr int kFmaXBytes = 16 * 1024;           // x rows, row-major [rows][kc], at kNtXOff
-constexpr int kFmaRedOff = kNtXOff + kFmaXBytes; // cross-warp sums of the shrink: [3][4][R] fp32 at most
+// small tiles (at most 16 rows): warp-level MMAs (m16n8k16), the tile's tokens as M
+constexpr int kSmRows = kBgmvRows;              // token rows of a small tile
+constexpr int kSmABytes = 40 * 1024;            // A chunk staging at 0: [kc/8][R][8]
+constexpr int kSmXOff = kSmABytes;              // x rows after it: [rows][kc + 8] (padded rows)
+constexpr int kSmXBytes = 16 * 1024;
+constexpr int kSmRedOff = kSmXOff + kSmXBytes;  // cross-warp sums of the shrink: [3][16][32] fp32 at most
+constexpr int kSmMaxUnit = 1024;                // output columns of one small expand unit, at most
+constexpr int kSmSStride = kMaxRank + 8;        // bf16 per row of S in shared memory (padded rows)
 constexpr int64_t kDirectLoads = 128 * 1024;    // partial loads of a tile's expand items below which they sum them
-constexpr int kBgUnitsPerItem = 2;              // CUDA-core expand units per item (one S per item)
 // tensor-core path
 constexpr int kTcRows = 128;                    // MMA M: rows of one tile
 constexpr int kTcKc = 512;                      // K elements of one shrink item (at least)
@@ -76,8 +75,7 @@ constexpr int kTcYOff = 16 * 1024;              // tensor-core stage: B [rp/8][1
 constexpr int kTcYStride = kTcCols * 2 + 16;    // padded rows: a warp (one row per lane) hits every bank group
 constexpr int kItemsPerCta = 2;                 // tensor-core expand items per CTA the plan aims for
 static_assert(kTcYOff + kTcRows * kTcYStride <= kStageBytes, "tensor-core expand stage");
-static_assert(kNtXOff + kNtXBytes <= kBgShrinkBytes, "narrow shrink staging");
-static_assert(kFmaRedOff + 3 * 4 * 32 * 4 <= kBgShrinkBytes, "vector shrink staging");
+static_assert(kSmRedOff + 3 * 16 * 32 * 4 <= kBgShrinkBytes, "small-tile shrink staging");
 static_assert(kSBytes >= (kMaxRank / 8) * kTcRows * 16, "S area");
 static_assert(sizeof(EngineParams) % 4 == 0, "parameter mirror");
 
@@ -94,20 +92,21 @@ __device__ __forceinline__ int es_off(int st) { return kPool - (st + 1) * kStage
 
 // One expand unit sitting in a stage; written by the thread that issued its copies.
 struct UnitRec {
-    int n0, nw, nrows, kgs, tw, yoff, ystride, kind;   // kind: 0 vector, 1 narrow, 2 wide
+    int n0, nw, nrows, kgs, tw, yoff, ystride, tc;
     float scale;
 };
 
 struct Plan {
-    int ta;      // target A bytes of one CUDA-core shrink item
-    int tb;      // target B bytes of one CUDA-core expand unit
-    int ue;      // tensor-core expand units per item
+    int ta;      // target A bytes of one small-tile shrink item
+    int tb;      // target B bytes of one small-tile expand unit
+    int ue;      // 128-row tile expand units per item
+    int ues;     // small-tile expand units per item
     int kctc;    // K elements of one tensor-core shrink item
 };
 
 struct GroupDims {
     int a, e, rows_off, count, rp, R;
-    bool tc, fma, fin;   // wide tensor-core tiles; vector (CUDA-core) tiles; otherwise narrow tensor-core tiles
+    bool tc, fin;   // 128-row tensor-core tiles (else small tiles); partials finished by finish items
     int tile_rows, rows1, tiles, kc, n_kc, uw, ue, ipt, fins;
     int64_t scratch;   // floats of hand-off scratch: partials, then S of each tile when finished
 };
@@ -126,7 +125,7 @@ struct IssState {
 
 struct __align__(1024) EngineSmem {
     __align__(1024) unsigned char pool[kPool];
-    uint64_t bar_shrink;                 // CUDA-core shrink copies
+    uint64_t bar_shrink;                 // small-tile shrink copies
     uint64_t bar_es[kEsDepth];           // expand stage copies
     uint64_t bar_s;                      // tensor-core expand: S copy
     uint64_t bar_stage[kTcMaxDepth];     // tensor-core shrink stage landed
@@ -135,7 +134,7 @@ struct __align__(1024) EngineSmem {
     EngineParams pc;                     // the launch parameters, mirrored (helpers read them from here)
     uint32_t tmem_base;
     int32_t G, flag, x_total;
-    int32_t ta, tb, ue, kctc;            // launch plan (see plan_launch)
+    int32_t ta, tb, ue, ues, kctc;       // launch plan (see plan_launch)
     UnitRec unit[kEsDepth];
     IssState iss;
     int32_t row_dst[kEsDepth][kTcRows];
@@ -159,6 +158,14 @@ size_t engine_smem_bytes(int) { return sizeof(EngineSmem); }
 __device__ __forceinline__ int floor_pow2(int v) { return v <= 0 ? 0 : 1 << (31 - __clz(v)); }
 __device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
 
+// Output columns of one small-tile expand unit: about tb bytes of B, a power of two from 128, and the
+// unit's B rows and y rows must fit a stage.
+__device__ __forceinline__ int sm_unit_width(int rp, int rows1, int tb)
+{
+    const int ucap = min(kSmMaxUnit, floor_pow2(kStageBytes / 2 / (rp + rows1)));
+    return min(max(kTcCols, floor_pow2(tb / (2 * rp))), ucap);
+}
+
 // Sizes of group g under plan pl, from scratch.
 __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, const EngineSmem &sm, int g, const Plan &pl)
 {
@@ -171,7 +178,6 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
     d.rp = d.a < kRankCache ? sm.rp_cache[d.a] : p.rpad[d.a];
     d.R = p.n_a * d.rp;
     d.tc = p.path == 2 || (p.path == 0 && d.count > p.tc_min_rows);
-    d.fma = !d.tc && (p.path == 1 || (p.path == 0 && d.count <= kFmaMaxRows));
     d.tile_rows = d.tc ? kTcRows : kBgmvRows;
     d.tiles = (d.count + d.tile_rows - 1) / d.tile_rows;
     d.rows1 = min(d.count, d.tile_rows);
@@ -181,15 +187,12 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
         d.uw = kTcCols;
         d.ue = pl.ue;
     } else {
-        // the x rows ([kc/8][16][8], or [rows][kc] for vector tiles) and the A chunk must fit their staging
-        const int xcap = d.fma ? kFmaXBytes / 2 / d.rows1 : kNtXBytes / (16 * kNtRows / 8);
-        const int cap = max(64, min(xcap, kNtABytes / 2 / d.R) & ~63);
+        // the x rows ([rows][kc + 8]) and the A chunk must fit their staging areas
+        const int cap = max(64, min((kSmXBytes / d.rows1 - 16) / 2, kSmABytes / 2 / d.R) & ~63);
         const int want = max(64, (pl.ta / (2 * d.R) + 63) & ~63);
         d.kc = min(min(cap, kmax), want);
-        // one unit's B rows and y rows must fit a stage; widths are powers of two from 128
-        const int ucap = min(kNtMaxUnit, floor_pow2(kStageBytes / 2 / (d.rp + d.rows1)));
-        d.uw = min(max(kTcCols, floor_pow2(pl.tb / (2 * d.rp))), ucap);
-        d.ue = kBgUnitsPerItem;
+        d.uw = sm_unit_width(d.rp, d.rows1, pl.tb);
+        d.ue = pl.ues;
     }
     d.n_kc = (p.K + d.kc - 1) / d.kc;
     int ipt = 0;
@@ -213,13 +216,10 @@ __device__ __noinline__ GroupDims group_dims_full(const EngineParams &p, const E
 }
 
 // Packed sizes of a cached group, written by the plan: (kc, flags, ipt, n_kc), flags = log2(uw) |
-// log2(ue) << 5 | fin << 10 | tc << 11 | fma << 12.
+// ue << 5 | fin << 13 | tc << 14 (ue < 256).
 __device__ __forceinline__ int4 pack_dims(const GroupDims &d)
 {
-    return make_int4(d.kc,
-                     ceil_log2(d.uw) | (ceil_log2(d.ue) << 5) | ((int)d.fin << 10) | ((int)d.tc << 11) |
-                         ((int)d.fma << 12),
-                     d.ipt,
+    return make_int4(d.kc, ceil_log2(d.uw) | (d.ue << 5) | ((int)d.fin << 13) | ((int)d.tc << 14), d.ipt,
                      d.n_kc);
 }
 
@@ -238,10 +238,9 @@ __device__ __forceinline__ GroupDims group_dims(const EngineParams &p, const Eng
     d.R = p.n_a * d.rp;
     d.kc = gd.x;
     d.uw = 1 << (gd.y & 31);
-    d.ue = 1 << ((gd.y >> 5) & 31);
-    d.fin = (gd.y >> 10) & 1;
-    d.tc = (gd.y >> 11) & 1;
-    d.fma = (gd.y >> 12) & 1;
+    d.ue = (gd.y >> 5) & 255;
+    d.fin = (gd.y >> 13) & 1;
+    d.tc = (gd.y >> 14) & 1;
     d.ipt = gd.z;
     d.n_kc = gd.w;
     d.tile_rows = d.tc ? kTcRows : kBgmvRows;
@@ -309,111 +308,53 @@ enum { PH_SHRINK = 0, PH_ES = 1 /* 3 bits */, PH_S = 4, PH_STAGE = 5 /* 4 bits *
        PH_MMAE = 13 /* 2 bits */ };
 
 // ===========================================================================
-// shrink items, narrow tiles
+// shrink items, small tiles (at most 16 rows)
 // ===========================================================================
 struct BgShrink {
     int r0, nrows, k0, kw;
 };
 
-// Put the item's A chunk ([kw/8][R][8], one run of the packed table) in
-// flight on bar_shrink and gather its x rows with 16-byte cp.async into the
-// K-major MMA layout [kc/8][16][8].  An odd K-group count leaves one K-group
-// of both operands zero so the MMAs can run whole K=16 steps.
-__device__ __forceinline__ BgShrink nt_shrink_issue(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x1(uint32_t addr, uint32_t &r0)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x1.shared.b16 {%0}, [%1];" : "=r"(r0) : "r"(addr));
+}
+// D[16][8] += A[16][16] B[16][8] (bf16 in, fp32 accumulate), warp-wide
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D[16][8] += A[16][8] B[8][8]
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Put the item's A chunk ([kw/8][R][8], one run of the packed table) and its
+// x rows (one bulk copy per row into padded rows of kc + 8 elements) in flight
+// on bar_shrink.
+__device__ __forceinline__ BgShrink sm_shrink_issue(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
                                                     int tile, int chunk)
 {
     BgShrink b;
-    const int tid = threadIdx.x;
-    b.r0 = tile * kNtRows;
-    b.nrows = min(kNtRows, d.count - b.r0);
-    b.k0 = chunk * d.kc;
-    b.kw = min(d.kc, p.K - b.k0);
-    const int kgs = b.kw / 8, kgp = (kgs + 1) & ~1;
-    if (tid == 0) {
-        const __nv_bfloat16 *ablk =
-            reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)]);
-        const uint32_t a_bytes = (uint32_t)kgs * d.R * 16;
-        mbar_arrive_expect_tx(&sm.bar_shrink, a_bytes);
-        bulk_g2s(sm.pool, ablk + (int64_t)(b.k0 / 8) * d.R * 8, a_bytes, &sm.bar_shrink);
-    }
-    if (kgs < kgp) {
-        uint4 *z = reinterpret_cast<uint4 *>(sm.pool + kgs * d.R * 16);
-        for (int i = tid; i < d.R; i += kT) z[i] = make_uint4(0u, 0u, 0u, 0u);
-        tc::fence_proxy_async_smem();
-    }
-    unsigned char *X = sm.pool + kNtXOff;
-    for (int idx = tid; idx < b.nrows * kgp; idx += kT) {
-        const int i = idx / kgp, c = idx - i * kgp;
-        const int src = p.rows[d.rows_off + b.r0 + i] / p.src_div;
-        const bool valid = c < kgs;
-        tc::cp_async16(X + (c * kNtRows + i) * 16, valid ? (const void *)(p.x + (int64_t)src * p.ldx + b.k0 + c * 8)
-                                                         : (const void *)p.x, valid);
-    }
-    tc::cp_async_commit();
-    return b;
-}
-
-// Wait for the operands, run D[R][16] = A_chunk X_rows^T on tcgen05 (tokens
-// as N; rows of D past R and columns past the tile's rows are never read) and
-// store the fp32 partial of every row to the tile's scratch slot.
-__device__ __forceinline__ bool nt_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
-                                              const BgShrink &b, int g, int chunk, Phases &ph, bool first)
-{
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    tc::cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    if (!cta_wait(&sm.bar_shrink, ph.get(PH_SHRINK), p)) return false;
-    ph.flip(PH_SHRINK);
-    if (first) stamp(p, TS_SH_STAGE);
-    const int R = d.R;
-    const int steps = ((b.kw / 8) + 1) / 2;
-    if (tid == 0) {
-        tc::fence_after_sync();
-        const uint32_t a0 = smem_u32(sm.pool), x0 = smem_u32(sm.pool + kNtXOff);
-        const uint32_t idesc = tc::idesc_bf16(kTcRows, kNtRows);
-        for (int st = 0; st < steps; ++st) {
-            const uint64_t bd = tc::smem_desc(x0 + st * 2 * kNtRows * 16, kNtRows * 16, 128);
-            tc::mma_bf16(sm.tmem_base, tc::smem_desc(a0 + st * 2 * R * 16, R * 16, 128), bd, idesc, st > 0);
-            if (R > kTcRows)
-                tc::mma_bf16(sm.tmem_base + kNtRows, tc::smem_desc(a0 + st * 2 * R * 16 + kTcRows * 16, R * 16, 128),
-                             bd, idesc, st > 0);
-        }
-        tc::mma_commit(&sm.bar_mma[0]);
-    }
-    if (!cta_wait(&sm.bar_mma[0], ph.get(PH_MMA + 0), p)) return false;
-    ph.flip(PH_MMA + 0);
-    tc::fence_after_sync();
-    if (first) stamp(p, TS_SH_COMPUTED);
-    // tensor memory -> partial: warp w reads A rows 128 (w / 4) + 32 (w % 4) + lane, one column per token
-    const int h = warp >> 2;
-    if (h == 0 || R > kTcRows) {
-        const int j = h * kTcRows + (warp & 3) * 32 + lane;
-        float v[16];
-        tc::tmem_ld16(sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + h * kNtRows, v);
-        float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * b.r0 * R + (int64_t)chunk * b.nrows * R;
-        if (j < R) {
-#pragma unroll
-            for (int t = 0; t < kNtRows; ++t)
-                if (t < b.nrows) dst[t * R + j] = v[t];
-        }
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    return true;
-}
-
-// ===========================================================================
-// shrink items, vector tiles (CUDA cores)
-// ===========================================================================
-// Put the item's A chunk and its x rows (one bulk copy per row, row-major
-// [rows][kc] at kNtXOff) in flight on bar_shrink.
-__device__ __forceinline__ BgShrink fma_shrink_issue(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
-                                                     int tile, int chunk)
-{
-    BgShrink b;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    b.r0 = tile * kNtRows;
-    b.nrows = min(kNtRows, d.count - b.r0);
+    b.r0 = tile * kSmRows;
+    b.nrows = min(kSmRows, d.count - b.r0);
     b.k0 = chunk * d.kc;
     b.kw = min(d.kc, p.K - b.k0);
     const uint32_t x_bytes = (uint32_t)b.kw * 2;
@@ -426,89 +367,87 @@ __device__ __forceinline__ BgShrink fma_shrink_issue(const EngineParams &p, Engi
     }
     if (warp == 1 && lane < b.nrows) {
         const int src = p.rows[d.rows_off + b.r0 + lane] / p.src_div;
-        bulk_g2s(sm.pool + kNtXOff + (size_t)lane * d.kc * 2, p.x + (int64_t)src * p.ldx + b.k0, x_bytes,
+        bulk_g2s(sm.pool + kSmXOff + (size_t)lane * (d.kc * 2 + 16), p.x + (int64_t)src * p.ldx + b.k0, x_bytes,
                  &sm.bar_shrink);
     }
     return b;
 }
 
-// Wait for the copies, form the fp32 partial of every row against the A
-// chunk by FMA and store it to the tile's scratch slot.  Thread (j, ks) takes
-// row j of A and K-groups ks, ks + nks, ...; the eight lanes of each
-// quarter-warp read eight consecutive rows of A (no bank conflicts) and the
-// sums of a row meet in a fixed order: a shuffle tree over the ks inside a
-// warp, then, for small R, over warps through shared memory.  Rows go four at
-// a time.
-__device__ __forceinline__ bool fma_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
-                                               const BgShrink &b, int g, int chunk, Phases &ph, bool first)
+// Wait for the copies and form the fp32 partial X_rows A_chunk^T with
+// m16n8k16 MMAs (rows past the tile read row 0; their results are dropped).
+// Warp w takes 8-column tiles of the partial; when there are fewer than
+// eight tiles, the warps of a tile split K and meet in shared memory in a
+// fixed order.  Each warp keeps two accumulators (even and odd K steps) and
+// adds them at the end, so the summation order is fixed.
+__device__ __forceinline__ bool sm_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+                                              const BgShrink &b, int g, int chunk, Phases &ph, bool first)
 {
     if (!cta_wait(&sm.bar_shrink, ph.get(PH_SHRINK), p)) return false;
     ph.flip(PH_SHRINK);
     if (first) stamp(p, TS_SH_STAGE);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int R = d.R;
-    int nks = 1;
-    while (nks * 2 * R <= kT) nks *= 2;
-    const int kq = min(nks, 4), jw = 32 / kq;            // ks values per warp, rows of A per warp
-    const int jblocks = (R + jw - 1) / jw;
-    const int j = (warp % jblocks) * jw + (lane % jw);
-    const int ksb = warp / jblocks;                      // block of kq ks values
-    const int ks = ksb * kq + lane / jw;
-    const bool act = warp < jblocks * (nks / kq) && j < R;
-    const uint4 *A = reinterpret_cast<const uint4 *>(sm.pool);
-    const uint4 *X = reinterpret_cast<const uint4 *>(sm.pool + kNtXOff);
-    float *red = reinterpret_cast<float *>(sm.pool + kFmaRedOff);   // [ksb - 1][4][R]
-    const int xs = d.kc / 8;
-    const int kgs = b.kw / 8;
+    const int ntiles = R / 8;
+    const int ksplit = ntiles >= 8 ? 1 : 8 / ntiles;
+    const int kgs = b.kw / 8, steps = (kgs + 1) / 2;
+    const int xstride = d.kc * 2 + 16;
+    const uint32_t a_base = smem_u32(sm.pool);
+    const int xrow = (lane & 15) < b.nrows ? (lane & 15) : 0;
+    const uint32_t x_base = smem_u32(sm.pool + kSmXOff) + xrow * xstride;
+    float *red = reinterpret_cast<float *>(sm.pool + kSmRedOff);   // [ksplit - 1][16][R]
     float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * b.r0 * R + (int64_t)chunk * b.nrows * R;
-    for (int i0 = 0; i0 < b.nrows; i0 += 4) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    const int gr = lane >> 2, qc = (lane & 3) * 2;
+    const int kpart = warp / min(ntiles, 8);
+    const int s_lo = steps * kpart / ksplit, s_hi = steps * (kpart + 1) / ksplit;
+    for (int nt0 = 0; nt0 < ntiles; nt0 += 8) {   // uniform: every warp runs the same number of rounds
+        const int nt = nt0 + warp % min(ntiles, 8);
+        const bool act = nt < ntiles && kpart < ksplit;
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
         if (act) {
+            const uint32_t a_row = a_base + (nt * 8 + (lane & 7)) * 16;
 #pragma unroll 2
-            for (int kg = ks; kg < kgs; kg += nks) {
-                float af[8];
-                bf16x8_to_f32(A[kg * R + j], af);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (i0 + i < b.nrows) {
-                        float xf[8];
-                        bf16x8_to_f32(X[(i0 + i) * xs + kg], xf);
-                        float s0 = acc[i], s1 = acc2[i];
-#pragma unroll
-                        for (int u = 0; u < 8; u += 2) {
-                            s0 = fmaf(xf[u], af[u], s0);
-                            s1 = fmaf(xf[u + 1], af[u + 1], s1);
-                        }
-                        acc[i] = s0;
-                        acc2[i] = s1;
-                    }
+            for (int st = s_lo; st < s_hi; ++st) {
+                if (2 * st + 1 < kgs) {
+                    uint32_t a0, a1, a2, a3, b0, b1;
+                    ldsm_x4(x_base + (2 * st + (lane >> 4)) * 16, a0, a1, a2, a3);
+                    ldsm_x2(a_row + (2 * st + ((lane >> 3) & 1)) * R * 16, b0, b1);
+                    if (st & 1) mma16816(d1, a0, a1, a2, a3, b0, b1);
+                    else mma16816(d0, a0, a1, a2, a3, b0, b1);
+                } else {   // a last odd K-group: one k8 step
+                    uint32_t a0, a1, b0;
+                    ldsm_x2(x_base + (2 * st) * 16, a0, a1);
+                    ldsm_x1(a_row + (2 * st) * R * 16, b0);
+                    if (st & 1) mma1688(d1, a0, a1, b0);
+                    else mma1688(d0, a0, a1, b0);
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[i] += acc2[i];
-            for (int o = jw; o < 32; o <<= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
-        }
-        const int nksb = nks / kq;
-        if (nksb > 1) {   // warps of ks blocks 1.. hand their sums to block 0
-            if (act && ksb > 0 && lane < jw) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) red[((ksb - 1) * 4 + i) * R + j] = acc[i];
+        for (int q = 0; q < 4; ++q) d0[q] += d1[q];
+        const int col = nt * 8 + qc;
+        if (ksplit > 1) {   // K slices 1.. hand their sums to slice 0
+            if (act && kpart > 0) {
+                float *rr = red + (size_t)(kpart - 1) * kSmRows * R;
+                rr[gr * R + col] = d0[0];
+                rr[gr * R + col + 1] = d0[1];
+                rr[(gr + 8) * R + col] = d0[2];
+                rr[(gr + 8) * R + col + 1] = d0[3];
             }
             __syncthreads();
-            if (act && ksb == 0 && lane < jw) {
-                for (int q = 0; q < nksb - 1; ++q) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[i] += red[(q * 4 + i) * R + j];
+            if (act && kpart == 0) {
+                for (int k = 0; k < ksplit - 1; ++k) {
+                    const float *rr = red + (size_t)k * kSmRows * R;
+                    d0[0] += rr[gr * R + col];
+                    d0[1] += rr[gr * R + col + 1];
+                    d0[2] += rr[(gr + 8) * R + col];
+                    d0[3] += rr[(gr + 8) * R + col + 1];
                 }
             }
             __syncthreads();
         }
-        if (act && ksb == 0 && lane < jw) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (i0 + i < b.nrows) dst[(i0 + i) * R + j] = acc[i];
+        if (act && kpart == 0) {
+            if (gr < b.nrows) *reinterpret_cast<float2 *>(dst + gr * R + col) = make_float2(d0[0], d0[1]);
+            if (gr + 8 < b.nrows) *reinterpret_cast<float2 *>(dst + (gr + 8) * R + col) = make_float2(d0[2], d0[3]);
         }
     }
     if (first) stamp(p, TS_SH_COMPUTED);
@@ -694,7 +633,7 @@ __device__ __forceinline__ bool tc_shrink_run(const EngineParams &p, const CUten
 // ===========================================================================
 // Scratch of a group: [tiles][n_kc][rows of the tile][R] fp32 partials, then
 // the finished S: per tile bf16 [R/8][128][8] (tensor cores), or fp32
-// [rows][R] of the whole group (CUDA cores).
+// [rows][R] of the whole group (small tiles).
 __device__ __forceinline__ float *fin_area(const EngineParams &p, const EngineSmem &sm, const GroupDims &d, int g,
                                            int tile)
 {
@@ -795,8 +734,7 @@ __device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const
 // Thread 0 moves the issuer (sm.iss) to the next unit: unit k + 1 of the
 // item, or the first unit of item `item` when start is set or the item is
 // used up (the CTA's items are e0, e0 + grid, ...).
-__device__ __noinline__ void iss_next(const EngineParams &p, EngineSmem &sm, int ta, int tb, int ue, int kctc, int G,
-                                      int n_expand, bool start, int item)
+__device__ __noinline__ void iss_next(const EngineParams &p, EngineSmem &sm, int G, int n_expand, bool start, int item)
 {
     if (!start) {
         if (++sm.iss.k < sm.iss.it.nu) return;
@@ -805,7 +743,7 @@ __device__ __noinline__ void iss_next(const EngineParams &p, EngineSmem &sm, int
     sm.iss.item = item;
     sm.iss.k = 0;
     if (item < n_expand) {
-        const Plan pl = {ta, tb, ue, kctc};
+        const Plan pl = {sm.ta, sm.tb, sm.ue, sm.ues, sm.kctc};
         sm.iss.it = decode_expand(p, sm, pl, G, item);
     }
 }
@@ -854,7 +792,7 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, i
         r.kgs = kgs;
         r.yoff = yoff;
         r.ystride = ystride / 2;
-        r.kind = d.tc ? 2 : (d.fma ? 0 : 1);
+        r.tc = d.tc;
         r.scale = p.scale[d.a];
         if (d.uw == kTcCols) {
             // 128 output columns = one half of a 256-row B tile: rp/8 runs of 128 x 16 bytes
@@ -879,7 +817,7 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, i
 
 // Wait until the item's tile has its shrink results, then bring S into
 // shared memory: bf16 [rp/8][128][8] by a bulk copy (tensor cores), fp32
-// [16][64] from the finished S or summed from the partials (CUDA cores).
+// [16][rp] (padded rows) from the finished S or summed from the partials (small tiles).
 // The last consumer of the tile resets its counters for the next launch.
 __device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm, const ExpandItem &it, Phases &ph, bool first)
 {
@@ -903,8 +841,7 @@ __device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm
     __syncthreads();
     bool ready = sm.flag != 0;
     if (ready && !d.tc) {
-        // vector tile: S fp32 [16][64]; narrow tile: S^T in bf16, K-major for the MMA B operand: [rp/8][16][8]
-        float *Sf = reinterpret_cast<float *>(sm.pool);
+        // small tile: S in bf16, row-major [16][rp] with padded rows (the MMA A operand)
         __nv_bfloat16 *S = reinterpret_cast<__nv_bfloat16 *>(sm.pool);
         const int rp = d.rp;
         const int64_t stride = (int64_t)it.nrows * d.R;
@@ -926,10 +863,8 @@ __device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm
                         if (q0 + u < d.n_kc) acc += v[u];
                 }
             }
-            if (d.fma) Sf[i * kMaxRank + jj] = acc;
-            else S[((jj >> 3) * kNtRows + i) * 8 + (jj & 7)] = __float2bfloat16_rn(acc);
+            S[i * kSmSStride + jj] = __float2bfloat16_rn(acc);
         }
-        tc::fence_proxy_async_smem();
     }
     if (ready && d.tc) {
         ready = cta_wait(&sm.bar_s, ph.get(PH_S), p);
@@ -948,94 +883,53 @@ __device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm
     return ready;
 }
 
-// Vector unit in stage st: thread per output column, rows four at a time;
-// y = bf16(y_base + scale * w_row * sum_j S[i][j] B[n][j]) with S fp32 [16][64].
-__device__ __noinline__ void fma_unit(const EngineParams &p, EngineSmem &sm, int st)
-{
-    const UnitRec r = sm.unit[st];
-    const unsigned char *base = sm.pool + es_off(st);
-    const uint4 *B = reinterpret_cast<const uint4 *>(base);
-    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(base + r.yoff);
-    const float *S = reinterpret_cast<const float *>(sm.pool);
-    for (int nl = threadIdx.x; nl < r.nw; nl += kT) {
-        const int tl = nl / r.tw, col = nl % r.tw;
-        for (int i0 = 0; i0 < r.nrows; i0 += 4) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-            for (int kg = 0; kg < r.kgs; ++kg) {
-                float bf[8];
-                bf16x8_to_f32(B[(tl * r.kgs + kg) * r.tw + col], bf);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float *sr = S + (i0 + i) * kMaxRank + kg * 8;
-                    float a = acc[i];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) a = fmaf(sr[u], bf[u], a);
-                    acc[i] = a;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int row = i0 + i;
-                if (row < r.nrows) {
-                    const float yb = __bfloat162float(ys[row * r.ystride + nl]);
-                    p.y[(int64_t)sm.row_dst[st][row] * p.ldy + r.n0 + nl] =
-                        __float2bfloat16_rn(fmaf(r.scale * sm.row_w[st][row], acc[i], yb));
-                }
-            }
-        }
-    }
-    __syncthreads();
-}
-
-// Narrow unit in stage st: D^T(buf) = B_unit S^T on tcgen05, the unit's
-// output columns as M (128 per MMA), the tile's tokens as N = 16 (one thread
-// issues, commit on bar_mmae[buf]).
-__device__ __noinline__ void nt_unit_mma(EngineSmem &sm, int st, int buf)
-{
-    const UnitRec r = sm.unit[st];
-    const uint32_t base = smem_u32(sm.pool + es_off(st));
-    const uint32_t s0 = smem_u32(sm.pool);
-    const uint32_t idesc = tc::idesc_bf16(kTcRows, kNtRows);
-    const int nb = (r.nw + kTcCols - 1) / kTcCols;
-    tc::fence_after_sync();
-    for (int bk = 0; bk < nb; ++bk) {
-        // block bk: half (bk & 1) of B tile bk / 2 ([kgs][tw][8] per tile)
-        const uint32_t a0 = base + ((bk >> 1) * r.kgs * r.tw + (bk & 1) * kTcCols) * 16;
-        const uint32_t acc = sm.tmem_base + kTmemExpandCol + buf * kTcCols + bk * kNtRows;
-        for (int j = 0; j < r.kgs / 2; ++j)
-            tc::mma_bf16(acc, tc::smem_desc(a0 + j * 2 * r.tw * 16, r.tw * 16, 128),
-                         tc::smem_desc(s0 + j * 2 * kNtRows * 16, kNtRows * 16, 128), idesc, j > 0 ? 1u : 0u);
-    }
-    tc::mma_commit(&sm.bar_mmae[buf]);
-}
-
-// Narrow epilogue: thread = output column (128-column block (w / 4) + 2i, row
-// 32 (w % 4) + lane of it), one accumulator column per token;
-// y = bf16(y_base + scale * w_row * D), coalesced 2-byte stores per token row.
-__device__ __noinline__ void nt_unit_epilogue(const EngineParams &p, EngineSmem &sm, int st, int buf)
+// Small-tile unit in stage st: D[16][nw] = S B_unit^T with m16n8k16 MMAs
+// (tokens as M, 8 output columns per MMA tile, warp w takes column tiles
+// w, w + 8, ...), then y = bf16(y_base + scale * w_row * D) for the tile's
+// rows, two columns per store.  Ends with a barrier: the stage is free again.
+__device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int st)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const UnitRec r = sm.unit[st];
-    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(sm.pool + es_off(st) + r.yoff);
-    const int nb = (r.nw + kTcCols - 1) / kTcCols;
-    for (int bk = warp >> 2; bk < nb; bk += 2) {
-        const int n = bk * kTcCols + (warp & 3) * 32 + lane;
-        float v[16];
-        tc::tmem_ld16(sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + kTmemExpandCol + buf * kTcCols +
-                          bk * kNtRows, v);
-        if (n < r.nw) {
+    const unsigned char *base = sm.pool + es_off(st);
+    const uint32_t b_base = smem_u32(base);
+    const uint32_t s_row = smem_u32(sm.pool) + (lane & 15) * kSmSStride * 2;
+    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(base + r.yoff);
+    const int gr = lane >> 2, qc = (lane & 3) * 2;
+    const float s0 = gr < r.nrows ? r.scale * sm.row_w[st][gr] : 0.f;
+    const float s1 = gr + 8 < r.nrows ? r.scale * sm.row_w[st][gr + 8] : 0.f;
+    __nv_bfloat16 *y0 = p.y + (int64_t)(gr < r.nrows ? sm.row_dst[st][gr] : 0) * p.ldy + r.n0;
+    __nv_bfloat16 *y1 = p.y + (int64_t)(gr + 8 < r.nrows ? sm.row_dst[st][gr + 8] : 0) * p.ldy + r.n0;
+    const int ntiles = r.nw / 8, steps = r.kgs / 2;
+    uint32_t sa[kMaxRank / 16][4];   // S fragments of every K step, shared by all column tiles
 #pragma unroll
-            for (int t = 0; t < kNtRows; ++t) {
-                if (t < r.nrows) {
-                    const float yb = __bfloat162float(ys[t * r.ystride + n]);
-                    p.y[(int64_t)sm.row_dst[st][t] * p.ldy + r.n0 + n] =
-                        __float2bfloat16_rn(fmaf(r.scale * sm.row_w[st][t], v[t], yb));
-                }
+    for (int k = 0; k < kMaxRank / 16; ++k)
+        if (k < steps) ldsm_x4(s_row + (2 * k + (lane >> 4)) * 16, sa[k][0], sa[k][1], sa[k][2], sa[k][3]);
+    for (int nt = warp; nt < ntiles; nt += 8) {
+        const int n = nt * 8, tl = n / r.tw, col = n % r.tw;
+        // B rows n .. n + 7 of K-group kg: [(tl * kgs + kg) * tw + col] in 16-byte units
+        const uint32_t b_row = b_base + ((tl * r.kgs) * r.tw + col + (lane & 7)) * 16;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kMaxRank / 16; ++k) {
+            if (k < steps) {
+                uint32_t b0, b1;
+                ldsm_x2(b_row + (2 * k + ((lane >> 3) & 1)) * r.tw * 16, b0, b1);
+                mma16816(d, sa[k][0], sa[k][1], sa[k][2], sa[k][3], b0, b1);
             }
         }
+        const int c = n + qc;
+        if (gr < r.nrows) {
+            const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162 *>(ys + gr * r.ystride + c);
+            *reinterpret_cast<__nv_bfloat162 *>(y0 + c) = __floats2bfloat162_rn(
+                fmaf(s0, d[0], __bfloat162float(yb.x)), fmaf(s0, d[1], __bfloat162float(yb.y)));
+        }
+        if (gr + 8 < r.nrows) {
+            const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162 *>(ys + (gr + 8) * r.ystride + c);
+            *reinterpret_cast<__nv_bfloat162 *>(y1 + c) = __floats2bfloat162_rn(
+                fmaf(s1, d[2], __bfloat162float(yb.x)), fmaf(s1, d[3], __bfloat162float(yb.y)));
+        }
     }
-    tc::fence_before_sync();
     __syncthreads();
 }
 
@@ -1104,6 +998,53 @@ __device__ __noinline__ void tc_unit_epilogue(const EngineParams &p, EngineSmem 
 // ===========================================================================
 // the kernel
 // ===========================================================================
+// Warp 1, while warp 0 makes the plan: this CTA's share (by bytes) of every
+// group's A block is asked into L2, so the shrink copies issued after the
+// plan find it there.
+__device__ __forceinline__ void prefetch_a_l2(const EngineParams &p, const EngineSmem &sm, int G)
+{
+    const int lane = threadIdx.x & 31;
+    const int grid = gridDim.x, b = blockIdx.x;
+    auto block = [&](int g, long long &bytes) -> uint64_t {
+        bytes = 0;
+        if (g >= G) return 0;
+        const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
+        if (gr.x < 0 || gr.x >= p.L || gr.y < 0 || gr.y >= p.num_experts) return 0;
+        const int rp = gr.x < kRankCache ? sm.rp_cache[gr.x] : p.rpad[gr.x];
+        bytes = (long long)p.n_a * rp * p.K * 2;
+        return p.a_ptr[gr.x * p.E_A + (p.E_A == 1 ? 0 : gr.y)];
+    };
+    long long total = 0;
+#pragma unroll 1
+    for (int base = 0; base < G; base += 32) {
+        long long bytes;
+        block(base + lane, bytes);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        total += bytes;
+    }
+    const long long lo = total * b / grid, hi = total * (b + 1) / grid;
+    long long carry = 0;
+#pragma unroll 1
+    for (int base = 0; base < G; base += 32) {
+        long long bytes;
+        const uint64_t addr = block(base + lane, bytes);
+        long long incl = bytes;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        const long long start = carry + incl - bytes;
+        const long long a = max(lo, start) & ~15ll, e = min(hi, start + bytes);
+        if (bytes > 0 && e > a) {
+            const uint32_t size = (uint32_t)min(((e - a) + 15) & ~15ll, start + bytes - a);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr + (a - start)), "r"(size) : "memory");
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
 // Warp 0: size the chunks and units for this launch and lay out the work
 // list (per-group prefix counts, packed sizes of the cached groups).
 // Returns false for a workspace that lora_build_segments never filled.
@@ -1117,7 +1058,7 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
         N += p.slice_n[s];
         tc_units += (p.slice_n[s] + kTcCols - 1) >> 7;
     }
-    // pass 1: validate; CUDA-core A and B bytes (in units of K and N bf16 elements), tensor-core units
+    // pass 1: validate; small-tile A and B bytes (in units of K and N bf16 elements), 128-row tile units
     bool bad = false;
     long long bga = 0, bgb = 0;
     int tcu = 0, tci = 0;
@@ -1153,14 +1094,33 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     bad = __any_sync(0xffffffffu, bad);
     any_tc = __any_sync(0xffffffffu, any_tc);
     if (bad) return false;
-    // CUDA-core chunks of about a CTA's share of the A bytes (a quarter more, so that rounding up to
+    // small-tile chunks of about a CTA's share of the A bytes (a quarter more, so that rounding up to
     // whole chunks rarely needs a second wave); expand units of about 2/5 of a CTA's B share
     Plan pl;
     const int spare = max(grid / 4, grid - tci);
     pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, 1.25f * 2.f * (float)p.K * (float)bga / spare));
     pl.tb = (int)fminf(268435456.f, fmaxf(4096.f, 2.f * (float)N * (float)bgb / (2.5f * grid)));
-    pl.ue = 1 << ceil_log2(max(1, (tcu + kItemsPerCta * grid - 1) / (kItemsPerCta * grid)));
+    pl.ue = min(128, 1 << ceil_log2(max(1, (tcu + kItemsPerCta * grid - 1) / (kItemsPerCta * grid))));
     pl.kctc = kTcKc;
+    // small-tile expand units of the launch -> units per item, so that the items fit one wave
+    {
+        int units = 0;
+#pragma unroll 1
+        for (int g = lane; g < G; g += 32) {
+            const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
+            const bool tc = p.path == 2 || (p.path == 0 && gr.w > p.tc_min_rows);
+            if (tc) continue;
+            const int rp = gr.x < kRankCache ? sm.rp_cache[gr.x] : p.rpad[gr.x];
+            const int uw = sm_unit_width(rp, min(gr.w, kSmRows), pl.tb);
+            int u = 0;
+#pragma unroll 1
+            for (int s = 0; s < p.n_slices; ++s) u += (p.slice_n[s] + uw - 1) / uw;
+            units += ((gr.w + kSmRows - 1) / kSmRows) * u;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
+        pl.ues = min(16, max(1, (units + grid - 1) / grid));
+    }
     // pass 2: per-group item counts and their exclusive prefix sums, 32 groups per step; larger chunks
     // until the hand-off scratch fits the workspace
 #pragma unroll 1
@@ -1215,6 +1175,7 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
             sm.tb = pl.tb;
             sm.ue = pl.ue;
             sm.kctc = pl.kctc;
+            sm.ues = pl.ues;
         }
         if (c_part <= p.partial_floats || (pl.ta >= (1 << 27) && pl.kctc >= p.K)) break;
         pl.ta = min(1 << 28, pl.ta * 4);
@@ -1271,6 +1232,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         bool any_tc = false;
         const bool good = plan_launch(p, sm, G, any_tc);
         if (tid == 0) sm.flag = good ? (any_tc ? 2 : 0) : 1;
+    } else if (warp == 1) {
+        prefetch_a_l2(p, sm, G);
     }
     __syncthreads();
     stamp(p, TS_PRO_PLANNED);
@@ -1294,7 +1257,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const Plan pl = {sm.ta, sm.tb, sm.ue, sm.kctc};
+    const Plan pl = {sm.ta, sm.tb, sm.ue, sm.ues, sm.kctc};
     stamp(p, TS_WORKLIST);
 
     Phases ph = {0u};
@@ -1306,10 +1269,10 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     // previous kind stopped, so CTAs with fewer shrink items take the next kind first
     const int f0 = ((b - n_shrink) % grid + grid) % grid;
     const int e0 = ((b - n_shrink - n_fin) % grid + grid) % grid;
-    if (tid == 0) iss_next(p, sm, pl.ta, pl.tb, pl.ue, pl.kctc, G, n_expand, true, e0);
+    if (tid == 0) iss_next(p, sm, G, n_expand, true, e0);
 
     // expand units that may be in flight while the shrink items run: stage 0 beside a tensor-core
-    // shrink, stages 0 and 1 beside a CUDA-core one
+    // shrink, stages 0 and 1 beside a small-tile one
     int npre = kEsDepth;
 #pragma unroll 1
     for (int item = b; item < n_shrink; item += grid)
@@ -1321,7 +1284,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
             inflight |= 1u << (issued % kEsDepth);
             issue_unit(p, sm, issued++);
             __syncthreads();
-            if (tid == 0) iss_next(p, sm, pl.ta, pl.tb, pl.ue, pl.kctc, G, n_expand, false, 0);
+            if (tid == 0) iss_next(p, sm, G, n_expand, false, 0);
             __syncthreads();
         }
     };
@@ -1338,12 +1301,10 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         TcShrink t;
         BgShrink bs;
         if (d.tc) t = tc_shrink_issue(p, &pk.x_map, sm, d, tile, chunk);
-        else if (d.fma) bs = fma_shrink_issue(p, sm, d, tile, chunk);
-        else bs = nt_shrink_issue(p, sm, d, tile, chunk);
+        else bs = sm_shrink_issue(p, sm, d, tile, chunk);
         if (first) prefetch(npre);
         const bool ok = d.tc ? tc_shrink_run(p, &pk.x_map, sm, d, t, g, chunk, ph, first)
-                             : (d.fma ? fma_shrink_run(p, sm, d, bs, g, chunk, ph, first)
-                                      : nt_shrink_run(p, sm, d, bs, g, chunk, ph, first));
+                             : sm_shrink_run(p, sm, d, bs, g, chunk, ph, first);
         if (!ok) {
             alive = false;
             break;
@@ -1367,8 +1328,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         if (!cta_wait(&sm.bar_mmae[buf], ph.get(PH_MMAE + buf), p)) return false;
         ph.flip(PH_MMAE + buf);
         tc::fence_after_sync();
-        if (sm.unit[st].kind == 2) tc_unit_epilogue(p, sm, st, buf);
-        else nt_unit_epilogue(p, sm, st, buf);
+        tc_unit_epilogue(p, sm, st, buf);
         if (q < 4) stamp(p, TS_EX_UNIT + 2 * q + 1);
         pend = -1;
         prefetch(q + 1 + kEsDepth);
@@ -1393,21 +1353,18 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
             ph.flip(PH_ES + st);
             inflight &= ~(1u << st);
             if (seq < 4) stamp(p, TS_EX_UNIT + 2 * seq);
-            if (it.d.fma) {
+            if (!it.d.tc) {
                 if (pend >= 0 && !drain()) {   // units leave the ring in order
                     alive = false;
                     break;
                 }
-                fma_unit(p, sm, st);   // ends with a barrier: stage st is free again
+                sm_unit(p, sm, st);   // ends with a barrier: stage st is free again
                 if (seq < 4) stamp(p, TS_EX_UNIT + 2 * seq + 1);
                 prefetch(seq + 1 + kEsDepth);
                 continue;
             }
             // this unit's MMAs go in while the previous unit's epilogue runs
-            if (tid == 0) {
-                if (it.d.tc) tc_unit_mma(sm, st, seq & 1);
-                else nt_unit_mma(sm, st, seq & 1);
-            }
+            if (tid == 0) tc_unit_mma(sm, st, seq & 1);
             if (pend >= 0 && !drain()) {
                 alive = false;
                 break;

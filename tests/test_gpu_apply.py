@@ -32,7 +32,8 @@ def problems():
 
 @pytest.mark.parametrize("name,make", list(problems()), ids=[n for n, _ in problems()])
 def test_apply_matches_oracle(name, make):
-    """Every path (auto, CUDA-core forced, tensor-core forced) against the oracle, full output and delta only."""
+    """Every path (auto, small tiles forced, 128-row tensor-core tiles forced) against the oracle, full
+    output and delta only."""
     for base in (True, False):
         p = make(base)
         ref = oracle_dense(p)
