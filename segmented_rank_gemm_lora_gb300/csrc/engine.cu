@@ -373,18 +373,23 @@ __device__ __forceinline__ BgShrink sm_shrink_issue(const EngineParams &p, Engin
     return b;
 }
 
-// Wait for the copies and form the fp32 partial X_rows A_chunk^T with
+// Form the fp32 partial X_rows A_chunk^T (operands in place) with
 // m16n8k16 MMAs (rows past the tile read row 0; their results are dropped).
 // Warp w takes 8-column tiles of the partial; when there are fewer than
 // eight tiles, the warps of a tile split K and meet in shared memory in a
 // fixed order.  Each warp keeps two accumulators (even and odd K steps) and
 // adds them at the end, so the summation order is fixed.
-__device__ __forceinline__ bool sm_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
-                                              const BgShrink &b, int g, int chunk, Phases &ph, bool first)
+__device__ __forceinline__ bool sm_shrink_wait(const EngineParams &p, EngineSmem &sm, Phases &ph, bool first)
 {
     if (!cta_wait(&sm.bar_shrink, ph.get(PH_SHRINK), p)) return false;
     ph.flip(PH_SHRINK);
     if (first) stamp(p, TS_SH_STAGE);
+    return true;
+}
+
+__device__ __forceinline__ void sm_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+                                              const BgShrink &b, int g, int chunk, bool first)
+{
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int R = d.R;
     const int ntiles = R / 8;
@@ -452,7 +457,6 @@ __device__ __forceinline__ bool sm_shrink_run(const EngineParams &p, EngineSmem 
     }
     if (first) stamp(p, TS_SH_COMPUTED);
     __syncthreads();
-    return true;
 }
 
 // ===========================================================================
@@ -1269,15 +1273,19 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     // previous kind stopped, so CTAs with fewer shrink items take the next kind first
     const int f0 = ((b - n_shrink) % grid + grid) % grid;
     const int e0 = ((b - n_shrink - n_fin) % grid + grid) % grid;
-    if (tid == 0) iss_next(p, sm, G, n_expand, true, e0);
-
-    // expand units that may be in flight while the shrink items run: stage 0 beside a tensor-core
-    // shrink, stages 0 and 1 beside a small-tile one
+    // the expand issuer starts at item e0; expand units may be in flight while the shrink items run:
+    // stage 0 beside a tensor-core shrink, stages 0 and 1 beside a small-tile one.  Set up after the
+    // first shrink item's copies are on their way.
     int npre = kEsDepth;
+    bool iss_ready = false;
+    auto setup_issuer = [&]() {
+        if (tid == 0) iss_next(p, sm, G, n_expand, true, e0);
 #pragma unroll 1
-    for (int item = b; item < n_shrink; item += grid)
-        npre = min(npre, group_dims(p, sm, find_group(sm.sh_pre, G, item), pl).tc ? 1 : 2);
-    __syncthreads();
+        for (int item = b; item < n_shrink; item += grid)
+            npre = min(npre, group_dims(p, sm, find_group(sm.sh_pre, G, item), pl).tc ? 1 : 2);
+        __syncthreads();
+        iss_ready = true;
+    };
     // put units in flight until `upto` have been issued (units must have left stage (upto - 1) % 3)
     auto prefetch = [&](int upto) {
         while (issued < upto && sm.iss.item < n_expand) {
@@ -1298,21 +1306,32 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         const int tg = sm.tile_pre[g] + tile;
         const bool first = item == b;
         if (first) stamp(p, TS_SH_START);
-        TcShrink t;
-        BgShrink bs;
-        if (d.tc) t = tc_shrink_issue(p, &pk.x_map, sm, d, tile, chunk);
-        else bs = sm_shrink_issue(p, sm, d, tile, chunk);
-        if (first) prefetch(npre);
-        const bool ok = d.tc ? tc_shrink_run(p, &pk.x_map, sm, d, t, g, chunk, ph, first)
-                             : sm_shrink_run(p, sm, d, bs, g, chunk, ph, first);
+        bool ok;
+        if (d.tc) {
+            const TcShrink t = tc_shrink_issue(p, &pk.x_map, sm, d, tile, chunk);
+            if (first) {
+                setup_issuer();
+                prefetch(npre);
+            }
+            ok = tc_shrink_run(p, &pk.x_map, sm, d, t, g, chunk, ph, first);
+        } else {
+            const BgShrink bs = sm_shrink_issue(p, sm, d, tile, chunk);
+            if (first) setup_issuer();
+            ok = sm_shrink_wait(p, sm, ph, first);
+            if (ok) sm_shrink_run(p, sm, d, bs, g, chunk, first);
+        }
         if (!ok) {
             alive = false;
             break;
         }
         if (tid == 0 && !p.withhold) release_add(&p.sync[tg * 4 + 0], 1);
         if (first) stamp(p, TS_SH_PUBLISHED);
+        // small tiles: the first expand units go in flight after the partial is published, so they
+        // neither compete with the shrink operands nor delay the hand-off
+        if (first && !d.tc) prefetch(npre);
     }
     // the shrink staging is free: the rest of the ring may fill while the finish items run
+    if (!iss_ready) setup_issuer();
     if (alive) prefetch(kEsDepth);
     stamp(p, TS_PREFETCHED);
 

@@ -244,8 +244,65 @@ __global__ void __launch_bounds__(kBuildThreads, 1) build_kernel(BuildParams p)
     }
 }
 
+// Dense batches of at most 32 tokens: one warp, one token per lane.  The
+// (key, token index) pairs are put in order by a bitonic network of lane
+// shuffles; comparing the index as well makes the order stable, so the
+// result equals the counting sort above.  Segments start where the key
+// changes.
+__global__ void __launch_bounds__(32, 1) build_warp_kernel(BuildParams p)
+{
+    const int lane = threadIdx.x;
+    const int32_t L = p.L, M = p.M;
+    uint32_t *err = reinterpret_cast<uint32_t *>(p.header + H_ERR);
+    for (int i = lane; i < p.sync_ints; i += 32) p.sync[i] = 0;
+    int key = INT32_MAX, v = lane;   // lanes past M sort after everything
+    if (lane < M) {
+        const int32_t i = p.ids[lane];
+        if (i < -1 || i >= L) atomicOr(err, kErrBadId);
+        key = (i >= 0 && i < L && (p.enabled == nullptr || p.enabled[i])) ? i : L;
+    }
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int ok = __shfl_xor_sync(0xffffffffu, key, stride);
+            const int ov = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool ascending = (lane & size) == 0;
+            const bool low = (lane & stride) == 0;
+            const bool greater = key > ok || (key == ok && v > ov);
+            // the lower lane of an ascending pair keeps the smaller pair, the upper lane the larger
+            if (low == ascending ? greater : !greater) {
+                key = ok;
+                v = ov;
+            }
+        }
+    }
+    if (lane < M) p.perm[lane] = v;
+    const bool valid = lane < M && key < L;
+    const int prev = __shfl_up_sync(0xffffffffu, key, 1);
+    const bool start = valid && (lane == 0 || prev != key);
+    const uint32_t starts = __ballot_sync(0xffffffffu, start);
+    const int num_valid = __popc(__ballot_sync(0xffffffffu, valid));
+    if (start) {
+        const uint32_t later = starts & ~((2u << lane) - 1u);   // segment starts after this lane
+        const int end = later ? __ffs(later) - 1 : num_valid;
+        p.segments[__popc(starts & ((1u << lane) - 1u))] = make_int4(key, 0, lane, end - lane);
+    }
+    if (lane == 0) {
+        p.header[H_M] = M;
+        p.header[H_NUM_SEGMENTS] = __popc(starts);
+        p.header[H_NUM_VALID] = num_valid;
+        p.header[H_NUM_MOE_GROUPS] = 0;
+        p.header[H_BLOCK_M] = 0;
+    }
+}
+
 cudaError_t launch_build(const BuildParams &p, cudaStream_t s)
 {
+    if (p.M <= 32 && (p.block_m <= 0 || p.topk_ids == nullptr)) {
+        build_warp_kernel<<<1, 32, 0, s>>>(p);
+        return cudaGetLastError();
+    }
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
