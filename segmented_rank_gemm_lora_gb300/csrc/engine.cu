@@ -116,12 +116,6 @@ struct ExpandItem {
     GroupDims d;
 };
 
-// Issue side of the expand ring: the next unit of this CTA's expand items to
-// put in flight (unit k of item `item`).
-struct IssState {
-    int item, k;
-    ExpandItem it;
-};
 
 struct __align__(1024) EngineSmem {
     __align__(1024) unsigned char pool[kPool];
@@ -136,7 +130,6 @@ struct __align__(1024) EngineSmem {
     int32_t G, flag, x_total;
     int32_t ta, tb, ue, ues, kctc;       // launch plan (see plan_launch)
     UnitRec unit[kEsDepth];
-    IssState iss;
     int32_t row_dst[kEsDepth][kTcRows];
     float row_w[kEsDepth][kTcRows];
     int32_t row_src[kTcRows];
@@ -735,45 +728,26 @@ __device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const
 
 // The issue side of the expand ring: the next unit of this CTA's expand
 // items to put in flight.
-// Thread 0 moves the issuer (sm.iss) to the next unit: unit k + 1 of the
-// item, or the first unit of item `item` when start is set or the item is
-// used up (the CTA's items are e0, e0 + grid, ...).
-__device__ __noinline__ void iss_next(const EngineParams &p, EngineSmem &sm, int G, int n_expand, bool start, int item)
-{
-    if (!start) {
-        if (++sm.iss.k < sm.iss.it.nu) return;
-        item = sm.iss.item + gridDim.x;
-    }
-    sm.iss.item = item;
-    sm.iss.k = 0;
-    if (item < n_expand) {
-        const Plan pl = {sm.ta, sm.tb, sm.ue, sm.ues, sm.kctc};
-        sm.iss.it = decode_expand(p, sm, pl, G, item);
-    }
-}
-
-// Put the issuer's next unit in flight into stage seq % 3: its B rows and its
-// output rows (bulk copies on bar_es), with a record of the unit.  The first
-// unit of an item reads the item's output rows from the row list; later ones
-// take them from the previous unit's stage.
-__device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, int seq)
+// Put one expand unit in flight into stage seq % 3: its B rows and its output
+// rows (bulk copies on bar_es), with a record of the unit.  The unit is column
+// unit uu of slice s of a tile whose output rows are rows[row_base ..
+// row_base + nrows); the first unit of an item reads them from the row list,
+// later ones take them from the previous unit's stage (same thread, same row).
+__device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, int seq, int s, int uu, int nrows,
+                                        int row_base, bool first, int a, int e, int rp, int uw, bool tc)
 {
     const int tid = threadIdx.x;
-    const IssState &is = sm.iss;
-    const ExpandItem &it = is.it;
-    const GroupDims &d = it.d;
     const int st = seq % kEsDepth;
     unsigned char *base = sm.pool + es_off(st);
-    const int uu = it.u0 + is.k;
-    const int n0 = p.slice_off[it.s] + uu * d.uw;
-    const int nw = min(d.uw, p.slice_n[it.s] - uu * d.uw);
-    const int ystride = d.tc ? kTcYStride : d.uw * 2;
-    const int yoff = d.tc ? kTcYOff : d.uw * d.rp * 2;
-    if (tid < it.nrows) {
+    const int n0 = p.slice_off[s] + uu * uw;
+    const int nw = min(uw, p.slice_n[s] - uu * uw);
+    const int ystride = tc ? kTcYStride : uw * 2;
+    const int yoff = tc ? kTcYOff : uw * rp * 2;
+    if (tid < nrows) {
         int row;
         float w;
-        if (is.k == 0) {
-            row = p.rows[d.rows_off + it.r0 + tid];
+        if (first) {
+            row = p.rows[row_base + tid];
             w = p.row_weight ? p.row_weight[row] : 1.0f;
         } else {
             const int pst = (seq + kEsDepth - 1) % kEsDepth;   // the previous unit, same item
@@ -785,22 +759,21 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, i
         bulk_g2s(base + yoff + tid * ystride, p.y + (int64_t)row * p.ldy + n0, (uint32_t)nw * 2, &sm.bar_es[st]);
     }
     if (tid == 0) {
-        const __nv_bfloat16 *bblk =
-            reinterpret_cast<const __nv_bfloat16 *>(p.b_ptr[d.a * p.E_B + (p.E_B == 1 ? 0 : d.e)]);
-        const uint32_t y_bytes = (uint32_t)it.nrows * nw * 2;
-        const int kgs = d.rp / 8;
+        const __nv_bfloat16 *bblk = reinterpret_cast<const __nv_bfloat16 *>(p.b_ptr[a * p.E_B + (p.E_B == 1 ? 0 : e)]);
+        const uint32_t y_bytes = (uint32_t)nrows * nw * 2;
+        const int kgs = rp / 8;
         UnitRec r;
         r.n0 = n0;
         r.nw = nw;
-        r.nrows = it.nrows;
+        r.nrows = nrows;
         r.kgs = kgs;
         r.yoff = yoff;
         r.ystride = ystride / 2;
-        r.tc = d.tc;
-        r.scale = p.scale[d.a];
-        if (d.uw == kTcCols) {
+        r.tc = tc;
+        r.scale = p.scale[a];
+        if (uw == kTcCols) {
             // 128 output columns = one half of a 256-row B tile: rp/8 runs of 128 x 16 bytes
-            const int btile = p.slice_tile_off[it.s] + uu / 2, half = uu & 1;
+            const int btile = p.slice_tile_off[s] + uu / 2, half = uu & 1;
             r.tw = kTcCols;
             mbar_arrive_expect_tx(&sm.bar_es[st], (uint32_t)kgs * kTcCols * 16 + y_bytes);
             for (int kg = 0; kg < kgs; ++kg)
@@ -808,12 +781,12 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, i
                          kTcCols * 16, &sm.bar_es[st]);
         } else {
             // whole 256-row B tiles: one contiguous run
-            const int tile0 = p.slice_tile_off[it.s] + uu * (d.uw / kNTile);
+            const int tile0 = p.slice_tile_off[s] + uu * (uw / kNTile);
             const int ntl = (nw + kNTile - 1) / kNTile;
-            const uint32_t b_bytes = (uint32_t)ntl * kNTile * d.rp * 2;
+            const uint32_t b_bytes = (uint32_t)ntl * kNTile * rp * 2;
             r.tw = kNTile;
             mbar_arrive_expect_tx(&sm.bar_es[st], b_bytes + y_bytes);
-            bulk_g2s(base, bblk + (int64_t)tile0 * kNTile * d.rp, b_bytes, &sm.bar_es[st]);
+            bulk_g2s(base, bblk + (int64_t)tile0 * kNTile * rp, b_bytes, &sm.bar_es[st]);
         }
         sm.unit[st] = r;
     }
@@ -1278,22 +1251,29 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     // first shrink item's copies are on their way.
     int npre = kEsDepth;
     bool iss_ready = false;
+    // issue side of the expand ring, kept by every thread alike: unit iss_k of item iss_item
+    int iss_item = n_expand, iss_k = 0;
+    ExpandItem iss_it;
     auto setup_issuer = [&]() {
-        if (tid == 0) iss_next(p, sm, G, n_expand, true, e0);
+        iss_item = e0;
+        if (e0 < n_expand) iss_it = decode_expand(p, sm, pl, G, e0);
 #pragma unroll 1
         for (int item = b; item < n_shrink; item += grid)
             npre = min(npre, group_dims(p, sm, find_group(sm.sh_pre, G, item), pl).tc ? 1 : 2);
-        __syncthreads();
         iss_ready = true;
     };
     // put units in flight until `upto` have been issued (units must have left stage (upto - 1) % 3)
     auto prefetch = [&](int upto) {
-        while (issued < upto && sm.iss.item < n_expand) {
+        while (issued < upto && iss_item < n_expand) {
             inflight |= 1u << (issued % kEsDepth);
-            issue_unit(p, sm, issued++);
-            __syncthreads();
-            if (tid == 0) iss_next(p, sm, G, n_expand, false, 0);
-            __syncthreads();
+            const GroupDims &d = iss_it.d;
+            issue_unit(p, sm, issued++, iss_it.s, iss_it.u0 + iss_k, iss_it.nrows, d.rows_off + iss_it.r0,
+                       iss_k == 0, d.a, d.e, d.rp, d.uw, d.tc);
+            if (++iss_k == iss_it.nu) {
+                iss_k = 0;
+                iss_item += grid;
+                if (iss_item < n_expand) iss_it = decode_expand(p, sm, pl, G, iss_item);
+            }
         }
     };
 
