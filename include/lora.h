@@ -246,7 +246,9 @@ const char *lora_status_string(lora_status status);
  *                              rows on small 16-row tiles with warp-level MMAs,
  *                              the rest on 128-row tcgen05 tiles), 1 every group
  *                              on small tiles, 2 every group on 128-row tiles.
- *   LORA_OPT_TC_MIN_ROWS     : groups with more rows take 128-row tcgen05 tiles.
+ *   LORA_OPT_TC_MIN_ROWS     : groups with more rows take 128-row tcgen05 tiles
+ *                              (default 32; groups whose A block has more than
+ *                              128 rows, n_a * stored rank, switch at half).
  *   LORA_OPT_WAIT_TIMEOUT_NS : limit of every in-kernel wait (default 1 s).
  *   LORA_OPT_GRID_CTAS       : persistent grid size (0 = one wave over all SMs).
  *   LORA_OPT_TEST_WITHHOLD_HANDOFF : test hook; nonzero makes the next launches

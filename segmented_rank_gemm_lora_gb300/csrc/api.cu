@@ -18,7 +18,7 @@ constexpr int64_t kPartialFloatsPerRow = 16384;   // L2 scratch for rank-sized p
 constexpr int64_t kMaxRows = 65536;               // tokens (or token/expert pairs) per build
 
 std::atomic<int64_t> g_opt_path{0};
-std::atomic<int64_t> g_opt_tc_min_rows{16};
+std::atomic<int64_t> g_opt_tc_min_rows{32};
 std::atomic<int64_t> g_opt_timeout_ns{1000000000LL};
 std::atomic<int64_t> g_opt_grid{0};
 std::atomic<int64_t> g_opt_withhold{0};
@@ -44,7 +44,18 @@ encode_tiled_fn g_encode = nullptr;
 
 // 2-D map over a bf16 [rows][K] matrix with row stride ld: box 64 columns x 128 rows, 128-byte swizzle,
 // reads outside the matrix return zero.
+static lora_status encode_2d(const void *base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
+                             CUtensorMap *out);
+
 lora_status encode_rows_map(const void *base, int64_t rows, int32_t K, int64_t ld, CUtensorMap *out)
+{
+    // the kernel only issues boxes that lie inside the rows of x, so the row extent may be rounded up to one box
+    return encode_2d(base, std::max<int64_t>(rows, 128), K, ld, 128, out);
+}
+
+// bf16 [rows][cols] with row stride ld elements; boxes of 64 columns x box_rows rows, 128-byte swizzle
+static lora_status encode_2d(const void *base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
+                             CUtensorMap *out)
 {
     {
         std::lock_guard<std::mutex> lk(g_encode_mu);
@@ -60,10 +71,9 @@ lora_status encode_rows_map(const void *base, int64_t rows, int32_t K, int64_t l
             g_encode = reinterpret_cast<encode_tiled_fn>(fn);
         }
     }
-    // the kernel only issues boxes that lie inside the rows of x, so the row extent may be rounded up to one box
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)std::max<int64_t>(rows, 128)};
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -437,6 +447,14 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
     }
     p.m_ptr = at<int32_t>(ws, w.header) + H_M;
     p.m_mult = (moe && src_div == 1) ? ws->topk : 1;
+    p.y_mult = moe ? ws->topk : 1;
+    if (t->N >= 128) {   // output tiles move as 2-D boxes only inside rows the last build produced
+        const int64_t y_rows = (int64_t)ws->max_M * p.y_mult;
+        st = encode_2d(y, std::max<int64_t>(y_rows, 128), t->N, ldy, 128, &p.y_map_ld);
+        if (st == LORA_OK) st = encode_2d(y, std::max<int64_t>(y_rows, 128), t->N, ldy, 32, &p.y_map_st);
+        if (st != LORA_OK) return st;
+        p.y_rows = (int32_t)y_rows;
+    }
     p.a_ptr = t->d_a_ptr;
     p.b_ptr = t->d_b_ptr;
     p.rpad = t->d_rpad;

@@ -17,7 +17,7 @@ namespace lora {
 constexpr int kMaxRank = 64;           // largest true rank
 constexpr int kMaxSlices = 4;
 constexpr int kNTile = 256;            // B is stored in tiles of 256 output rows
-constexpr int kBgmvRows = 16;          // rows of one CUDA-core tile
+constexpr int kBgmvRows = 16;          // rows of one small tile
 constexpr int kEngineThreads = 256;
 constexpr int kHeaderInts = 16;
 constexpr int kTraceSlots = 32;        // uint64 phase stamps per thread block (lora_set_trace)
@@ -57,6 +57,13 @@ struct EngineParams {
     int32_t x_rows;          // rows the map spans; 0 = no map (every load takes the cp.async gather)
     const int32_t *m_ptr;    // token count of the last build (device)
     int32_t m_mult;          // rows of x per token (topk for the per-pair MoE input, else 1)
+    // 2-D tensor maps over the output (bf16 [y_rows][N], row stride ldy; 128-byte swizzle): 128-column
+    // units of 128-row tiles whose rows are one run of consecutive rows load through a 64 x 128 box and
+    // store through 64 x 32 boxes
+    CUtensorMap y_map_ld;
+    CUtensorMap y_map_st;
+    int32_t y_rows;          // rows the maps span; 0 = no maps (every unit takes per-row bulk copies)
+    int32_t y_mult;          // rows of y per token
     // weight table
     const uint64_t *a_ptr;   // [L * E_A] packed A block addresses
     const uint64_t *b_ptr;   // [L * E_B] packed B block addresses
@@ -84,9 +91,9 @@ struct EngineParams {
     uint32_t *err;
     uint64_t timeout_ns;
     int32_t withhold;        // test hook: do not publish shrink results
-    int32_t path;            // 0 auto, 1 every group on CUDA cores, 2 every group on tensor cores
-    int32_t tc_min_rows;     // groups with more rows take the tensor-core path
-    uint64_t *trace;         // optional [trace_ctas][8] phase stamps
+    int32_t path;            // 0 auto, 1 every group on small tiles, 2 every group on 128-row tiles
+    int32_t tc_min_rows;     // groups with more rows take 128-row tiles
+    uint64_t *trace;         // optional [trace_ctas][32] phase stamps
     int32_t trace_ctas;
 };
 

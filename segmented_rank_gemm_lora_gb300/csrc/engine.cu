@@ -29,12 +29,13 @@
 // Shrink items never wait on other CTAs, finish items wait only on shrink
 // items and expand items only on the other two, and the whole grid is
 // co-resident, so every wait ends.  The chunk sizes are picked per launch from
-// the total bytes so that each SM gets about one shrink item and two to three
-// expand units.  Expand units stream through a three-stage ring that runs
-// across item boundaries; the first units are put in flight while the shrink
-// work is still running.  Operands move as bulk async copies (whole rows of
-// x and y, contiguous runs of the packed table) or 2-D TMA tiles on
-// mbarriers; tensor-core results leave as bulk row stores.  The summation
+// the total bytes so that the items of each kind fill whole waves of the
+// grid.  Expand units stream through a
+// three-stage ring that runs across item boundaries; the first units are put
+// in flight while the shrink work is still running.  Operands move as bulk
+// async copies (whole rows of x and y, contiguous runs of the packed table) or
+// 2-D TMA tiles on mbarriers; tensor-core results leave as 2-D TMA boxes or
+// bulk row stores.  The summation
 // order never depends on timing or on which rows share a tile, so the same
 // inputs always give the same bits.
 #include "common.cuh"
@@ -44,8 +45,8 @@ namespace lora {
 
 constexpr int kT = kEngineThreads;
 constexpr int kGroupCap = 2048;                 // groups per launch held in shared memory
-constexpr int kGroupCache = 256;                // group records and sizes cached in shared memory
-constexpr int kRankCache = 1024;                // stored ranks cached in shared memory
+constexpr int kGroupCache = 128;                // group records and sizes cached in shared memory
+constexpr int kRankCache = 512;                 // stored ranks cached in shared memory
 // shared-memory pool: S at [0, 16K), three expand stages of 50 KB above it (stage 0 on top)
 constexpr int kStageBytes = 50 * 1024;
 constexpr int kEsDepth = 3;
@@ -73,7 +74,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemExpandCol = 256;        // shrink accumulator: [0, R); expand: [256, 384), [384, 512)
 constexpr int kTcYOff = 16 * 1024;              // tensor-core stage: B [rp/8][128][8] at 0, y rows after
 constexpr int kTcYStride = kTcCols * 2 + 16;    // padded rows: a warp (one row per lane) hits every bank group
-constexpr int kItemsPerCta = 2;                 // tensor-core expand items per CTA the plan aims for
+constexpr int kItemsPerCta = 2;                 // 128-row tile expand items per CTA the plan aims for
 static_assert(kTcYOff + kTcRows * kTcYStride <= kStageBytes, "tensor-core expand stage");
 static_assert(kSmRedOff + 3 * 16 * 32 * 4 <= kBgShrinkBytes, "small-tile shrink staging");
 static_assert(kSBytes >= (kMaxRank / 8) * kTcRows * 16, "S area");
@@ -93,6 +94,7 @@ __device__ __forceinline__ int es_off(int st) { return kPool - (st + 1) * kStage
 // One expand unit sitting in a stage; written by the thread that issued its copies.
 struct UnitRec {
     int n0, nw, nrows, kgs, tw, yoff, ystride, tc;
+    int run;   // 128-row tile of consecutive rows: y moves as 2-D TMA boxes ([2][128][128 B], 128-byte swizzle)
     float scale;
 };
 
@@ -133,7 +135,8 @@ struct __align__(1024) EngineSmem {
     int32_t row_dst[kEsDepth][kTcRows];
     float row_w[kEsDepth][kTcRows];
     int32_t row_src[kTcRows];
-    int32_t sh_pre[kGroupCap + 1];       // shrink items before group g
+    int32_t sh_pre[kGroupCap + 1];       // 128-row tile shrink items before group g
+    int32_t shs_pre[kGroupCap + 1];      // small-tile shrink items before group g
     int32_t fin_pre[kGroupCap + 1];      // finish items before group g
     int32_t ex_pre[kGroupCap + 1];       // expand items before group g
     int32_t tile_pre[kGroupCap + 1];     // tiles before group g
@@ -147,6 +150,14 @@ static_assert(sizeof(EngineSmem) <= 227 * 1024, "shared memory per CTA");
 size_t engine_smem_bytes(int) { return sizeof(EngineSmem); }
 
 
+
+// A group runs on 128-row tcgen05 tiles when it has more than tc_min_rows rows; groups whose A block has
+// more than 128 rows switch at half that count, because their small-tile K-chunks (A staging / 2R)
+// get short.
+__device__ __forceinline__ bool group_on_tc(const EngineParams &p, int count, int R)
+{
+    return p.path == 2 || (p.path == 0 && count > (R > 128 ? p.tc_min_rows / 2 : p.tc_min_rows));
+}
 
 __device__ __forceinline__ int floor_pow2(int v) { return v <= 0 ? 0 : 1 << (31 - __clz(v)); }
 __device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
@@ -170,7 +181,7 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
     d.count = gr.w;
     d.rp = d.a < kRankCache ? sm.rp_cache[d.a] : p.rpad[d.a];
     d.R = p.n_a * d.rp;
-    d.tc = p.path == 2 || (p.path == 0 && d.count > p.tc_min_rows);
+    d.tc = group_on_tc(p, d.count, d.R);
     d.tile_rows = d.tc ? kTcRows : kBgmvRows;
     d.tiles = (d.count + d.tile_rows - 1) / d.tile_rows;
     d.rows1 = min(d.count, d.tile_rows);
@@ -733,8 +744,9 @@ __device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const
 // unit uu of slice s of a tile whose output rows are rows[row_base ..
 // row_base + nrows); the first unit of an item reads them from the row list,
 // later ones take them from the previous unit's stage (same thread, same row).
-__device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, int seq, int s, int uu, int nrows,
-                                        int row_base, bool first, int a, int e, int rp, int uw, bool tc)
+__device__ __noinline__ void issue_unit(const EngineParams &p, const CUtensorMap *ymap, EngineSmem &sm, int seq, int s,
+                                        int uu, int nrows, int row_base, bool first, int a, int e, int rp, int uw,
+                                        bool tc)
 {
     const int tid = threadIdx.x;
     const int st = seq % kEsDepth;
@@ -756,11 +768,22 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, i
         }
         sm.row_dst[st][tid] = row;
         sm.row_w[st][tid] = w;
-        bulk_g2s(base + yoff + tid * ystride, p.y + (int64_t)row * p.ldy + n0, (uint32_t)nw * 2, &sm.bar_es[st]);
     }
+    // a full 128-column unit of a 128-row tile whose rows are one run inside the rows of y moves as 2-D boxes
+    bool run = false;
+    if (tc) {
+        __syncthreads();
+        const int row0 = sm.row_dst[st][0];
+        const bool mine = tid >= nrows || sm.row_dst[st][tid] == row0 + tid;
+        run = __syncthreads_and(mine ? 1 : 0) != 0 && p.y_rows > 0 && nw == kTcCols &&
+              row0 + kTcRows <= sm.x_total / p.m_mult * p.y_mult;
+    }
+    if (!run && tid < nrows)
+        bulk_g2s(base + yoff + tid * ystride, p.y + (int64_t)sm.row_dst[st][tid] * p.ldy + n0, (uint32_t)nw * 2,
+                 &sm.bar_es[st]);
     if (tid == 0) {
         const __nv_bfloat16 *bblk = reinterpret_cast<const __nv_bfloat16 *>(p.b_ptr[a * p.E_B + (p.E_B == 1 ? 0 : e)]);
-        const uint32_t y_bytes = (uint32_t)nrows * nw * 2;
+        const uint32_t y_bytes = run ? 2u * kTcRows * 128 : (uint32_t)nrows * nw * 2;
         const int kgs = rp / 8;
         UnitRec r;
         r.n0 = n0;
@@ -770,6 +793,7 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, i
         r.yoff = yoff;
         r.ystride = ystride / 2;
         r.tc = tc;
+        r.run = run;
         r.scale = p.scale[a];
         if (uw == kTcCols) {
             // 128 output columns = one half of a 256-row B tile: rp/8 runs of 128 x 16 bytes
@@ -779,6 +803,10 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, EngineSmem &sm, i
             for (int kg = 0; kg < kgs; ++kg)
                 bulk_g2s(base + kg * kTcCols * 16, bblk + ((int64_t)(btile * kgs + kg) * kNTile + half * kTcCols) * 8,
                          kTcCols * 16, &sm.bar_es[st]);
+            if (run)
+                for (int h = 0; h < 2; ++h)
+                    tc::tma_tile2d(base + kTcYOff + h * kTcRows * 128, ymap, n0 + 64 * h, sm.row_dst[st][0],
+                                   &sm.bar_es[st]);
         } else {
             // whole 256-row B tiles: one contiguous run
             const int tile0 = p.slice_tile_off[s] + uu * (uw / kNTile);
@@ -929,7 +957,8 @@ __device__ __forceinline__ void tc_unit_mma(EngineSmem &sm, int st, int buf)
 // owns row 32 (w % 4) + lane and 64 columns from 64 (w / 4); the result
 // bf16(y_base + scale * w_row * D) overwrites the staged y row, which then
 // leaves as one bulk store per row.  On return the stage is free again.
-__device__ __noinline__ void tc_unit_epilogue(const EngineParams &p, EngineSmem &sm, int st, int buf)
+__device__ __noinline__ void tc_unit_epilogue(const EngineParams &p, const CUtensorMap *ymap_st, EngineSmem &sm,
+                                              int st, int buf)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const UnitRec r = sm.unit[st];
@@ -938,7 +967,11 @@ __device__ __noinline__ void tc_unit_epilogue(const EngineParams &p, EngineSmem 
     const int cbase = (warp >> 2) * 64;
     const bool live = row < r.nrows;
     const float sc = r.scale * (live ? sm.row_w[st][row] : 0.f);
-    __nv_bfloat16 *ys = reinterpret_cast<__nv_bfloat16 *>(base + r.yoff + row * kTcYStride);
+    // run tiles: rows below nrows rounded down to 32 go back to shared memory for the box stores, the
+    // rest straight to y
+    const int boxed = r.run ? (r.nrows & ~31) : 0;
+    const bool to_smem = !r.run || row < boxed;
+    __nv_bfloat16 *yg = p.y + (int64_t)(live ? sm.row_dst[st][row] : 0) * p.ldy + r.n0;
     const uint32_t acc = sm.tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + kTmemExpandCol + buf * kTcCols;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -950,12 +983,17 @@ __device__ __noinline__ void tc_unit_epilogue(const EngineParams &p, EngineSmem 
             for (int q = 0; q < 4; ++q) {
                 const int c = c0 + 8 * q;
                 if (c < r.nw) {
+                    // padded rows, or 16-byte chunk (c % 64) / 8 of the row swizzled within its 1 KB atom
+                    unsigned char *yp = r.run ? base + r.yoff + (c >> 6) * kTcRows * 128 + row * 128 +
+                                                    ((((c & 63) >> 3) ^ (row & 7)) << 4)
+                                              : base + r.yoff + row * kTcYStride + c * 2;
                     float yf[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(ys + c), yf);
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(yp), yf);
                     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o[e] = __float2bfloat16_rn(fmaf(sc, v[8 * q + e], yf[e]));
-                    *reinterpret_cast<uint4 *>(ys + c) = *reinterpret_cast<const uint4 *>(o);
+                    if (to_smem) *reinterpret_cast<uint4 *>(yp) = *reinterpret_cast<const uint4 *>(o);
+                    else *reinterpret_cast<uint4 *>(yg + c) = *reinterpret_cast<const uint4 *>(o);
                 }
             }
         }
@@ -963,7 +1001,16 @@ __device__ __noinline__ void tc_unit_epilogue(const EngineParams &p, EngineSmem 
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
-    if (tid < r.nrows) {
+    if (r.run) {
+        if (tid == 0 && boxed > 0) {
+            const int row0 = sm.row_dst[st][0];
+            for (int rb = 0; rb < boxed; rb += 32)
+                for (int h = 0; h < 2; ++h)
+                    tc::tma_store2d(ymap_st, r.n0 + 64 * h, row0 + rb, base + r.yoff + h * kTcRows * 128 + rb * 128);
+            bulk_commit();
+            bulk_wait_read();
+        }
+    } else if (tid < r.nrows) {
         bulk_s2g(p.y + (int64_t)sm.row_dst[st][tid] * p.ldy + r.n0, base + r.yoff + tid * kTcYStride,
                  (uint32_t)r.nw * 2);
         bulk_commit();
@@ -1049,12 +1096,12 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
             continue;
         }
         const int rp = gr.x < kRankCache ? sm.rp_cache[gr.x] : p.rpad[gr.x];
-        const bool tc = p.path == 2 || (p.path == 0 && gr.w > p.tc_min_rows);
+        const bool tc = group_on_tc(p, gr.w, p.n_a * rp);
         if (tc) {
             const int tiles = (gr.w + kTcRows - 1) >> 7;
             any_tc = true;
             tcu += tiles * tc_units;
-            tci += tiles * ((p.K + kTcKc - 1) >> 9);
+            tci += tiles;
         } else {
             const int tiles = (gr.w + kBgmvRows - 1) >> 4;
             bga += (long long)tiles * p.n_a * rp;
@@ -1074,20 +1121,28 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     // small-tile chunks of about a CTA's share of the A bytes (a quarter more, so that rounding up to
     // whole chunks rarely needs a second wave); expand units of about 2/5 of a CTA's B share
     Plan pl;
+    // 128-row tile K-chunks of kTcKc; when that would make between one and two waves of shrink items
+    // (some CTAs with two, most with one), chunks just long enough for one wave instead
+    const int kmax = (p.K + 63) & ~63;
+    int kctc = kTcKc;
+    if (tci > 0 && tci * ((p.K + kTcKc - 1) / kTcKc) < 2 * grid) {
+        const int nk = max(1, grid / tci);
+        kctc = min(kmax, max(kTcKc, ((p.K + nk - 1) / nk + 63) & ~63));
+    }
+    tci *= (p.K + kctc - 1) / kctc;   // 128-row tile shrink items
     const int spare = max(grid / 4, grid - tci);
     pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, 1.25f * 2.f * (float)p.K * (float)bga / spare));
     pl.tb = (int)fminf(268435456.f, fmaxf(4096.f, 2.f * (float)N * (float)bgb / (2.5f * grid)));
-    pl.ue = min(128, 1 << ceil_log2(max(1, (tcu + kItemsPerCta * grid - 1) / (kItemsPerCta * grid))));
-    pl.kctc = kTcKc;
+    pl.ue = min(128, max(1, (tcu + kItemsPerCta * grid - 1) / (kItemsPerCta * grid)));
+    pl.kctc = kctc;
     // small-tile expand units of the launch -> units per item, so that the items fit one wave
     {
         int units = 0;
 #pragma unroll 1
         for (int g = lane; g < G; g += 32) {
             const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
-            const bool tc = p.path == 2 || (p.path == 0 && gr.w > p.tc_min_rows);
-            if (tc) continue;
             const int rp = gr.x < kRankCache ? sm.rp_cache[gr.x] : p.rpad[gr.x];
+            if (group_on_tc(p, gr.w, p.n_a * rp)) continue;
             const int uw = sm_unit_width(rp, min(gr.w, kSmRows), pl.tb);
             int u = 0;
 #pragma unroll 1
@@ -1102,41 +1157,44 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     // until the hand-off scratch fits the workspace
 #pragma unroll 1
     for (int iter = 0; iter < 8; ++iter) {
-        int c_sh = 0, c_fin = 0, c_ex = 0, c_tile = 0;
+        int c_sh = 0, c_shs = 0, c_fin = 0, c_ex = 0, c_tile = 0;
         long long c_part = 0;
 #pragma unroll 1
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
-            int v_sh = 0, v_fin = 0, v_ex = 0, v_tile = 0;
+            int v_sh = 0, v_shs = 0, v_fin = 0, v_ex = 0, v_tile = 0;
             long long v_part = 0;
             if (g < G) {
                 const GroupDims d = group_dims_calc(p, sm, g, pl);
-                v_sh = d.tiles * d.n_kc;
+                (d.tc ? v_sh : v_shs) = d.tiles * d.n_kc;
                 v_fin = d.fins;
                 v_ex = d.tiles * d.ipt;
                 v_tile = d.tiles;
                 v_part = d.scratch;
                 if (g < kGroupCache) sm.gdim[g] = pack_dims(d);
             }
-            int i_sh = v_sh, i_fin = v_fin, i_ex = v_ex, i_tile = v_tile;
+            int i_sh = v_sh, i_shs = v_shs, i_fin = v_fin, i_ex = v_ex, i_tile = v_tile;
             long long i_part = v_part;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int a = __shfl_up_sync(0xffffffffu, i_sh, o), b = __shfl_up_sync(0xffffffffu, i_fin, o);
                 const int c = __shfl_up_sync(0xffffffffu, i_ex, o), e = __shfl_up_sync(0xffffffffu, i_tile, o);
                 const long long f = __shfl_up_sync(0xffffffffu, i_part, o);
+                const int h = __shfl_up_sync(0xffffffffu, i_shs, o);
                 if (lane >= o) {
-                    i_sh += a; i_fin += b; i_ex += c; i_tile += e; i_part += f;
+                    i_sh += a; i_fin += b; i_ex += c; i_tile += e; i_part += f; i_shs += h;
                 }
             }
             if (g < G) {
                 sm.sh_pre[g] = c_sh + i_sh - v_sh;
+                sm.shs_pre[g] = c_shs + i_shs - v_shs;
                 sm.fin_pre[g] = c_fin + i_fin - v_fin;
                 sm.ex_pre[g] = c_ex + i_ex - v_ex;
                 sm.tile_pre[g] = c_tile + i_tile - v_tile;
                 sm.part_pre[g] = (int)min(c_part + i_part - v_part, (long long)INT32_MAX);
             }
             c_sh += __shfl_sync(0xffffffffu, i_sh, 31);
+            c_shs += __shfl_sync(0xffffffffu, i_shs, 31);
             c_fin += __shfl_sync(0xffffffffu, i_fin, 31);
             c_ex += __shfl_sync(0xffffffffu, i_ex, 31);
             c_tile += __shfl_sync(0xffffffffu, i_tile, 31);
@@ -1144,6 +1202,7 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
         }
         if (lane == 0) {
             sm.sh_pre[G] = c_sh;
+            sm.shs_pre[G] = c_shs;
             sm.fin_pre[G] = c_fin;
             sm.ex_pre[G] = c_ex;
             sm.tile_pre[G] = c_tile;
@@ -1219,7 +1278,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         return;
     }
     const bool use_tc = sm.flag == 2;
-    const int n_shrink = sm.sh_pre[G], n_fin = sm.fin_pre[G], n_expand = sm.ex_pre[G];
+    const int n_sh_tc = sm.sh_pre[G], n_sh_sm = sm.shs_pre[G];
+    const int n_shrink = n_sh_tc + n_sh_sm, n_fin = sm.fin_pre[G], n_expand = sm.ex_pre[G];
     if (sm.tile_pre[G] > p.max_tiles || (int64_t)sm.part_pre[G] > p.partial_floats ||
         sm.part_pre[G] == INT32_MAX) {
         if (b == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
@@ -1242,8 +1302,24 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     int issued = 0;          // expand units put in flight
     bool alive = true;
 
-    // this CTA's items: shrink b, b + grid, ...; then finish and expand items dealt on from where the
-    // previous kind stopped, so CTAs with fewer shrink items take the next kind first
+    // this CTA's items, each kind dealt on from where the previous one stopped (so CTAs with less of one
+    // kind take the next first): 128-row tile shrink items b, b + grid, ...; small-tile shrink items;
+    // finish items; expand items
+    const int my_tc = b < n_sh_tc ? (n_sh_tc - b + grid - 1) / grid : 0;
+    const int s0 = ((b - n_sh_tc) % grid + grid) % grid;
+    const int my_shrink = my_tc + (s0 < n_sh_sm ? (n_sh_sm - s0 + grid - 1) / grid : 0);
+    // the CTA's j-th shrink item: group and index within the group
+    auto shrink_item = [&](int j, int &g, int &local) {
+        if (j < my_tc) {
+            const int t = b + j * grid;
+            g = find_group(sm.sh_pre, G, t);
+            local = t - sm.sh_pre[g];
+        } else {
+            const int u = s0 + (j - my_tc) * grid;
+            g = find_group(sm.shs_pre, G, u);
+            local = u - sm.shs_pre[g];
+        }
+    };
     const int f0 = ((b - n_shrink) % grid + grid) % grid;
     const int e0 = ((b - n_shrink - n_fin) % grid + grid) % grid;
     // the expand issuer starts at item e0; expand units may be in flight while the shrink items run:
@@ -1257,9 +1333,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     auto setup_issuer = [&]() {
         iss_item = e0;
         if (e0 < n_expand) iss_it = decode_expand(p, sm, pl, G, e0);
-#pragma unroll 1
-        for (int item = b; item < n_shrink; item += grid)
-            npre = min(npre, group_dims(p, sm, find_group(sm.sh_pre, G, item), pl).tc ? 1 : 2);
+        if (my_tc > 0) npre = 1;
+        else if (my_shrink > 0) npre = 2;
         iss_ready = true;
     };
     // put units in flight until `upto` have been issued (units must have left stage (upto - 1) % 3)
@@ -1267,8 +1342,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         while (issued < upto && iss_item < n_expand) {
             inflight |= 1u << (issued % kEsDepth);
             const GroupDims &d = iss_it.d;
-            issue_unit(p, sm, issued++, iss_it.s, iss_it.u0 + iss_k, iss_it.nrows, d.rows_off + iss_it.r0,
-                       iss_k == 0, d.a, d.e, d.rp, d.uw, d.tc);
+            issue_unit(p, &pk.y_map_ld, sm, issued++, iss_it.s, iss_it.u0 + iss_k, iss_it.nrows,
+                       d.rows_off + iss_it.r0, iss_k == 0, d.a, d.e, d.rp, d.uw, d.tc);
             if (++iss_k == iss_it.nu) {
                 iss_k = 0;
                 iss_item += grid;
@@ -1278,13 +1353,13 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     };
 
     // ------------------------------------------------------------------ shrink items
-    for (int item = b; item < n_shrink && alive; item += grid) {
-        const int g = find_group(sm.sh_pre, G, item);
+    for (int j = 0; j < my_shrink && alive; ++j) {
+        int g, local;
+        shrink_item(j, g, local);
         const GroupDims d = group_dims(p, sm, g, pl);
-        const int local = item - sm.sh_pre[g];
         const int tile = local / d.n_kc, chunk = local % d.n_kc;
         const int tg = sm.tile_pre[g] + tile;
-        const bool first = item == b;
+        const bool first = j == 0;
         if (first) stamp(p, TS_SH_START);
         bool ok;
         if (d.tc) {
@@ -1327,7 +1402,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         if (!cta_wait(&sm.bar_mmae[buf], ph.get(PH_MMAE + buf), p)) return false;
         ph.flip(PH_MMAE + buf);
         tc::fence_after_sync();
-        tc_unit_epilogue(p, sm, st, buf);
+        tc_unit_epilogue(p, &pk.y_map_st, sm, st, buf);
         if (q < 4) stamp(p, TS_EX_UNIT + 2 * q + 1);
         pend = -1;
         prefetch(q + 1 + kEsDepth);

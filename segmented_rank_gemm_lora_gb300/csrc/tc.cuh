@@ -54,6 +54,15 @@ __device__ __forceinline__ void tma_tile2d(void *dst_smem, const void *tmap, int
         : "memory");
 }
 
+// 2-D TMA tile store (box from the tensor map) of src_smem to (col, row), in this
+// thread's bulk group.  Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store2d(const void *tmap, int col, int row, const void *src_smem)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(col),
+                 "r"(row), "r"(smem_u32(src_smem))
+                 : "memory");
+}
+
 // Instruction descriptor for kind::f16: D fp32, A and B bf16, both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
