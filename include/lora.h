@@ -295,7 +295,7 @@ lora_status lora_set_trace(void *d_trace, size_t bytes);
  * library holds until the process exits.  Limits: M <= 4096 tokens, and
  * R * (M * (ceil(K / kc) + 1) + 64 * min(M, L)) <= 2^21 partial floats, where
  * R is the table's largest A block (n_a * stored rank) and kc = clamp(floor(
- * 20480 / R) rounded down to a multiple of 64, 64, 512), the smallest K-chunk
+ * 20480 / R) rounded down to a multiple of 64, 64, 448), the smallest K-chunk
  * the engine falls back to; larger calls return LORA_ERR_WORKSPACE before
  * launching anything.  Same argument rules as lora_apply (dense tables only).
  *

@@ -429,11 +429,11 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
                               const float *row_weight, lora_stream_t stream)
 {
     // scratch needed per row of work at this table's largest A block, at the largest K-chunk of a
-    // 16-row small tile (x rows <= 16 KB, A chunk <= 40 KB), plus the row's finished S
+    // 16-row small tile (x rows <= 15 KB, A chunk <= 40 KB), plus the row's finished S
     {
         const int64_t R = t->max_R;
         int64_t kc = (20480 / R) / 64 * 64;
-        kc = std::max<int64_t>(64, std::min<int64_t>(512, kc));
+        kc = std::max<int64_t>(64, std::min<int64_t>(448, kc));
         if ((ceil_div(t->K, kc) + 1) * R > kPartialFloatsPerRow) return LORA_ERR_UNSUPPORTED;
     }
     DeviceInfo di;
@@ -676,12 +676,12 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
         return LORA_ERR_INVALID_ARG;
     if (M > kStaticMaxM) return LORA_ERR_WORKSPACE;
     // the hand-off scratch of M rows at this table's largest A block must fit the fixed array even at
-    // the largest K-chunks the engine picks when scratch is short (16-row tiles: x rows <= 16 KB,
+    // the largest K-chunks the engine picks when scratch is short (16-row tiles: x rows <= 15 KB,
     // A chunk <= 40 KB), plus the finished S of every tile
     {
         const int64_t R = t->max_R;
         int64_t kc = (20480 / R) / 64 * 64;
-        kc = std::max<int64_t>(64, std::min<int64_t>(512, kc));
+        kc = std::max<int64_t>(64, std::min<int64_t>(448, kc));
         const int64_t need = R * ((int64_t)M * (ceil_div(t->K, kc) + 1) + 64 * std::min<int64_t>(M, t->L));
         if (need > kStaticPartialFloats) return LORA_ERR_WORKSPACE;
     }

@@ -52,14 +52,15 @@ constexpr int kStageBytes = 50 * 1024;
 constexpr int kEsDepth = 3;
 constexpr int kSBytes = 16 * 1024;
 constexpr int kPool = kSBytes + kEsDepth * kStageBytes;
-constexpr int kBgShrinkBytes = kPool - 2 * kStageBytes;   // small-tile shrink leaves stages 0 and 1 alone
-constexpr int kTcShrinkBytes = kPool - kStageBytes;       // tensor-core shrink leaves stage 0 alone
+constexpr int kTcShrinkBytes = kPool - kStageBytes;       // the shrink staging leaves expand stage 0 alone
 // small tiles (at most 16 rows): warp-level MMAs (m16n8k16), the tile's tokens as M
 constexpr int kSmRows = kBgmvRows;              // token rows of a small tile
-constexpr int kSmABytes = 40 * 1024;            // A chunk staging at 0: [kc/8][R][8]
+// two staging slots (the next item's operands land while this one computes), then the cross-warp sums
+constexpr int kSmSlotBytes = 55 * 1024;
+constexpr int kSmABytes = 40 * 1024;            // A chunk at the slot's start: [kc/8][R][8]
 constexpr int kSmXOff = kSmABytes;              // x rows after it: [rows][kc + 8] (padded rows)
-constexpr int kSmXBytes = 16 * 1024;
-constexpr int kSmRedOff = kSmXOff + kSmXBytes;  // cross-warp sums of the shrink: [3][16][32] fp32 at most
+constexpr int kSmXBytes = kSmSlotBytes - kSmABytes;
+constexpr int kSmRedOff = 2 * kSmSlotBytes;     // cross-warp sums of the shrink: [3][16][32] fp32 at most
 constexpr int kSmMaxUnit = 1024;                // output columns of one small expand unit, at most
 constexpr int kSmSStride = kMaxRank + 8;        // bf16 per row of S in shared memory (padded rows)
 constexpr int64_t kDirectLoads = 128 * 1024;    // partial loads of a tile's expand items below which they sum them
@@ -76,7 +77,7 @@ constexpr int kTcYOff = 16 * 1024;              // tensor-core stage: B [rp/8][1
 constexpr int kTcYStride = kTcCols * 2 + 16;    // padded rows: a warp (one row per lane) hits every bank group
 constexpr int kItemsPerCta = 2;                 // 128-row tile expand items per CTA the plan aims for
 static_assert(kTcYOff + kTcRows * kTcYStride <= kStageBytes, "tensor-core expand stage");
-static_assert(kSmRedOff + 3 * 16 * 32 * 4 <= kBgShrinkBytes, "small-tile shrink staging");
+static_assert(kSmRedOff + 3 * 16 * 32 * 4 <= kTcShrinkBytes, "small-tile shrink staging");
 static_assert(kSBytes >= (kMaxRank / 8) * kTcRows * 16, "S area");
 static_assert(sizeof(EngineParams) % 4 == 0, "parameter mirror");
 
@@ -121,7 +122,7 @@ struct ExpandItem {
 
 struct __align__(1024) EngineSmem {
     __align__(1024) unsigned char pool[kPool];
-    uint64_t bar_shrink;                 // small-tile shrink copies
+    uint64_t bar_sh[2];                  // small-tile shrink copies, per staging slot
     uint64_t bar_es[kEsDepth];           // expand stage copies
     uint64_t bar_s;                      // tensor-core expand: S copy
     uint64_t bar_stage[kTcMaxDepth];     // tensor-core shrink stage landed
@@ -309,7 +310,8 @@ struct Phases {
     __device__ __forceinline__ void flip(int b) { bits ^= 1u << b; }
 };
 enum { PH_SHRINK = 0, PH_ES = 1 /* 3 bits */, PH_S = 4, PH_STAGE = 5 /* 4 bits */, PH_MMA = 9 /* 4 bits */,
-       PH_MMAE = 13 /* 2 bits */ };
+       PH_MMAE = 13 /* 2 bits */, PH_SHRINK1 = 15 };
+__device__ __forceinline__ int ph_shrink(int slot) { return slot ? PH_SHRINK1 : PH_SHRINK; }
 
 // ===========================================================================
 // shrink items, small tiles (at most 16 rows)
@@ -349,50 +351,55 @@ __device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1,
                  : "r"(a0), "r"(a1), "r"(b0));
 }
 
-// Put the item's A chunk ([kw/8][R][8], one run of the packed table) and its
-// x rows (one bulk copy per row into padded rows of kc + 8 elements) in flight
-// on bar_shrink.
-__device__ __forceinline__ BgShrink sm_shrink_issue(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
-                                                    int tile, int chunk)
+__device__ __forceinline__ BgShrink sm_shrink_desc(const EngineParams &p, const GroupDims &d, int tile, int chunk)
 {
     BgShrink b;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     b.r0 = tile * kSmRows;
     b.nrows = min(kSmRows, d.count - b.r0);
     b.k0 = chunk * d.kc;
     b.kw = min(d.kc, p.K - b.k0);
+    return b;
+}
+
+// Put the item's A chunk ([kw/8][R][8], one run of the packed table) and its
+// x rows (one bulk copy per row into padded rows of kc + 8 elements) in flight
+// into staging slot `slot`, on bar_sh[slot].
+__device__ __forceinline__ void sm_shrink_issue(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
+                                                const BgShrink &b, int slot)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned char *base = sm.pool + slot * kSmSlotBytes;
+    uint64_t *bar = &sm.bar_sh[slot];
     const uint32_t x_bytes = (uint32_t)b.kw * 2;
     if (tid == 0) {
         const __nv_bfloat16 *ablk =
             reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)]);
         const uint32_t a_bytes = (uint32_t)(b.kw / 8) * d.R * 16;
-        mbar_arrive_expect_tx(&sm.bar_shrink, a_bytes + b.nrows * x_bytes);
-        bulk_g2s(sm.pool, ablk + (int64_t)(b.k0 / 8) * d.R * 8, a_bytes, &sm.bar_shrink);
+        mbar_arrive_expect_tx(bar, a_bytes + b.nrows * x_bytes);
+        bulk_g2s(base, ablk + (int64_t)(b.k0 / 8) * d.R * 8, a_bytes, bar);
     }
     if (warp == 1 && lane < b.nrows) {
         const int src = p.rows[d.rows_off + b.r0 + lane] / p.src_div;
-        bulk_g2s(sm.pool + kSmXOff + (size_t)lane * (d.kc * 2 + 16), p.x + (int64_t)src * p.ldx + b.k0, x_bytes,
-                 &sm.bar_shrink);
+        bulk_g2s(base + kSmXOff + (size_t)lane * (d.kc * 2 + 16), p.x + (int64_t)src * p.ldx + b.k0, x_bytes, bar);
     }
-    return b;
 }
 
 // Form the fp32 partial X_rows A_chunk^T (operands in place) with
 // m16n8k16 MMAs (rows past the tile read row 0; their results are dropped).
 // Warp w takes 8-column tiles of the partial; when there are fewer than
 // eight tiles, the warps of a tile split K and meet in shared memory in a
-// fixed order.  Each warp keeps two accumulators (even and odd K steps) and
-// adds them at the end, so the summation order is fixed.
-__device__ __forceinline__ bool sm_shrink_wait(const EngineParams &p, EngineSmem &sm, Phases &ph, bool first)
+// fixed order.  Each warp keeps four accumulators (K steps in fours) and adds
+// them at the end, so the summation order is fixed by the sizes alone.
+__device__ __forceinline__ bool sm_shrink_wait(const EngineParams &p, EngineSmem &sm, Phases &ph, int slot, bool first)
 {
-    if (!cta_wait(&sm.bar_shrink, ph.get(PH_SHRINK), p)) return false;
-    ph.flip(PH_SHRINK);
+    if (!cta_wait(&sm.bar_sh[slot], ph.get(ph_shrink(slot)), p)) return false;
+    ph.flip(ph_shrink(slot));
     if (first) stamp(p, TS_SH_STAGE);
     return true;
 }
 
 __device__ __forceinline__ void sm_shrink_run(const EngineParams &p, EngineSmem &sm, const GroupDims &d,
-                                              const BgShrink &b, int g, int chunk, bool first)
+                                              const BgShrink &b, int g, int chunk, int slot, bool first)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int R = d.R;
@@ -400,9 +407,9 @@ __device__ __forceinline__ void sm_shrink_run(const EngineParams &p, EngineSmem 
     const int ksplit = ntiles >= 8 ? 1 : 8 / ntiles;
     const int kgs = b.kw / 8, steps = (kgs + 1) / 2;
     const int xstride = d.kc * 2 + 16;
-    const uint32_t a_base = smem_u32(sm.pool);
+    const uint32_t a_base = smem_u32(sm.pool + slot * kSmSlotBytes);
     const int xrow = (lane & 15) < b.nrows ? (lane & 15) : 0;
-    const uint32_t x_base = smem_u32(sm.pool + kSmXOff) + xrow * xstride;
+    const uint32_t x_base = a_base + kSmXOff + xrow * xstride;
     float *red = reinterpret_cast<float *>(sm.pool + kSmRedOff);   // [ksplit - 1][16][R]
     float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * b.r0 * R + (int64_t)chunk * b.nrows * R;
     const int gr = lane >> 2, qc = (lane & 3) * 2;
@@ -412,27 +419,34 @@ __device__ __forceinline__ void sm_shrink_run(const EngineParams &p, EngineSmem 
         const int nt = nt0 + warp % min(ntiles, 8);
         const bool act = nt < ntiles && kpart < ksplit;
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        float d2[4] = {0.f, 0.f, 0.f, 0.f}, d3[4] = {0.f, 0.f, 0.f, 0.f};
         if (act) {
             const uint32_t a_row = a_base + (nt * 8 + (lane & 7)) * 16;
-#pragma unroll 2
-            for (int st = s_lo; st < s_hi; ++st) {
-                if (2 * st + 1 < kgs) {
-                    uint32_t a0, a1, a2, a3, b0, b1;
-                    ldsm_x4(x_base + (2 * st + (lane >> 4)) * 16, a0, a1, a2, a3);
-                    ldsm_x2(a_row + (2 * st + ((lane >> 3) & 1)) * R * 16, b0, b1);
-                    if (st & 1) mma16816(d1, a0, a1, a2, a3, b0, b1);
-                    else mma16816(d0, a0, a1, a2, a3, b0, b1);
-                } else {   // a last odd K-group: one k8 step
-                    uint32_t a0, a1, b0;
-                    ldsm_x2(x_base + (2 * st) * 16, a0, a1);
-                    ldsm_x1(a_row + (2 * st) * R * 16, b0);
-                    if (st & 1) mma1688(d1, a0, a1, b0);
-                    else mma1688(d0, a0, a1, b0);
-                }
+            auto full_step = [&](int st, float (&d)[4]) {
+                uint32_t a0, a1, a2, a3, b0, b1;
+                ldsm_x4(x_base + (2 * st + (lane >> 4)) * 16, a0, a1, a2, a3);
+                ldsm_x2(a_row + (2 * st + ((lane >> 3) & 1)) * R * 16, b0, b1);
+                mma16816(d, a0, a1, a2, a3, b0, b1);
+            };
+            // four independent accumulators over K steps st, st + 1, st + 2, st + 3
+            const int full_hi = min(s_hi, kgs / 2);   // steps with both of their K-groups present
+            int st = s_lo;
+            for (; st + 3 < full_hi; st += 4) {
+                full_step(st, d0);
+                full_step(st + 1, d1);
+                full_step(st + 2, d2);
+                full_step(st + 3, d3);
+            }
+            for (; st < full_hi; ++st) full_step(st, d0);
+            if (s_hi > full_hi && full_hi >= s_lo) {   // a last odd K-group: one k8 step
+                uint32_t a0, a1, b0;
+                ldsm_x2(x_base + (2 * full_hi) * 16, a0, a1);
+                ldsm_x1(a_row + (2 * full_hi) * R * 16, b0);
+                mma1688(d0, a0, a1, b0);
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) d0[q] += d1[q];
+        for (int q = 0; q < 4; ++q) d0[q] += (d1[q] + d2[q]) + d3[q];
         const int col = nt * 8 + qc;
         if (ksplit > 1) {   // K slices 1.. hand their sums to slice 0
             if (act && kpart > 0) {
@@ -1242,7 +1256,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         sm.G = *pk.num_groups;
         sm.x_total = *pk.m_ptr * pk.m_mult;
         sm.flag = 0;
-        mbar_init(&sm.bar_shrink, 1);
+        mbar_init(&sm.bar_sh[0], 1);
+        mbar_init(&sm.bar_sh[1], 1);
         for (int i = 0; i < kEsDepth; ++i) mbar_init(&sm.bar_es[i], 1);
         mbar_init(&sm.bar_s, 1);
         for (int i = 0; i < kTcMaxDepth; ++i) {
@@ -1333,7 +1348,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     auto setup_issuer = [&]() {
         iss_item = e0;
         if (e0 < n_expand) iss_it = decode_expand(p, sm, pl, G, e0);
-        if (my_tc > 0) npre = 1;
+        if (my_tc > 0 || my_shrink > 1) npre = 1;   // the shrink staging reaches into stage 1
         else if (my_shrink > 0) npre = 2;
         iss_ready = true;
     };
@@ -1353,6 +1368,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     };
 
     // ------------------------------------------------------------------ shrink items
+    uint32_t sh_inflight = 0;   // small-tile staging slots whose copies have not been waited for
     for (int j = 0; j < my_shrink && alive; ++j) {
         int g, local;
         shrink_item(j, g, local);
@@ -1370,10 +1386,25 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
             }
             ok = tc_shrink_run(p, &pk.x_map, sm, d, t, g, chunk, ph, first);
         } else {
-            const BgShrink bs = sm_shrink_issue(p, sm, d, tile, chunk);
+            // small tiles alternate between two staging slots: the next item's operands are put in flight
+            // before this one's are waited for
+            const int slot = (j - my_tc) & 1;
+            const BgShrink bs = sm_shrink_desc(p, d, tile, chunk);
+            if (j == my_tc) {
+                sm_shrink_issue(p, sm, d, bs, slot);
+                sh_inflight |= 1u << slot;
+            }
             if (first) setup_issuer();
-            ok = sm_shrink_wait(p, sm, ph, first);
-            if (ok) sm_shrink_run(p, sm, d, bs, g, chunk, first);
+            if (j + 1 < my_shrink) {
+                int g2, local2;
+                shrink_item(j + 1, g2, local2);
+                const GroupDims d2 = group_dims(p, sm, g2, pl);
+                sm_shrink_issue(p, sm, d2, sm_shrink_desc(p, d2, local2 / d2.n_kc, local2 % d2.n_kc), slot ^ 1);
+                sh_inflight |= 1u << (slot ^ 1);
+            }
+            ok = sm_shrink_wait(p, sm, ph, slot, first);
+            sh_inflight &= ~(1u << slot);
+            if (ok) sm_shrink_run(p, sm, d, bs, g, chunk, slot, first);
         }
         if (!ok) {
             alive = false;
@@ -1449,6 +1480,9 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     if (alive && pend >= 0 && !drain()) alive = false;
 
     // a CTA that gave up still lets its copies land and its MMAs finish before it leaves
+    for (int sl = 0; sl < 2; ++sl)
+        if (sh_inflight & (1u << sl))
+            mbar_wait_bounded(&sm.bar_sh[sl], ph.get(ph_shrink(sl)), p.timeout_ns, p.err);
     for (int st = 0; st < kEsDepth; ++st)
         if (inflight & (1u << st)) mbar_wait_bounded(&sm.bar_es[st], ph.get(PH_ES + st), p.timeout_ns, p.err);
     if (pend >= 0) mbar_wait_bounded(&sm.bar_mmae[pend & 1], ph.get(PH_MMAE + (pend & 1)), p.timeout_ns, p.err);
