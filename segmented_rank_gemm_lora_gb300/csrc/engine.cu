@@ -904,7 +904,7 @@ __device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm
 
 // Small-tile unit in stage st: D[16][nw] = S B_unit^T with m16n8k16 MMAs
 // (tokens as M, 8 output columns per MMA tile, warp w takes column tiles
-// w, w + 8, ...), then y = bf16(y_base + scale * w_row * D) for the tile's
+// w, w + 8, ..., four at a time), then y = bf16(y_base + scale * w_row * D) for the tile's
 // rows, two columns per store.  Ends with a barrier: the stage is free again.
 __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int st)
 {
@@ -924,29 +924,43 @@ __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int 
 #pragma unroll
     for (int k = 0; k < kMaxRank / 16; ++k)
         if (k < steps) ldsm_x4(s_row + (2 * k + (lane >> 4)) * 16, sa[k][0], sa[k][1], sa[k][2], sa[k][3]);
-    for (int nt = warp; nt < ntiles; nt += 8) {
-        const int n = nt * 8, tl = n / r.tw, col = n % r.tw;
-        // B rows n .. n + 7 of K-group kg: [(tl * kgs + kg) * tw + col] in 16-byte units
-        const uint32_t b_row = b_base + ((tl * r.kgs) * r.tw + col + (lane & 7)) * 16;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+    const int twl = r.tw == kNTile ? 8 : 7;   // log2 of the B tile width (256 rows, or a 128-row half)
+    // four column tiles per round (w, w + 8, w + 16, w + 24), their MMAs interleaved
+    for (int nt0 = warp; nt0 < ntiles; nt0 += 32) {
+        float d[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
 #pragma unroll
         for (int k = 0; k < kMaxRank / 16; ++k) {
             if (k < steps) {
-                uint32_t b0, b1;
-                ldsm_x2(b_row + (2 * k + ((lane >> 3) & 1)) * r.tw * 16, b0, b1);
-                mma16816(d, sa[k][0], sa[k][1], sa[k][2], sa[k][3], b0, b1);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int n = (nt0 + 8 * i) * 8;
+                    if (n < r.nw) {
+                        // B rows n .. n + 7 of K-group kg: [(tl * kgs + kg) * tw + col] in 16-byte units
+                        const int tl = n >> twl, col = n & (r.tw - 1);
+                        uint32_t b0, b1;
+                        ldsm_x2(b_base + ((tl * r.kgs + 2 * k + ((lane >> 3) & 1)) * r.tw + col + (lane & 7)) * 16,
+                                b0, b1);
+                        mma16816(d[i], sa[k][0], sa[k][1], sa[k][2], sa[k][3], b0, b1);
+                    }
+                }
             }
         }
-        const int c = n + qc;
-        if (gr < r.nrows) {
-            const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162 *>(ys + gr * r.ystride + c);
-            *reinterpret_cast<__nv_bfloat162 *>(y0 + c) = __floats2bfloat162_rn(
-                fmaf(s0, d[0], __bfloat162float(yb.x)), fmaf(s0, d[1], __bfloat162float(yb.y)));
-        }
-        if (gr + 8 < r.nrows) {
-            const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162 *>(ys + (gr + 8) * r.ystride + c);
-            *reinterpret_cast<__nv_bfloat162 *>(y1 + c) = __floats2bfloat162_rn(
-                fmaf(s1, d[2], __bfloat162float(yb.x)), fmaf(s1, d[3], __bfloat162float(yb.y)));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = (nt0 + 8 * i) * 8 + qc;
+            if (c >= r.nw) continue;
+            if (gr < r.nrows) {
+                const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162 *>(ys + gr * r.ystride + c);
+                *reinterpret_cast<__nv_bfloat162 *>(y0 + c) = __floats2bfloat162_rn(
+                    fmaf(s0, d[i][0], __bfloat162float(yb.x)), fmaf(s0, d[i][1], __bfloat162float(yb.y)));
+            }
+            if (gr + 8 < r.nrows) {
+                const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162 *>(ys + (gr + 8) * r.ystride + c);
+                *reinterpret_cast<__nv_bfloat162 *>(y1 + c) = __floats2bfloat162_rn(
+                    fmaf(s1, d[i][2], __bfloat162float(yb.x)), fmaf(s1, d[i][3], __bfloat162float(yb.y)));
+            }
         }
     }
     __syncthreads();
