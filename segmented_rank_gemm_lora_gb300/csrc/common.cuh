@@ -16,7 +16,7 @@ namespace lora {
 // ---------------------------------------------------------------------------
 constexpr int kMaxRank = 64;           // largest true rank
 constexpr int kMaxSlices = 4;
-constexpr int kNTile = 256;            // B is stored in tiles of 256 output rows
+constexpr int kNTile = 128;            // B is stored in tiles of 128 output rows
 constexpr int kBgmvRows = 16;          // rows of one small tile
 constexpr int kEngineThreads = 256;
 constexpr int kHeaderInts = 16;

@@ -809,27 +809,17 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, const CUtensorMap
         r.tc = tc;
         r.run = run;
         r.scale = p.scale[a];
-        if (uw == kTcCols) {
-            // 128 output columns = one half of a 256-row B tile: rp/8 runs of 128 x 16 bytes
-            const int btile = p.slice_tile_off[s] + uu / 2, half = uu & 1;
-            r.tw = kTcCols;
-            mbar_arrive_expect_tx(&sm.bar_es[st], (uint32_t)kgs * kTcCols * 16 + y_bytes);
-            for (int kg = 0; kg < kgs; ++kg)
-                bulk_g2s(base + kg * kTcCols * 16, bblk + ((int64_t)(btile * kgs + kg) * kNTile + half * kTcCols) * 8,
-                         kTcCols * 16, &sm.bar_es[st]);
-            if (run)
-                for (int h = 0; h < 2; ++h)
-                    tc::tma_tile2d(base + kTcYOff + h * kTcRows * 128, ymap, n0 + 64 * h, sm.row_dst[st][0],
-                                   &sm.bar_es[st]);
-        } else {
-            // whole 256-row B tiles: one contiguous run
-            const int tile0 = p.slice_tile_off[s] + uu * (uw / kNTile);
-            const int ntl = (nw + kNTile - 1) / kNTile;
-            const uint32_t b_bytes = (uint32_t)ntl * kNTile * rp * 2;
-            r.tw = kNTile;
-            mbar_arrive_expect_tx(&sm.bar_es[st], b_bytes + y_bytes);
-            bulk_g2s(base, bblk + (int64_t)tile0 * kNTile * rp, b_bytes, &sm.bar_es[st]);
-        }
+        // the unit's 128-row B tiles are consecutive in the packed block: one bulk copy
+        const int tile0 = p.slice_tile_off[s] + uu * (uw / kNTile);
+        const int ntl = (nw + kNTile - 1) / kNTile;
+        const uint32_t b_bytes = (uint32_t)ntl * kNTile * rp * 2;
+        r.tw = kNTile;
+        mbar_arrive_expect_tx(&sm.bar_es[st], b_bytes + y_bytes);
+        bulk_g2s(base, bblk + (int64_t)tile0 * kNTile * rp, b_bytes, &sm.bar_es[st]);
+        if (run)
+            for (int h = 0; h < 2; ++h)
+                tc::tma_tile2d(base + kTcYOff + h * kTcRows * 128, ymap, n0 + 64 * h, sm.row_dst[st][0],
+                               &sm.bar_es[st]);
         sm.unit[st] = r;
     }
 }
@@ -924,7 +914,6 @@ __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int 
 #pragma unroll
     for (int k = 0; k < kMaxRank / 16; ++k)
         if (k < steps) ldsm_x4(s_row + (2 * k + (lane >> 4)) * 16, sa[k][0], sa[k][1], sa[k][2], sa[k][3]);
-    const int twl = r.tw == kNTile ? 8 : 7;   // log2 of the B tile width (256 rows, or a 128-row half)
     // four column tiles per round (w, w + 8, w + 16, w + 24), their MMAs interleaved
     for (int nt0 = warp; nt0 < ntiles; nt0 += 32) {
         float d[4][4];
@@ -938,7 +927,7 @@ __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int 
                     const int n = (nt0 + 8 * i) * 8;
                     if (n < r.nw) {
                         // B rows n .. n + 7 of K-group kg: [(tl * kgs + kg) * tw + col] in 16-byte units
-                        const int tl = n >> twl, col = n & (r.tw - 1);
+                        const int tl = n / kNTile, col = n % kNTile;
                         uint32_t b0, b1;
                         ldsm_x2(b_base + ((tl * r.kgs + 2 * k + ((lane >> 3) & 1)) * r.tw + col + (lane & 7)) * 16,
                                 b0, b1);

@@ -13,11 +13,12 @@
 // in the no-swizzle canonical tcgen05 layout (core matrix = 8 rows x 16 bytes;
 // rows 16 bytes apart, K core matrices n_a*rpad*16 bytes apart).
 //
-// Packed B (one block): for each slice s, ceil(N_s/256) tiles of
-// [rpad/8][256][8]: element B[off_s + n][j] sits in tile n/256 of the slice at
-// ((j/8) * 256 + n%256) * 8 + j%8.  Rows past N_s and columns past r are zero.
-// Each tile is contiguous, the 16-byte vector of one row holds eight
-// consecutive j, and a tile is a K-major canonical operand for the expand.
+// Packed B (one block): for each slice s, ceil(N_s/128) tiles of
+// [rpad/8][128][8]: element B[off_s + n][j] sits in tile n/128 of the slice at
+// ((j/8) * 128 + n%128) * 8 + j%8.  Rows past N_s and columns past r are zero.
+// Each tile is contiguous (a run of consecutive tiles is one bulk copy), the
+// 16-byte vector of one row holds eight consecutive j, and a tile is a K-major
+// canonical operand of the expand MMA (N = 128).
 #include "common.cuh"
 
 namespace lora {
