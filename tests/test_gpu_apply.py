@@ -193,3 +193,39 @@ def test_graph_capture_replays():
     torch.cuda.synchronize()
     assert lora.lora_get_status(ws) == lora.LORA_OK
     check_close(host_f64(y), oracle_dense(p))
+
+
+def test_widest_a_block_every_path():
+    """Four stacked slices of rank up to 64 (an A block of 256 rows, the widest the table stores): groups
+    small and large, on every path, against the oracle."""
+    rng = np.random.default_rng(21)
+    ids = np.concatenate([np.full(n, a, np.int32) for a, n in [(0, 3), (1, 40), (2, 150), (3, 17), (4, 9)]])
+    ids = np.concatenate([ids, rng.integers(-1, 5, 30).astype(np.int32)])
+    p = synth.make_dense("widest", 21, ids, 1024, [256, 128, 384, 136], [64, 48, 16, 64, 32], y_base="random")
+    ref = oracle_dense(p)
+    table = pack_dense(p)
+    ws = lora.Workspace(p.M, p.L)
+    for path in PATHS:
+        with forced_path(path):
+            y, _, _ = run_dense(p, table=table, ws=ws)
+        assert lora.lora_get_status(ws) == lora.LORA_OK
+        check_close(host_f64(y), ref, "widest path=%d" % path)
+    table.destroy()
+
+
+def test_large_batch_sampled_rows():
+    """A 4096-token batch (prefill-like runs over 24 adapters, K = N = 4096) checked on 96 sampled rows:
+    a token's delta depends on its own row only, so the oracle runs on the sample."""
+    rng = np.random.default_rng(22)
+    lens = synth.power_law_lengths(rng, 64, 16, 512)
+    ids = np.concatenate([np.full(int(n), j % 24, np.int32) for j, n in enumerate(lens)])[:4096]
+    ids = np.concatenate([ids, rng.integers(-1, 24, 4096 - len(ids)).astype(np.int32)])
+    assert len(ids) == 4096
+    p = synth.make_dense("large", 22, ids, 4096, [4096], synth.cycle_ranks(24), y_base="random")
+    y, table, ws = run_dense(p)
+    assert lora.lora_get_status(ws) == lora.LORA_OK
+    rows = np.sort(rng.choice(4096, 96, replace=False))
+    sub = synth.DenseProblem(**{**p.__dict__})
+    sub.ids, sub.x, sub.y_base, sub.M = p.ids[rows], p.x[rows], p.y_base[rows], len(rows)
+    check_close(host_f64(y)[rows], oracle_dense(sub), "large batch, sampled rows")
+    table.destroy()
