@@ -72,7 +72,7 @@ typedef struct {
 
 /*
  * Shape of one LoRA-wrapped projection.
- *   K        : in-features, a multiple of 8.
+ *   K        : in-features, a multiple of 8, at most 2^20.
  *   n_slices : 1..4 output slices ("[SGLang] LoRA Layers": q/k/v, gate/up).
  *   slice_n  : slice widths, each a multiple of 8; N = sum; slice s occupies
  *              output columns [off_s, off_s + slice_n[s]).

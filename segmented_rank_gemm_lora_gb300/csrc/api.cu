@@ -151,7 +151,7 @@ extern "C" lora_status lora_pack_weights(const lora_adapter_desc *adapters, int3
     if (!adapters || !shape || !out || L < 1) return LORA_ERR_INVALID_ARG;
     *out = nullptr;
     const lora_proj_shape &sh = *shape;
-    if (sh.K < 8 || sh.K % 8 != 0) return LORA_ERR_INVALID_ARG;
+    if (sh.K < 8 || sh.K % 8 != 0 || sh.K > (1 << 20)) return LORA_ERR_INVALID_ARG;
     if (sh.n_slices < 1 || sh.n_slices > kMaxSlices) return LORA_ERR_INVALID_ARG;
     if (!(sh.n_a == 1 || sh.n_a == sh.n_slices)) return LORA_ERR_INVALID_ARG;
     if (sh.E_A < 1 || sh.E_B < 1) return LORA_ERR_INVALID_ARG;

@@ -47,6 +47,7 @@ constexpr int kT = kEngineThreads;
 constexpr int kGroupCap = 2048;                 // groups per launch held in shared memory
 constexpr int kGroupCache = 128;                // group records and sizes cached in shared memory
 constexpr int kRankCache = 512;                 // stored ranks cached in shared memory
+constexpr int kPtrCache = 64;                   // groups whose table entries (A, B block, scale) are cached
 // shared-memory pool: S at [0, 16K), three expand stages of 50 KB above it (stage 0 on top)
 constexpr int kStageBytes = 50 * 1024;
 constexpr int kEsDepth = 3;
@@ -109,6 +110,8 @@ struct Plan {
 
 struct GroupDims {
     int a, e, rows_off, count, rp, R;
+    uint64_t ablk, bblk;   // packed A and B blocks of (a, e) (not filled by the plan's own size pass)
+    float scale;
     bool tc, fin;   // 128-row tensor-core tiles (else small tiles); partials finished by finish items
     int tile_rows, rows1, tiles, kc, n_kc, uw, ue, ipt, fins;
     int64_t scratch;   // floats of hand-off scratch: partials, then S of each tile when finished
@@ -145,6 +148,9 @@ struct __align__(1024) EngineSmem {
     int4 grp[kGroupCache];               // (adapter, expert, rows_off, count) of the first groups
     int4 gdim[kGroupCache];              // their packed sizes under the launch plan (pack_dims)
     int32_t rp_cache[kRankCache];        // stored rank of the first adapters
+    uint64_t a_blk[kPtrCache];           // table entries of the first groups, loaded beside the plan
+    uint64_t b_blk[kPtrCache];
+    float g_scale[kPtrCache];
 };
 
 static_assert(sizeof(EngineSmem) <= 227 * 1024, "shared memory per CTA");
@@ -161,14 +167,38 @@ __device__ __forceinline__ bool group_on_tc(const EngineParams &p, int count, in
 }
 
 __device__ __forceinline__ int floor_pow2(int v) { return v <= 0 ? 0 : 1 << (31 - __clz(v)); }
+
+// floor(a / b) for 0 <= a < 2^21, b >= 1.  The work-list arithmetic sits on every CTA's critical path,
+// where an integer divide by a runtime value is a long instruction sequence; a single-precision
+// reciprocal estimate of the quotient is off by less than one half here (relative error under
+// 1.5 x 2^-23), so one correction step makes it exact.
+__device__ __forceinline__ int qdiv_s(int a, int b)
+{
+    float rb;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rb) : "f"(__int2float_rn(b)));
+    int q = __float2int_rz(__int2float_rn(a) * rb);
+    const int r = a - q * b;
+    q += r >= b ? 1 : (r < 0 ? -1 : 0);
+    return q;
+}
+__device__ __noinline__ int qdiv_wide(int a, int b) { return a / b; }
+// floor(a / b) for any a >= 0 (larger values out of line)
+__device__ __forceinline__ int qdiv(int a, int b) { return a < (1 << 21) ? qdiv_s(a, b) : qdiv_wide(a, b); }
+// x mod m in [0, m) for any x, m >= 1
+__device__ __forceinline__ int pmod(int x, int m)
+{
+    if (x >= 0) return x - m * qdiv(x, m);
+    return x + m * (qdiv(-x - 1, m) + 1);
+}
 __device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
 
 // Output columns of one small-tile expand unit: about tb bytes of B, a power of two from 128, and the
 // unit's B rows and y rows must fit a stage.
 __device__ __forceinline__ int sm_unit_width(int rp, int rows1, int tb)
 {
-    const int ucap = min(kSmMaxUnit, floor_pow2(kStageBytes / 2 / (rp + rows1)));
-    return min(max(kTcCols, floor_pow2(tb / (2 * rp))), ucap);
+    // (tb is clipped below 2^21: any larger target is past the stage cap anyway)
+    const int ucap = min(kSmMaxUnit, floor_pow2(qdiv_s(kStageBytes / 2, rp + rows1)));
+    return min(max(kTcCols, floor_pow2(qdiv_s(min(tb, (1 << 21) - 1), 2 * rp))), ucap);
 }
 
 // Sizes of group g under plan pl, from scratch.
@@ -184,7 +214,7 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
     d.R = p.n_a * d.rp;
     d.tc = group_on_tc(p, d.count, d.R);
     d.tile_rows = d.tc ? kTcRows : kBgmvRows;
-    d.tiles = (d.count + d.tile_rows - 1) / d.tile_rows;
+    d.tiles = d.tc ? (d.count + kTcRows - 1) >> 7 : (d.count + kBgmvRows - 1) >> 4;
     d.rows1 = min(d.count, d.tile_rows);
     const int kmax = (p.K + 63) & ~63;
     if (d.tc) {
@@ -193,18 +223,20 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
         d.ue = pl.ue;
     } else {
         // the x rows ([rows][kc + 8]) and the A chunk must fit their staging areas
-        const int cap = max(64, min((kSmXBytes / d.rows1 - 16) / 2, kSmABytes / 2 / d.R) & ~63);
-        const int want = max(64, (pl.ta / (2 * d.R) + 63) & ~63);
+        // (ta is clipped below 2^21: any larger target is past the staging cap anyway)
+        const int cap = max(64, min((qdiv_s(kSmXBytes, d.rows1) - 16) / 2, qdiv_s(kSmABytes / 2, d.R)) & ~63);
+        const int want = max(64, (qdiv_s(min(pl.ta, (1 << 21) - 1), 2 * d.R) + 63) & ~63);
         d.kc = min(min(cap, kmax), want);
         d.uw = sm_unit_width(d.rp, d.rows1, pl.tb);
         d.ue = pl.ues;
     }
-    d.n_kc = (p.K + d.kc - 1) / d.kc;
+    d.n_kc = qdiv_s(p.K + d.kc - 1, d.kc);   // K <= 2^20
+    const int lw = ceil_log2(d.uw);   // unit widths are powers of two
     int ipt = 0;
     #pragma unroll 1
     for (int s = 0; s < p.n_slices; ++s) {
-        const int us = (p.slice_n[s] + d.uw - 1) / d.uw;
-        ipt += (us + d.ue - 1) / d.ue;
+        const int us = (p.slice_n[s] + d.uw - 1) >> lw;
+        ipt += qdiv_s(us + d.ue - 1, d.ue);
     }
     d.ipt = ipt;
     d.fin = d.tc || (int64_t)d.rows1 * d.rp * d.n_kc * ipt > kDirectLoads;
@@ -217,7 +249,11 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
 // The same for groups past the shared-memory cache (rare: out of line).
 __device__ __noinline__ GroupDims group_dims_full(const EngineParams &p, const EngineSmem &sm, int g, const Plan &pl)
 {
-    return group_dims_calc(p, sm, g, pl);
+    GroupDims d = group_dims_calc(p, sm, g, pl);
+    d.ablk = p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)];
+    d.bblk = p.b_ptr[d.a * p.E_B + (p.E_B == 1 ? 0 : d.e)];
+    d.scale = p.scale[d.a];
+    return d;
 }
 
 // Packed sizes of a cached group, written by the plan: (kc, flags, ipt, n_kc), flags = log2(uw) |
@@ -248,6 +284,15 @@ __device__ __forceinline__ GroupDims group_dims(const EngineParams &p, const Eng
     d.tc = (gd.y >> 14) & 1;
     d.ipt = gd.z;
     d.n_kc = gd.w;
+    if (g < kPtrCache) {
+        d.ablk = sm.a_blk[g];
+        d.bblk = sm.b_blk[g];
+        d.scale = sm.g_scale[g];
+    } else {
+        d.ablk = p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)];
+        d.bblk = p.b_ptr[d.a * p.E_B + (p.E_B == 1 ? 0 : d.e)];
+        d.scale = p.scale[d.a];
+    }
     d.tile_rows = d.tc ? kTcRows : kBgmvRows;
     d.tiles = (d.count + d.tile_rows - 1) >> (d.tc ? 7 : 4);
     d.rows1 = min(d.count, d.tile_rows);
@@ -372,14 +417,13 @@ __device__ __forceinline__ void sm_shrink_issue(const EngineParams &p, EngineSme
     uint64_t *bar = &sm.bar_sh[slot];
     const uint32_t x_bytes = (uint32_t)b.kw * 2;
     if (tid == 0) {
-        const __nv_bfloat16 *ablk =
-            reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[d.a * p.E_A + (p.E_A == 1 ? 0 : d.e)]);
+        const __nv_bfloat16 *ablk = reinterpret_cast<const __nv_bfloat16 *>(d.ablk);
         const uint32_t a_bytes = (uint32_t)(b.kw / 8) * d.R * 16;
         mbar_arrive_expect_tx(bar, a_bytes + b.nrows * x_bytes);
         bulk_g2s(base, ablk + (int64_t)(b.k0 / 8) * d.R * 8, a_bytes, bar);
     }
     if (warp == 1 && lane < b.nrows) {
-        const int src = p.rows[d.rows_off + b.r0 + lane] / p.src_div;
+        const int v = p.rows[d.rows_off + b.r0 + lane], src = p.src_div == 1 ? v : qdiv_s(v, p.src_div);
         bulk_g2s(base + kSmXOff + (size_t)lane * (d.kc * 2 + 16), p.x + (int64_t)src * p.ldx + b.k0, x_bytes, bar);
     }
 }
@@ -404,7 +448,8 @@ __device__ __forceinline__ void sm_shrink_run(const EngineParams &p, EngineSmem 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int R = d.R;
     const int ntiles = R / 8;
-    const int ksplit = ntiles >= 8 ? 1 : 8 / ntiles;
+    const int nw8 = min(ntiles, 8);                     // warps per K slice
+    const int ksplit = ntiles >= 8 ? 1 : qdiv_s(8, ntiles);
     const int kgs = b.kw / 8, steps = (kgs + 1) / 2;
     const int xstride = d.kc * 2 + 16;
     const uint32_t a_base = smem_u32(sm.pool + slot * kSmSlotBytes);
@@ -413,10 +458,10 @@ __device__ __forceinline__ void sm_shrink_run(const EngineParams &p, EngineSmem 
     float *red = reinterpret_cast<float *>(sm.pool + kSmRedOff);   // [ksplit - 1][16][R]
     float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * b.r0 * R + (int64_t)chunk * b.nrows * R;
     const int gr = lane >> 2, qc = (lane & 3) * 2;
-    const int kpart = warp / min(ntiles, 8);
-    const int s_lo = steps * kpart / ksplit, s_hi = steps * (kpart + 1) / ksplit;
+    const int kpart = qdiv_s(warp, nw8);
+    const int s_lo = qdiv_s(steps * kpart, ksplit), s_hi = qdiv_s(steps * (kpart + 1), ksplit);
     for (int nt0 = 0; nt0 < ntiles; nt0 += 8) {   // uniform: every warp runs the same number of rounds
-        const int nt = nt0 + warp % min(ntiles, 8);
+        const int nt = nt0 + warp - kpart * nw8;
         const bool act = nt < ntiles && kpart < ksplit;
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
         float d2[4] = {0.f, 0.f, 0.f, 0.f}, d3[4] = {0.f, 0.f, 0.f, 0.f};
@@ -493,11 +538,12 @@ struct TcShrink {
 // 128-row box inside x, a single TMA tile load brings them; otherwise every
 // thread gathers 16-byte pieces with cp.async into the same swizzled places
 // (zero for rows past the tile or columns past K).
-__device__ __noinline__ void tc_issue_stage(const EngineParams &p, const CUtensorMap *xmap, EngineSmem &sm, int a,
-                                            int e, int R, int nrows, int k0, int kw, int depth, int run, int s)
+__device__ __noinline__ void tc_issue_stage(const EngineParams &p, const CUtensorMap *xmap, EngineSmem &sm,
+                                            uint64_t ablk_addr, int R, int nrows, int k0, int kw, int depth, int run,
+                                            int s)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int slot = s % depth;
+    const int slot = s - depth * qdiv_s(s, depth);
     unsigned char *Xs = sm.pool + slot * tc_stage_bytes(R);
     unsigned char *As = Xs + kTcRows * kTcStageK * 2;
     const int kb = k0 + s * kTcStageK;
@@ -524,7 +570,7 @@ __device__ __noinline__ void tc_issue_stage(const EngineParams &p, const CUtenso
         tc::cp_async_commit();
     }
     if (tid == 0) {
-        const __nv_bfloat16 *ablk = reinterpret_cast<const __nv_bfloat16 *>(p.a_ptr[a * p.E_A + (p.E_A == 1 ? 0 : e)]);
+        const __nv_bfloat16 *ablk = reinterpret_cast<const __nv_bfloat16 *>(ablk_addr);
         const uint32_t bytes = (uint32_t)vkg * R * 16;
         mbar_arrive_expect_tx(&sm.bar_stage[slot], bytes + (run ? kTcRows * kTcStageK * 2 : 0));
         bulk_g2s(As, ablk + (int64_t)(kb / 8) * R * 8, bytes, &sm.bar_stage[slot]);
@@ -552,10 +598,11 @@ __device__ __forceinline__ TcShrink tc_shrink_issue(const EngineParams &p, const
     t.k0 = chunk * d.kc;
     t.kw = min(d.kc, p.K - t.k0);
     t.nst = (t.kw + kTcStageK - 1) / kTcStageK;
-    t.depth = min(min(kTcMaxDepth, kTcShrinkBytes / tc_stage_bytes(d.R)), t.nst);
+    t.depth = min(min(kTcMaxDepth, qdiv_s(kTcShrinkBytes, tc_stage_bytes(d.R))), t.nst);
     int my_row = 0;
     if (tid < kTcRows) {
-        my_row = tid < t.nrows ? p.rows[d.rows_off + t.r0 + tid] / p.src_div : 0;
+        const int v = tid < t.nrows ? p.rows[d.rows_off + t.r0 + tid] : 0;
+        my_row = p.src_div == 1 ? v : qdiv_s(v, p.src_div);
         sm.row_src[tid] = my_row;
     }
     __syncthreads();
@@ -563,7 +610,7 @@ __device__ __forceinline__ TcShrink tc_shrink_issue(const EngineParams &p, const
     const int x_total = sm.x_total;
     const bool consecutive = tid >= t.nrows || my_row == sm.row_src[0] + tid;
     t.run = __syncthreads_and(consecutive ? 1 : 0) != 0 && p.x_rows > 0 && sm.row_src[0] + kTcRows <= x_total;
-    for (int s = 0; s < t.depth; ++s) tc_issue_stage(p, xmap, sm, d.a, d.e, d.R, t.nrows, t.k0, t.kw, t.depth, t.run, s);
+    for (int s = 0; s < t.depth; ++s) tc_issue_stage(p, xmap, sm, d.ablk, d.R, t.nrows, t.k0, t.kw, t.depth, t.run, s);
     return t;
 }
 
@@ -580,14 +627,14 @@ __device__ __forceinline__ bool tc_shrink_run(const EngineParams &p, const CUten
     uint32_t pending = 0;   // slots whose MMA commit has not been waited for
     bool ok = true;
     for (int s = 0; s < t.nst && ok; ++s) {
-        const int slot = s % t.depth;
+        const int slot = s - t.depth * qdiv_s(s, t.depth);
         if (s >= 1 && s - 1 + t.depth < t.nst) {   // refill the previous stage's slot
-            const int ps = (s - 1) % t.depth;
+            const int ps = (s - 1) - t.depth * qdiv_s(s - 1, t.depth);
             ok = cta_wait(&sm.bar_mma[ps], ph.get(PH_MMA + ps), p);
             ph.flip(PH_MMA + ps);
             pending &= ~(1u << ps);
             if (!ok) break;
-            tc_issue_stage(p, xmap, sm, d.a, d.e, d.R, t.nrows, t.k0, t.kw, t.depth, t.run, s - 1 + t.depth);
+            tc_issue_stage(p, xmap, sm, d.ablk, d.R, t.nrows, t.k0, t.kw, t.depth, t.run, s - 1 + t.depth);
         }
         if (!t.run) {
             cp_wait_pending(min(t.nst, s + t.depth) - (s + 1));
@@ -687,7 +734,8 @@ __device__ __forceinline__ bool finish_item(const EngineParams &p, EngineSmem &s
     float *fa = fin_area(p, sm, d, g, tile);
     #pragma unroll 1
     for (int u = tid; u < kFinRows * c4s; u += kT) {
-        const int row = sl * kFinRows + u / c4s, c = (u % c4s) * 4;
+        const int uq = qdiv_s(u, c4s);
+        const int row = sl * kFinRows + uq, c = (u - uq * c4s) * 4;
         if (row >= nrows) continue;
         const float *src = part + (int64_t)row * R + c;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -731,16 +779,17 @@ __device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const
     it.g = find_group(sm.ex_pre, G, item);
     it.d = group_dims(p, sm, it.g, pl);
     const int local = item - sm.ex_pre[it.g];
-    it.tile = local / it.d.ipt;
-    int q = local % it.d.ipt;
+    it.tile = qdiv(local, it.d.ipt);
+    int q = local - it.tile * it.d.ipt;
+    const int lw = ceil_log2(it.d.uw);
     int s = 0;
     #pragma unroll 1
-    for (; s < p.n_slices; ++s) {
-        const int is = ((p.slice_n[s] + it.d.uw - 1) / it.d.uw + it.d.ue - 1) / it.d.ue;
+    for (; s < p.n_slices - 1; ++s) {
+        const int is = qdiv_s(((p.slice_n[s] + it.d.uw - 1) >> lw) + it.d.ue - 1, it.d.ue);
         if (q < is) break;
         q -= is;
     }
-    const int us = (p.slice_n[s] + it.d.uw - 1) / it.d.uw;
+    const int us = (p.slice_n[s] + it.d.uw - 1) >> lw;
     it.s = s;
     it.u0 = q * it.d.ue;
     it.nu = min(it.d.ue, us - it.u0);
@@ -755,12 +804,13 @@ __device__ __forceinline__ ExpandItem decode_expand(const EngineParams &p, const
 // items to put in flight.
 // Put one expand unit in flight into stage seq % 3: its B rows and its output
 // rows (bulk copies on bar_es), with a record of the unit.  The unit is column
-// unit uu of slice s of a tile whose output rows are rows[row_base ..
-// row_base + nrows); the first unit of an item reads them from the row list,
-// later ones take them from the previous unit's stage (same thread, same row).
+// unit uu of slice s of a tile of nrows output rows; for the first unit of an
+// item, thread t brings the tile's row t and its weight (read ahead by the
+// caller), later units take them from the previous unit's stage (same thread,
+// same row).  bblk_addr and scale are the group's B block and adapter scale.
 __device__ __noinline__ void issue_unit(const EngineParams &p, const CUtensorMap *ymap, EngineSmem &sm, int seq, int s,
-                                        int uu, int nrows, int row_base, bool first, int a, int e, int rp, int uw,
-                                        bool tc)
+                                        int uu, int nrows, bool first, int first_row, float first_w,
+                                        uint64_t bblk_addr, float scale, int rp, int uw, bool tc)
 {
     const int tid = threadIdx.x;
     const int st = seq % kEsDepth;
@@ -773,8 +823,8 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, const CUtensorMap
         int row;
         float w;
         if (first) {
-            row = p.rows[row_base + tid];
-            w = p.row_weight ? p.row_weight[row] : 1.0f;
+            row = first_row;
+            w = first_w;
         } else {
             const int pst = (seq + kEsDepth - 1) % kEsDepth;   // the previous unit, same item
             row = sm.row_dst[pst][tid];
@@ -796,7 +846,7 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, const CUtensorMap
         bulk_g2s(base + yoff + tid * ystride, p.y + (int64_t)sm.row_dst[st][tid] * p.ldy + n0, (uint32_t)nw * 2,
                  &sm.bar_es[st]);
     if (tid == 0) {
-        const __nv_bfloat16 *bblk = reinterpret_cast<const __nv_bfloat16 *>(p.b_ptr[a * p.E_B + (p.E_B == 1 ? 0 : e)]);
+        const __nv_bfloat16 *bblk = reinterpret_cast<const __nv_bfloat16 *>(bblk_addr);
         const uint32_t y_bytes = run ? 2u * kTcRows * 128 : (uint32_t)nrows * nw * 2;
         const int kgs = rp / 8;
         UnitRec r;
@@ -808,7 +858,7 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, const CUtensorMap
         r.ystride = ystride / 2;
         r.tc = tc;
         r.run = run;
-        r.scale = p.scale[a];
+        r.scale = scale;
         // the unit's 128-row B tiles are consecutive in the packed block: one bulk copy
         const int tile0 = p.slice_tile_off[s] + uu * (uw / kNTile);
         const int ntl = (nw + kNTile - 1) / kNTile;
@@ -857,7 +907,7 @@ __device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm
         const float *part = p.partials + sm.part_pre[it.g] + (int64_t)d.n_kc * it.r0 * d.R + it.sa * rp;
         const float *fin = d.fin ? fin_area(p, sm, d, it.g, it.tile) + it.sa * rp : nullptr;
         for (int idx = tid; idx < it.nrows * rp; idx += kT) {
-            const int i = idx / rp, jj = idx - i * rp;
+            const int i = qdiv_s(idx, rp), jj = idx - i * rp;
             float acc = 0.f;
             if (d.fin) {
                 acc = __ldcg(fin + (int64_t)i * d.R + jj);
@@ -1101,7 +1151,7 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     }
     // pass 1: validate; small-tile A and B bytes (in units of K and N bf16 elements), 128-row tile units
     bool bad = false;
-    long long bga = 0, bgb = 0;
+    int bga = 0, bgb = 0;   // (below 2^21: at most 65536 / 16 + 2048 tiles of at most 256 rows)
     int tcu = 0, tci = 0;
     any_tc = false;
 #pragma unroll 1
@@ -1121,8 +1171,8 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
             tci += tiles;
         } else {
             const int tiles = (gr.w + kBgmvRows - 1) >> 4;
-            bga += (long long)tiles * p.n_a * rp;
-            bgb += (long long)tiles * rp;
+            bga += tiles * p.n_a * rp;
+            bgb += tiles * rp;
         }
     }
 #pragma unroll
@@ -1143,14 +1193,15 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     const int kmax = (p.K + 63) & ~63;
     int kctc = kTcKc;
     if (tci > 0 && tci * ((p.K + kTcKc - 1) / kTcKc) < 2 * grid) {
-        const int nk = max(1, grid / tci);
-        kctc = min(kmax, max(kTcKc, ((p.K + nk - 1) / nk + 63) & ~63));
+        const int nk = max(1, qdiv_s(grid, tci));
+        kctc = min(kmax, max(kTcKc, (qdiv_s(p.K + nk - 1, nk) + 63) & ~63));
     }
-    tci *= (p.K + kctc - 1) / kctc;   // 128-row tile shrink items
+    tci *= qdiv_s(p.K + kctc - 1, kctc);   // 128-row tile shrink items
     const int spare = max(grid / 4, grid - tci);
-    pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, 1.25f * 2.f * (float)p.K * (float)bga / spare));
-    pl.tb = (int)fminf(268435456.f, fmaxf(4096.f, 2.f * (float)N * (float)bgb / (2.5f * grid)));
-    pl.ue = min(128, max(1, (tcu + kItemsPerCta * grid - 1) / (kItemsPerCta * grid)));
+    // (targets, not sizes: the fast divides only need to agree between CTAs, and they run the same code)
+    pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, __fdividef(2.5f * (float)p.K * (float)bga, (float)spare)));
+    pl.tb = (int)fminf(268435456.f, fmaxf(4096.f, __fdividef(2.f * (float)N * (float)bgb, 2.5f * grid)));
+    pl.ue = min(128, max(1, qdiv(tcu + kItemsPerCta * grid - 1, kItemsPerCta * grid)));
     pl.kctc = kctc;
     // small-tile expand units of the launch -> units per item, so that the items fit one wave
     {
@@ -1160,46 +1211,47 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
             const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
             const int rp = gr.x < kRankCache ? sm.rp_cache[gr.x] : p.rpad[gr.x];
             if (group_on_tc(p, gr.w, p.n_a * rp)) continue;
-            const int uw = sm_unit_width(rp, min(gr.w, kSmRows), pl.tb);
+            const int lw = ceil_log2(sm_unit_width(rp, min(gr.w, kSmRows), pl.tb));
             int u = 0;
 #pragma unroll 1
-            for (int s = 0; s < p.n_slices; ++s) u += (p.slice_n[s] + uw - 1) / uw;
+            for (int s = 0; s < p.n_slices; ++s) u += (p.slice_n[s] + (1 << lw) - 1) >> lw;
             units += ((gr.w + kSmRows - 1) / kSmRows) * u;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
-        pl.ues = min(16, max(1, (units + grid - 1) / grid));
+        pl.ues = min(16, max(1, qdiv(units + grid - 1, grid)));
     }
     // pass 2: per-group item counts and their exclusive prefix sums, 32 groups per step; larger chunks
     // until the hand-off scratch fits the workspace
 #pragma unroll 1
     for (int iter = 0; iter < 8; ++iter) {
         int c_sh = 0, c_shs = 0, c_fin = 0, c_ex = 0, c_tile = 0;
-        long long c_part = 0;
+        unsigned c_part = 0;   // scratch floats, saturating at 2^31 - 1 (a workspace error)
 #pragma unroll 1
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
             int v_sh = 0, v_shs = 0, v_fin = 0, v_ex = 0, v_tile = 0;
-            long long v_part = 0;
+            unsigned v_part = 0;
             if (g < G) {
                 const GroupDims d = group_dims_calc(p, sm, g, pl);
                 (d.tc ? v_sh : v_shs) = d.tiles * d.n_kc;
                 v_fin = d.fins;
                 v_ex = d.tiles * d.ipt;
                 v_tile = d.tiles;
-                v_part = d.scratch;
+                v_part = (unsigned)min(d.scratch, (int64_t)INT32_MAX);
                 if (g < kGroupCache) sm.gdim[g] = pack_dims(d);
             }
             int i_sh = v_sh, i_shs = v_shs, i_fin = v_fin, i_ex = v_ex, i_tile = v_tile;
-            long long i_part = v_part;
+            unsigned i_part = v_part;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int a = __shfl_up_sync(0xffffffffu, i_sh, o), b = __shfl_up_sync(0xffffffffu, i_fin, o);
                 const int c = __shfl_up_sync(0xffffffffu, i_ex, o), e = __shfl_up_sync(0xffffffffu, i_tile, o);
-                const long long f = __shfl_up_sync(0xffffffffu, i_part, o);
+                const unsigned f = __shfl_up_sync(0xffffffffu, i_part, o);
                 const int h = __shfl_up_sync(0xffffffffu, i_shs, o);
                 if (lane >= o) {
-                    i_sh += a; i_fin += b; i_ex += c; i_tile += e; i_part += f; i_shs += h;
+                    i_sh += a; i_fin += b; i_ex += c; i_tile += e; i_shs += h;
+                    i_part = min(i_part + f, 0x7FFFFFFFu);
                 }
             }
             if (g < G) {
@@ -1208,14 +1260,14 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
                 sm.fin_pre[g] = c_fin + i_fin - v_fin;
                 sm.ex_pre[g] = c_ex + i_ex - v_ex;
                 sm.tile_pre[g] = c_tile + i_tile - v_tile;
-                sm.part_pre[g] = (int)min(c_part + i_part - v_part, (long long)INT32_MAX);
+                sm.part_pre[g] = (int)min(c_part + (i_part - v_part), 0x7FFFFFFFu);
             }
             c_sh += __shfl_sync(0xffffffffu, i_sh, 31);
             c_shs += __shfl_sync(0xffffffffu, i_shs, 31);
             c_fin += __shfl_sync(0xffffffffu, i_fin, 31);
             c_ex += __shfl_sync(0xffffffffu, i_ex, 31);
             c_tile += __shfl_sync(0xffffffffu, i_tile, 31);
-            c_part += __shfl_sync(0xffffffffu, i_part, 31);
+            c_part = min(c_part + __shfl_sync(0xffffffffu, i_part, 31), 0x7FFFFFFFu);
         }
         if (lane == 0) {
             sm.sh_pre[G] = c_sh;
@@ -1223,14 +1275,14 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
             sm.fin_pre[G] = c_fin;
             sm.ex_pre[G] = c_ex;
             sm.tile_pre[G] = c_tile;
-            sm.part_pre[G] = (int)min(c_part, (long long)INT32_MAX);
+            sm.part_pre[G] = (int)c_part;
             sm.ta = pl.ta;
             sm.tb = pl.tb;
             sm.ue = pl.ue;
             sm.kctc = pl.kctc;
             sm.ues = pl.ues;
         }
-        if (c_part <= p.partial_floats || (pl.ta >= (1 << 27) && pl.kctc >= p.K)) break;
+        if ((int64_t)c_part <= p.partial_floats || (pl.ta >= (1 << 27) && pl.kctc >= p.K)) break;
         pl.ta = min(1 << 28, pl.ta * 4);
         pl.kctc = min(1 << 20, pl.kctc * 4);
     }
@@ -1288,6 +1340,15 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         if (tid == 0) sm.flag = good ? (any_tc ? 2 : 0) : 1;
     } else if (warp == 1) {
         prefetch_a_l2(p, sm, G);
+    } else if (warp == 2) {
+        // the first groups' table entries, so that no copy issue waits on a table read
+        for (int g = tid - 64; g < min(G, kPtrCache); g += 32) {
+            const int4 gr = sm.grp[g];
+            const bool ok = gr.x >= 0 && gr.x < p.L && gr.y >= 0 && gr.y < p.num_experts;
+            sm.a_blk[g] = ok ? p.a_ptr[gr.x * p.E_A + (p.E_A == 1 ? 0 : gr.y)] : 0;
+            sm.b_blk[g] = ok ? p.b_ptr[gr.x * p.E_B + (p.E_B == 1 ? 0 : gr.y)] : 0;
+            sm.g_scale[g] = ok ? p.scale[gr.x] : 0.f;
+        }
     }
     __syncthreads();
     stamp(p, TS_PRO_PLANNED);
@@ -1307,11 +1368,13 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         if (b == 0 && tid == 0) atomicOr(p.err, kErrWorkspace);
         return;
     }
-    // one warp allocates the tensor memory this CTA's MMAs accumulate into
-    if (warp == 0) tc::tmem_alloc(&sm.tmem_base, kTmemCols);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+    // one warp allocates the tensor memory this CTA's MMAs accumulate into (launches with 128-row tiles only)
+    if (use_tc) {
+        if (warp == 0) tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
     const Plan pl = {sm.ta, sm.tb, sm.ue, sm.ues, sm.kctc};
     stamp(p, TS_WORKLIST);
 
@@ -1323,9 +1386,9 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     // this CTA's items, each kind dealt on from where the previous one stopped (so CTAs with less of one
     // kind take the next first): 128-row tile shrink items b, b + grid, ...; small-tile shrink items;
     // finish items; expand items
-    const int my_tc = b < n_sh_tc ? (n_sh_tc - b + grid - 1) / grid : 0;
-    const int s0 = ((b - n_sh_tc) % grid + grid) % grid;
-    const int my_shrink = my_tc + (s0 < n_sh_sm ? (n_sh_sm - s0 + grid - 1) / grid : 0);
+    const int my_tc = b < n_sh_tc ? qdiv(n_sh_tc - b + grid - 1, grid) : 0;
+    const int s0 = pmod(b - n_sh_tc, grid);
+    const int my_shrink = my_tc + (s0 < n_sh_sm ? qdiv(n_sh_sm - s0 + grid - 1, grid) : 0);
     // the CTA's j-th shrink item: group and index within the group
     auto shrink_item = [&](int j, int &g, int &local) {
         if (j < my_tc) {
@@ -1338,8 +1401,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
             local = u - sm.shs_pre[g];
         }
     };
-    const int f0 = ((b - n_shrink) % grid + grid) % grid;
-    const int e0 = ((b - n_shrink - n_fin) % grid + grid) % grid;
+    const int f0 = pmod(b - n_shrink, grid);
+    const int e0 = pmod(b - n_shrink - n_fin, grid);
     // the expand issuer starts at item e0; expand units may be in flight while the shrink items run:
     // stage 0 beside a tensor-core shrink, stages 0 and 1 beside a small-tile one.  Set up after the
     // first shrink item's copies are on their way.
@@ -1348,11 +1411,20 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     // issue side of the expand ring, kept by every thread alike: unit iss_k of item iss_item
     int iss_item = n_expand, iss_k = 0;
     ExpandItem iss_it;
+    int iss_row = 0;        // this thread's output row of the item's tile, and its weight (read ahead)
+    float iss_w = 1.f;
+    auto iss_enter = [&](int item) {
+        iss_item = item;
+        if (item >= n_expand) return;
+        iss_it = decode_expand(p, sm, pl, G, item);
+        if (tid < iss_it.nrows) {
+            iss_row = p.rows[iss_it.d.rows_off + iss_it.r0 + tid];
+            iss_w = p.row_weight ? p.row_weight[iss_row] : 1.f;
+        }
+    };
     auto setup_issuer = [&]() {
-        iss_item = e0;
-        if (e0 < n_expand) iss_it = decode_expand(p, sm, pl, G, e0);
-        if (my_tc > 0 || my_shrink > 1) npre = 1;   // the shrink staging reaches into stage 1
-        else if (my_shrink > 0) npre = 2;
+        iss_enter(e0);
+        if (my_shrink > 0) npre = 1;   // the shrink staging (and its cross-warp sums) reach into stage 1
         iss_ready = true;
     };
     // put units in flight until `upto` have been issued (units must have left stage (upto - 1) % 3)
@@ -1360,12 +1432,11 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         while (issued < upto && iss_item < n_expand) {
             inflight |= 1u << (issued % kEsDepth);
             const GroupDims &d = iss_it.d;
-            issue_unit(p, &pk.y_map_ld, sm, issued++, iss_it.s, iss_it.u0 + iss_k, iss_it.nrows,
-                       d.rows_off + iss_it.r0, iss_k == 0, d.a, d.e, d.rp, d.uw, d.tc);
+            issue_unit(p, &pk.y_map_ld, sm, issued++, iss_it.s, iss_it.u0 + iss_k, iss_it.nrows, iss_k == 0, iss_row,
+                       iss_w, d.bblk, d.scale, d.rp, d.uw, d.tc);
             if (++iss_k == iss_it.nu) {
                 iss_k = 0;
-                iss_item += grid;
-                if (iss_item < n_expand) iss_it = decode_expand(p, sm, pl, G, iss_item);
+                iss_enter(iss_item + grid);
             }
         }
     };
@@ -1376,7 +1447,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         int g, local;
         shrink_item(j, g, local);
         const GroupDims d = group_dims(p, sm, g, pl);
-        const int tile = local / d.n_kc, chunk = local % d.n_kc;
+        const int tile = qdiv(local, d.n_kc), chunk = local - tile * d.n_kc;
         const int tg = sm.tile_pre[g] + tile;
         const bool first = j == 0;
         if (first) stamp(p, TS_SH_START);
@@ -1402,9 +1473,13 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
                 int g2, local2;
                 shrink_item(j + 1, g2, local2);
                 const GroupDims d2 = group_dims(p, sm, g2, pl);
-                sm_shrink_issue(p, sm, d2, sm_shrink_desc(p, d2, local2 / d2.n_kc, local2 % d2.n_kc), slot ^ 1);
+                const int tile2 = qdiv(local2, d2.n_kc);
+                sm_shrink_issue(p, sm, d2, sm_shrink_desc(p, d2, tile2, local2 - tile2 * d2.n_kc), slot ^ 1);
                 sh_inflight |= 1u << (slot ^ 1);
             }
+            // the first expand units go in flight while the shrink operands land: issuing them is
+            // longer than their bytes are large, so it stays off the hand-off's path
+            if (first) prefetch(npre);
             ok = sm_shrink_wait(p, sm, ph, slot, first);
             sh_inflight &= ~(1u << slot);
             if (ok) sm_shrink_run(p, sm, d, bs, g, chunk, slot, first);
@@ -1415,9 +1490,6 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         }
         if (tid == 0 && !p.withhold) release_add(&p.sync[tg * 4 + 0], 1);
         if (first) stamp(p, TS_SH_PUBLISHED);
-        // small tiles: the first expand units go in flight after the partial is published, so they
-        // neither compete with the shrink operands nor delay the hand-off
-        if (first && !d.tc) prefetch(npre);
     }
     // the shrink staging is free: the rest of the ring may fill while the finish items run
     if (!iss_ready) setup_issuer();
@@ -1491,9 +1563,11 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
     if (pend >= 0) mbar_wait_bounded(&sm.bar_mmae[pend & 1], ph.get(PH_MMAE + (pend & 1)), p.timeout_ns, p.err);
     bulk_wait_all();
     stamp(p, TS_EXIT);
-    tc::fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(sm.tmem_base, kTmemCols);
+    if (use_tc) {
+        tc::fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tc::tmem_dealloc(sm.tmem_base, kTmemCols);
+    }
 }
 
 const void *engine_kernel_ptr() { return reinterpret_cast<const void *>(engine_kernel); }
