@@ -254,6 +254,15 @@ const char *lora_status_string(lora_status status);
  *   LORA_OPT_TEST_WITHHOLD_HANDOFF : test hook; nonzero makes the next launches
  *                              skip publishing shrink results so the waits of
  *                              the expand work run out (checks the timeout path).
+ *   LORA_OPT_PDL             : 1 (default) launches the one-warp segment
+ *                              build (dense, at most 32 tokens) with
+ *                              programmatic stream serialization, and the
+ *                              engine too when its workspace holds at most 32
+ *                              tokens (dense): such a kernel may be scheduled
+ *                              while the kernel before it on the stream
+ *                              finishes, and waits on the device
+ *                              (griddepcontrol) before it reads anything; 0
+ *                              launches every kernel in plain stream order.
  * Returns LORA_ERR_INVALID_ARG for an unknown option or value.
  */
 typedef enum {
@@ -261,7 +270,8 @@ typedef enum {
     LORA_OPT_TC_MIN_ROWS = 1,
     LORA_OPT_WAIT_TIMEOUT_NS = 2,
     LORA_OPT_GRID_CTAS = 3,
-    LORA_OPT_TEST_WITHHOLD_HANDOFF = 4
+    LORA_OPT_TEST_WITHHOLD_HANDOFF = 4,
+    LORA_OPT_PDL = 5
 } lora_option;
 lora_status lora_set_option(int32_t option, int64_t value);
 int64_t lora_get_option(int32_t option);

@@ -22,6 +22,7 @@ std::atomic<int64_t> g_opt_tc_min_rows{32};
 std::atomic<int64_t> g_opt_timeout_ns{1000000000LL};
 std::atomic<int64_t> g_opt_grid{0};
 std::atomic<int64_t> g_opt_withhold{0};
+std::atomic<int64_t> g_opt_pdl{1};
 std::atomic<void *> g_trace{nullptr};
 std::atomic<int64_t> g_trace_bytes{0};
 
@@ -421,7 +422,7 @@ extern "C" lora_status lora_build_segments(const lora_workspace *ws, const int32
     p.moe_group_capacity = w.moe_group_capacity;
     p.sync = at<int32_t>(ws, w.sync);
     p.sync_ints = w.max_tiles * 4;
-    return cuda_status(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_build(p, reinterpret_cast<cudaStream_t>(stream), g_opt_pdl.load() != 0));
 }
 
 static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLayout &w, bool moe, int32_t src_div,
@@ -507,7 +508,11 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
     const int64_t want = g_opt_grid.load();
     if (want > 0 && want < grid) grid = (int)want;
     cudaError_t e;
-    launch_engine(p, grid, engine_smem_bytes(0), reinterpret_cast<cudaStream_t>(stream), &e);
+    // Early scheduling only behind the one-warp build (dense workspaces of at most 32 tokens): an engine
+    // block fits beside it, while the block-wide build holds its SM's shared memory, so behind it one
+    // engine block would start late and hold up the whole grid.
+    const bool pdl = g_opt_pdl.load() != 0 && !moe && ws->max_M <= 32;
+    launch_engine(p, grid, engine_smem_bytes(0), reinterpret_cast<cudaStream_t>(stream), pdl, &e);
     return cuda_status(e);
 }
 
@@ -599,6 +604,10 @@ extern "C" lora_status lora_set_option(int32_t option, int64_t value)
     case LORA_OPT_TEST_WITHHOLD_HANDOFF:
         g_opt_withhold = value != 0;
         return LORA_OK;
+    case LORA_OPT_PDL:
+        if (value < 0 || value > 1) return LORA_ERR_INVALID_ARG;
+        g_opt_pdl = value;
+        return LORA_OK;
     }
     return LORA_ERR_INVALID_ARG;
 }
@@ -619,6 +628,7 @@ extern "C" int64_t lora_get_option(int32_t option)
     case LORA_OPT_WAIT_TIMEOUT_NS: return g_opt_timeout_ns.load();
     case LORA_OPT_GRID_CTAS: return g_opt_grid.load();
     case LORA_OPT_TEST_WITHHOLD_HANDOFF: return g_opt_withhold.load();
+    case LORA_OPT_PDL: return g_opt_pdl.load();
     }
     return -1;
 }
@@ -706,7 +716,7 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
     b.seg_capacity = kStaticMaxM;
     b.sync = reinterpret_cast<int32_t *>(base + kStaticSync);   // zeroed by the build kernel
     b.sync_ints = kStaticMaxTiles * 4;
-    if (launch_build(b, s) != cudaSuccess) return LORA_ERR_CUDA;
+    if (launch_build(b, s, g_opt_pdl.load() != 0) != cudaSuccess) return LORA_ERR_CUDA;
 
     EngineParams p{};
     if (M > 0 && t->K >= 64) {
@@ -758,6 +768,6 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
     const int64_t want = g_opt_grid.load();
     if (want > 0 && want < grid) grid = (int)want;
     cudaError_t e;
-    launch_engine(p, grid, engine_smem_bytes(0), s, &e);
+    launch_engine(p, grid, engine_smem_bytes(0), s, g_opt_pdl.load() != 0 && M <= 32, &e);
     return cuda_status(e);
 }

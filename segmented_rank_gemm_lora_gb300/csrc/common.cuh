@@ -97,7 +97,7 @@ struct EngineParams {
     int32_t trace_ctas;
 };
 
-void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s, cudaError_t *err);
+void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s, bool pdl, cudaError_t *err);
 size_t engine_smem_bytes(int group_capacity);
 const void *engine_kernel_ptr();
 
@@ -114,7 +114,7 @@ struct BuildParams {
     int32_t *sync;                // zeroed
     int32_t sync_ints;
 };
-cudaError_t launch_build(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_build(const BuildParams &p, cudaStream_t s, bool pdl);
 
 cudaError_t launch_pack_a(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int32_t K, int32_t n_a, int32_t rank,
                           int32_t rpad, cudaStream_t s);
@@ -231,6 +231,13 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *p, int v)
     asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start
+// while the kernel before it on the stream still runs; it must wait here before it reads anything that
+// kernel (or any earlier work) wrote.  Outside such a launch the wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel on the stream (if launched with programmatic serialization) start launching.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns)
 {

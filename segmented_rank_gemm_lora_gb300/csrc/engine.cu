@@ -1305,11 +1305,10 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         for (int i = tid; i < (int)(sizeof(EngineParams) / 4); i += kT) dst[i] = src[i];
     }
     const EngineParams &p = sm.pc;
+    pdl_trigger();
 
     // ---- prologue: one round trip for the count, the first group records and the stored ranks ----
     if (tid == 0) {
-        sm.G = *pk.num_groups;
-        sm.x_total = *pk.m_ptr * pk.m_mult;
         sm.flag = 0;
         mbar_init(&sm.bar_sh[0], 1);
         mbar_init(&sm.bar_sh[1], 1);
@@ -1322,6 +1321,11 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         mbar_init(&sm.bar_mmae[0], 1);
         mbar_init(&sm.bar_mmae[1], 1);
         fence_mbar_init();
+    }
+    pdl_wait();   // everything below may read what earlier work on the stream wrote
+    if (tid == 0) {
+        sm.G = *pk.num_groups;
+        sm.x_total = *pk.m_ptr * pk.m_mult;
     }
     const int gpre = min(pk.group_capacity, kGroupCache);
     for (int g = tid; g < gpre; g += kT) sm.grp[g] = pk.groups[g];
@@ -1572,18 +1576,20 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
 
 const void *engine_kernel_ptr() { return reinterpret_cast<const void *>(engine_kernel); }
 
-void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s, cudaError_t *err)
+void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s, bool pdl, cudaError_t *err)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kEngineThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     *err = cudaLaunchKernelEx(&cfg, engine_kernel, p);
 }
 

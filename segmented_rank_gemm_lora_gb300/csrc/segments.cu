@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(kBuildThreads, 1) build_kernel(BuildParams p)
     int32_t *tmp = smem;   // 33 ints of scan scratch
     uint32_t *err = reinterpret_cast<uint32_t *>(p.header + H_ERR);
     const int32_t L = p.L, M = p.M;
+    pdl_trigger();
+    pdl_wait();   // the previous launch on the stream may still read this workspace
 
     for (int i = threadIdx.x; i < p.sync_ints; i += kBuildThreads) p.sync[i] = 0;
 
@@ -254,6 +256,8 @@ __global__ void __launch_bounds__(32, 1) build_warp_kernel(BuildParams p)
     const int lane = threadIdx.x;
     const int32_t L = p.L, M = p.M;
     uint32_t *err = reinterpret_cast<uint32_t *>(p.header + H_ERR);
+    pdl_trigger();
+    pdl_wait();   // the previous launch on the stream may still read this workspace
     for (int i = lane; i < p.sync_ints; i += 32) p.sync[i] = 0;
     int key = INT32_MAX, v = lane;   // lanes past M sort after everything
     if (lane < M) {
@@ -297,12 +301,23 @@ __global__ void __launch_bounds__(32, 1) build_warp_kernel(BuildParams p)
     }
 }
 
-cudaError_t launch_build(const BuildParams &p, cudaStream_t s)
+cudaError_t launch_build(const BuildParams &p, cudaStream_t s, bool pdl)
 {
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
     if (p.M <= 32 && (p.block_m <= 0 || p.topk_ids == nullptr)) {
-        build_warp_kernel<<<1, 32, 0, s>>>(p);
-        return cudaGetLastError();
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(32);
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, build_warp_kernel, p);
     }
+    // (the block-wide build starts in plain stream order: scheduled early, it was measured to slow the
+    // step down)
+    cfg.numAttrs = 0;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -310,8 +325,10 @@ cudaError_t launch_build(const BuildParams &p, cudaStream_t s)
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    build_kernel<<<1, kBuildThreads, kBuildSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kBuildThreads);
+    cfg.dynamicSmemBytes = kBuildSmemBytes;
+    return cudaLaunchKernelEx(&cfg, build_kernel, p);
 }
 
 }  // namespace lora

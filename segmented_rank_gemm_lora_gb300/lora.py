@@ -23,7 +23,8 @@ STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_CUDA", 3: "LORA_
 LORA_OK, LORA_ERR_INVALID_ARG, LORA_ERR_CUDA, LORA_ERR_OOM = 0, 1, 2, 3
 LORA_ERR_BAD_ADAPTER_ID, LORA_ERR_BAD_EXPERT_ID, LORA_ERR_TIMEOUT, LORA_ERR_WORKSPACE, LORA_ERR_UNSUPPORTED = 4, 5, 6, 7, 8
 LORA_MOE_GATE_UP, LORA_MOE_DOWN = 0, 1
-LORA_OPT_PATH, LORA_OPT_TC_MIN_ROWS, LORA_OPT_WAIT_TIMEOUT_NS, LORA_OPT_GRID_CTAS, LORA_OPT_TEST_WITHHOLD_HANDOFF = range(5)
+LORA_OPT_PATH, LORA_OPT_TC_MIN_ROWS, LORA_OPT_WAIT_TIMEOUT_NS, LORA_OPT_GRID_CTAS, LORA_OPT_TEST_WITHHOLD_HANDOFF, \
+    LORA_OPT_PDL = range(6)
 
 EXPORTED = ["lora_pack_weights", "lora_table_destroy", "lora_table_info", "lora_table_stored_rank",
             "lora_workspace_bytes", "lora_workspace_layout", "lora_build_segments", "lora_apply",

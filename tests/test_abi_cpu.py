@@ -60,6 +60,12 @@ def test_options_roundtrip_and_validation(lib):
     lora.lora_set_option(lora.LORA_OPT_WAIT_TIMEOUT_NS, 5_000_000)
     assert lora.lora_get_option(lora.LORA_OPT_WAIT_TIMEOUT_NS) == 5_000_000
     lora.lora_set_option(lora.LORA_OPT_WAIT_TIMEOUT_NS, old)
+    assert lora.lora_get_option(lora.LORA_OPT_PDL) == 1          # on by default
+    lora.lora_set_option(lora.LORA_OPT_PDL, 0)
+    assert lora.lora_get_option(lora.LORA_OPT_PDL) == 0
+    lora.lora_set_option(lora.LORA_OPT_PDL, 1)
+    with pytest.raises(lora.LoraError):
+        lora.lora_set_option(lora.LORA_OPT_PDL, 2)
     with pytest.raises(lora.LoraError):
         lora.lora_set_option(lora.LORA_OPT_PATH, 7)
     with pytest.raises(lora.LoraError):

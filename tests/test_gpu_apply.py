@@ -229,3 +229,62 @@ def test_large_batch_sampled_rows():
     sub.ids, sub.x, sub.y_base, sub.M = p.ids[rows], p.x[rows], p.y_base[rows], len(rows)
     check_close(host_f64(y)[rows], oracle_dense(sub), "large batch, sampled rows")
     table.destroy()
+
+
+def test_back_to_back_steps_on_one_workspace_with_and_without_pdl():
+    """Steps with different ids enqueued back to back on one workspace (no host sync between them): with
+    programmatic dependent launches the next build may be scheduled while the previous apply still runs,
+    so every kernel must wait before it touches the workspace.  The outputs equal those of plain stream
+    order, bit for bit, eager and replayed from a CUDA graph."""
+    base = synth.decode(11, y_base="random")
+    probs = [base]
+    for q in [synth.decode(12, y_base="random"), synth.decode(13, y_base="random"),
+              synth.prefill(14, y_base="random")]:   # same weights, other batches
+        r = synth.DenseProblem(**{**base.__dict__})
+        r.ids, r.x, r.y_base, r.M = q.ids, q.x, q.y_base, q.M
+        probs.append(r)
+    L = base.L
+    M = max(p.M for p in probs)
+    table = pack_dense(base)
+    ws = lora.Workspace(M, L)
+    ids = [torch.from_numpy(p.ids).cuda() for p in probs]
+    xs = [dev_bf16(p.x) for p in probs]
+
+    def steps(ys):
+        for k in range(3):
+            for i, p in enumerate(probs):
+                lora.lora_build_segments(ws, ids[i])
+                lora.lora_apply(table, ws, xs[i], ys[3 * i + k])
+
+    outs = {}
+    old = lora.lora_get_option(lora.LORA_OPT_PDL)
+    try:
+        for pdl in (0, 1):
+            lora.lora_set_option(lora.LORA_OPT_PDL, pdl)
+            ys = [dev_bf16(p.y_base) for p in probs for _ in range(3)]
+            steps(ys)
+            torch.cuda.synchronize()
+            assert lora.lora_get_status(ws) == lora.LORA_OK
+            outs[pdl] = [host_bits(y) for y in ys]
+        # graph capture with PDL on
+        lora.lora_set_option(lora.LORA_OPT_PDL, 1)
+        ys = [dev_bf16(p.y_base) for p in probs for _ in range(3)]
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            steps(ys)
+        for i, p in enumerate(probs):
+            for k in range(3):
+                ys[3 * i + k].copy_(dev_bf16(p.y_base))
+        g.replay()
+        torch.cuda.synchronize()
+        assert lora.lora_get_status(ws) == lora.LORA_OK
+        outs["graph"] = [host_bits(y) for y in ys]
+    finally:
+        lora.lora_set_option(lora.LORA_OPT_PDL, old)
+    for a, b, c in zip(outs[0], outs[1], outs["graph"]):
+        assert np.array_equal(a, b) and np.array_equal(a, c)
+    for i, p in enumerate(probs):
+        check_close(synth.bf16_bits_to_f32(outs[1][3 * i]).astype(np.float64), oracle_dense(p), "step %d" % i)
+    table.destroy()
