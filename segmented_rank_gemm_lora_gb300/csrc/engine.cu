@@ -874,17 +874,39 @@ __device__ __noinline__ void issue_unit(const EngineParams &p, const CUtensorMap
     }
 }
 
+// The last consumer of a tile resets its counters for the next launch.  Thread 0 counts itself in as
+// soon as its wait is over, and looks at the count only here, an item later (or at exit), so that the
+// atomic's round trip stays off the path.
+struct ConsumerTick {
+    int tg = -1, old = 0, ipt = 0;
+};
+__device__ __forceinline__ void settle_tick(const EngineParams &p, ConsumerTick &c)
+{
+    if (threadIdx.x == 0 && c.tg >= 0 && c.old == c.ipt - 1) {
+        p.sync[c.tg * 4 + 0] = 0;
+        p.sync[c.tg * 4 + 1] = 0;
+        p.sync[c.tg * 4 + 2] = 0;
+    }
+    c.tg = -1;
+}
+
 // Wait until the item's tile has its shrink results, then bring S into
 // shared memory: bf16 [rp/8][128][8] by a bulk copy (tensor cores), fp32
 // [16][rp] (padded rows) from the finished S or summed from the partials (small tiles).
-// The last consumer of the tile resets its counters for the next launch.
-__device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm, const ExpandItem &it, Phases &ph, bool first)
+__device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm, const ExpandItem &it, Phases &ph,
+                                           bool first, ConsumerTick &tick)
 {
     const int tid = threadIdx.x;
     const GroupDims &d = it.d;
+    settle_tick(p, tick);
     if (tid == 0) {
         const bool ok = d.fin ? wait_counter(&p.sync[it.tg * 4 + 2], d.tc ? (it.nrows + kFinRows - 1) / kFinRows : 1, p)
                               : wait_counter(&p.sync[it.tg * 4 + 0], d.n_kc, p);
+        if (ok) {
+            tick.tg = it.tg;
+            tick.ipt = d.ipt;
+            tick.old = atomicAdd(&p.sync[it.tg * 4 + 1], 1);
+        }
         if (ok && d.tc) {
             // S was written by other CTAs through ordinary stores: order them before the async copy
             asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -931,39 +953,36 @@ __device__ __forceinline__ bool item_ready(const EngineParams &p, EngineSmem &sm
     }
     __syncthreads();
     if (first) stamp(p, TS_EX_S);
-    if (tid == 0 && ready) {
-        const int old = atomicAdd(&p.sync[it.tg * 4 + 1], 1);
-        if (old == d.ipt - 1) {   // last consumer of this tile
-            p.sync[it.tg * 4 + 0] = 0;
-            p.sync[it.tg * 4 + 1] = 0;
-            p.sync[it.tg * 4 + 2] = 0;
-        }
-    }
     return ready;
 }
 
-// Small-tile unit in stage st: D[16][nw] = S B_unit^T with m16n8k16 MMAs
-// (tokens as M, 8 output columns per MMA tile, warp w takes column tiles
-// w, w + 8, ..., four at a time), then y = bf16(y_base + scale * w_row * D) for the tile's
-// rows, two columns per store.  Ends with a barrier: the stage is free again.
-__device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int st)
+// Small-tile units in stages st, st + 1, ..., st + n - 1 (mod 3), consecutive units of one item (same
+// rows, same S): D[16][nw] = S B_unit^T with m16n8k16 MMAs (tokens as M, 8 output columns per MMA
+// tile, warp w takes column tiles w, w + 8, ..., four at a time), then y = bf16(y_base + scale * w_row
+// * D) for the tile's rows, two columns per store.  Ends with a barrier: the stages are free again.
+__device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int st, int n)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const UnitRec r = sm.unit[st];
-    const unsigned char *base = sm.pool + es_off(st);
-    const uint32_t b_base = smem_u32(base);
+    const UnitRec r0 = sm.unit[st];
     const uint32_t s_row = smem_u32(sm.pool) + (lane & 15) * kSmSStride * 2;
-    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(base + r.yoff);
     const int gr = lane >> 2, qc = (lane & 3) * 2;
-    const float s0 = gr < r.nrows ? r.scale * sm.row_w[st][gr] : 0.f;
-    const float s1 = gr + 8 < r.nrows ? r.scale * sm.row_w[st][gr + 8] : 0.f;
-    __nv_bfloat16 *y0 = p.y + (int64_t)(gr < r.nrows ? sm.row_dst[st][gr] : 0) * p.ldy + r.n0;
-    __nv_bfloat16 *y1 = p.y + (int64_t)(gr + 8 < r.nrows ? sm.row_dst[st][gr + 8] : 0) * p.ldy + r.n0;
-    const int ntiles = r.nw / 8, steps = r.kgs / 2;
+    const float s0 = gr < r0.nrows ? r0.scale * sm.row_w[st][gr] : 0.f;
+    const float s1 = gr + 8 < r0.nrows ? r0.scale * sm.row_w[st][gr + 8] : 0.f;
+    __nv_bfloat16 *const y0row = p.y + (int64_t)(gr < r0.nrows ? sm.row_dst[st][gr] : 0) * p.ldy;
+    __nv_bfloat16 *const y1row = p.y + (int64_t)(gr + 8 < r0.nrows ? sm.row_dst[st][gr + 8] : 0) * p.ldy;
+    const int steps = r0.kgs / 2;
     uint32_t sa[kMaxRank / 16][4];   // S fragments of every K step, shared by all column tiles
 #pragma unroll
     for (int k = 0; k < kMaxRank / 16; ++k)
         if (k < steps) ldsm_x4(s_row + (2 * k + (lane >> 4)) * 16, sa[k][0], sa[k][1], sa[k][2], sa[k][3]);
+    for (int j = 0; j < n; ++j) {
+    const int sj = st + j < kEsDepth ? st + j : st + j - kEsDepth;
+    const UnitRec r = sm.unit[sj];
+    const unsigned char *base = sm.pool + es_off(sj);
+    const uint32_t b_base = smem_u32(base);
+    const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(base + r.yoff);
+    __nv_bfloat16 *y0 = y0row + r.n0, *y1 = y1row + r.n0;
+    const int ntiles = r.nw / 8;
     // four column tiles per round (w, w + 8, w + 16, w + 24), their MMAs interleaved
     for (int nt0 = warp; nt0 < ntiles; nt0 += 32) {
         float d[4][4];
@@ -1001,6 +1020,7 @@ __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int 
                     fmaf(s1, d[i][2], __bfloat162float(yb.x)), fmaf(s1, d[i][3], __bfloat162float(yb.y)));
             }
         }
+    }
     }
     __syncthreads();
 }
@@ -1506,6 +1526,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
 
     // ------------------------------------------------------------------ expand items
     int seq = 0;     // units computed
+    ConsumerTick tick;   // thread 0: the last tile this CTA counted itself in on
     int pend = -1;   // unit whose MMAs are issued and whose epilogue is pending
     auto drain = [&]() -> bool {   // epilogue of the pending unit, then refill its stage
         const int q = pend, st = q % kEsDepth, buf = q & 1;
@@ -1524,7 +1545,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
             alive = false;
             break;
         }
-        if (!item_ready(p, sm, it, ph, item == e0)) {
+        if (!item_ready(p, sm, it, ph, item == e0, tick)) {
             alive = false;
             break;
         }
@@ -1542,7 +1563,18 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
                     alive = false;
                     break;
                 }
-                sm_unit(p, sm, st);   // ends with a barrier: stage st is free again
+                // the item's next units whose copies have already landed join this pass
+                int n = 1;
+                while (n < it.nu - k && n < issued - seq) {
+                    const int sn = (seq + n) % kEsDepth;
+                    if (!__syncthreads_and(mbar_try_wait(&sm.bar_es[sn], ph.get(PH_ES + sn)) ? 1 : 0)) break;
+                    ph.flip(PH_ES + sn);
+                    inflight &= ~(1u << sn);
+                    ++n;
+                }
+                sm_unit(p, sm, st, n);   // ends with a barrier: the n stages are free again
+                seq += n - 1;
+                k += n - 1;
                 if (seq < 4) stamp(p, TS_EX_UNIT + 2 * seq + 1);
                 prefetch(seq + 1 + kEsDepth);
                 continue;
@@ -1557,6 +1589,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         }
     }
     if (alive && pend >= 0 && !drain()) alive = false;
+    settle_tick(p, tick);
 
     // a CTA that gave up still lets its copies land and its MMAs finish before it leaves
     for (int sl = 0; sl < 2; ++sl)
