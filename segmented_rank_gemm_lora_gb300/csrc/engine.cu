@@ -102,7 +102,6 @@ struct UnitRec {
 
 struct Plan {
     int ta;      // target A bytes of one small-tile shrink item
-    int tb;      // target B bytes of one small-tile expand unit
     int ue;      // 128-row tile expand units per item
     int ues;     // small-tile expand units per item
     int kctc;    // K elements of one tensor-core shrink item
@@ -134,7 +133,7 @@ struct __align__(1024) EngineSmem {
     EngineParams pc;                     // the launch parameters, mirrored (helpers read them from here)
     uint32_t tmem_base;
     int32_t G, flag, x_total;
-    int32_t ta, tb, ue, ues, kctc;       // launch plan (see plan_launch)
+    int32_t ta, ue, ues, kctc;           // launch plan (see plan_launch)
     UnitRec unit[kEsDepth];
     int32_t row_dst[kEsDepth][kTcRows];
     float row_w[kEsDepth][kTcRows];
@@ -192,13 +191,11 @@ __device__ __forceinline__ int pmod(int x, int m)
 }
 __device__ __forceinline__ int ceil_log2(int v) { return v <= 1 ? 0 : 32 - __clz(v - 1); }
 
-// Output columns of one small-tile expand unit: about tb bytes of B, a power of two from 128, and the
-// unit's B rows and y rows must fit a stage.
-__device__ __forceinline__ int sm_unit_width(int rp, int rows1, int tb)
+// Output columns of one small-tile expand unit: the widest power of two whose B rows and y rows fit a
+// stage (at least 256 at the largest rank; measured faster than narrower units that pipeline more).
+__device__ __forceinline__ int sm_unit_width(int rp, int rows1)
 {
-    // (tb is clipped below 2^21: any larger target is past the stage cap anyway)
-    const int ucap = min(kSmMaxUnit, floor_pow2(qdiv_s(kStageBytes / 2, rp + rows1)));
-    return min(max(kTcCols, floor_pow2(qdiv_s(min(tb, (1 << 21) - 1), 2 * rp))), ucap);
+    return max(kTcCols, min(kSmMaxUnit, floor_pow2(qdiv_s(kStageBytes / 2, rp + rows1))));
 }
 
 // Sizes of group g under plan pl, from scratch.
@@ -227,7 +224,7 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
         const int cap = max(64, min((qdiv_s(kSmXBytes, d.rows1) - 16) / 2, qdiv_s(kSmABytes / 2, d.R)) & ~63);
         const int want = max(64, (qdiv_s(min(pl.ta, (1 << 21) - 1), 2 * d.R) + 63) & ~63);
         d.kc = min(min(cap, kmax), want);
-        d.uw = sm_unit_width(d.rp, d.rows1, pl.tb);
+        d.uw = sm_unit_width(d.rp, d.rows1);
         d.ue = pl.ues;
     }
     d.n_kc = qdiv_s(p.K + d.kc - 1, d.kc);   // K <= 2^20
@@ -1163,15 +1160,13 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
 {
     const int lane = threadIdx.x & 31;
     const int grid = gridDim.x;
-    int N = 0, tc_units = 0;   // output columns; 128-column units of one tile over all slices
+    int tc_units = 0;   // 128-column units of one tile over all slices
 #pragma unroll 1
-    for (int s = 0; s < p.n_slices; ++s) {
-        N += p.slice_n[s];
-        tc_units += (p.slice_n[s] + kTcCols - 1) >> 7;
-    }
+    for (int s = 0; s < p.n_slices; ++s) tc_units += (p.slice_n[s] + kTcCols - 1) >> 7;
     // pass 1: validate; small-tile A and B bytes (in units of K and N bf16 elements), 128-row tile units
     bool bad = false;
-    int bga = 0, bgb = 0;   // (below 2^21: at most 65536 / 16 + 2048 tiles of at most 256 rows)
+    int bga = 0;            // (below 2^21: at most 65536 / 16 + 2048 tiles of at most 256 rows)
+    int units = 0;          // small-tile expand units
     int tcu = 0, tci = 0;
     any_tc = false;
 #pragma unroll 1
@@ -1192,13 +1187,17 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
         } else {
             const int tiles = (gr.w + kBgmvRows - 1) >> 4;
             bga += tiles * p.n_a * rp;
-            bgb += tiles * rp;
+            const int lw = ceil_log2(sm_unit_width(rp, min(gr.w, kSmRows)));
+            int u = 0;
+#pragma unroll 1
+            for (int s = 0; s < p.n_slices; ++s) u += (p.slice_n[s] + (1 << lw) - 1) >> lw;
+            units += tiles * u;
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         bga += __shfl_xor_sync(0xffffffffu, bga, o);
-        bgb += __shfl_xor_sync(0xffffffffu, bgb, o);
+        units += __shfl_xor_sync(0xffffffffu, units, o);
         tcu += __shfl_xor_sync(0xffffffffu, tcu, o);
         tci += __shfl_xor_sync(0xffffffffu, tci, o);
     }
@@ -1206,7 +1205,7 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     any_tc = __any_sync(0xffffffffu, any_tc);
     if (bad) return false;
     // small-tile chunks of about a CTA's share of the A bytes (a quarter more, so that rounding up to
-    // whole chunks rarely needs a second wave); expand units of about 2/5 of a CTA's B share
+    // whole chunks rarely needs a second wave)
     Plan pl;
     // 128-row tile K-chunks of kTcKc; when that would make between one and two waves of shrink items
     // (some CTAs with two, most with one), chunks just long enough for one wave instead
@@ -1220,27 +1219,10 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     const int spare = max(grid / 4, grid - tci);
     // (targets, not sizes: the fast divides only need to agree between CTAs, and they run the same code)
     pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, __fdividef(2.5f * (float)p.K * (float)bga, (float)spare)));
-    pl.tb = (int)fminf(268435456.f, fmaxf(4096.f, __fdividef(2.f * (float)N * (float)bgb, 2.5f * grid)));
     pl.ue = min(128, max(1, qdiv(tcu + kItemsPerCta * grid - 1, kItemsPerCta * grid)));
     pl.kctc = kctc;
-    // small-tile expand units of the launch -> units per item, so that the items fit one wave
-    {
-        int units = 0;
-#pragma unroll 1
-        for (int g = lane; g < G; g += 32) {
-            const int4 gr = g < kGroupCache ? sm.grp[g] : p.groups[g];
-            const int rp = gr.x < kRankCache ? sm.rp_cache[gr.x] : p.rpad[gr.x];
-            if (group_on_tc(p, gr.w, p.n_a * rp)) continue;
-            const int lw = ceil_log2(sm_unit_width(rp, min(gr.w, kSmRows), pl.tb));
-            int u = 0;
-#pragma unroll 1
-            for (int s = 0; s < p.n_slices; ++s) u += (p.slice_n[s] + (1 << lw) - 1) >> lw;
-            units += ((gr.w + kSmRows - 1) / kSmRows) * u;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
-        pl.ues = min(16, max(1, qdiv(units + grid - 1, grid)));
-    }
+    // small-tile expand units per item, so that the items fit one wave
+    pl.ues = min(16, max(1, qdiv(units + grid - 1, grid)));
     // pass 2: per-group item counts and their exclusive prefix sums, 32 groups per step; larger chunks
     // until the hand-off scratch fits the workspace
 #pragma unroll 1
@@ -1297,7 +1279,6 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
             sm.tile_pre[G] = c_tile;
             sm.part_pre[G] = (int)c_part;
             sm.ta = pl.ta;
-            sm.tb = pl.tb;
             sm.ue = pl.ue;
             sm.kctc = pl.kctc;
             sm.ues = pl.ues;
@@ -1399,7 +1380,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         __syncthreads();
         tc::fence_after_sync();
     }
-    const Plan pl = {sm.ta, sm.tb, sm.ue, sm.ues, sm.kctc};
+    const Plan pl = {sm.ta, sm.ue, sm.ues, sm.kctc};
     stamp(p, TS_WORKLIST);
 
     Phases ph = {0u};
