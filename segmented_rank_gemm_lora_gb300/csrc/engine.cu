@@ -103,7 +103,7 @@ struct UnitRec {
 struct Plan {
     int ta;      // target A bytes of one small-tile shrink item
     int ue;      // 128-row tile expand units per item
-    int ues;     // small-tile expand units per item
+    int ccol;    // output columns of one small-tile expand item the plan aims for
     int kctc;    // K elements of one tensor-core shrink item
 };
 
@@ -133,7 +133,7 @@ struct __align__(1024) EngineSmem {
     EngineParams pc;                     // the launch parameters, mirrored (helpers read them from here)
     uint32_t tmem_base;
     int32_t G, flag, x_total;
-    int32_t ta, ue, ues, kctc;           // launch plan (see plan_launch)
+    int32_t ta, ue, ccol, kctc;          // launch plan (see plan_launch)
     UnitRec unit[kEsDepth];
     int32_t row_dst[kEsDepth][kTcRows];
     float row_w[kEsDepth][kTcRows];
@@ -225,7 +225,9 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
         const int want = max(64, (qdiv_s(min(pl.ta, (1 << 21) - 1), 2 * d.R) + 63) & ~63);
         d.kc = min(min(cap, kmax), want);
         d.uw = sm_unit_width(d.rp, d.rows1);
-        d.ue = pl.ues;
+        // units per item: about ccol columns whatever the unit width, so that items of narrow-unit (high
+        // rank) and wide-unit groups cost about the same
+        d.ue = max(1, min(16, (pl.ccol + (d.uw >> 1)) >> ceil_log2(d.uw)));
     }
     d.n_kc = qdiv_s(p.K + d.kc - 1, d.kc);   // K <= 2^20
     const int lw = ceil_log2(d.uw);   // unit widths are powers of two
@@ -1160,13 +1162,16 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
 {
     const int lane = threadIdx.x & 31;
     const int grid = gridDim.x;
-    int tc_units = 0;   // 128-column units of one tile over all slices
+    int N = 0, tc_units = 0;   // output columns; 128-column units of one tile over all slices
 #pragma unroll 1
-    for (int s = 0; s < p.n_slices; ++s) tc_units += (p.slice_n[s] + kTcCols - 1) >> 7;
+    for (int s = 0; s < p.n_slices; ++s) {
+        N += p.slice_n[s];
+        tc_units += (p.slice_n[s] + kTcCols - 1) >> 7;
+    }
     // pass 1: validate; small-tile A and B bytes (in units of K and N bf16 elements), 128-row tile units
     bool bad = false;
     int bga = 0;            // (below 2^21: at most 65536 / 16 + 2048 tiles of at most 256 rows)
-    int units = 0;          // small-tile expand units
+    int stiles = 0;         // small tiles
     int tcu = 0, tci = 0;
     any_tc = false;
 #pragma unroll 1
@@ -1187,17 +1192,13 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
         } else {
             const int tiles = (gr.w + kBgmvRows - 1) >> 4;
             bga += tiles * p.n_a * rp;
-            const int lw = ceil_log2(sm_unit_width(rp, min(gr.w, kSmRows)));
-            int u = 0;
-#pragma unroll 1
-            for (int s = 0; s < p.n_slices; ++s) u += (p.slice_n[s] + (1 << lw) - 1) >> lw;
-            units += tiles * u;
+            stiles += tiles;
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         bga += __shfl_xor_sync(0xffffffffu, bga, o);
-        units += __shfl_xor_sync(0xffffffffu, units, o);
+        stiles += __shfl_xor_sync(0xffffffffu, stiles, o);
         tcu += __shfl_xor_sync(0xffffffffu, tcu, o);
         tci += __shfl_xor_sync(0xffffffffu, tci, o);
     }
@@ -1221,8 +1222,8 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, __fdividef(2.5f * (float)p.K * (float)bga, (float)spare)));
     pl.ue = min(128, max(1, qdiv(tcu + kItemsPerCta * grid - 1, kItemsPerCta * grid)));
     pl.kctc = kctc;
-    // small-tile expand units per item, so that the items fit one wave
-    pl.ues = min(16, max(1, qdiv(units + grid - 1, grid)));
+    // small-tile expand items of about one wave's share of all (tile, output column) pairs
+    pl.ccol = (int)fminf(1073741824.f, __fdividef((float)stiles * (float)N, (float)grid) + 1.f);
     // pass 2: per-group item counts and their exclusive prefix sums, 32 groups per step; larger chunks
     // until the hand-off scratch fits the workspace
 #pragma unroll 1
@@ -1281,7 +1282,7 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
             sm.ta = pl.ta;
             sm.ue = pl.ue;
             sm.kctc = pl.kctc;
-            sm.ues = pl.ues;
+            sm.ccol = pl.ccol;
         }
         if ((int64_t)c_part <= p.partial_floats || (pl.ta >= (1 << 27) && pl.kctc >= p.K)) break;
         pl.ta = min(1 << 28, pl.ta * 4);
@@ -1380,7 +1381,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         __syncthreads();
         tc::fence_after_sync();
     }
-    const Plan pl = {sm.ta, sm.ue, sm.ues, sm.kctc};
+    const Plan pl = {sm.ta, sm.ue, sm.ccol, sm.kctc};
     stamp(p, TS_WORKLIST);
 
     Phases ph = {0u};
