@@ -970,10 +970,8 @@ __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int 
     __nv_bfloat16 *const y0row = p.y + (int64_t)(gr < r0.nrows ? sm.row_dst[st][gr] : 0) * p.ldy;
     __nv_bfloat16 *const y1row = p.y + (int64_t)(gr + 8 < r0.nrows ? sm.row_dst[st][gr + 8] : 0) * p.ldy;
     const int steps = r0.kgs / 2;
-    uint32_t sa[kMaxRank / 16][4];   // S fragments of every K step, shared by all column tiles
-#pragma unroll
-    for (int k = 0; k < kMaxRank / 16; ++k)
-        if (k < steps) ldsm_x4(s_row + (2 * k + (lane >> 4)) * 16, sa[k][0], sa[k][1], sa[k][2], sa[k][3]);
+    // (the K loop stays rolled and reloads its S fragment: this code runs about once per launch, where
+    // its size, not its instruction count, sets the time)
     for (int j = 0; j < n; ++j) {
     const int sj = st + j < kEsDepth ? st + j : st + j - kEsDepth;
     const UnitRec r = sm.unit[sj];
@@ -987,20 +985,20 @@ __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int 
         float d[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < steps; ++k) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(s_row + (2 * k + (lane >> 4)) * 16, a0, a1, a2, a3);
 #pragma unroll
-        for (int k = 0; k < kMaxRank / 16; ++k) {
-            if (k < steps) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int n = (nt0 + 8 * i) * 8;
-                    if (n < r.nw) {
-                        // B rows n .. n + 7 of K-group kg: [(tl * kgs + kg) * tw + col] in 16-byte units
-                        const int tl = n / kNTile, col = n % kNTile;
-                        uint32_t b0, b1;
-                        ldsm_x2(b_base + ((tl * r.kgs + 2 * k + ((lane >> 3) & 1)) * r.tw + col + (lane & 7)) * 16,
-                                b0, b1);
-                        mma16816(d[i], sa[k][0], sa[k][1], sa[k][2], sa[k][3], b0, b1);
-                    }
+            for (int i = 0; i < 4; ++i) {
+                const int n = (nt0 + 8 * i) * 8;
+                if (n < r.nw) {
+                    // B rows n .. n + 7 of K-group kg: [(tl * kgs + kg) * tw + col] in 16-byte units
+                    const int tl = n / kNTile, col = n % kNTile;
+                    uint32_t b0, b1;
+                    ldsm_x2(b_base + ((tl * r.kgs + 2 * k + ((lane >> 3) & 1)) * r.tw + col + (lane & 7)) * 16,
+                            b0, b1);
+                    mma16816(d[i], a0, a1, a2, a3, b0, b1);
                 }
             }
         }
