@@ -62,6 +62,7 @@ constexpr int kSmABytes = 40 * 1024;            // A chunk at the slot's start: 
 constexpr int kSmXOff = kSmABytes;              // x rows after it: [rows][kc + 8] (padded rows)
 constexpr int kSmXBytes = kSmSlotBytes - kSmABytes;
 constexpr int kSmRedOff = 2 * kSmSlotBytes;     // cross-warp sums of the shrink: [3][16][32] fp32 at most
+constexpr int kFmaRows = 2;                     // small tiles of at most this many rows expand on CUDA cores
 constexpr int kSmMaxUnit = 1024;                // output columns of one small expand unit, at most
 constexpr int kSmSStride = kMaxRank + 8;        // bf16 per row of S in shared memory (padded rows)
 constexpr int64_t kDirectLoads = 128 * 1024;    // partial loads of a tile's expand items below which they sum them
@@ -969,6 +970,68 @@ __device__ __noinline__ void sm_unit(const EngineParams &p, EngineSmem &sm, int 
     const float s1 = gr + 8 < r0.nrows ? r0.scale * sm.row_w[st][gr + 8] : 0.f;
     __nv_bfloat16 *const y0row = p.y + (int64_t)(gr < r0.nrows ? sm.row_dst[st][gr] : 0) * p.ldy;
     __nv_bfloat16 *const y1row = p.y + (int64_t)(gr + 8 < r0.nrows ? sm.row_dst[st][gr + 8] : 0) * p.ldy;
+    if (r0.nrows <= kFmaRows) {
+        // a few rows: CUDA-core dot products, two adjacent output columns per thread (the MMAs' 16-row
+        // tiles would be mostly empty, and their dependent rounds cost more than the arithmetic)
+        const __nv_bfloat16 *S = reinterpret_cast<const __nv_bfloat16 *>(sm.pool);
+        const int tid = threadIdx.x, nr = r0.nrows;
+        float sc[kFmaRows];
+        __nv_bfloat16 *yr[kFmaRows];
+#pragma unroll
+        for (int i = 0; i < kFmaRows; ++i) {
+            sc[i] = i < nr ? r0.scale * sm.row_w[st][i] : 0.f;
+            yr[i] = p.y + (int64_t)sm.row_dst[st][i < nr ? i : 0] * p.ldy;
+        }
+        // column pairs of all n units, spread over every thread
+        int pairs = 0;
+        for (int j = 0; j < n; ++j) pairs += sm.unit[st + j < kEsDepth ? st + j : st + j - kEsDepth].nw >> 1;
+        for (int q = tid; q < pairs; q += kT) {
+            int j = 0, c = 2 * q;
+            int sj = st;
+            UnitRec r = sm.unit[sj];
+            while (c >= r.nw) {   // (at most three units)
+                c -= r.nw;
+                ++j;
+                sj = st + j < kEsDepth ? st + j : st + j - kEsDepth;
+                r = sm.unit[sj];
+            }
+            const unsigned char *base = sm.pool + es_off(sj);
+            const __nv_bfloat16 *ys = reinterpret_cast<const __nv_bfloat16 *>(base + r.yoff);
+            // B rows c, c + 1 of K-group kg: [(tl * kgs + kg) * tw + col] in 16-byte units
+            const uint4 *bp = reinterpret_cast<const uint4 *>(base) + ((c >> 7) * r.kgs) * r.tw + (c & 127);
+            float acc[kFmaRows][2];
+#pragma unroll
+            for (int i = 0; i < kFmaRows; ++i) acc[i][0] = acc[i][1] = 0.f;
+#pragma unroll 1
+            for (int kg = 0; kg < r.kgs; ++kg, bp += r.tw) {
+                float b0[8], b1[8];
+                bf16x8_to_f32(bp[0], b0);
+                bf16x8_to_f32(bp[1], b1);
+#pragma unroll
+                for (int i = 0; i < kFmaRows; ++i) {
+                    if (i < nr) {
+                        float sv[8];
+                        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(S + i * kSmSStride + kg * 8), sv);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            acc[i][0] = fmaf(sv[e], b0[e], acc[i][0]);
+                            acc[i][1] = fmaf(sv[e], b1[e], acc[i][1]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kFmaRows; ++i) {
+                if (i < nr) {
+                    const __nv_bfloat162 yb = *reinterpret_cast<const __nv_bfloat162 *>(ys + i * r.ystride + c);
+                    *reinterpret_cast<__nv_bfloat162 *>(yr[i] + r.n0 + c) = __floats2bfloat162_rn(
+                        fmaf(sc[i], acc[i][0], __bfloat162float(yb.x)), fmaf(sc[i], acc[i][1], __bfloat162float(yb.y)));
+                }
+            }
+        }
+        __syncthreads();
+        return;
+    }
     const int steps = r0.kgs / 2;
     // (the K loop stays rolled and reloads its S fragment: this code runs about once per launch, where
     // its size, not its instruction count, sets the time)
