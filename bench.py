@@ -2,9 +2,10 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config decode]
 
-One step = lora_build_segments + lora_apply (the MoE config: build +
-gate/up delta + down delta) over one batch of synthetic inputs, already
-resident in HBM.  To keep L2 (129 MB) from serving the weights, every step
+One step = lora_build_segments + lora_apply, made as the one public call
+lora_build_and_apply (one launch for decode-sized batches), or for the MoE
+config build + gate/up delta + down delta, over one batch of synthetic inputs,
+already resident in HBM.  To keep L2 (129 MB) from serving the weights, every step
 uses the next of R independent input sets (own adapter table, ids, x, y),
 with R * bytes-per-set above 2x L2.  Steps are issued as one CUDA graph and
 timed with CUDA events on the launching stream, bracketed by a barrier and a
@@ -318,6 +319,10 @@ def build_sets(config, R, torch, lora, dev, first=0):
             s["x"] = _to_dev(p.x, torch, dev)
             s["y"] = _to_dev(p.y_base, torch, dev)
             s["ws"] = lora.Workspace(p.M, p.L, device=dev)
+            # the rule lora_build_and_apply follows under the default options (lora.h): one launch when no
+            # group can reach the tensor-core threshold (32 rows, 16 for A blocks over 128 rows)
+            max_R = p.n_a * max(lora.lora_rank_padded(r) for r in p.ranks)
+            s["fused"] = 0 < p.M <= (16 if max_R > 128 else 32)
             s["alg"] = dense_algorithmic(p)
             s["tokens"] = p.M
             s["bytes"] = s["x"].numel() * 2 + s["y"].numel() * 2 + s["table"].info().device_bytes
@@ -334,9 +339,11 @@ def step(s, lora, build=True):
         lora.lora_moe_delta(s["dn"], lora.LORA_MOE_DOWN, s["ws"], s["c2"], s["c3"])
         return (1 if build else 0) + 2
     if build:
-        lora.lora_build_segments(s["ws"], s["ids"])
+        # lora_build_segments + lora_apply as one public call: one launch for decode-sized batches
+        lora.lora_build_and_apply(s["table"], s["ws"], s["ids"], s["x"], s["y"])
+        return 1 if s["fused"] else 2
     lora.lora_apply(s["table"], s["ws"], s["x"], s["y"])
-    return (1 if build else 0) + 1
+    return 1
 
 
 def capture(torch, fn, stream):
@@ -462,7 +469,9 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": "%s: %s" % (args.config, CONFIGS[args.config]),
-                           "step": "build_segments + " + ("gate/up + down deltas" if "gu" in sets[0] else "apply"),
+                           "step": ("build_segments + gate/up + down deltas" if "gu" in sets[0] else
+                                    "lora_build_and_apply (build_segments + apply; %s)" %
+                                    ("one launch" if sets[0].get("fused") else "two launches")),
                            "l2": "inputs larger than L2: %d rotating input sets, %.0f MB each" % (R, per_set / 1e6),
                            "parallelism": "replicas x%d" % world},
                 "gpu_launches": gpu_launches, "roofline": roofline, "e2e": e2e, "clocks": clk,

@@ -213,6 +213,22 @@ lora_status lora_build_segments(const lora_workspace *ws, const int32_t *d_lora_
 lora_status lora_apply(lora_table table, const lora_workspace *ws, const void *d_x, int64_t ldx, void *d_y,
                        int64_t ldy, lora_stream_t stream);
 
+/*
+ * lora_build_segments(ws, d_lora_id_map, M, NULL, NULL) followed by
+ * lora_apply(table, ws, d_x, ldx, d_y, ldy): the same results, bit for bit,
+ * and the same segment table left in `ws` for later lora_apply calls.  When
+ * every group is sure to run on small tiles (dense, M <= 32, M at most
+ * LORA_OPT_TC_MIN_ROWS, or half of it when the table's largest A block has
+ * more than 128 rows, or LORA_OPT_PATH = 1) both run in one launch: each
+ * thread block sorts the ids itself, and one of them writes the table.  That
+ * launch does not reset the workspace scratch; it needs the scratch as every
+ * launch that completed without error leaves it (a fresh zero-filled
+ * workspace, or one that lora_build_segments has reset, after an error).
+ * Otherwise it makes the two calls.  Errors: those of the two calls.
+ */
+lora_status lora_build_and_apply(lora_table table, const lora_workspace *ws, const int32_t *d_lora_id_map, int32_t M,
+                                 const void *d_x, int64_t ldx, void *d_y, int64_t ldy, lora_stream_t stream);
+
 typedef enum { LORA_MOE_GATE_UP = 0, LORA_MOE_DOWN = 1 } lora_moe_stage;
 
 /*

@@ -427,7 +427,8 @@ extern "C" lora_status lora_build_segments(const lora_workspace *ws, const int32
 
 static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLayout &w, bool moe, int32_t src_div,
                               const void *x, int64_t ldx, int64_t x_rows, void *y, int64_t ldy,
-                              const float *row_weight, lora_stream_t stream)
+                              const float *row_weight, lora_stream_t stream, const int32_t *fused_ids = nullptr,
+                              int32_t fused_M = 0)
 {
     // scratch needed per row of work at this table's largest A block, at the largest K-chunk of a
     // 16-row small tile (x rows <= 15 KB, A chunk <= 40 KB), plus the row's finished S
@@ -504,6 +505,13 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
     p.tc_min_rows = (int32_t)g_opt_tc_min_rows.load();
     p.trace = static_cast<uint64_t *>(g_trace.load());
     p.trace_ctas = p.trace ? (int32_t)(g_trace_bytes.load() / (8 * kTraceSlots)) : 0;
+    if (fused_ids) {
+        p.ids = fused_ids;
+        p.ids_M = fused_M;
+        p.ws_header = header;
+        p.ws_perm = at<int32_t>(ws, w.perm);
+        p.ws_segments = at<int4>(ws, w.segments);
+    }
     int grid = di.sms * di.engine_blocks_per_sm;
     const int64_t want = g_opt_grid.load();
     if (want > 0 && want < grid) grid = (int)want;
@@ -527,6 +535,31 @@ extern "C" lora_status lora_apply(lora_table t, const lora_workspace *ws, const 
     if (t->E_A != 1 || t->E_B != 1) return LORA_ERR_INVALID_ARG;
     if (ldx < t->K || ldy < t->N || ldx % 8 || ldy % 8 || !aligned16(d_x) || !aligned16(d_y)) return LORA_ERR_INVALID_ARG;
     return run_engine(t, ws, w, false, 1, d_x, ldx, ws->max_M, d_y, ldy, nullptr, stream);
+}
+
+extern "C" lora_status lora_build_and_apply(lora_table t, const lora_workspace *ws, const int32_t *d_ids, int32_t M,
+                                            const void *d_x, int64_t ldx, void *d_y, int64_t ldy,
+                                            lora_stream_t stream)
+{
+    if (!valid_table(t) || !d_x || !d_y) return LORA_ERR_INVALID_ARG;
+    WsLayout w;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    if (ws->L != t->L) return LORA_ERR_INVALID_ARG;
+    if (t->E_A != 1 || t->E_B != 1) return LORA_ERR_INVALID_ARG;
+    if (ldx < t->K || ldy < t->N || ldx % 8 || ldy % 8 || !aligned16(d_x) || !aligned16(d_y)) return LORA_ERR_INVALID_ARG;
+    if (M < 0 || (M > 0 && !d_ids)) return LORA_ERR_INVALID_ARG;
+    if (M > ws->max_M) return LORA_ERR_WORKSPACE;
+    // one launch when every group is sure to run on small tiles (no group can exceed the tensor-core
+    // threshold), else the two calls it stands for
+    const int64_t path = g_opt_path.load(), thr = g_opt_tc_min_rows.load();
+    const bool all_small = path == 1 || (path == 0 && M <= (t->max_R > 128 ? thr / 2 : thr));
+    if (M == 0 || M > 32 || !all_small) {
+        st = lora_build_segments(ws, d_ids, M, nullptr, nullptr, stream);
+        if (st != LORA_OK) return st;
+        return lora_apply(t, ws, d_x, ldx, d_y, ldy, stream);
+    }
+    return run_engine(t, ws, w, false, 1, d_x, ldx, ws->max_M, d_y, ldy, nullptr, stream, d_ids, M);
 }
 
 extern "C" lora_status lora_moe_delta(lora_table t, int32_t stage, const lora_workspace *ws, const void *d_in,

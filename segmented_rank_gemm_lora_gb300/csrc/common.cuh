@@ -95,6 +95,12 @@ struct EngineParams {
     int32_t tc_min_rows;     // groups with more rows take 128-row tiles
     uint64_t *trace;         // optional [trace_ctas][32] phase stamps
     int32_t trace_ctas;
+    // segment build fused into the launch (dense, at most 32 tokens): every CTA sorts ids itself and
+    // CTA 0 also writes the segment table to the workspace; ids == nullptr reads the last build's table
+    const int32_t *ids;
+    int32_t ids_M;
+    int32_t *ws_header, *ws_perm;
+    int4 *ws_segments;
 };
 
 void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s, bool pdl, cudaError_t *err);
@@ -242,6 +248,41 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns)
 {
     asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+
+// Dense batches of at most 32 tokens, one token per lane of one warp: the (key, token index) pairs go
+// through a bitonic network of lane shuffles, ascending; comparing the index as well makes the order
+// stable, so it equals a stable counting sort on the key.  key = adapter id, or L for tokens without one
+// (-1, bad or disabled ids; lanes past M sort after everything).  Returns this lane's pair after the
+// sort; `bad` is set on lanes whose id is neither -1 nor in [0, L).
+__device__ __forceinline__ void warp_sort_ids(const int32_t *ids, const uint8_t *enabled, int M, int L, int &key,
+                                              int &v, bool &bad)
+{
+    const int lane = threadIdx.x & 31;
+    key = INT32_MAX;
+    v = lane;
+    bad = false;
+    if (lane < M) {
+        const int32_t i = ids[lane];
+        bad = i < -1 || i >= L;
+        key = (i >= 0 && i < L && (enabled == nullptr || enabled[i])) ? i : L;
+    }
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int ok = __shfl_xor_sync(0xffffffffu, key, stride);
+            const int ov = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool ascending = (lane & size) == 0;
+            const bool low = (lane & stride) == 0;
+            const bool greater = key > ok || (key == ok && v > ov);
+            // the lower lane of an ascending pair keeps the smaller pair, the upper lane the larger
+            if (low == ascending ? greater : !greater) {
+                key = ok;
+                v = ov;
+            }
+        }
+    }
 }
 
 // 8 bf16 (one uint4) -> 8 floats

@@ -138,7 +138,7 @@ struct __align__(1024) EngineSmem {
     UnitRec unit[kEsDepth];
     int32_t row_dst[kEsDepth][kTcRows];
     float row_w[kEsDepth][kTcRows];
-    int32_t row_src[kTcRows];
+    int32_t row_src[kTcRows];            // (with the build fused in, where every tile is small: the row list)
     int32_t sh_pre[kGroupCap + 1];       // 128-row tile shrink items before group g
     int32_t shs_pre[kGroupCap + 1];      // small-tile shrink items before group g
     int32_t fin_pre[kGroupCap + 1];      // finish items before group g
@@ -1386,12 +1386,54 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         fence_mbar_init();
     }
     pdl_wait();   // everything below may read what earlier work on the stream wrote
-    if (tid == 0) {
-        sm.G = *pk.num_groups;
-        sm.x_total = *pk.m_ptr * pk.m_mult;
+    if (pk.ids != nullptr) {
+        // the segment build fused in (dense, at most 32 tokens): warp 0 of every CTA sorts the ids itself,
+        // and CTA 0 also leaves the table in the workspace for later launches
+        if (warp == 0) {
+            const int lane = tid, M = pk.ids_M, L = pk.L;
+            int key, v;
+            bool bad;
+            warp_sort_ids(pk.ids, nullptr, M, L, key, v, bad);
+            const bool valid = lane < M && key < L;
+            const int prev = __shfl_up_sync(0xffffffffu, key, 1);
+            const bool start = valid && (lane == 0 || prev != key);
+            const uint32_t starts = __ballot_sync(0xffffffffu, start);
+            const int num_valid = __popc(__ballot_sync(0xffffffffu, valid));
+            sm.row_src[lane] = v;
+            int4 seg = make_int4(0, 0, 0, 0);
+            const int si = __popc(starts & ((1u << lane) - 1u));
+            if (start) {
+                const uint32_t later = starts & ~((2u << lane) - 1u);   // segment starts after this lane
+                seg = make_int4(key, 0, lane, (later ? __ffs(later) - 1 : num_valid) - lane);
+                sm.grp[si] = seg;
+            }
+            if (lane == 0) {
+                sm.G = __popc(starts);
+                sm.x_total = M;
+            }
+            if (b == 0) {
+                if (lane < M) pk.ws_perm[lane] = v;
+                if (start) pk.ws_segments[si] = seg;
+                if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(pk.err, kErrBadId);
+                if (lane == 0) {
+                    pk.ws_header[H_M] = M;
+                    pk.ws_header[H_NUM_SEGMENTS] = __popc(starts);
+                    pk.ws_header[H_NUM_VALID] = num_valid;
+                    pk.ws_header[H_NUM_MOE_GROUPS] = 0;
+                    pk.ws_header[H_BLOCK_M] = 0;
+                }
+            }
+            // the row list is read through the parameter mirror: point it at this CTA's copy
+            if (lane == 0) sm.pc.rows = sm.row_src;
+        }
+    } else {
+        if (tid == 0) {
+            sm.G = *pk.num_groups;
+            sm.x_total = *pk.m_ptr * pk.m_mult;
+        }
+        const int gpre = min(pk.group_capacity, kGroupCache);
+        for (int g = tid; g < gpre; g += kT) sm.grp[g] = pk.groups[g];
     }
-    const int gpre = min(pk.group_capacity, kGroupCache);
-    for (int g = tid; g < gpre; g += kT) sm.grp[g] = pk.groups[g];
     for (int a = tid; a < min(pk.L, kRankCache); a += kT) sm.rp_cache[a] = pk.rpad[a];
     __syncthreads();
     stamp(p, TS_PRO_LOADED);

@@ -246,11 +246,9 @@ __global__ void __launch_bounds__(kBuildThreads, 1) build_kernel(BuildParams p)
     }
 }
 
-// Dense batches of at most 32 tokens: one warp, one token per lane.  The
-// (key, token index) pairs are put in order by a bitonic network of lane
-// shuffles; comparing the index as well makes the order stable, so the
-// result equals the counting sort above.  Segments start where the key
-// changes.
+// Dense batches of at most 32 tokens: one warp, one token per lane, sorted by
+// warp_sort_ids (a stable bitonic network of lane shuffles, so the result
+// equals the counting sort above).  Segments start where the key changes.
 __global__ void __launch_bounds__(32, 1) build_warp_kernel(BuildParams p)
 {
     const int lane = threadIdx.x;
@@ -259,28 +257,10 @@ __global__ void __launch_bounds__(32, 1) build_warp_kernel(BuildParams p)
     pdl_trigger();
     pdl_wait();   // the previous launch on the stream may still read this workspace
     for (int i = lane; i < p.sync_ints; i += 32) p.sync[i] = 0;
-    int key = INT32_MAX, v = lane;   // lanes past M sort after everything
-    if (lane < M) {
-        const int32_t i = p.ids[lane];
-        if (i < -1 || i >= L) atomicOr(err, kErrBadId);
-        key = (i >= 0 && i < L && (p.enabled == nullptr || p.enabled[i])) ? i : L;
-    }
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int ok = __shfl_xor_sync(0xffffffffu, key, stride);
-            const int ov = __shfl_xor_sync(0xffffffffu, v, stride);
-            const bool ascending = (lane & size) == 0;
-            const bool low = (lane & stride) == 0;
-            const bool greater = key > ok || (key == ok && v > ov);
-            // the lower lane of an ascending pair keeps the smaller pair, the upper lane the larger
-            if (low == ascending ? greater : !greater) {
-                key = ok;
-                v = ov;
-            }
-        }
-    }
+    int key, v;
+    bool bad;
+    warp_sort_ids(p.ids, p.enabled, M, L, key, v, bad);
+    if (bad) atomicOr(err, kErrBadId);
     if (lane < M) p.perm[lane] = v;
     const bool valid = lane < M && key < L;
     const int prev = __shfl_up_sync(0xffffffffu, key, 1);

@@ -29,7 +29,7 @@ LORA_OPT_PATH, LORA_OPT_TC_MIN_ROWS, LORA_OPT_WAIT_TIMEOUT_NS, LORA_OPT_GRID_CTA
 EXPORTED = ["lora_pack_weights", "lora_table_destroy", "lora_table_info", "lora_table_stored_rank",
             "lora_workspace_bytes", "lora_workspace_layout", "lora_build_segments", "lora_apply",
             "lora_moe_delta", "lora_get_status", "lora_status_string", "lora_set_option", "lora_get_option",
-            "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch"]
+            "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch", "lora_build_and_apply"]
 
 
 class LoraError(RuntimeError):
@@ -100,6 +100,7 @@ def load(build_if_missing: bool = False):
         "lora_rank_padded": (_c_i32, [_c_i32]),
         "lora_set_trace": (_c_i32, [P, _c_sz]),
         "lora_apply_static_scratch": (_c_i32, [P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
+        "lora_build_and_apply": (_c_i32, [P, P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -263,6 +264,23 @@ def lora_apply(table: Table, ws: Workspace, x: torch.Tensor, y: torch.Tensor, st
         raise ValueError("x and y need the %d rows of the last lora_build_segments" % ws.built_M)
     _check(load().lora_apply(table.handle, ws.ref, x.data_ptr(), x.stride(0), y.data_ptr(), y.stride(0),
                              _stream(stream)), "lora_apply")
+
+
+def lora_build_and_apply(table: Table, ws: Workspace, ids: torch.Tensor, x: torch.Tensor, y: torch.Tensor,
+                         stream=None):
+    """lora_build_segments(ws, ids) then lora_apply(table, ws, x, y), in one launch for decode-sized batches."""
+    if ids.dtype != torch.int32 or not ids.is_cuda or not ids.is_contiguous():
+        raise TypeError("ids must be a contiguous CUDA int32 tensor")
+    _bf16_dev(x, "x")
+    _bf16_dev(y, "y")
+    if x.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("x and y need unit column stride")
+    M = int(ids.numel())
+    if x.shape[0] < M or y.shape[0] < M:
+        raise ValueError("x and y need a row for each of the %d ids" % M)
+    _check(load().lora_build_and_apply(table.handle, ws.ref, ids.data_ptr(), M, x.data_ptr(), x.stride(0),
+                                       y.data_ptr(), y.stride(0), _stream(stream)), "lora_build_and_apply")
+    ws.built_M = M
 
 
 def lora_moe_delta(table: Table, stage: int, ws: Workspace, inp: torch.Tensor, cache: torch.Tensor,

@@ -288,3 +288,95 @@ def test_back_to_back_steps_on_one_workspace_with_and_without_pdl():
     for i, p in enumerate(probs):
         check_close(synth.bf16_bits_to_f32(outs[1][3 * i]).astype(np.float64), oracle_dense(p), "step %d" % i)
     table.destroy()
+
+
+def _fused_vs_separate(p, table, ws_a, ws_b):
+    ids = torch.from_numpy(p.ids).cuda()
+    x = dev_bf16(p.x)
+    ya, yb = dev_bf16(p.y_base), dev_bf16(p.y_base)
+    lora.lora_build_and_apply(table, ws_a, ids, x, ya)
+    lora.lora_build_segments(ws_b, ids)
+    lora.lora_apply(table, ws_b, x, yb)
+    torch.cuda.synchronize()
+    return ya, yb
+
+
+@pytest.mark.parametrize("case", ["decode", "one_token", "all_none", "bad_ids", "ragged_small", "stacked_16"])
+def test_build_and_apply_equals_the_two_calls(case):
+    """lora_build_and_apply (one launch for decode-sized batches) against lora_build_segments + lora_apply:
+    the same output bits, the same segment table left in the workspace, the same status; a later
+    lora_apply on that workspace reads the table it left."""
+    if case == "stacked_16":
+        q = synth.stacked("qkv", y_base="random")    # A blocks of 192 rows: one launch only up to 16 tokens
+        p = synth.DenseProblem(**{**q.__dict__})
+        p.ids, p.x, p.y_base, p.M = q.ids[:16].copy(), q.x[:16], q.y_base[:16], 16
+    else:
+        p = synth.decode(31, y_base="random")
+        if case == "one_token":
+            p.ids, p.x, p.y_base, p.M = p.ids[:1].copy(), p.x[:1], p.y_base[:1], 1
+            p.ids[0] = 3
+        elif case == "all_none":
+            p.ids[:] = -1
+        elif case == "bad_ids":
+            p.ids[[1, 7]] = [p.L + 3, -9]
+        elif case == "ragged_small":
+            p.ids[:] = np.random.default_rng(5).integers(0, 3, p.M)   # a few groups of up to ~16 rows
+    table = pack_dense(p)
+    for path in PATHS:
+        ws_a, ws_b = lora.Workspace(p.M, p.L), lora.Workspace(p.M, p.L)
+        with forced_path(path):
+            ya, yb = _fused_vs_separate(p, table, ws_a, ws_b)
+            assert lora.lora_get_status(ws_a) == lora.lora_get_status(ws_b), "path %d" % path
+            assert np.array_equal(host_bits(ya), host_bits(yb)), "path %d" % path
+            sa, sb = ws_a.read_segments(), ws_b.read_segments()
+            for k in ("M", "num_segments", "num_valid"):
+                assert sa[k] == sb[k]
+            assert np.array_equal(sa["perm"], sb["perm"]) and np.array_equal(sa["segments"], sb["segments"])
+            # a later apply on the fused call's workspace uses the table it left
+            yc = dev_bf16(p.y_base)
+            lora.lora_apply(table, ws_a, dev_bf16(p.x), yc)
+            torch.cuda.synchronize()
+            assert np.array_equal(host_bits(yc), host_bits(yb)), "path %d" % path
+    if case != "bad_ids":
+        check_close(host_f64(ya), oracle_dense(p))
+    table.destroy()
+
+
+def test_build_and_apply_back_to_back_in_a_graph():
+    """Fused decode steps with different ids, back to back on one workspace, eager and replayed from a
+    CUDA graph: each equals its own two-call reference."""
+    base = synth.decode(41, y_base="random")
+    probs = [base]
+    for sd in (42, 43):
+        q = synth.decode(sd, y_base="random")
+        r = synth.DenseProblem(**{**base.__dict__})
+        r.ids, r.x, r.y_base = q.ids, q.x, q.y_base
+        probs.append(r)
+    table = pack_dense(base)
+    ws = lora.Workspace(base.M, base.L)
+    ids = [torch.from_numpy(p.ids).cuda() for p in probs]
+    xs = [dev_bf16(p.x) for p in probs]
+    ref = []
+    for i, p in enumerate(probs):
+        y = dev_bf16(p.y_base)
+        w2 = lora.Workspace(p.M, p.L)
+        lora.lora_build_segments(w2, ids[i])
+        lora.lora_apply(table, w2, xs[i], y)
+        ref.append(host_bits(y))
+    ys = [dev_bf16(p.y_base) for p in probs]
+    for i in range(len(probs)):
+        lora.lora_build_and_apply(table, ws, ids[i], xs[i], ys[i])
+    torch.cuda.synchronize()
+    assert all(np.array_equal(host_bits(ys[i]), ref[i]) for i in range(len(probs)))
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(len(probs)):
+            lora.lora_build_and_apply(table, ws, ids[i], xs[i], ys[i])
+    for i, p in enumerate(probs):
+        ys[i].copy_(dev_bf16(p.y_base))
+    g.replay()
+    torch.cuda.synchronize()
+    assert lora.lora_get_status(ws) == lora.LORA_OK
+    assert all(np.array_equal(host_bits(ys[i]), ref[i]) for i in range(len(probs)))
+    table.destroy()
