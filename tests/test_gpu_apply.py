@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from segmented_rank_gemm_lora_gb300 import lora, synth
-from gpu_util import PATHS, check_close, dev_bf16, forced_path, host_bits, host_f64, oracle_dense, pack_dense, run_dense
+from gpu_util import PATHS, check_close, dev_bf16, forced_path, host_bits, host_f64, oracle_dense, pack_dense, padded, run_dense
 
 pytestmark = pytest.mark.gpu
 
@@ -379,4 +379,40 @@ def test_build_and_apply_back_to_back_in_a_graph():
     torch.cuda.synchronize()
     assert lora.lora_get_status(ws) == lora.LORA_OK
     assert all(np.array_equal(host_bits(ys[i]), ref[i]) for i in range(len(probs)))
+    table.destroy()
+
+
+@pytest.mark.parametrize("case", ["prefill_two_calls", "few_adapters_padded_ranks", "strided_rows"])
+def test_build_and_apply_more_shapes(case):
+    """lora_build_and_apply beyond the plain decode batch: a prefill batch (more than 32 tokens, so the
+    two calls it stands for), fewer adapters than tokens with ranks that need padding (20, 40), and x / y
+    with row strides past K and N (canary columns stay untouched)."""
+    x_extra = y_extra = 0
+    if case == "prefill_two_calls":
+        p = synth.prefill(15, y_base="random")
+    elif case == "few_adapters_padded_ranks":
+        ids = np.random.default_rng(16).integers(-1, 4, 32).astype(np.int32)
+        p = synth.make_dense("padded", 16, ids, 512, [264], [20, 40, 8, 64], y_base="random")
+    else:
+        p = synth.decode(17, y_base="random")
+        x_extra, y_extra = 16, 24
+    table = pack_dense(p)
+    ws = lora.Workspace(p.M, p.L)
+    ids = torch.from_numpy(p.ids).cuda()
+    x = dev_bf16(padded(p.x, x_extra))
+    y = dev_bf16(padded(p.y_base, y_extra))
+    lora.lora_build_and_apply(table, ws, ids, x[:, :p.K] if x_extra else x, y[:, :p.N] if y_extra else y)
+    torch.cuda.synchronize()
+    assert lora.lora_get_status(ws) == lora.LORA_OK
+    yb = host_bits(y)
+    if y_extra:
+        assert (yb[:, p.N:] == 0x7FC1).all()
+    check_close(synth.bf16_bits_to_f32(yb[:, :p.N]).astype(np.float64), oracle_dense(p), case)
+    none = p.ids < 0
+    assert np.array_equal(yb[:, :p.N][none], p.y_base[none])
+    seg = ws.read_segments()
+    ws2 = lora.Workspace(p.M, p.L)
+    lora.lora_build_segments(ws2, ids)
+    ref = ws2.read_segments()
+    assert np.array_equal(seg["perm"], ref["perm"]) and np.array_equal(seg["segments"], ref["segments"])
     table.destroy()
