@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -185,10 +186,15 @@ def barrier(world: int):
 # traffic recorded by ncu for the current engine source (null if stale)
 # ---------------------------------------------------------------------------
 def engine_source_sha() -> str:
+    """Hash of the engine's code: engine.cu and common.cuh with comments and blank space taken out, so that
+    an edit of the comments alone does not retire the traffic counters taken on the same code."""
     h = hashlib.sha256()
     for name in ("engine.cu", "common.cuh"):
-        with open(os.path.join(ROOT, "segmented_rank_gemm_lora_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "segmented_rank_gemm_lora_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

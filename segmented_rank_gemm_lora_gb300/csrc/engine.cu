@@ -12,9 +12,10 @@
 // Each group (an adapter segment, or an (adapter, expert) group of the MoE
 // variant) takes one of two paths:
 //   * small tiles (at most LORA_OPT_TC_MIN_ROWS rows, decode-sized): up to
-//     16 rows, warp-level m16n8k16 MMAs with the tokens as M.  At these sizes
-//     the per-batch issue-to-commit latency of tcgen05 exceeds the whole
-//     product, while warp-level MMAs finish in registers;
+//     16 rows, warp-level m16n8k16 MMAs with the tokens as M (tiles of one or
+//     two rows expand on CUDA cores).  At these sizes the per-batch
+//     issue-to-commit latency of tcgen05 exceeds the whole product, while
+//     warp-level MMAs finish in registers;
 //   * 128-row tiles (more rows, prefill-sized): tcgen05 with the
 //     accumulators in tensor memory.
 // Three kinds of work item, in this order on every CTA:
@@ -38,6 +39,16 @@
 // bulk row stores.  The summation
 // order never depends on timing or on which rows share a tile, so the same
 // inputs always give the same bits.
+//
+// For decode-sized batches the segment build can run inside the launch
+// (lora_build_and_apply): every CTA sorts the ids itself.  Launches may be
+// scheduled while the kernel before them finishes (programmatic dependent
+// launch); everything the previous work wrote is read after the wait on it.
+//
+// Most of a CTA's serial path runs once per launch, and there the size of the
+// code, not its instruction count, sets the time: loops that run once stay
+// rolled where that does not lengthen a latency chain, and no helper is
+// duplicated on that path without a measured reason.
 #include "common.cuh"
 #include "tc.cuh"
 
