@@ -68,9 +68,9 @@ constexpr int kTcShrinkBytes = kPool - kStageBytes;       // the shrink staging 
 // small tiles (at most 16 rows): warp-level MMAs (m16n8k16), the tile's tokens as M
 constexpr int kSmRows = kBgmvRows;              // token rows of a small tile
 // two staging slots (the next item's operands land while this one computes), then the cross-warp sums
+// (a slot holds the A chunk [kc/8][R][8] at its start and the x rows [rows][kc + 8] right after it)
 constexpr int kSmSlotBytes = 55 * 1024;
-constexpr int kSmABytes = 40 * 1024;            // A chunk at the slot's start: [kc/8][R][8]
-constexpr int kSmXOff = kSmABytes;              // x rows after it: [rows][kc + 8] (padded rows)
+constexpr int kSmABytes = 40 * 1024;            // A chunk bytes, at most, while the items are about one per CTA
 constexpr int kSmXBytes = kSmSlotBytes - kSmABytes;
 constexpr int kSmRedOff = 2 * kSmSlotBytes;     // cross-warp sums of the shrink: [3][16][32] fp32 at most
 constexpr int kFmaRows = 2;                     // small tiles of at most this many rows expand on CUDA cores
@@ -231,9 +231,14 @@ __device__ __forceinline__ GroupDims group_dims_calc(const EngineParams &p, cons
         d.uw = kTcCols;
         d.ue = pl.ue;
     } else {
-        // the x rows ([rows][kc + 8]) and the A chunk must fit their staging areas
+        // the A chunk and the x rows ([rows][kc + 8]) must fit one staging slot.  Where the chunk target is
+        // past two chunks of kSmABytes (each CTA runs a chain of items, one or two in flight) A may fill
+        // what the x rows leave of the slot, so the chain has fewer, larger steps; otherwise A stays
+        // within kSmABytes, which spreads the about one item per CTA of small batches wider.
         // (ta is clipped below 2^21: any larger target is past the staging cap anyway)
-        const int cap = max(64, min((qdiv_s(kSmXBytes, d.rows1) - 16) / 2, qdiv_s(kSmABytes / 2, d.R)) & ~63);
+        const int cap = max(64, (pl.ta > 2 * kSmABytes
+                                     ? qdiv_s(kSmSlotBytes - 16 * d.rows1, 2 * (d.R + d.rows1))
+                                     : min((qdiv_s(kSmXBytes, d.rows1) - 16) / 2, qdiv_s(kSmABytes / 2, d.R))) & ~63);
         const int want = max(64, (qdiv_s(min(pl.ta, (1 << 21) - 1), 2 * d.R) + 63) & ~63);
         d.kc = min(min(cap, kmax), want);
         d.uw = sm_unit_width(d.rp, d.rows1);
@@ -435,7 +440,8 @@ __device__ __forceinline__ void sm_shrink_issue(const EngineParams &p, EngineSme
     }
     if (warp == 1 && lane < b.nrows) {
         const int v = p.rows[d.rows_off + b.r0 + lane], src = p.src_div == 1 ? v : qdiv_s(v, p.src_div);
-        bulk_g2s(base + kSmXOff + (size_t)lane * (d.kc * 2 + 16), p.x + (int64_t)src * p.ldx + b.k0, x_bytes, bar);
+        bulk_g2s(base + (size_t)d.kc * d.R * 2 + (size_t)lane * (d.kc * 2 + 16), p.x + (int64_t)src * p.ldx + b.k0,
+                 x_bytes, bar);
     }
 }
 
@@ -465,7 +471,7 @@ __device__ __forceinline__ void sm_shrink_run(const EngineParams &p, EngineSmem 
     const int xstride = d.kc * 2 + 16;
     const uint32_t a_base = smem_u32(sm.pool + slot * kSmSlotBytes);
     const int xrow = (lane & 15) < b.nrows ? (lane & 15) : 0;
-    const uint32_t x_base = a_base + kSmXOff + xrow * xstride;
+    const uint32_t x_base = a_base + d.kc * R * 2 + xrow * xstride;
     float *red = reinterpret_cast<float *>(sm.pool + kSmRedOff);   // [ksplit - 1][16][R]
     float *dst = p.partials + sm.part_pre[g] + (int64_t)d.n_kc * b.r0 * R + (int64_t)chunk * b.nrows * R;
     const int gr = lane >> 2, qc = (lane & 3) * 2;
