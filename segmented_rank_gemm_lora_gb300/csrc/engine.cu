@@ -88,7 +88,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemExpandCol = 256;        // shrink accumulator: [0, R); expand: [256, 384), [384, 512)
 constexpr int kTcYOff = 16 * 1024;              // tensor-core stage: B [rp/8][128][8] at 0, y rows after
 constexpr int kTcYStride = kTcCols * 2 + 16;    // padded rows: a warp (one row per lane) hits every bank group
-constexpr int kItemsPerCta = 2;                 // 128-row tile expand items per CTA the plan aims for
+constexpr int kItemsPerCta = 3;                 // 128-row tile expand items per CTA the plan aims for
 static_assert(kTcYOff + kTcRows * kTcYStride <= kStageBytes, "tensor-core expand stage");
 static_assert(kSmRedOff + 3 * 16 * 32 * 4 <= kTcShrinkBytes, "small-tile shrink staging");
 static_assert(kSBytes >= (kMaxRank / 8) * kTcRows * 16, "S area");
@@ -1300,8 +1300,8 @@ __device__ __forceinline__ bool plan_launch(const EngineParams &p, EngineSmem &s
     pl.ta = (int)fminf(268435456.f, fmaxf(8192.f, __fdividef(2.5f * (float)p.K * (float)bga, (float)spare)));
     pl.ue = min(128, max(1, qdiv(tcu + kItemsPerCta * grid - 1, kItemsPerCta * grid)));
     pl.kctc = kctc;
-    // small-tile expand items of about one wave's share of all (tile, output column) pairs
-    pl.ccol = (int)fminf(1073741824.f, __fdividef((float)stiles * (float)N, (float)grid) + 1.f);
+    // small-tile expand items of about half a CTA's share of all (tile, output column) pairs
+    pl.ccol = (int)fminf(1073741824.f, __fdividef((float)stiles * (float)N, (float)(2 * grid)) + 1.f);
     // pass 2: per-group item counts and their exclusive prefix sums, 32 groups per step; larger chunks
     // until the hand-off scratch fits the workspace
 #pragma unroll 1
