@@ -29,9 +29,11 @@
 //      step 2: their expand items sum the few partials they need themselves.
 // Shrink items never wait on other CTAs, finish items wait only on shrink
 // items and expand items only on the other two, and the whole grid is
-// co-resident, so every wait ends.  The chunk sizes are picked per launch from
-// the total bytes so that the items of each kind fill whole waves of the
-// grid.  Expand units stream through a
+// co-resident, so every wait ends.  Chunk and item sizes are picked per
+// launch from the totals: small-tile K-chunks of about a CTA's share of the A
+// bytes (as large as a staging slot holds where every CTA runs a long chain of
+// them), and expand items of about a third (128-row tiles) or half (small
+// tiles) of a CTA's share of the output.  Expand units stream through a
 // three-stage ring that runs across item boundaries; the first units are put
 // in flight while the shrink work is still running.  Operands move as bulk
 // async copies (whole rows of x and y, contiguous runs of the packed table) or
