@@ -250,39 +250,51 @@ __device__ __forceinline__ void nanosleep_ns(uint32_t ns)
     asm volatile("nanosleep.u32 %0;" ::"r"(ns));
 }
 
-// Dense batches of at most 32 tokens, one token per lane of one warp: the (key, token index) pairs go
-// through a bitonic network of lane shuffles, ascending; comparing the index as well makes the order
-// stable, so it equals a stable counting sort on the key.  key = adapter id, or L for tokens without one
-// (-1, bad or disabled ids; lanes past M sort after everything).  Returns this lane's pair after the
-// sort; `bad` is set on lanes whose id is neither -1 nor in [0, L).
-__device__ __forceinline__ void warp_sort_ids(const int32_t *ids, const uint8_t *enabled, int M, int L, int &key,
-                                              int &v, bool &bad)
+// Dense batches of at most 32 tokens, one token per lane of one warp: each token's slot in the stable
+// counting sort on key = adapter id, or L for tokens without one (-1, bad or disabled ids; lanes past M
+// take L + 1).  The key bits are compared from the top, one ballot per bit: a lane counts the lanes that
+// share its higher bits and have a 0 where it has a 1 (the smaller keys) and narrows its set of equal
+// lanes; the slot is the smaller keys plus the equal keys on lower lanes.
+struct WarpRank {
+    int key;        // this lane's key
+    int rank;       // its slot in the sorted order
+    int count;      // lanes with the same key
+    int seg;        // on the first lane of a key: keys smaller than it (the segment's index)
+    bool first;     // the lowest lane of its key
+    bool bad;       // the id is neither -1 nor in [0, L)
+};
+__device__ __forceinline__ WarpRank warp_rank_ids(const int32_t *ids, const uint8_t *enabled, int M, int L)
 {
     const int lane = threadIdx.x & 31;
-    key = INT32_MAX;
-    v = lane;
-    bad = false;
+    const uint32_t below = (1u << lane) - 1u;
+    WarpRank r;
+    r.key = L + 1;
+    r.bad = false;
     if (lane < M) {
         const int32_t i = ids[lane];
-        bad = i < -1 || i >= L;
-        key = (i >= 0 && i < L && (enabled == nullptr || enabled[i])) ? i : L;
+        r.bad = i < -1 || i >= L;
+        r.key = (i >= 0 && i < L && (enabled == nullptr || enabled[i])) ? i : L;
     }
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int ok = __shfl_xor_sync(0xffffffffu, key, stride);
-            const int ov = __shfl_xor_sync(0xffffffffu, v, stride);
-            const bool ascending = (lane & size) == 0;
-            const bool low = (lane & stride) == 0;
-            const bool greater = key > ok || (key == ok && v > ov);
-            // the lower lane of an ascending pair keeps the smaller pair, the upper lane the larger
-            if (low == ascending ? greater : !greater) {
-                key = ok;
-                v = ov;
-            }
+    uint32_t same = 0xffffffffu;
+    int less = 0;
+#pragma unroll 1
+    for (int b = 31 - __clz(L + 1); b >= 0; --b) {
+        const uint32_t ones = __ballot_sync(0xffffffffu, (r.key >> b) & 1);
+        if ((r.key >> b) & 1) {
+            less += __popc(same & ~ones);
+            same &= ones;
+        } else {
+            same &= ~ones;
         }
     }
+    r.rank = less + __popc(same & below);
+    r.count = __popc(same);
+    r.first = (same & below) == 0;
+    // first lanes hold the smallest slot of their key: the keys below this one are the first lanes on lower
+    // slots
+    const uint32_t first_slots = __reduce_or_sync(0xffffffffu, r.first ? 1u << r.rank : 0u);
+    r.seg = __popc(first_slots & ((1u << r.rank) - 1u));
+    return r;
 }
 
 // 8 bf16 (one uint4) -> 8 floats

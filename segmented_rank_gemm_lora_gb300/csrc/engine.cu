@@ -1410,33 +1410,24 @@ __global__ void __launch_bounds__(kEngineThreads, 1) engine_kernel(const __grid_
         // and CTA 0 also leaves the table in the workspace for later launches
         if (warp == 0) {
             const int lane = tid, M = pk.ids_M, L = pk.L;
-            int key, v;
-            bool bad;
-            warp_sort_ids(pk.ids, nullptr, M, L, key, v, bad);
-            const bool valid = lane < M && key < L;
-            const int prev = __shfl_up_sync(0xffffffffu, key, 1);
-            const bool start = valid && (lane == 0 || prev != key);
-            const uint32_t starts = __ballot_sync(0xffffffffu, start);
-            const int num_valid = __popc(__ballot_sync(0xffffffffu, valid));
-            sm.row_src[lane] = v;
-            int4 seg = make_int4(0, 0, 0, 0);
-            const int si = __popc(starts & ((1u << lane) - 1u));
-            if (start) {
-                const uint32_t later = starts & ~((2u << lane) - 1u);   // segment starts after this lane
-                seg = make_int4(key, 0, lane, (later ? __ffs(later) - 1 : num_valid) - lane);
-                sm.grp[si] = seg;
-            }
+            const WarpRank r = warp_rank_ids(pk.ids, nullptr, M, L);
+            const bool start = r.first && r.key < L;
+            const int num_segments = __popc(__ballot_sync(0xffffffffu, start));
+            const int num_valid = __popc(__ballot_sync(0xffffffffu, lane < M && r.key < L));
+            sm.row_src[r.rank] = lane;   // (the slots are a permutation of the 32 lanes)
+            const int4 seg = make_int4(r.key, 0, r.rank, r.count);
+            if (start) sm.grp[r.seg] = seg;
             if (lane == 0) {
-                sm.G = __popc(starts);
+                sm.G = num_segments;
                 sm.x_total = M;
             }
             if (b == 0) {
-                if (lane < M) pk.ws_perm[lane] = v;
-                if (start) pk.ws_segments[si] = seg;
-                if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(pk.err, kErrBadId);
+                if (lane < M) pk.ws_perm[r.rank] = lane;
+                if (start) pk.ws_segments[r.seg] = seg;
+                if (__any_sync(0xffffffffu, r.bad) && lane == 0) atomicOr(pk.err, kErrBadId);
                 if (lane == 0) {
                     pk.ws_header[H_M] = M;
-                    pk.ws_header[H_NUM_SEGMENTS] = __popc(starts);
+                    pk.ws_header[H_NUM_SEGMENTS] = num_segments;
                     pk.ws_header[H_NUM_VALID] = num_valid;
                     pk.ws_header[H_NUM_MOE_GROUPS] = 0;
                     pk.ws_header[H_BLOCK_M] = 0;

@@ -246,9 +246,9 @@ __global__ void __launch_bounds__(kBuildThreads, 1) build_kernel(BuildParams p)
     }
 }
 
-// Dense batches of at most 32 tokens: one warp, one token per lane, sorted by
-// warp_sort_ids (a stable bitonic network of lane shuffles, so the result
-// equals the counting sort above).  Segments start where the key changes.
+// Dense batches of at most 32 tokens: one warp, one token per lane, placed by
+// warp_rank_ids (the slots of the stable counting sort above, from one ballot
+// per key bit).  The first lane of each adapter writes its segment.
 __global__ void __launch_bounds__(32, 1) build_warp_kernel(BuildParams p)
 {
     const int lane = threadIdx.x;
@@ -257,24 +257,16 @@ __global__ void __launch_bounds__(32, 1) build_warp_kernel(BuildParams p)
     pdl_trigger();
     pdl_wait();   // the previous launch on the stream may still read this workspace
     for (int i = lane; i < p.sync_ints; i += 32) p.sync[i] = 0;
-    int key, v;
-    bool bad;
-    warp_sort_ids(p.ids, p.enabled, M, L, key, v, bad);
-    if (bad) atomicOr(err, kErrBadId);
-    if (lane < M) p.perm[lane] = v;
-    const bool valid = lane < M && key < L;
-    const int prev = __shfl_up_sync(0xffffffffu, key, 1);
-    const bool start = valid && (lane == 0 || prev != key);
-    const uint32_t starts = __ballot_sync(0xffffffffu, start);
-    const int num_valid = __popc(__ballot_sync(0xffffffffu, valid));
-    if (start) {
-        const uint32_t later = starts & ~((2u << lane) - 1u);   // segment starts after this lane
-        const int end = later ? __ffs(later) - 1 : num_valid;
-        p.segments[__popc(starts & ((1u << lane) - 1u))] = make_int4(key, 0, lane, end - lane);
-    }
+    const WarpRank r = warp_rank_ids(p.ids, p.enabled, M, L);
+    if (r.bad) atomicOr(err, kErrBadId);
+    if (lane < M) p.perm[r.rank] = lane;
+    const bool start = r.first && r.key < L;
+    if (start) p.segments[r.seg] = make_int4(r.key, 0, r.rank, r.count);
+    const int num_segments = __popc(__ballot_sync(0xffffffffu, start));
+    const int num_valid = __popc(__ballot_sync(0xffffffffu, lane < M && r.key < L));
     if (lane == 0) {
         p.header[H_M] = M;
-        p.header[H_NUM_SEGMENTS] = __popc(starts);
+        p.header[H_NUM_SEGMENTS] = num_segments;
         p.header[H_NUM_VALID] = num_valid;
         p.header[H_NUM_MOE_GROUPS] = 0;
         p.header[H_BLOCK_M] = 0;
