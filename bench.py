@@ -1,22 +1,27 @@
 """Benchmark of the multi-adapter LoRA hot path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config decode]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config stacked_gate_up] [--no-per-workload]
 
 One step = lora_build_segments + lora_apply, made as the one public call
-lora_build_and_apply (one launch for decode-sized batches), or for the MoE
-config build + gate/up delta + down delta, over one batch of synthetic inputs,
-already resident in HBM.  To keep L2 (129 MB) from serving the weights, every step
-uses the next of R independent input sets (own adapter table, ids, x, y),
-with R * bytes-per-set above 2x L2.  Steps are issued as one CUDA graph and
-timed with CUDA events on the launching stream, bracketed by a barrier and a
-device synchronize; rank 0 prints one JSON line.
+lora_build_and_apply, or for the MoE config build + gate/up delta + down
+delta, over one batch of synthetic inputs already resident in HBM.  The
+headline line is the largest single-GPU workload (the stacked gate/up
+projection, 277 MB of algorithmic traffic per step); the same line carries a
+per_workload map with every workload of the benchmark (decode, prefill,
+stacked QKV / gate-up / down, MoE) measured the same way in the same run.
+To keep L2 (129 MB) from serving the weights, every step uses the next of R
+independent input sets (own adapter table, ids, x, y), with R * bytes-per-set
+above 2x L2.  Steps are issued as CUDA-graph replays and timed with CUDA
+events on the launching stream, bracketed by a barrier and a device
+synchronize; rank 0 prints one JSON line.
 
 Multi-GPU runs are independent replicas (the path has no exchange step):
 every rank processes its own batches, the elapsed time is the max over ranks
 and the value counts the tokens of all ranks.
 
 --impl reference times the CPU oracle (plain C, fp64) on the host cores on
-the same workload; under torchrun only rank 0 runs it.
+a bounded sample of the same workload; under torchrun only rank 0 runs it.
 """
 from __future__ import annotations
 
@@ -186,10 +191,10 @@ def barrier(world: int):
 # traffic recorded by ncu for the current engine source (null if stale)
 # ---------------------------------------------------------------------------
 def engine_source_sha() -> str:
-    """Hash of the engine's code: engine.cu and common.cuh with comments and blank space taken out, so that
-    an edit of the comments alone does not retire the traffic counters taken on the same code."""
+    """Hash of the kernels' code (every csrc source) with comments and blank space taken out, so that an
+    edit of the comments alone does not retire the traffic counters taken on the same code."""
     h = hashlib.sha256()
-    for name in ("engine.cu", "common.cuh"):
+    for name in ("engine.cu", "stream.cu", "segments.cu", "common.cuh", "tc.cuh"):
         with open(os.path.join(ROOT, "segmented_rank_gemm_lora_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -233,8 +238,13 @@ def oracle_step(p):
 
 
 def sample_problem(config: str, p, max_tokens: int):
-    """A bounded sample of the workload: the first max_tokens tokens of the batch."""
-    if hasattr(p, "A_gu") or p.M <= max_tokens:
+    """A bounded sample of the workload: the first tokens of the batch, at most max_tokens and about
+    5e7 multiply-adds of the oracle's per-token loops."""
+    if hasattr(p, "A_gu"):
+        return p, p.M
+    per_token = max(1, (p.n_a * p.K + p.N) * max(p.ranks))
+    max_tokens = max(8, min(max_tokens, int(5e7 // per_token)))
+    if p.M <= max_tokens:
         return p, p.M
     from segmented_rank_gemm_lora_gb300 import synth
     q = synth.DenseProblem(**{**p.__dict__})
@@ -445,31 +455,22 @@ def capture(torch, fn, stream):
     return g
 
 
-def run_ours(args, world, rank, local):
-    import torch
-    from segmented_rank_gemm_lora_gb300 import lora
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    lora.load()
-
-    sets = build_sets(args.config, 1, torch, lora, dev)
+def measure(config, K, W, args, torch, lora, dev, world, e2e_steps, clocks=None):
+    """One workload: K timed steps (build + apply, as CUDA-graph replays over R rotating input sets), the
+    applies alone, and the end-to-end leg through host buffers.  Returns the numbers of one bench line."""
+    sets = build_sets(config, 1, torch, lora, dev)
     per_set = sets[0]["bytes"]
     R = max(4, min(64, int(np.ceil(2.5 * L2_BYTES / max(per_set, 1)))))
-    sets += build_sets(args.config, R - 1, torch, lora, dev, first=1)
-    # warm every set once eagerly (first launches set kernel attributes)
-    for s in sets:
+    sets += build_sets(config, R - 1, torch, lora, dev, first=1)
+    for s in sets:   # warm every set once eagerly (first launches set kernel attributes)
         step(s, lora)
     torch.cuda.synchronize()
     for s in sets:
         st = lora.lora_get_status(s["ws"])
         if st != lora.LORA_OK:
-            raise RuntimeError("device status %s" % lora.STATUS[st])
+            raise RuntimeError("%s: device status %s" % (config, lora.STATUS[st]))
 
     stream = torch.cuda.Stream(device=dev)
-    K, W = args.steps, args.warmup
     launches = {"n": 0}
 
     def steps_fn(n, build=True):
@@ -480,8 +481,8 @@ def run_ours(args, world, rank, local):
             launches["n"] = c
         return fn
 
-    # K steps are issued as replays of a graph of C = R steps (one rotation over the sets) plus one
-    # graph with the remaining K mod C steps, so exactly K steps run in the timed region.
+    # K steps are issued as replays of a graph of C = R steps (one rotation over the sets) plus one graph
+    # with the remaining K mod C steps, so exactly K steps run in the timed region.
     C = R
     g_chunk = capture(torch, steps_fn(C), stream)
     launches_chunk = launches["n"]
@@ -497,19 +498,19 @@ def run_ours(args, world, rank, local):
         if with_tail and g_tail is not None:
             g_tail.replay()
 
-    # ---------------- warm-up (W steps) and a load period so clock samples see a busy GPU ----------------
-    clocks = ClockSampler(local)
-    clocks.start()
+    # warm-up (W steps), and a load period so clock samples see a busy GPU
+    if clocks is not None:
+        clocks.start()
     with torch.cuda.stream(stream):
-        for i in range(max(1, (W + C - 1) // C)):
+        for _ in range(max(1, (W + C - 1) // C)):
             g_chunk.replay()
         torch.cuda.synchronize()
-        t_end = time.perf_counter() + args.load_seconds
+        t_end = time.perf_counter() + (args.load_seconds if clocks is not None else 0.0)
         while time.perf_counter() < t_end:
             run_steps(8, False)
             torch.cuda.synchronize()
 
-    # ---------------- timed region: exactly K steps ----------------
+    # timed region: exactly K steps
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -520,10 +521,10 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     ms = e0.elapsed_time(e1)
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks is not None else None
     ms_max = max_over_ranks(ms, world)
 
-    # ---------------- dominant kernel alone: the same rotation of applies ----------------
+    # the applies alone: the same rotation without the segment builds
     reps = max(1, K // C)
     with torch.cuda.stream(stream):
         g_apply.replay()
@@ -535,46 +536,80 @@ def run_ours(args, world, rank, local):
         a1.record(stream)
     torch.cuda.synchronize()
     apply_ms = a0.elapsed_time(a1) / (reps * C)
-    if "gu" in sets[0]:
+    moe = "gu" in sets[0]
+    if moe:
         apply_ms /= 2.0     # two delta launches per step
 
     tokens_step = np.mean([sets[i % R]["tokens"] for i in range(K)])
     value = world * tokens_step * K / (ms_max / 1e3)
     alg_bytes = np.mean([sets[i % R]["alg"][0] for i in range(K)])
     alg_flops = np.mean([sets[i % R]["alg"][1] for i in range(K)])
-    if "gu" in sets[0]:
+    if moe:
         alg_bytes /= 2.0
         alg_flops /= 2.0
     hbm, tc, src = peaks()
     achieved = alg_bytes / (apply_ms / 1e3) / 1e9
+    dense_small = (not moe) and sets[0]["fused"]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": recorded_traffic(args.config), "kernel": "engine_kernel",
+                "traffic": recorded_traffic(config),
+                "kernel": "engine_kernel" if dense_small else "shrink_kernel + expand_kernel",
                 "kernel_ms": apply_ms, "algorithmic_bytes": alg_bytes,
                 "tflops": alg_flops / (apply_ms / 1e3) / 1e12, "peak_source": src + " (burst)"}
+    e2e = run_e2e(args, sets, torch, lora, dev, stream, world, e2e_steps)
+    out = {"value": value, "unit": "tokens/s", "ms_per_step": ms_max / K, "steps": K, "kernel_ms": apply_ms,
+           "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clk,
+           "step": ("build_segments + gate/up + down deltas" if moe else
+                    "lora_build_and_apply (build_segments + apply; %s)" %
+                    ("one launch" if dense_small else "build, shrink and expand launches")),
+           "l2": "inputs larger than L2: %d rotating input sets, %.0f MB each" % (R, per_set / 1e6)}
+    del sets, g_chunk, g_tail, g_apply
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
-    # ---------------- end to end through host buffers ----------------
-    e2e = run_e2e(args, sets, torch, lora, dev, stream, world)
+
+WORKLOADS = ("decode", "prefill", "stacked_qkv", "stacked_gate_up", "stacked_down", "moe")
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from segmented_rank_gemm_lora_gb300 import lora
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lora.load()
+
+    K, W = args.steps, args.warmup
+    head = measure(args.config, K, W, args, torch, lora, dev, world, min(args.steps, args.e2e_steps),
+                   clocks=ClockSampler(local))
+    # every workload of the benchmark, measured the same way in the same run (fewer steps each)
+    per = {}
+    if args.per_workload:
+        for name in WORKLOADS:
+            r = head if name == args.config else measure(name, max(50, min(K, args.workload_steps)), W, args,
+                                                         torch, lora, dev, world, min(args.workload_steps, 100))
+            per[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "kernel_ms", "roofline", "e2e",
+                                            "gpu_launches")}
+            per[name]["workload"] = CONFIGS[name]
 
     cpu = cpu_baseline(args.config, args.cpu_seconds) if (rank == 0 and world == 1 and args.cpu_seconds > 0) else None
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
-                "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": "%s: %s" % (args.config, CONFIGS[args.config]),
-                           "step": ("build_segments + gate/up + down deltas" if "gu" in sets[0] else
-                                    "lora_build_and_apply (build_segments + apply; %s)" %
-                                    ("one launch" if sets[0].get("fused") else "two launches")),
-                           "l2": "inputs larger than L2: %d rotating input sets, %.0f MB each" % (R, per_set / 1e6),
-                           "parallelism": "replicas x%d" % world},
-                "gpu_launches": gpu_launches, "roofline": roofline, "e2e": e2e, "clocks": clk,
-                "cpu_baseline": cpu}
+        line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
+                "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "%s: %s" % (args.config, CONFIGS[args.config]), "step": head["step"],
+                           "l2": head["l2"], "parallelism": "replicas x%d" % world},
+                "gpu_launches": head["gpu_launches"], "roofline": head["roofline"], "e2e": head["e2e"],
+                "clocks": head["clocks"], "cpu_baseline": cpu, "per_workload": per}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def run_e2e(args, sets, torch, lora, dev, stream, world):
+def run_e2e(args, sets, torch, lora, dev, stream, world, e2e_steps):
     """Same metric through the public API with host-resident inputs: every step copies its inputs (ids, x
     and y_base, or the MoE caches) from pinned host memory, as one copy of the buffer they share on the
     device, builds, applies, and copies the result back."""
@@ -596,7 +631,7 @@ def run_e2e(args, sets, torch, lora, dev, stream, world):
             o[k].copy_(s[k], non_blocking=True)
             d2h += o[k].numel() * o[k].element_size()
 
-    K = min(args.steps, args.e2e_steps)
+    K = max(1, e2e_steps)
     H = len(host)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # eager: every step's copies and calls issued from Python
@@ -664,13 +699,16 @@ def run_e2e(args, sets, torch, lora, dev, stream, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--load-seconds", type=float, default=1.0)
-    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="decode", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="stacked_gate_up", choices=sorted(CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload-steps", type=int, default=1000,
+                    help="timed steps of each per_workload entry (the headline workload uses --steps)")
+    ap.add_argument("--no-per-workload", dest="per_workload", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -22,7 +22,7 @@
  *   [P5] "[SGLang] LoRA Layers: QKV, Gate/Up" (secrett2633 blog): stacked
  *        projections, A = (n*r, in), B = (sum of slice widths, r).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - a per-adapter scale multiplies the expand result (1.0 reproduces [P1]);
  *   - ids >= L or < -1 behave like -1 and are counted as bad;
  *   - segments are in ascending adapter id, tokens ascending inside one,

@@ -425,11 +425,90 @@ extern "C" lora_status lora_build_segments(const lora_workspace *ws, const int32
     return cuda_status(launch_build(p, reinterpret_cast<cudaStream_t>(stream), g_opt_pdl.load() != 0));
 }
 
+// The streaming path (plan -> shrink -> expand) over the groups of the last build on `ws`.  Its plan, tile
+// records, S and fp32 partials live in the workspace's scratch area, its tile counters in the sync area.
+static lora_status run_stream(lora_table t, const lora_workspace *ws, const WsLayout &w, bool moe, int32_t src_div,
+                              const void *x, int64_t ldx, void *y, int64_t ldy, const float *row_weight,
+                              int32_t tile_max, lora_stream_t stream)
+{
+    DeviceInfo di;
+    lora_status st = device_info(&di);
+    if (st != LORA_OK) return st;
+    StreamParams p{};
+    p.a_ptr = t->d_a_ptr;
+    p.b_ptr = t->d_b_ptr;
+    p.rpad = t->d_rpad;
+    p.scale = t->d_scale;
+    p.L = t->L;
+    p.E_A = t->E_A;
+    p.E_B = t->E_B;
+    p.K = t->K;
+    p.n_slices = t->n_slices;
+    p.n_a = t->n_a;
+    for (int s = 0; s < kMaxSlices; ++s) {
+        p.slice_n[s] = t->slice_n[s];
+        p.slice_off[s] = t->slice_off[s];
+        p.slice_tile_off[s] = t->slice_tile_off[s];
+    }
+    int32_t *header = at<int32_t>(ws, w.header);
+    if (moe) {
+        p.groups = at<int4>(ws, w.moe_groups);
+        p.num_groups = header + H_NUM_MOE_GROUPS;
+        p.group_capacity = w.moe_group_capacity;
+        p.rows = at<int32_t>(ws, w.sorted_ids);
+    } else {
+        p.groups = at<int4>(ws, w.segments);
+        p.num_groups = header + H_NUM_SEGMENTS;
+        p.group_capacity = w.seg_capacity;
+        p.rows = at<int32_t>(ws, w.perm);
+    }
+    p.src_div = src_div;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.ldx = ldx;
+    p.y = static_cast<__nv_bfloat16 *>(y);
+    p.ldy = ldy;
+    p.row_weight = row_weight;
+    // the scratch area: plan (header, tiles, prefixes, block starts), S, then the fp32 partials
+    const int64_t max_rows = w.partial_floats / kPartialFloatsPerRow;
+    const size_t plan_bytes = stream_plan_bytes(w.max_tiles);
+    const size_t s_cap = (size_t)round_up(512 * (max_rows + 16 * (int64_t)w.max_tiles), 256);
+    if (plan_bytes + s_cap >= (size_t)w.partial_floats * 4) return LORA_ERR_WORKSPACE;
+    unsigned char *area = at<unsigned char>(ws, w.partials);
+    p.plan_hdr = reinterpret_cast<int32_t *>(area);
+    p.tiles = reinterpret_cast<TileRec *>(area + 256);
+    p.sh_start = reinterpret_cast<int2 *>(area + 256 + (size_t)w.max_tiles * sizeof(TileRec));
+    p.ex_start = p.sh_start + (kStreamMaxGrid + 1);
+    p.rd_start = p.ex_start + (kStreamMaxGrid + 1);
+    p.s_area = area + plan_bytes;
+    p.s_cap = (int64_t)s_cap;
+    p.partials = reinterpret_cast<float *>(area + plan_bytes + s_cap);
+    p.partial_cap = ((int64_t)w.partial_floats * 4 - (int64_t)plan_bytes - (int64_t)s_cap) / 4;
+    p.max_tiles = w.max_tiles;
+    p.cnt = at<int32_t>(ws, w.sync);
+    const int grid = stream_grid(di.sms);
+    const int64_t want = g_opt_grid.load();
+    p.grid_s = p.grid_e = (want > 0 && want < grid) ? (int)want : grid;
+    p.tile_max = tile_max;
+    p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
+    p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
+    p.withhold = g_opt_withhold.load() != 0;
+    p.trace = static_cast<uint64_t *>(g_trace.load());
+    p.trace_ctas = p.trace ? (int32_t)(g_trace_bytes.load() / (3 * 8 * kTraceSlots)) : 0;
+    return cuda_status(launch_stream(p, reinterpret_cast<cudaStream_t>(stream), g_opt_pdl.load() != 0));
+}
+
 static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLayout &w, bool moe, int32_t src_div,
                               const void *x, int64_t ldx, int64_t x_rows, void *y, int64_t ldy,
                               const float *row_weight, lora_stream_t stream, const int32_t *fused_ids = nullptr,
                               int32_t fused_M = 0)
 {
+    // the streaming path serves every batch but the dense ones of at most 32 tokens, where one launch of
+    // the persistent engine (small tiles, the segment build fused in) is faster
+    {
+        const int64_t path = g_opt_path.load();
+        if (!fused_ids && (path == 3 || (path == 0 && (moe || ws->max_M > 32))))
+            return run_stream(t, ws, w, moe, src_div, x, ldx, y, ldy, row_weight, path == 3 ? 16 : 128, stream);
+    }
     // scratch needed per row of work at this table's largest A block, at the largest K-chunk of a
     // 16-row small tile (x rows <= 15 KB, A chunk <= 40 KB), plus the row's finished S
     {
@@ -553,7 +632,7 @@ extern "C" lora_status lora_build_and_apply(lora_table t, const lora_workspace *
     // one launch when every group is sure to run on small tiles (no group can exceed the tensor-core
     // threshold), else the two calls it stands for
     const int64_t path = g_opt_path.load(), thr = g_opt_tc_min_rows.load();
-    const bool all_small = path == 1 || (path == 0 && M <= (t->max_R > 128 ? thr / 2 : thr));
+    const bool all_small = path == 1 || (path == 0 && ws->max_M <= 32 && M <= (t->max_R > 128 ? thr / 2 : thr));
     if (M == 0 || M > 32 || !all_small) {
         st = lora_build_segments(ws, d_ids, M, nullptr, nullptr, stream);
         if (st != LORA_OK) return st;
@@ -619,7 +698,7 @@ extern "C" lora_status lora_set_option(int32_t option, int64_t value)
 {
     switch (option) {
     case LORA_OPT_PATH:
-        if (value < 0 || value > 2) return LORA_ERR_INVALID_ARG;
+        if (value < 0 || value > 3) return LORA_ERR_INVALID_ARG;
         g_opt_path = value;
         return LORA_OK;
     case LORA_OPT_TC_MIN_ROWS:

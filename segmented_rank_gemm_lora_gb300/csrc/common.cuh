@@ -107,6 +107,68 @@ void launch_engine(const EngineParams &p, int grid, size_t smem, cudaStream_t s,
 size_t engine_smem_bytes(int group_capacity);
 const void *engine_kernel_ptr();
 
+// ---------------------------------------------------------------------------
+// streaming path (csrc/stream.cu): plan -> shrink -> expand, three kernels chained on the stream
+// ---------------------------------------------------------------------------
+// One row tile of a group, as the plan lays it out.  The tile's shrink is cut into n_kc K-chunks of kc
+// columns (the same cut for every tile of a group), each streamed in stages of ks columns; its expand is
+// cut into n_units units of W output columns of one slice.
+struct TileRec {
+    int32_t a, e, row0, m;          // adapter, expert, first entry in the row list, rows
+    int32_t rp, R, n_pad, kc;       // stored rank, A-block rows (n_a * rp), rows rounded up to 16, chunk K
+    int32_t n_kc, ks, W, n_units;   // chunks, stage K, expand unit width, expand units
+    int32_t p_off, s_off;           // fp32 partial offset (floats), S offset (bytes)
+    int32_t sh_pos, ex_pos;         // position of the tile's first chunk / unit in the launch's cost order
+};
+static_assert(sizeof(TileRec) == 64, "tile record");
+
+// Plan header slots (int32)
+enum PlanSlot { PL_TILES = 0, PL_ARRIVED = 1 };
+
+struct StreamParams {
+    // weight table
+    const uint64_t *a_ptr, *b_ptr;   // [L * E_A], [L * E_B] packed block addresses
+    const int32_t *rpad;             // [L] stored rank
+    const float *scale;              // [L]
+    int32_t L, E_A, E_B, K, n_slices, n_a;
+    int32_t slice_n[kMaxSlices], slice_off[kMaxSlices], slice_tile_off[kMaxSlices];
+    // groups written by lora_build_segments: (adapter, expert, index into rows, count)
+    const int4 *groups;
+    const int32_t *num_groups;
+    int32_t group_capacity;
+    const int32_t *rows;             // row list: y row of each entry; the x row is rows[i] / src_div
+    int32_t src_div;
+    // operands
+    const __nv_bfloat16 *x;  int64_t ldx;
+    __nv_bfloat16 *y;        int64_t ldy;
+    const float *row_weight;         // optional, indexed by the y row
+    // plan area (caller's workspace)
+    int32_t *plan_hdr;               // [16]
+    TileRec *tiles;                  // [max_tiles]
+    int2 *sh_start, *ex_start;       // [grid + 1] first (tile, item) of every block
+    int2 *rd_start;                  // [grid + 1] first (tile, S chunk) each shrink block reduces
+    int32_t *cnt;                    // [max_tiles] chunks of a tile done (zeroed by the plan)
+    float *partials;                 // fp32 chunk partials
+    int64_t partial_cap;             // floats
+    unsigned char *s_area;           // finished S, bf16, per tile [n_a][rp / 8][n_pad][8]
+    int64_t s_cap;                   // bytes
+    int32_t max_tiles;
+    int32_t grid_s, grid_e;          // blocks of the shrink and of the expand launch
+    int32_t tile_max;                // rows of a tile at most (128; smaller values force more tiles)
+    uint32_t *err;
+    uint64_t timeout_ns;
+    int32_t withhold;                // test hook: the expand never loads S, so its waits run out
+    uint64_t *trace;                 // optional phase stamps: [3][trace_ctas][32] (shrink, expand, plan)
+    int32_t trace_ctas;
+};
+
+cudaError_t launch_stream(const StreamParams &p, cudaStream_t s, bool pdl);
+// Bytes of the plan area (header, tiles, prefixes, block starts) for max_tiles tiles and grids up to
+// kStreamMaxGrid blocks; the S area and the partials follow it.
+constexpr int kStreamMaxGrid = 1024;
+size_t stream_plan_bytes(int32_t max_tiles);
+int stream_grid(int sms);
+
 struct BuildParams {
     const int32_t *ids;
     const int32_t *topk_ids;      // nullable
@@ -185,6 +247,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         }
     }
     return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Retire `bytes` of an mbarrier's expected transactions that will never arrive.

@@ -1,0 +1,1113 @@
+// The streaming path behind lora_apply and lora_moe_delta: two kernels
+// chained on the stream with programmatic dependent launch.
+//
+// "vLLM-Ascend dynamic LoRA fused operator", section 2.3: every segment is a
+// shrink X_seg A_i^T followed by an expand with B_i^T added to the base rows,
+// all segments in one operator instance spread over the cores; section 2.4:
+// the work of every core is fixed before the compute starts, the token
+// dimension is tiled first and then K, so a piece of A fits on chip and the
+// pieces are accumulated; section 4.2: the rank-sized intermediate S
+// accumulates in fp32.
+//
+// GB300 form.  Every byte the delta needs crosses HBM once, so the kernels
+// are built to keep the memory system busy rather than the tensor cores.
+// Contiguous runs (packed A and B, S) move as bulk copies; gathered rows of
+// x and y move as 16-byte cp.async pieces from several warps, because the
+// bulk-copy engine spends a fixed time per copy and rows of a few hundred
+// bytes would leave it far below the memory's bandwidth.
+//   plan    one warp.  Cuts every group (an adapter segment, or an
+//           (adapter, expert) group of the MoE variant) into row tiles of at
+//           most 64 rows, every tile's shrink into K-chunks (the same cut for
+//           all tiles of a group) and its expand into units of W output
+//           columns of one slice, and gives every block of the next two
+//           launches a contiguous run of that work of about equal bytes.
+//   shrink  one block per SM, eight warps, launched cooperatively.  An
+//           eight-stage ring: each stage is the chunk's next K columns of A
+//           (one bulk copy) and of the tile's x rows (cp.async pieces); the
+//           warps multiply them with m16n8k16 MMAs (the tile's rows as M, its
+//           rank columns as N) into fp32 registers, and each chunk's partial
+//           goes to L2 scratch.  Once every block has stored its partials (one
+//           grid-wide arrival count), the blocks split the sums of the partials
+//           in K order among themselves and store S as bf16 in the operand
+//           layout the expand reads.
+//   expand  one block per SM, warp-specialised.  Warp 0 streams the packed B
+//           columns of every unit into a five-stage ring; warp 1 waits for
+//           the shrink grid and then loads S; warp 2 issues tcgen05 MMAs
+//           D = B_unit S^T (the unit's output columns as the 128-row M
+//           operand, the tile's rows as N) into a tensor-memory accumulator,
+//           four of them in rotation; two warpgroups (warps 3-6 and 7-10) take
+//           alternate units: each gathers its units' y rows two units ahead,
+//           reads the accumulator, adds scale * D into the staged rows and
+//           stores them.  The hand-offs are mbarriers; no block ever
+//           waits on another block.
+// The expand may start before the shrink ends: everything it reads before its
+// wait on the shrink grid (plan, row list, B, y_base) was written by work
+// that had completed before the shrink passed its own wait.
+//
+// Summation orders depend only on a group's sizes (its K-chunk cut, the MMA
+// shapes), never on timing, on which block ran a piece, or on which rows
+// share a tile, so the same inputs give the same bits and permuting tokens
+// permutes the output bits.
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace lora {
+
+constexpr int kPlanItems = 3;                   // shrink chunks per block the plan aims for
+constexpr int kPartialPerRow = 8192;            // fp32 partials per row of a tile, at most (bounds the K-chunk from below)
+constexpr int kTileRows = 64;                   // rows of a tile, at most
+constexpr int kShWarps = 8;                     // MMA warps of the shrink; one more warp streams A
+constexpr int kShThreads = 32 * (kShWarps + 1);
+constexpr int kShAStages = 5;
+constexpr int kShABytes = 16 * 1024;            // A columns of one stage, at most
+constexpr int kShXBytes = 56 * 1024;            // x rows of one chunk, at most
+constexpr int kExThreads = 352;                 // B producer, S loader, MMA issuer, two epilogue warpgroups
+constexpr int kExEpi = 128;                     // threads of one epilogue warpgroup
+constexpr int kExBStages = 5;
+constexpr int kExBBytes = 16 * 1024;            // B columns of one unit, at most
+constexpr int kExYSlots = 3;                    // y slots of one epilogue warpgroup
+constexpr int kExYBytes = 16 * 1024;            // y rows of one unit, at most
+constexpr int kExSBytes = 8 * 1024;             // S of one slice block: at most 64 ranks x 64 rows, bf16
+constexpr int kExAcc = 4;                       // tensor-memory accumulators of kExAccCols columns
+constexpr int kExAccCols = 128;
+constexpr uint32_t kExTmemCols = kExAcc * kExAccCols;
+constexpr int kCostUnit = 512;                  // bytes per unit of the plan's cost positions
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ TileRec load_tile(const TileRec *t)
+{
+    const int4 *q = reinterpret_cast<const int4 *>(t);
+    const int4 v0 = __ldcg(q), v1 = __ldcg(q + 1), v2 = __ldcg(q + 2), v3 = __ldcg(q + 3);
+    TileRec r;
+    r.a = v0.x; r.e = v0.y; r.row0 = v0.z; r.m = v0.w;
+    r.rp = v1.x; r.R = v1.y; r.n_pad = v1.z; r.kc = v1.w;
+    r.n_kc = v2.x; r.ks = v2.y; r.W = v2.z; r.n_units = v2.w;
+    r.p_off = v3.x; r.s_off = v3.y; r.sh_pos = v3.z; r.ex_pos = v3.w;
+    return r;
+}
+
+// (t, j) comes before the end marker e in the (tile, item) order
+__device__ __forceinline__ bool before(int t, int j, int2 e) { return t < e.x || (t == e.x && j < e.y); }
+
+// Named barrier over `count` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x1(uint32_t addr, uint32_t &r0)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x1.shared.b16 {%0}, [%1];" : "=r"(r0) : "r"(addr));
+}
+// D[16][8] += A[16][16] B[16][8] (bf16 in, fp32 accumulate), warp-wide
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D[16][8] += A[16][8] B[8][8]
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Phase stamps (lora_set_trace): kernel k (0 shrink, 1 expand), slot s of this block.
+__device__ __forceinline__ void tstamp(const StreamParams &p, int k, int s)
+{
+    if (p.trace != nullptr && (int)blockIdx.x < p.trace_ctas)
+        p.trace[((size_t)k * p.trace_ctas + blockIdx.x) * kTraceSlots + s] = globaltimer();
+}
+
+// ===========================================================================
+// plan (block 0 of the shrink grid)
+// ===========================================================================
+template <class T>
+__device__ __forceinline__ T warp_sum(T v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+template <class T>
+__device__ __forceinline__ T warp_inclusive(T v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const T u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    return v;
+}
+
+// The plan of one group: its row tiles (m = base + 1 for the first rem tiles, else base), the shrink
+// chunk cut and stage K, the expand unit width.
+struct GroupPlan {
+    int a, e, row_off, count, rp, R, ntl, base, rem, kc, n_kc, ks, W, n_units;
+};
+
+__device__ __forceinline__ int group_tiles(const StreamParams &p, int count)
+{
+    const int tmax = min(p.tile_max, kTileRows);
+    return (count + tmax - 1) / tmax;
+}
+
+// `target` is the shrink bytes the plan aims to give one chunk.  Only 32-bit integer and fp32 arithmetic:
+// a 64-bit integer divide is a long emulated sequence on this GPU.
+__device__ __forceinline__ GroupPlan group_plan(const StreamParams &p, int4 gr, int rp, float target)
+{
+    GroupPlan g;
+    g.a = gr.x;
+    g.e = gr.y;
+    g.row_off = gr.z;
+    g.count = gr.w;
+    g.rp = rp;
+    g.R = p.n_a * rp;
+    g.ntl = group_tiles(p, g.count);
+    g.base = g.count / g.ntl;
+    g.rem = g.count - g.base * g.ntl;
+    const int m_max = g.base + (g.rem > 0 ? 1 : 0);
+    const int K = p.K;
+    // shrink: the x rows of one chunk fill at most one x buffer (xcap columns); a stage of A (ks columns) at
+    // most one A stage; the chunk (the same cut for every tile of the group) is about `target` bytes, and
+    // gives no more than kPartialPerRow partial floats per row where the x buffer allows it
+    const int xcap = ((kShXBytes / 2) / m_max - 8) / 16 * 16;
+    const int ks = min(min(512, (kShABytes / 2) / g.R), xcap) / 16 * 16;
+    const int k_all = (K + ks - 1) / ks * ks;
+    const int kcap = min(k_all, xcap / ks * ks);
+    const int kc_min = min(((K * g.R + kPartialPerRow - 1) / kPartialPerRow + ks - 1) / ks * ks, kcap);   // K R < 2^29
+    const float want = fminf(target / (2.f * (g.R + m_max)), (float)k_all);
+    int kc = (int)ceilf(want / ks) * ks;
+    kc = min(max(kc, max(ks, kc_min)), kcap);
+    g.ks = ks;
+    g.kc = kc;
+    g.n_kc = (K + kc - 1) / kc;
+    // expand: unit width W (its B columns and its y rows each fill at most one stage; its accumulator fits
+    // kExAccCols tensor-memory columns)
+    const int npad_max = (m_max + 15) & ~15;
+    int W = 1024;
+    while (W > 128 && (W * g.rp * 2 > kExBBytes || W * m_max * 2 > kExYBytes || (W / 128) * npad_max > kExAccCols))
+        W >>= 1;
+    g.W = W;
+    int n_units = 0;
+#pragma unroll
+    for (int s = 0; s < kMaxSlices; ++s)
+        if (s < p.n_slices) n_units += (p.slice_n[s] + W - 1) / W;
+    g.n_units = n_units;
+    return g;
+}
+
+// Cost of one shrink chunk and of one expand unit of a tile of m rows, in units of kCostUnit bytes (at
+// least 1).
+__device__ __forceinline__ int chunk_cost(int kc, int R, int m) { return max(1, kc * (R + m) * 2 / kCostUnit); }
+__device__ __forceinline__ int unit_cost(int W, int rp, int m) { return max(1, W * (rp + 2 * m) * 2 / kCostUnit); }
+
+// A launch of G blocks over total cost T: block c starts at position c q + min(c, r), q = T / G, r = T % G
+// (contiguous shares that differ by at most one).
+struct Split {
+    int G, q, r;
+    __device__ __forceinline__ Split(int T, int G_) : G(G_), q(T / G_), r(T - (T / G_) * G_) {}
+    __device__ __forceinline__ int start(int c) const { return c * q + min(c, r); }
+};
+
+// Block c's first (tile, item): the first item at or past its start position, given the tiles' positions,
+// per-item costs and item counts in shared memory.
+__device__ __forceinline__ int2 block_start(const Split &sp, int T, int c, int nt, const int32_t *pos,
+                                            const int32_t *per, const int32_t *n)
+{
+    if (c >= sp.G) return make_int2(nt, 0);
+    const int lo = sp.start(c);
+    if (lo >= T) return make_int2(nt, 0);
+    int l = 0, h = nt;   // pos[l] <= lo < pos[h] (pos[nt] = T)
+    while (h - l > 1) {
+        const int mid = (l + h) >> 1;
+        if (pos[mid] <= lo) l = mid;
+        else h = mid;
+    }
+    const int j = (lo - pos[l] + per[l] - 1) / per[l];
+    return j >= n[l] ? make_int2(l + 1, 0) : make_int2(l, j);
+}
+
+// Shared memory of block 0 while it plans: for the shrink chunks (0), the expand units (1) and the S chunks
+// of the reduction (2), each tile's position, per-item cost and item count.
+constexpr int kPlanCap = 4096;   // tiles whose positions fit; a larger plan fails with LORA_ERR_WORKSPACE
+struct PlanSmem {
+    int32_t pos[3][kPlanCap + 1];
+    int32_t per[3][kPlanCap];
+    int32_t n[3][kPlanCap];
+    int32_t nt, T[3], bad;
+};
+
+// Block 0 of the shrink grid: tile records (global) and the first item of every block of the shrink, of
+// its reduction and of the expand.  Warp 0 walks the groups; every thread then places blocks.
+__device__ void make_plan(const StreamParams &p, PlanSmem &ps)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid < 32) {
+        const int G = max(0, min(__ldcg(p.num_groups), p.group_capacity));
+        // tiles, and the shrink bytes of the whole launch
+        long long est = 0;
+        int ntot = 0;
+        for (int g = lane; g < G; g += 32) {
+            const int4 gr = __ldcg(p.groups + g);
+            const int R = p.n_a * __ldg(p.rpad + gr.x);
+            const int ntl = group_tiles(p, gr.w);
+            ntot += ntl;
+            est += (long long)p.K * 2 * ((long long)R * ntl + gr.w);
+        }
+        est = warp_sum(est);
+        ntot = warp_sum(ntot);
+        const float target = fmaxf(1.f, (float)est / ((float)p.grid_s * kPlanItems));
+        const bool fit = ntot <= p.max_tiles && ntot <= kPlanCap;
+        // tile records: offsets of the partials and of S, positions in the three cost orders
+        int t_run = 0;
+        long long sh_run = 0, ex_run = 0, P_run = 0, S_run = 0;
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            GroupPlan gp;
+            int nt_g = 0;
+            long long sh_g = 0, ex_g = 0, P_g = 0, S_g = 0;
+            if (g < G) {
+                const int4 gr = __ldcg(p.groups + g);
+                gp = group_plan(p, gr, __ldg(p.rpad + gr.x), target);
+                nt_g = gp.ntl;
+                for (int i = 0; i < gp.ntl; ++i) {
+                    const int m = gp.base + (i < gp.rem ? 1 : 0);
+                    sh_g += (long long)gp.n_kc * chunk_cost(gp.kc, gp.R, m);
+                    ex_g += (long long)gp.n_units * unit_cost(gp.W, gp.rp, m);
+                    P_g += (long long)gp.n_kc * m * gp.R;
+                    S_g += gp.R * ((m + 15) & ~15) * 2;
+                }
+            }
+            const int it = warp_inclusive(nt_g);
+            const long long ish = warp_inclusive(sh_g), iex = warp_inclusive(ex_g);
+            const long long iP = warp_inclusive(P_g), iS = warp_inclusive(S_g);
+            if (g < G && fit) {
+                int t = t_run + it - nt_g;
+                long long sh = sh_run + ish - sh_g, ex = ex_run + iex - ex_g, P = P_run + iP - P_g;
+                long long S = S_run + iS - S_g;
+                int row = gp.row_off;
+                for (int i = 0; i < gp.ntl; ++i, ++t) {
+                    const int m = gp.base + (i < gp.rem ? 1 : 0);
+                    const int cs = chunk_cost(gp.kc, gp.R, m), cu = unit_cost(gp.W, gp.rp, m);
+                    TileRec r;
+                    r.a = gp.a;
+                    r.e = gp.e;
+                    r.row0 = row;
+                    r.m = m;
+                    r.rp = gp.rp;
+                    r.R = gp.R;
+                    r.n_pad = (m + 15) & ~15;
+                    r.kc = gp.kc;
+                    r.n_kc = gp.n_kc;
+                    r.ks = gp.ks;
+                    r.W = gp.W;
+                    r.n_units = gp.n_units;
+                    r.p_off = (int)P;
+                    r.s_off = (int)S;
+                    r.sh_pos = (int)sh;
+                    r.ex_pos = (int)ex;
+                    p.tiles[t] = r;
+                    ps.pos[0][t] = (int)sh;
+                    ps.per[0][t] = cs;
+                    ps.n[0][t] = gp.n_kc;
+                    ps.pos[1][t] = (int)ex;
+                    ps.per[1][t] = cu;
+                    ps.n[1][t] = gp.n_units;
+                    ps.pos[2][t] = (int)(S / 16);
+                    ps.per[2][t] = 1;
+                    ps.n[2][t] = gp.R * r.n_pad / 8;
+                    sh += (long long)gp.n_kc * cs;
+                    ex += (long long)gp.n_units * cu;
+                    P += (long long)gp.n_kc * m * gp.R;
+                    S += gp.R * r.n_pad * 2;
+                    row += m;
+                }
+            }
+            t_run += __shfl_sync(0xffffffffu, it, 31);
+            sh_run += __shfl_sync(0xffffffffu, ish, 31);
+            ex_run += __shfl_sync(0xffffffffu, iex, 31);
+            P_run += __shfl_sync(0xffffffffu, iP, 31);
+            S_run += __shfl_sync(0xffffffffu, iS, 31);
+        }
+        const bool bad = !fit || P_run > p.partial_cap || S_run > p.s_cap || sh_run >= (1ll << 31) ||
+                         ex_run >= (1ll << 31) || S_run >= (1ll << 31);
+        if (lane == 0) {
+            const int nt = bad ? 0 : t_run;
+            ps.nt = nt;
+            ps.bad = bad;
+            ps.T[0] = bad ? 0 : (int)sh_run;
+            ps.T[1] = bad ? 0 : (int)ex_run;
+            ps.T[2] = bad ? 0 : (int)(S_run / 16);
+            for (int k = 0; k < 3; ++k) ps.pos[k][nt] = ps.T[k];
+            if (bad) atomicOr(p.err, kErrWorkspace);
+            p.plan_hdr[PL_TILES] = nt;
+        }
+    }
+    __syncthreads();
+    const int nt = ps.nt;
+    const Split ss(ps.T[0], p.grid_s), se(ps.T[1], p.grid_e), sr(ps.T[2], p.grid_s);
+    for (int c = tid; c <= p.grid_s; c += blockDim.x) {
+        p.sh_start[c] = block_start(ss, ps.T[0], c, nt, ps.pos[0], ps.per[0], ps.n[0]);
+        p.rd_start[c] = block_start(sr, ps.T[2], c, nt, ps.pos[2], ps.per[2], ps.n[2]);
+    }
+    for (int c = tid; c <= p.grid_e; c += blockDim.x)
+        p.ex_start[c] = block_start(se, ps.T[1], c, nt, ps.pos[1], ps.per[1], ps.n[1]);
+}
+
+// ===========================================================================
+// shrink
+// ===========================================================================
+struct __align__(128) ShrinkSmem {
+    union {
+        struct {
+            unsigned char a[kShAStages][kShABytes];   // A columns of one stage: [ks/8][R][8]
+            unsigned char x[2][kShXBytes];            // x rows of one chunk: [m][kc + 8]
+        } buf;
+        PlanSmem plan;                                // block 0, before the streams start
+    };
+    uint64_t full[kShAStages], empty[kShAStages];
+    int32_t flag;
+};
+
+// Grid-wide barrier of the (cooperatively launched, so co-resident) shrink grid: the round-th arrival
+// of every block on a counter that the build zeroes and the expand resets.  Bounded: false when it ran out.
+__device__ __forceinline__ bool grid_barrier(const StreamParams &p, ShrinkSmem &sm, int round)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();   // release: this block's global writes before its arrival
+        atomicAdd(p.cnt, 1);
+        const int target = round * (int)gridDim.x;
+        bool in = ld_acquire_gpu(p.cnt) >= target;
+        if (!in) {
+            const uint64_t t0 = globaltimer();
+            while (!(in = ld_acquire_gpu(p.cnt) >= target)) {
+                if (globaltimer() - t0 > p.timeout_ns) {
+                    atomicOr(p.err, kErrTimeout);
+                    break;
+                }
+                nanosleep_ns(32);
+            }
+        }
+        __threadfence();
+        sm.flag = in ? 1 : 0;
+    }
+    __syncthreads();
+    return sm.flag != 0;
+}
+
+// Walks this block's chunks (tile, chunk) in order; the tile record is reloaded when the tile changes.
+struct ChunkWalk {
+    int t, j, cur;
+    int2 end;
+    TileRec tr;
+    __device__ __forceinline__ ChunkWalk(int2 b0, int2 b1) : t(b0.x), j(b0.y), cur(-1), end(b1) {}
+    __device__ __forceinline__ bool valid(const StreamParams &p)
+    {
+        if (!before(t, j, end)) return false;
+        if (t != cur) {
+            tr = load_tile(p.tiles + t);
+            cur = t;
+        }
+        return true;
+    }
+    __device__ __forceinline__ void next()
+    {
+        if (++j == tr.n_kc) {
+            ++t;
+            j = 0;
+        }
+    }
+};
+
+// Warp 8, one thread: the A columns of every stage of this block's chunks (one bulk copy each) into the
+// A ring.
+__device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1)
+{
+    uint32_t s = 0;
+    bool ok = true;
+    for (ChunkWalk w(b0, b1); ok && w.valid(p); w.next()) {
+        const TileRec &tr = w.tr;
+        const unsigned char *ablk =
+            reinterpret_cast<const unsigned char *>(__ldg(p.a_ptr + tr.a * p.E_A + (p.E_A == 1 ? 0 : tr.e)));
+        const int k0 = w.j * tr.kc, kend = min(k0 + tr.kc, p.K);
+        for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
+            const int slot = s % kShAStages;
+            if (s >= kShAStages &&
+                !(ok = mbar_wait_bounded(&sm.empty[slot], ((s / kShAStages) - 1) & 1, p.timeout_ns, p.err)))
+                break;
+            const uint32_t bytes = (uint32_t)tr.R * min(tr.ks, kend - kb) * 2;
+            mbar_arrive_expect_tx(&sm.full[slot], bytes);
+            bulk_g2s(sm.buf.a[slot], ablk + (size_t)(kb / 8) * tr.R * 16, bytes, &sm.full[slot]);
+            if (s < 8) tstamp(p, 0, 12 + s);
+        }
+    }
+    for (uint32_t q = s > kShAStages ? s - kShAStages : 0; q < s; ++q)
+        mbar_wait_bounded(&sm.full[q % kShAStages], (q / kShAStages) & 1, p.timeout_ns, p.err);
+}
+
+// x rows of one chunk into x buffer xb: thread tid takes row tid / 4 (its source row xr) and every fourth
+// 16-byte piece of the chunk's columns.  Commits one cp.async group either way.
+__device__ __forceinline__ void shrink_issue_x(const StreamParams &p, ShrinkSmem &sm, const TileRec &tr, int j, int xr,
+                                               int xb, bool live)
+{
+    const int tid = threadIdx.x, row = tid >> 2;
+    if (live && row < tr.m) {
+        const int k0 = j * tr.kc, kw = min(tr.kc, p.K - k0), cpr = kw >> 3;
+        unsigned char *dst = sm.buf.x[xb] + row * (tr.kc + 8) * 2;
+        const __nv_bfloat16 *src = p.x + (int64_t)xr * p.ldx + k0;
+        for (int c = tid & 3; c < cpr; c += 4) tc::cp_async16(dst + c * 16, src + c * 8, true);
+    }
+    tc::cp_async_commit();
+}
+
+// One chunk of one tile on the eight MMA warps: the fp32 partial X_rows A_chunk^T in registers, then to the
+// tile's partial slot.  Warp (ni0, mi0) owns 8-column blocks ni0, ni0 + wn, ... (MN of them) and 16-row
+// blocks mi0, mi0 + wm, ... (MM of them).  Each output element accumulates its K steps in order, one
+// m16n8k16 per 16 K, so its sum depends on the chunk cut alone.
+template <int MM, int MN>
+__device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &sm, const TileRec &tr, int j, int xb,
+                                             uint32_t &s)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ntc = tr.R >> 3, mtc = (tr.m + 15) >> 4;
+    const int wn = ntc >= 8 ? 8 : ntc, wm = 8 / wn;
+    const bool active = warp < wn * wm;
+    const int ni0 = warp % wn, mi0 = warp / wn;
+    float acc[MM * MN][4];
+#pragma unroll
+    for (int i = 0; i < MM * MN; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    const int xstride = (tr.kc + 8) * 2;
+    const uint32_t x_s = smem_u32(sm.buf.x[xb]);
+    uint32_t xrow[MM];
+#pragma unroll
+    for (int mi = 0; mi < MM; ++mi) {
+        const int row = min((mi0 + mi * wm) * 16 + (lane & 15), tr.m - 1);
+        xrow[mi] = x_s + row * xstride;
+    }
+    const int k0 = j * tr.kc, kend = min(k0 + tr.kc, p.K);
+    for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
+        const int slot = s % kShAStages;
+        const int kk = min(tr.ks, kend - kb), koff = (kb - k0) * 2;
+        if (!mbar_wait_bounded(&sm.full[slot], (s / kShAStages) & 1, p.timeout_ns, p.err)) return false;
+        if (s < 8 && lane == 0 && warp == 0) tstamp(p, 0, 20 + s);
+        const int steps = kk >> 4;
+        const uint32_t a_s = smem_u32(sm.buf.a[slot]);
+        if (active) {
+            const uint32_t arow = a_s + ((lane >> 3) & 1) * tr.R * 16 + (lane & 7) * 16;
+#pragma unroll 2
+            for (int st = 0; st < steps; ++st) {
+                uint32_t b[MN][2];
+#pragma unroll
+                for (int ni = 0; ni < MN; ++ni) {
+                    const int nt = ni0 + ni * wn;
+                    if (nt < ntc) ldsm_x2(arow + (2 * st * tr.R + nt * 8) * 16, b[ni][0], b[ni][1]);
+                }
+#pragma unroll
+                for (int mi = 0; mi < MM; ++mi) {
+                    if (mi0 + mi * wm < mtc) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(xrow[mi] + koff + (2 * st + (lane >> 4)) * 16, a0, a1, a2, a3);
+#pragma unroll
+                        for (int ni = 0; ni < MN; ++ni)
+                            if (ni0 + ni * wn < ntc) mma16816(acc[mi * MN + ni], a0, a1, a2, a3, b[ni][0], b[ni][1]);
+                    }
+                }
+            }
+            if (kk & 8) {   // a last K-group of 8
+                uint32_t b[MN];
+#pragma unroll
+                for (int ni = 0; ni < MN; ++ni) {
+                    const int nt = ni0 + ni * wn;
+                    if (nt < ntc) ldsm_x1(a_s + ((2 * steps) * tr.R + nt * 8 + (lane & 7)) * 16, b[ni]);
+                }
+#pragma unroll
+                for (int mi = 0; mi < MM; ++mi) {
+                    if (mi0 + mi * wm < mtc) {
+                        uint32_t a0, a1;
+                        ldsm_x2(xrow[mi] + koff + (2 * steps) * 16, a0, a1);
+#pragma unroll
+                        for (int ni = 0; ni < MN; ++ni)
+                            if (ni0 + ni * wn < ntc) mma1688(acc[mi * MN + ni], a0, a1, b[ni]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    }
+    if (active) {
+        float *dst = p.partials + tr.p_off + (int64_t)j * tr.m * tr.R;
+#pragma unroll
+        for (int mi = 0; mi < MM; ++mi) {
+#pragma unroll
+            for (int ni = 0; ni < MN; ++ni) {
+                const int mt = mi0 + mi * wm, nt = ni0 + ni * wn;
+                if (mt < mtc && nt < ntc) {
+                    const int row = mt * 16 + (lane >> 2), col = nt * 8 + (lane & 3) * 2;
+                    const float *c = acc[mi * MN + ni];
+                    if (row < tr.m) *reinterpret_cast<float2 *>(dst + row * tr.R + col) = make_float2(c[0], c[1]);
+                    if (row + 8 < tr.m)
+                        *reinterpret_cast<float2 *>(dst + (row + 8) * tr.R + col) = make_float2(c[2], c[3]);
+                }
+            }
+        }
+    }
+    return true;
+}
+
+// Warps 0-7: every chunk of this block.  The x rows of chunk q + 1 are put in flight as chunk q starts (two
+// x buffers), and the source rows of chunk q + 2 are fetched then too, so no copy waits on the row list.
+__device__ __forceinline__ void shrink_consume(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1)
+{
+    const int tid = threadIdx.x, row = tid >> 2;
+    ChunkWalk cw(b0, b1), xw(b0, b1), rw(b0, b1);
+    // source row of this thread's x row for the chunks at the x cursor (xr) and one past it (nr)
+    auto src_row = [&](ChunkWalk &w) -> int {
+        if (!w.valid(p) || row >= w.tr.m) return 0;
+        return __ldcg(p.rows + w.tr.row0 + row) / p.src_div;
+    };
+    int xr = src_row(rw);
+    if (rw.valid(p)) rw.next();
+    bool live = xw.valid(p);
+    shrink_issue_x(p, sm, xw.tr, xw.j, xr, 0, live);
+    if (live) xw.next();
+    xr = src_row(rw);
+    if (rw.valid(p)) rw.next();
+    uint32_t s = 0;
+    bool ok = true;
+    for (int q = 0; cw.valid(p); ++q) {
+        if (!bar_and(1, kShWarps * 32, ok)) break;   // every warp is done with chunk q - 1 and its x buffer
+        live = xw.valid(p);
+        shrink_issue_x(p, sm, xw.tr, xw.j, xr, (q + 1) & 1, live);
+        if (live) xw.next();
+        xr = src_row(rw);
+        if (rw.valid(p)) rw.next();
+        tc::cp_async_wait<1>();   // this thread's x pieces of chunk q
+        bar_sync(1, kShWarps * 32);
+        const TileRec tr = cw.tr;
+        if (tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, tr, cw.j, q & 1, s);
+        else if (tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, tr, cw.j, q & 1, s);
+        else ok = shrink_chunk<4, 4>(p, sm, tr, cw.j, q & 1, s);
+        if (tid == 0 && q < 4) tstamp(p, 0, 3 + q);
+        cw.next();
+    }
+    tc::cp_async_wait<0>();
+}
+
+// S chunk i of a tile (16 bytes of its S layout: slice block sb, rank group kg, row): the tile's partials
+// of those 8 rank columns summed in chunk order, rounded once to bf16.  S is stored per slice block sb as
+// [rp / 8][n_pad][8], the operand layout the expand reads; rows past m are zero.
+__device__ __forceinline__ void reduce_s_chunk(const StreamParams &p, const TileRec &tr, int i)
+{
+    const int per_sb = (tr.rp >> 3) * tr.n_pad;
+    const int sb = i / per_sb, rem = i - sb * per_sb;
+    const int kg = rem / tr.n_pad, row = rem - kg * tr.n_pad;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (row < tr.m) {
+        const float *q = p.partials + tr.p_off + row * tr.R + sb * tr.rp + kg * 8;
+        const int64_t cstride = (int64_t)tr.m * tr.R;
+        for (int c = 0; c < tr.n_kc; ++c, q += cstride) {
+            const float4 u = __ldcg(reinterpret_cast<const float4 *>(q));
+            const float4 w = __ldcg(reinterpret_cast<const float4 *>(q) + 1);
+            a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
+            a[4] += w.x; a[5] += w.y; a[6] += w.z; a[7] += w.w;
+        }
+    }
+    __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = __float2bfloat16_rn(a[e]);
+    *reinterpret_cast<uint4 *>(p.s_area + tr.s_off + (int64_t)i * 16) = *reinterpret_cast<const uint4 *>(o);
+}
+
+__global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_constant__ StreamParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    ShrinkSmem &sm = *reinterpret_cast<ShrinkSmem *>(smem_raw);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        tstamp(p, 0, 0);
+        for (int s = 0; s < kShAStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kShWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();      // the segment table of the build, and everything before it
+    pdl_trigger();   // the expand may launch now; it waits for this grid before it reads anything
+    if (tid == 0) tstamp(p, 0, 1);
+    if (blockIdx.x == 0) make_plan(p, sm.plan);
+    if (grid_barrier(p, sm, 1)) {   // the plan is out
+        if (tid == 0) tstamp(p, 0, 2);
+        const int2 b0 = __ldcg(p.sh_start + blockIdx.x), b1 = __ldcg(p.sh_start + blockIdx.x + 1);
+        if (tid < kShWarps * 32) shrink_consume(p, sm, b0, b1);
+        else if (tid == kShWarps * 32) shrink_produce(p, sm, b0, b1);
+        __syncwarp();
+        if (tid == 0) tstamp(p, 0, 8);
+    }
+    // every block has stored its partials
+    if (!grid_barrier(p, sm, 2)) return;
+    if (tid == 0) tstamp(p, 0, 9);
+
+    // this block's share of S
+    const int2 r0 = __ldcg(p.rd_start + blockIdx.x), r1 = __ldcg(p.rd_start + blockIdx.x + 1);
+    for (int t = r0.x; t < r1.x || (t == r1.x && r1.y > 0); ++t) {
+        const TileRec tr = load_tile(p.tiles + t);
+        const int lo = t == r0.x ? r0.y : 0;
+        const int hi = t == r1.x ? r1.y : tr.R * tr.n_pad / 8;
+        for (int i = lo + tid; i < hi; i += kShThreads) reduce_s_chunk(p, tr, i);
+    }
+    if (tid == 0) tstamp(p, 0, 31);
+}
+
+// ===========================================================================
+// expand
+// ===========================================================================
+struct ExBMeta {
+    int32_t t, sb, n_pad, rp, w_eff;
+};
+struct ExYMeta {
+    int32_t row[kTileRows];   // y row of every tile row
+    float f[kTileRows];       // scale * row weight
+    int32_t col, w_eff, m, n_pad, W;
+};
+
+struct __align__(1024) ExpandSmem {
+    unsigned char bstage[kExBStages][kExBBytes];     // B tiles [W/128][rp/8][128][8]
+    unsigned char ystage[2 * kExYSlots][kExYBytes];  // y rows [m][W]; warpgroup g uses slots g * kExYSlots + k
+    unsigned char sbuf[2][kExSBytes];                // S of one (tile, slice block): [rp/8][n_pad][8]
+    ExBMeta bmeta[kExBStages];
+    ExYMeta ymeta[2 * kExYSlots];
+    int32_t yrow[2][kTileRows];                      // per warpgroup: y rows of the tile its loads are in
+    float yf[2][kTileRows];
+    uint64_t full_b[kExBStages], empty_b[kExBStages];
+    uint64_t s_full[2], s_empty[2];
+    uint64_t acc_full[kExAcc], acc_empty[kExAcc];
+    uint64_t drain;                                  // the MMA issuer's last MMAs are done
+    uint32_t tmem_base;
+};
+
+// Slice and column block of unit u of a tile whose units are W columns wide.
+__device__ __forceinline__ void unit_slice(const StreamParams &p, int W, int u, int &s, int &cb)
+{
+    s = 0;
+    for (; s < p.n_slices - 1; ++s) {
+        const int c = (p.slice_n[s] + W - 1) / W;
+        if (u < c) break;
+        u -= c;
+    }
+    cb = u;
+}
+
+// Walks this block's units in order; the tile record is reloaded when the tile changes.
+struct UnitWalk {
+    int t, u;
+    int2 end;
+    int cur;
+    TileRec tr;
+    __device__ __forceinline__ UnitWalk(int2 b0, int2 b1) : t(b0.x), u(b0.y), end(b1), cur(-1) {}
+    __device__ __forceinline__ bool valid(const StreamParams &p)
+    {
+        if (!before(t, u, end)) return false;
+        if (t != cur) {
+            tr = load_tile(p.tiles + t);
+            cur = t;
+        }
+        return true;
+    }
+    __device__ __forceinline__ void next()
+    {
+        if (++u == tr.n_units) {
+            ++t;
+            u = 0;
+        }
+    }
+};
+
+// Warp 0, one thread: the packed B columns of every unit (one bulk copy), and the unit's description for
+// the MMA issuer.
+__device__ __forceinline__ void expand_produce(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+{
+    uint32_t i = 0;
+    const unsigned char *bblk = nullptr;
+    int blk_t = -1;
+    for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
+        const TileRec &tr = w.tr;
+        if (blk_t != w.t) {
+            bblk = reinterpret_cast<const unsigned char *>(__ldg(p.b_ptr + tr.a * p.E_B + (p.E_B == 1 ? 0 : tr.e)));
+            blk_t = w.t;
+        }
+        int s, cb;
+        unit_slice(p, tr.W, w.u, s, cb);
+        const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
+        const int slot = i % kExBStages;
+        if (i >= kExBStages &&
+            !mbar_wait_bounded(&sm.empty_b[slot], ((i / kExBStages) - 1) & 1, p.timeout_ns, p.err))
+            break;
+        ExBMeta &mt = sm.bmeta[slot];
+        mt.t = w.t;
+        mt.sb = p.n_a == 1 ? 0 : s;
+        mt.n_pad = tr.n_pad;
+        mt.rp = tr.rp;
+        mt.w_eff = w_eff;
+        const uint32_t bbytes = (uint32_t)((w_eff + 127) >> 7) * tr.rp * 256;
+        mbar_arrive_expect_tx(&sm.full_b[slot], bbytes);
+        bulk_g2s(sm.bstage[slot], bblk + (size_t)(p.slice_tile_off[s] + cb * (tr.W >> 7)) * tr.rp * 256, bbytes,
+                 &sm.full_b[slot]);
+    }
+    for (uint32_t q = i > kExBStages ? i - kExBStages : 0; q < i; ++q)
+        mbar_wait_bounded(&sm.full_b[q % kExBStages], (q / kExBStages) & 1, p.timeout_ns, p.err);
+}
+
+// Warp 1, one thread: S of every (tile, slice block) this block meets, into two buffers in rotation.
+__device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+{
+    tstamp(p, 1, 3);
+    uint32_t k = 0;
+    int prev_t = -1, prev_sb = -1;
+    for (UnitWalk w(b0, b1); w.valid(p); w.next()) {
+        int s, cb;
+        unit_slice(p, w.tr.W, w.u, s, cb);
+        const int sb = p.n_a == 1 ? 0 : s;
+        if (w.t == prev_t && sb == prev_sb) continue;
+        const int slot = k & 1;
+        if (k >= 2 && !mbar_wait_bounded(&sm.s_empty[slot], ((k >> 1) - 1) & 1, p.timeout_ns, p.err)) break;
+        const uint32_t bytes = (uint32_t)w.tr.rp * w.tr.n_pad * 2;
+        mbar_arrive_expect_tx(&sm.s_full[slot], bytes);
+        if (!p.withhold) bulk_g2s(sm.sbuf[slot], p.s_area + w.tr.s_off + (size_t)sb * bytes, bytes, &sm.s_full[slot]);
+        ++k;
+        prev_t = w.t;
+        prev_sb = sb;
+    }
+    if (!p.withhold)
+        for (uint32_t q = k > 2 ? k - 2 : 0; q < k; ++q)
+            mbar_wait_bounded(&sm.s_full[q & 1], (q >> 1) & 1, p.timeout_ns, p.err);
+}
+
+// Warp 2, one thread: D(acc) = B_unit S^T for every unit (M = 128 output columns per B tile, N = the tile's
+// rows rounded up to 16, K = the stored rank).
+__device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+{
+    uint32_t i = 0, k = 0;
+    int prev_t = -1, prev_sb = -1;
+    for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
+        const int slot = i % kExBStages;
+        if (!mbar_wait_bounded(&sm.full_b[slot], (i / kExBStages) & 1, p.timeout_ns, p.err)) break;
+        if (i == 0) tstamp(p, 1, 2);
+        if (i < 8) tstamp(p, 1, 9 + i);
+        const ExBMeta mt = sm.bmeta[slot];
+        if (mt.t != prev_t || mt.sb != prev_sb) {
+            if (k > 0) tc::mma_commit(&sm.s_empty[(k - 1) & 1]);   // the previous S is free once these MMAs end
+            if (!mbar_wait_bounded(&sm.s_full[k & 1], (k >> 1) & 1, p.timeout_ns, p.err)) break;
+            if (k == 0) tstamp(p, 1, 4);
+            ++k;
+            prev_t = mt.t;
+            prev_sb = mt.sb;
+        }
+        const int b = i % kExAcc;
+        if (i >= kExAcc && !mbar_wait_bounded(&sm.acc_empty[b], ((i / kExAcc) - 1) & 1, p.timeout_ns, p.err)) break;
+        tc::fence_after_sync();
+        const uint32_t idesc = tc::idesc_bf16(128, mt.n_pad);
+        const uint32_t s_addr = smem_u32(sm.sbuf[(k - 1) & 1]);
+        const uint32_t b_addr = smem_u32(sm.bstage[slot]);
+        const int nq = (mt.w_eff + 127) >> 7, nk = mt.rp >> 4;
+        for (int q = 0; q < nq; ++q) {
+            for (int kk = 0; kk < nk; ++kk) {
+                const uint64_t ad = tc::smem_desc(b_addr + q * mt.rp * 256 + kk * 2 * 2048, 2048, 128);
+                const uint64_t bd = tc::smem_desc(s_addr + kk * 2 * mt.n_pad * 16, mt.n_pad * 16, 128);
+                tc::mma_bf16(sm.tmem_base + b * kExAccCols + q * mt.n_pad, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+        }
+        tc::mma_commit(&sm.acc_full[b]);
+        tc::mma_commit(&sm.empty_b[slot]);
+    }
+    // tensor memory is freed when the block ends: every MMA issued must be done by then
+    if (i > 0) {
+        tc::mma_commit(&sm.drain);
+        mbar_wait_bounded(&sm.drain, 0, p.timeout_ns, p.err);
+    }
+}
+
+// Runs f(row, chunk) over the m x cpr 16-byte chunks of a unit, spread over the 128 threads of a warpgroup
+// (a shift and a mask when cpr is a power of two, the usual case).
+template <class F>
+__device__ __forceinline__ void for_chunks(int et, int m, int cpr, F f)
+{
+    if ((cpr & (cpr - 1)) == 0) {
+        const int sh = __ffs(cpr) - 1;
+        for (int q = et; q < (m << sh); q += kExEpi) f(q >> sh, q & (cpr - 1));
+    } else {
+        for (int q = et; q < m * cpr; q += kExEpi) {
+            const int row = q / cpr;
+            f(row, q - row * cpr);
+        }
+    }
+}
+
+// Warpgroup wg: put the y rows of its unit at the load cursor in flight into its slot k (16-byte cp.async
+// pieces over its 128 threads), with the unit's rows and factors; commits one cp.async group either way.
+__device__ __forceinline__ void expand_issue_y(const StreamParams &p, ExpandSmem &sm, UnitWalk &lw, int wg, int k,
+                                               int &y_tile)
+{
+    const int et = (threadIdx.x - 96) & 127;
+    if (lw.valid(p)) {
+        const TileRec &tr = lw.tr;
+        if (lw.t != y_tile) {   // a new tile: its rows and factors into the cache (every thread takes this branch)
+            int v = 0;
+            float f = 0.f;
+            if (et < tr.m) {
+                v = __ldcg(p.rows + tr.row0 + et);
+                const float sc = __ldg(p.scale + tr.a);
+                f = p.row_weight ? sc * __ldg(p.row_weight + v) : sc;
+            }
+            bar_sync(1 + wg, kExEpi);   // every thread is done with the last tile's rows
+            if (et < tr.m) {
+                sm.yrow[wg][et] = v;
+                sm.yf[wg][et] = f;
+            }
+            bar_sync(1 + wg, kExEpi);
+            y_tile = lw.t;
+        }
+        int s, cb;
+        unit_slice(p, tr.W, lw.u, s, cb);
+        const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
+        const int col = p.slice_off[s] + cb * tr.W;
+        const int slot = wg * kExYSlots + k % kExYSlots;
+        ExYMeta &mt = sm.ymeta[slot];
+        if (et < tr.m) {
+            mt.row[et] = sm.yrow[wg][et];
+            mt.f[et] = sm.yf[wg][et];
+        }
+        if (et == 0) {
+            mt.col = col;
+            mt.w_eff = w_eff;
+            mt.m = tr.m;
+            mt.n_pad = tr.n_pad;
+            mt.W = tr.W;
+        }
+        unsigned char *ys = sm.ystage[slot];
+        const int W = tr.W;
+        const int32_t *yrow = sm.yrow[wg];
+        for_chunks(et, tr.m, w_eff >> 3, [&](int row, int c) {
+            tc::cp_async16(ys + row * W * 2 + c * 16, p.y + (int64_t)yrow[row] * p.ldy + col + c * 8, true);
+        });
+        // the other warpgroup takes the next unit
+        lw.next();
+        if (lw.valid(p)) lw.next();
+    }
+    tc::cp_async_commit();
+}
+
+// Warpgroup wg (warps 3-6 or 7-10) takes units wg, wg + 2, ...  Thread (quarter qw, lane) owns output
+// column 32 qw + lane of every 128-column group of a unit: it reads that column's accumulator for all rows
+// and adds it into the staged y rows; the rows then leave as 16-byte stores.  The y rows of a unit are put
+// in flight two of its units ahead.
+__device__ __forceinline__ void expand_epilogue(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1, int wg)
+{
+    const int lane = threadIdx.x & 31, qw = (threadIdx.x >> 5) & 3, et = (threadIdx.x - 96) & 127;
+    const int bar = 1 + wg;
+    UnitWalk lw(b0, b1), w(b0, b1);
+    if (wg == 1) {   // this warpgroup starts at the second unit
+        if (lw.valid(p)) lw.next();
+        if (w.valid(p)) w.next();
+    }
+    int y_tile = -1;
+    for (int k = 0; k < kExYSlots - 1; ++k) expand_issue_y(p, sm, lw, wg, k, y_tile);
+    bool ok = true;
+    for (int k = 0; w.valid(p); ++k) {
+        const uint32_t i = 2 * k + wg;   // the unit's index in the block's sequence
+        tc::cp_async_wait<kExYSlots - 2>();     // this thread's y pieces of unit k
+        if (!bar_and(bar, kExEpi, ok)) break;   // unit k's y visible to all; unit k - 1 done by all
+        expand_issue_y(p, sm, lw, wg, k + kExYSlots - 1, y_tile);
+        const int slot = wg * kExYSlots + k % kExYSlots, b = i % kExAcc;
+        const bool got = mbar_wait_bounded(&sm.acc_full[b], (i / kExAcc) & 1, p.timeout_ns, p.err);
+        ok = __all_sync(0xffffffffu, got);
+        if (i < 8 && et == 0) tstamp(p, 1, 17 + i);
+        if (ok) {
+            tc::fence_after_sync();
+            const ExYMeta &mt = sm.ymeta[slot];
+            const int m = mt.m, W = mt.W, w_eff = mt.w_eff, n_pad = mt.n_pad;
+            __nv_bfloat16 *ys = reinterpret_cast<__nv_bfloat16 *>(sm.ystage[slot]);
+            const uint32_t tbase = sm.tmem_base + ((uint32_t)(qw * 32) << 16) + b * kExAccCols;
+            const int nq = (w_eff + 127) >> 7;
+            for (int q = 0; q < nq; ++q) {
+                const int c = q * 128 + qw * 32 + lane;
+                const bool live = c < w_eff;
+                __nv_bfloat16 *yc = ys + c;
+                for (int j0 = 0; j0 < n_pad; j0 += 32) {
+                    float v[32];
+                    // the second half re-reads the first when only 16 rows remain (stays inside the
+                    // accumulator)
+                    const uint32_t ta = tbase + q * n_pad + j0;
+                    tc::tmem_ld16x2(ta, j0 + 16 < n_pad ? ta + 16 : ta, v);
+                    const int nrow = min(32, m - j0);
+                    if (live) {
+#pragma unroll 4
+                        for (int h = 0; h < 32; h += 8) {
+                            if (h < nrow) {
+                                float yv[8];
+#pragma unroll
+                                for (int jj = 0; jj < 8; ++jj)
+                                    yv[jj] = h + jj < nrow ? __bfloat162float(yc[(j0 + h + jj) * W]) : 0.f;
+#pragma unroll
+                                for (int jj = 0; jj < 8; ++jj)
+                                    if (h + jj < nrow)
+                                        yc[(j0 + h + jj) * W] =
+                                            __float2bfloat16_rn(fmaf(mt.f[j0 + h + jj], v[h + jj], yv[jj]));
+                            }
+                        }
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+            bar_sync(bar, kExEpi);   // every column of the unit updated
+            const int col = mt.col;
+            const unsigned char *yb = sm.ystage[slot];
+            for_chunks(et, m, w_eff >> 3, [&](int row, int c) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(yb + row * W * 2 + c * 16);
+                *reinterpret_cast<uint4 *>(p.y + (int64_t)mt.row[row] * p.ldy + col + c * 8) = v;
+            });
+            if (k == 0 && et == 0) tstamp(p, 1, 5 + wg);
+        }
+        w.next();
+        if (w.valid(p)) w.next();
+    }
+    tc::cp_async_wait<0>();
+    if (et == 0) tstamp(p, 1, 7 + wg);
+}
+
+__global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_constant__ StreamParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    ExpandSmem &sm = *reinterpret_cast<ExpandSmem *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        tstamp(p, 1, 0);
+        for (int s = 0; s < kExBStages; ++s) {
+            mbar_init(&sm.full_b[s], 1);
+            mbar_init(&sm.empty_b[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.s_full[s], 1);
+            mbar_init(&sm.s_empty[s], 1);
+        }
+        for (int s = 0; s < kExAcc; ++s) {
+            mbar_init(&sm.acc_full[s], 1);
+            mbar_init(&sm.acc_empty[s], 4);
+        }
+        mbar_init(&sm.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 2) tc::tmem_alloc(&sm.tmem_base, kExTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    pdl_wait();   // the plan, S and everything else of the shrink grid
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.cnt = 0;   // the shrink's grid barrier counter, for the next launch
+    const int2 b0 = __ldcg(p.ex_start + blockIdx.x), b1 = __ldcg(p.ex_start + blockIdx.x + 1);
+    if (threadIdx.x == 0) tstamp(p, 1, 1);
+    if (warp == 0) {
+        if (lane == 0) expand_produce(p, sm, b0, b1);
+    } else if (warp == 1) {
+        if (lane == 0) expand_load_s(p, sm, b0, b1);
+    } else if (warp == 2) {
+        if (lane == 0) expand_mma(p, sm, b0, b1);
+    } else {
+        expand_epilogue(p, sm, b0, b1, warp >= 7 ? 1 : 0);
+    }
+    __syncwarp();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(sm.tmem_base, kExTmemCols);
+    }
+    if (threadIdx.x == 0) tstamp(p, 1, 31);
+}
+
+// ===========================================================================
+// host side
+// ===========================================================================
+size_t stream_plan_bytes(int32_t max_tiles)
+{
+    const size_t a = 256 + (size_t)max_tiles * sizeof(TileRec) + 3 * ((size_t)kStreamMaxGrid + 1) * 8;
+    return (a + 255) / 256 * 256;
+}
+
+int stream_grid(int sms) { return sms < kStreamMaxGrid ? sms : kStreamMaxGrid; }
+
+cudaError_t launch_stream(const StreamParams &p, cudaStream_t s, bool pdl)
+{
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (attr_dev != dev) {   // the attributes are per device; the first launch on each sets them
+        e = cudaFuncSetAttribute(shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ShrinkSmem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sizeof(ExpandSmem));
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    if (p.grid_s > kStreamMaxGrid || p.grid_e > kStreamMaxGrid) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+
+    // the shrink waits twice for every block of its grid: a cooperative launch keeps them all resident
+    cfg.attrs = pdl ? attr : attr + 1;
+    cfg.numAttrs = pdl ? 2 : 1;
+    cfg.gridDim = dim3(p.grid_s);
+    cfg.blockDim = dim3(kShThreads);
+    cfg.dynamicSmemBytes = sizeof(ShrinkSmem);
+    e = cudaLaunchKernelEx(&cfg, shrink_kernel, p);
+    if (e != cudaSuccess) return e;
+
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.gridDim = dim3(p.grid_e);
+    cfg.blockDim = dim3(kExThreads);
+    cfg.dynamicSmemBytes = sizeof(ExpandSmem);
+    return cudaLaunchKernelEx(&cfg, expand_kernel, p);
+}
+
+}  // namespace lora

@@ -67,8 +67,8 @@ def check_close(got, ref, what=""):
 
 
 class forced_path:
-    """Context manager: LORA_OPT_PATH = path (0 auto, 1 small tiles, 2 128-row tensor-core tiles)
-    inside the block."""
+    """Context manager: LORA_OPT_PATH = path inside the block (0 the streaming path, 3 the streaming path
+    on 16-row tiles, 1 the persistent engine on small tiles, 2 the persistent engine on 128-row tiles)."""
 
     def __init__(self, path):
         self.path = path
@@ -81,4 +81,4 @@ class forced_path:
         lora.lora_set_option(lora.LORA_OPT_PATH, self.old)
 
 
-PATHS = (0, 1, 2)
+PATHS = (0, 1, 2, 3)

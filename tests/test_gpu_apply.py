@@ -77,7 +77,7 @@ def test_integer_inputs_bit_exact_with_ragged_k_on_tensor_cores():
     p = synth.make_dense_int(13, ids, 200, [136, 72], [16, 48, 8])
     ref = oracle_dense(p)
     assert np.abs(ref).max() <= 256
-    for path in (1, 2):
+    for path in PATHS:
         with forced_path(path):
             y, _, ws = run_dense(p)
         assert lora.lora_get_status(ws) == lora.LORA_OK
@@ -153,7 +153,7 @@ def test_stored_ranks_follow_the_padding_rule():
     assert info.num_rank_groups == 4 and info.L == 5 and info.N == 64
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", PATHS)
 def test_handoff_wait_times_out_cleanly_and_recovers(path):
     p = synth.decode(1, y_base="random")
     table = pack_dense(p)
