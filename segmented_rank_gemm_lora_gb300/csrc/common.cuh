@@ -254,6 +254,33 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Wait for phase `parity` of an mbarrier with a time limit, letting the hardware suspend the thread until
+// the phase completes (up to 20 us per try) instead of polling, so a waiting thread takes no issue slots from
+// the warps that work beside it.  Returns false (and sets the timeout bit) when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity, uint64_t limit_ns, uint32_t *err)
+{
+    auto try_wait = [&]() {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+            : "memory");
+        return ok != 0;
+    };
+    if (try_wait()) return true;
+    const uint64_t t0 = globaltimer();
+    while (!try_wait()) {
+        if (globaltimer() - t0 > limit_ns) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Retire `bytes` of an mbarrier's expected transactions that will never arrive.
 __device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
 {

@@ -61,11 +61,12 @@ constexpr int kShThreads = 32 * (kShWarps + 1);
 constexpr int kShAStages = 5;
 constexpr int kShABytes = 16 * 1024;            // A columns of one stage, at most
 constexpr int kShXBytes = 56 * 1024;            // x rows of one chunk, at most
-constexpr int kExThreads = 352;                 // B producer, S loader, MMA issuer, two epilogue warpgroups
+constexpr int kExGroups = 3;                    // epilogue warpgroups (units dealt round-robin)
+constexpr int kExThreads = 128 + 128 * kExGroups;   // B producer, S loader, MMA issuer, y producer, epilogue groups
 constexpr int kExEpi = 128;                     // threads of one epilogue warpgroup
 constexpr int kExBStages = 5;
 constexpr int kExBBytes = 16 * 1024;            // B columns of one unit, at most
-constexpr int kExYSlots = 3;                    // y slots of one epilogue warpgroup
+constexpr int kExYStages = 6;
 constexpr int kExYBytes = 16 * 1024;            // y rows of one unit, at most
 constexpr int kExSBytes = 8 * 1024;             // S of one slice block: at most 64 ranks x 64 rows, bf16
 constexpr int kExAcc = 4;                       // tensor-memory accumulators of kExAccCols columns
@@ -274,19 +275,30 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     if (tid < 32) {
+        // the group count, the first 32 group records and the first 32 stored ranks in one round trip
         const int G = max(0, min(__ldcg(p.num_groups), p.group_capacity));
+        const int4 gr0 = lane < p.group_capacity ? __ldcg(p.groups + lane) : make_int4(0, 0, 0, 0);
+        const int rp0 = lane < p.L ? __ldg(p.rpad + lane) : 0;
+        auto rank_of = [&](int a) {   // stored rank of adapter a (a shuffle for the first 32)
+            const int v = __shfl_sync(0xffffffffu, rp0, a & 31);
+            return a < 32 ? v : __ldg(p.rpad + a);
+        };
         // tiles, and the shrink bytes of the whole launch
         long long est = 0;
         int ntot = 0;
-        for (int g = lane; g < G; g += 32) {
-            const int4 gr = __ldcg(p.groups + g);
-            const int R = p.n_a * __ldg(p.rpad + gr.x);
-            const int ntl = group_tiles(p, gr.w);
-            ntot += ntl;
-            est += (long long)p.K * 2 * ((long long)R * ntl + gr.w);
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            const int4 gr = g0 == 0 ? gr0 : (g < G ? __ldcg(p.groups + g) : make_int4(0, 0, 0, 0));
+            const int rp = rank_of(gr.x);
+            if (g < G) {
+                const int ntl = group_tiles(p, gr.w);
+                ntot += ntl;
+                est += (long long)p.K * 2 * ((long long)p.n_a * rp * ntl + gr.w);
+            }
         }
         est = warp_sum(est);
         ntot = warp_sum(ntot);
+        if (lane == 0) tstamp(p, 0, 10);
         const float target = fmaxf(1.f, (float)est / ((float)p.grid_s * kPlanItems));
         const bool fit = ntot <= p.max_tiles && ntot <= kPlanCap;
         // tile records: offsets of the partials and of S, positions in the three cost orders
@@ -297,9 +309,10 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
             GroupPlan gp;
             int nt_g = 0;
             long long sh_g = 0, ex_g = 0, P_g = 0, S_g = 0;
+            const int4 gr = g0 == 0 ? gr0 : (g < G ? __ldcg(p.groups + g) : make_int4(0, 0, 0, 0));
+            const int rp = rank_of(gr.x);
             if (g < G) {
-                const int4 gr = __ldcg(p.groups + g);
-                gp = group_plan(p, gr, __ldg(p.rpad + gr.x), target);
+                gp = group_plan(p, gr, rp, target);
                 nt_g = gp.ntl;
                 for (int i = 0; i < gp.ntl; ++i) {
                     const int m = gp.base + (i < gp.rem ? 1 : 0);
@@ -360,6 +373,7 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
             P_run += __shfl_sync(0xffffffffu, iP, 31);
             S_run += __shfl_sync(0xffffffffu, iS, 31);
         }
+        if (lane == 0) tstamp(p, 0, 11);
         const bool bad = !fit || P_run > p.partial_cap || S_run > p.s_cap || sh_run >= (1ll << 31) ||
                          ex_run >= (1ll << 31) || S_run >= (1ll << 31);
         if (lane == 0) {
@@ -465,7 +479,7 @@ __device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem
         for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
             const int slot = s % kShAStages;
             if (s >= kShAStages &&
-                !(ok = mbar_wait_bounded(&sm.empty[slot], ((s / kShAStages) - 1) & 1, p.timeout_ns, p.err)))
+                !(ok = mbar_wait_suspend(&sm.empty[slot], ((s / kShAStages) - 1) & 1, p.timeout_ns, p.err)))
                 break;
             const uint32_t bytes = (uint32_t)tr.R * min(tr.ks, kend - kb) * 2;
             mbar_arrive_expect_tx(&sm.full[slot], bytes);
@@ -474,7 +488,7 @@ __device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem
         }
     }
     for (uint32_t q = s > kShAStages ? s - kShAStages : 0; q < s; ++q)
-        mbar_wait_bounded(&sm.full[q % kShAStages], (q / kShAStages) & 1, p.timeout_ns, p.err);
+        mbar_wait_suspend(&sm.full[q % kShAStages], (q / kShAStages) & 1, p.timeout_ns, p.err);
 }
 
 // x rows of one chunk into x buffer xb: thread tid takes row tid / 4 (its source row xr) and every fourth
@@ -520,7 +534,7 @@ __device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &
     for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
         const int slot = s % kShAStages;
         const int kk = min(tr.ks, kend - kb), koff = (kb - k0) * 2;
-        if (!mbar_wait_bounded(&sm.full[slot], (s / kShAStages) & 1, p.timeout_ns, p.err)) return false;
+        if (!mbar_wait_suspend(&sm.full[slot], (s / kShAStages) & 1, p.timeout_ns, p.err)) return false;
         if (s < 8 && lane == 0 && warp == 0) tstamp(p, 0, 20 + s);
         const int steps = kk >> 4;
         const uint32_t a_s = smem_u32(sm.buf.a[slot]);
@@ -695,24 +709,25 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
 // ===========================================================================
 // expand
 // ===========================================================================
+// A unit's B columns in a B stage (for the MMA issuer) and its y rows in a y slot (for the epilogue), each
+// described by the warp that filled it.
 struct ExBMeta {
     int32_t t, sb, n_pad, rp, w_eff;
 };
-struct ExYMeta {
+struct __align__(16) ExYMeta {
+    float f[kTileRows];       // scale * row weight (read as float4)
     int32_t row[kTileRows];   // y row of every tile row
-    float f[kTileRows];       // scale * row weight
-    int32_t col, w_eff, m, n_pad, W;
+    int32_t W, m, w_eff, n_pad, col;
 };
 
 struct __align__(1024) ExpandSmem {
     unsigned char bstage[kExBStages][kExBBytes];     // B tiles [W/128][rp/8][128][8]
-    unsigned char ystage[2 * kExYSlots][kExYBytes];  // y rows [m][W]; warpgroup g uses slots g * kExYSlots + k
+    unsigned char ystage[kExYStages][kExYBytes];     // y rows [m][W]
     unsigned char sbuf[2][kExSBytes];                // S of one (tile, slice block): [rp/8][n_pad][8]
     ExBMeta bmeta[kExBStages];
-    ExYMeta ymeta[2 * kExYSlots];
-    int32_t yrow[2][kTileRows];                      // per warpgroup: y rows of the tile its loads are in
-    float yf[2][kTileRows];
+    ExYMeta ymeta[kExYStages];
     uint64_t full_b[kExBStages], empty_b[kExBStages];
+    uint64_t full_y[kExYStages], empty_y[kExYStages];
     uint64_t s_full[2], s_empty[2];
     uint64_t acc_full[kExAcc], acc_empty[kExAcc];
     uint64_t drain;                                  // the MMA issuer's last MMAs are done
@@ -756,9 +771,9 @@ struct UnitWalk {
     }
 };
 
-// Warp 0, one thread: the packed B columns of every unit (one bulk copy), and the unit's description for
-// the MMA issuer.
-__device__ __forceinline__ void expand_produce(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+// Warp 0, one thread: the packed B columns of every unit (one bulk copy each) into the B ring, with the
+// unit's description for the MMA issuer.
+__device__ __forceinline__ void expand_produce_b(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
 {
     uint32_t i = 0;
     const unsigned char *bblk = nullptr;
@@ -774,7 +789,7 @@ __device__ __forceinline__ void expand_produce(const StreamParams &p, ExpandSmem
         const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
         const int slot = i % kExBStages;
         if (i >= kExBStages &&
-            !mbar_wait_bounded(&sm.empty_b[slot], ((i / kExBStages) - 1) & 1, p.timeout_ns, p.err))
+            !mbar_wait_suspend(&sm.empty_b[slot], ((i / kExBStages) - 1) & 1, p.timeout_ns, p.err))
             break;
         ExBMeta &mt = sm.bmeta[slot];
         mt.t = w.t;
@@ -788,7 +803,70 @@ __device__ __forceinline__ void expand_produce(const StreamParams &p, ExpandSmem
                  &sm.full_b[slot]);
     }
     for (uint32_t q = i > kExBStages ? i - kExBStages : 0; q < i; ++q)
-        mbar_wait_bounded(&sm.full_b[q % kExBStages], (q / kExBStages) & 1, p.timeout_ns, p.err);
+        mbar_wait_suspend(&sm.full_b[q % kExBStages], (q / kExBStages) & 1, p.timeout_ns, p.err);
+}
+
+// Warp 3: the y rows of every unit (16-byte cp.async pieces over the 32 lanes) into the y ring, with the
+// unit's rows and factors for the epilogue.  Each lane's pieces complete on the slot's mbarrier.
+__device__ __forceinline__ void expand_produce_y(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t i = 0;
+    int cur = -1;
+    int yr0 = 0, yr1 = 0;      // y rows lane and lane + 32 of the current tile
+    float yf0 = 0.f, yf1 = 0.f;
+    for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
+        const TileRec &tr = w.tr;
+        if (cur != w.t) {
+            const float sc = __ldg(p.scale + tr.a);
+            yr0 = lane < tr.m ? __ldcg(p.rows + tr.row0 + lane) : 0;
+            yr1 = lane + 32 < tr.m ? __ldcg(p.rows + tr.row0 + lane + 32) : 0;
+            yf0 = p.row_weight ? sc * __ldg(p.row_weight + yr0) : sc;
+            yf1 = p.row_weight ? sc * __ldg(p.row_weight + yr1) : sc;
+            cur = w.t;
+        }
+        int s, cb;
+        unit_slice(p, tr.W, w.u, s, cb);
+        const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
+        const int slot = i % kExYStages;
+        if (i >= kExYStages &&
+            !mbar_wait_suspend(&sm.empty_y[slot], ((i / kExYStages) - 1) & 1, p.timeout_ns, p.err))
+            break;
+        ExYMeta &mt = sm.ymeta[slot];
+        const int col = p.slice_off[s] + cb * tr.W;
+        if (lane < tr.m) {
+            mt.row[lane] = yr0;
+            mt.f[lane] = yf0;
+        }
+        if (lane + 32 < tr.m) {
+            mt.row[lane + 32] = yr1;
+            mt.f[lane + 32] = yf1;
+        }
+        if (lane == 0) {
+            mt.W = tr.W;
+            mt.m = tr.m;
+            mt.w_eff = w_eff;
+            mt.n_pad = tr.n_pad;
+            mt.col = col;
+        }
+        __syncwarp();
+        unsigned char *ys = sm.ystage[slot];
+        const int cpr = w_eff >> 3, W2 = tr.W * 2;
+        if ((cpr & (cpr - 1)) == 0) {
+            const int sh = __ffs(cpr) - 1;
+            for (int q = lane; q < (tr.m << sh); q += 32) {
+                const int row = q >> sh, c = q & (cpr - 1);
+                tc::cp_async16(ys + row * W2 + c * 16, p.y + (int64_t)mt.row[row] * p.ldy + col + c * 8, true);
+            }
+        } else {
+            for (int q = lane; q < tr.m * cpr; q += 32) {
+                const int row = q / cpr, c = q - row * cpr;
+                tc::cp_async16(ys + row * W2 + c * 16, p.y + (int64_t)mt.row[row] * p.ldy + col + c * 8, true);
+            }
+        }
+        tc::cp_async_arrive_noinc(&sm.full_y[slot]);   // once every piece of this lane has landed
+    }
+    tc::cp_async_wait<0>();
 }
 
 // Warp 1, one thread: S of every (tile, slice block) this block meets, into two buffers in rotation.
@@ -803,7 +881,7 @@ __device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem 
         const int sb = p.n_a == 1 ? 0 : s;
         if (w.t == prev_t && sb == prev_sb) continue;
         const int slot = k & 1;
-        if (k >= 2 && !mbar_wait_bounded(&sm.s_empty[slot], ((k >> 1) - 1) & 1, p.timeout_ns, p.err)) break;
+        if (k >= 2 && !mbar_wait_suspend(&sm.s_empty[slot], ((k >> 1) - 1) & 1, p.timeout_ns, p.err)) break;
         const uint32_t bytes = (uint32_t)w.tr.rp * w.tr.n_pad * 2;
         mbar_arrive_expect_tx(&sm.s_full[slot], bytes);
         if (!p.withhold) bulk_g2s(sm.sbuf[slot], p.s_area + w.tr.s_off + (size_t)sb * bytes, bytes, &sm.s_full[slot]);
@@ -813,7 +891,7 @@ __device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem 
     }
     if (!p.withhold)
         for (uint32_t q = k > 2 ? k - 2 : 0; q < k; ++q)
-            mbar_wait_bounded(&sm.s_full[q & 1], (q >> 1) & 1, p.timeout_ns, p.err);
+            mbar_wait_suspend(&sm.s_full[q & 1], (q >> 1) & 1, p.timeout_ns, p.err);
 }
 
 // Warp 2, one thread: D(acc) = B_unit S^T for every unit (M = 128 output columns per B tile, N = the tile's
@@ -824,189 +902,119 @@ __device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm
     int prev_t = -1, prev_sb = -1;
     for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
         const int slot = i % kExBStages;
-        if (!mbar_wait_bounded(&sm.full_b[slot], (i / kExBStages) & 1, p.timeout_ns, p.err)) break;
+        if (!mbar_wait_suspend(&sm.full_b[slot], (i / kExBStages) & 1, p.timeout_ns, p.err)) break;
         if (i == 0) tstamp(p, 1, 2);
         if (i < 8) tstamp(p, 1, 9 + i);
-        const ExBMeta mt = sm.bmeta[slot];
-        if (mt.t != prev_t || mt.sb != prev_sb) {
+        const ExBMeta &mt = sm.bmeta[slot];
+        const int t = mt.t, sb = mt.sb, n_pad = mt.n_pad, rp = mt.rp, w_eff = mt.w_eff;
+        if (t != prev_t || sb != prev_sb) {
             if (k > 0) tc::mma_commit(&sm.s_empty[(k - 1) & 1]);   // the previous S is free once these MMAs end
-            if (!mbar_wait_bounded(&sm.s_full[k & 1], (k >> 1) & 1, p.timeout_ns, p.err)) break;
+            if (!mbar_wait_suspend(&sm.s_full[k & 1], (k >> 1) & 1, p.timeout_ns, p.err)) break;
             if (k == 0) tstamp(p, 1, 4);
             ++k;
-            prev_t = mt.t;
-            prev_sb = mt.sb;
+            prev_t = t;
+            prev_sb = sb;
         }
         const int b = i % kExAcc;
-        if (i >= kExAcc && !mbar_wait_bounded(&sm.acc_empty[b], ((i / kExAcc) - 1) & 1, p.timeout_ns, p.err)) break;
+        if (i >= kExAcc && !mbar_wait_suspend(&sm.acc_empty[b], ((i / kExAcc) - 1) & 1, p.timeout_ns, p.err)) break;
         tc::fence_after_sync();
-        const uint32_t idesc = tc::idesc_bf16(128, mt.n_pad);
+        const uint32_t idesc = tc::idesc_bf16(128, n_pad);
         const uint32_t s_addr = smem_u32(sm.sbuf[(k - 1) & 1]);
         const uint32_t b_addr = smem_u32(sm.bstage[slot]);
-        const int nq = (mt.w_eff + 127) >> 7, nk = mt.rp >> 4;
+        const int nq = (w_eff + 127) >> 7, nk = rp >> 4;
         for (int q = 0; q < nq; ++q) {
             for (int kk = 0; kk < nk; ++kk) {
-                const uint64_t ad = tc::smem_desc(b_addr + q * mt.rp * 256 + kk * 2 * 2048, 2048, 128);
-                const uint64_t bd = tc::smem_desc(s_addr + kk * 2 * mt.n_pad * 16, mt.n_pad * 16, 128);
-                tc::mma_bf16(sm.tmem_base + b * kExAccCols + q * mt.n_pad, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                const uint64_t ad = tc::smem_desc(b_addr + q * rp * 256 + kk * 2 * 2048, 2048, 128);
+                const uint64_t bd = tc::smem_desc(s_addr + kk * 2 * n_pad * 16, n_pad * 16, 128);
+                tc::mma_bf16(sm.tmem_base + b * kExAccCols + q * n_pad, ad, bd, idesc, kk > 0 ? 1u : 0u);
             }
         }
         tc::mma_commit(&sm.acc_full[b]);
-        tc::mma_commit(&sm.empty_b[slot]);
+        tc::mma_commit(&sm.empty_b[slot]);   // the B columns are free once these MMAs end
     }
     // tensor memory is freed when the block ends: every MMA issued must be done by then
     if (i > 0) {
         tc::mma_commit(&sm.drain);
-        mbar_wait_bounded(&sm.drain, 0, p.timeout_ns, p.err);
+        mbar_wait_suspend(&sm.drain, 0, p.timeout_ns, p.err);
     }
 }
 
-// Runs f(row, chunk) over the m x cpr 16-byte chunks of a unit, spread over the 128 threads of a warpgroup
-// (a shift and a mask when cpr is a power of two, the usual case).
-template <class F>
-__device__ __forceinline__ void for_chunks(int et, int m, int cpr, F f)
-{
-    if ((cpr & (cpr - 1)) == 0) {
-        const int sh = __ffs(cpr) - 1;
-        for (int q = et; q < (m << sh); q += kExEpi) f(q >> sh, q & (cpr - 1));
-    } else {
-        for (int q = et; q < m * cpr; q += kExEpi) {
-            const int row = q / cpr;
-            f(row, q - row * cpr);
-        }
-    }
-}
-
-// Warpgroup wg: put the y rows of its unit at the load cursor in flight into its slot k (16-byte cp.async
-// pieces over its 128 threads), with the unit's rows and factors; commits one cp.async group either way.
-__device__ __forceinline__ void expand_issue_y(const StreamParams &p, ExpandSmem &sm, UnitWalk &lw, int wg, int k,
-                                               int &y_tile)
-{
-    const int et = (threadIdx.x - 96) & 127;
-    if (lw.valid(p)) {
-        const TileRec &tr = lw.tr;
-        if (lw.t != y_tile) {   // a new tile: its rows and factors into the cache (every thread takes this branch)
-            int v = 0;
-            float f = 0.f;
-            if (et < tr.m) {
-                v = __ldcg(p.rows + tr.row0 + et);
-                const float sc = __ldg(p.scale + tr.a);
-                f = p.row_weight ? sc * __ldg(p.row_weight + v) : sc;
-            }
-            bar_sync(1 + wg, kExEpi);   // every thread is done with the last tile's rows
-            if (et < tr.m) {
-                sm.yrow[wg][et] = v;
-                sm.yf[wg][et] = f;
-            }
-            bar_sync(1 + wg, kExEpi);
-            y_tile = lw.t;
-        }
-        int s, cb;
-        unit_slice(p, tr.W, lw.u, s, cb);
-        const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
-        const int col = p.slice_off[s] + cb * tr.W;
-        const int slot = wg * kExYSlots + k % kExYSlots;
-        ExYMeta &mt = sm.ymeta[slot];
-        if (et < tr.m) {
-            mt.row[et] = sm.yrow[wg][et];
-            mt.f[et] = sm.yf[wg][et];
-        }
-        if (et == 0) {
-            mt.col = col;
-            mt.w_eff = w_eff;
-            mt.m = tr.m;
-            mt.n_pad = tr.n_pad;
-            mt.W = tr.W;
-        }
-        unsigned char *ys = sm.ystage[slot];
-        const int W = tr.W;
-        const int32_t *yrow = sm.yrow[wg];
-        for_chunks(et, tr.m, w_eff >> 3, [&](int row, int c) {
-            tc::cp_async16(ys + row * W * 2 + c * 16, p.y + (int64_t)yrow[row] * p.ldy + col + c * 8, true);
-        });
-        // the other warpgroup takes the next unit
-        lw.next();
-        if (lw.valid(p)) lw.next();
-    }
-    tc::cp_async_commit();
-}
-
-// Warpgroup wg (warps 3-6 or 7-10) takes units wg, wg + 2, ...  Thread (quarter qw, lane) owns output
-// column 32 qw + lane of every 128-column group of a unit: it reads that column's accumulator for all rows
-// and adds it into the staged y rows; the rows then leave as 16-byte stores.  The y rows of a unit are put
-// in flight two of its units ahead.
+// Warpgroup wg (warps 4 + 4 wg .. 7 + 4 wg) takes units wg, wg + kExGroups, ...  Thread (quarter qw, lane)
+// owns output column 32 qw + lane of every 128-column group of a unit: it reads that column's accumulator
+// for all rows and adds it into the staged y rows; the rows then leave as 16-byte stores.
 __device__ __forceinline__ void expand_epilogue(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1, int wg)
 {
-    const int lane = threadIdx.x & 31, qw = (threadIdx.x >> 5) & 3, et = (threadIdx.x - 96) & 127;
+    const int lane = threadIdx.x & 31, qw = (threadIdx.x >> 5) & 3, et = threadIdx.x & 127;
     const int bar = 1 + wg;
-    UnitWalk lw(b0, b1), w(b0, b1);
-    if (wg == 1) {   // this warpgroup starts at the second unit
-        if (lw.valid(p)) lw.next();
-        if (w.valid(p)) w.next();
-    }
-    int y_tile = -1;
-    for (int k = 0; k < kExYSlots - 1; ++k) expand_issue_y(p, sm, lw, wg, k, y_tile);
-    bool ok = true;
+    UnitWalk w(b0, b1);
+    for (int g = 0; g < wg && w.valid(p); ++g) w.next();   // this warpgroup starts at unit wg
     for (int k = 0; w.valid(p); ++k) {
-        const uint32_t i = 2 * k + wg;   // the unit's index in the block's sequence
-        tc::cp_async_wait<kExYSlots - 2>();     // this thread's y pieces of unit k
-        if (!bar_and(bar, kExEpi, ok)) break;   // unit k's y visible to all; unit k - 1 done by all
-        expand_issue_y(p, sm, lw, wg, k + kExYSlots - 1, y_tile);
-        const int slot = wg * kExYSlots + k % kExYSlots, b = i % kExAcc;
-        const bool got = mbar_wait_bounded(&sm.acc_full[b], (i / kExAcc) & 1, p.timeout_ns, p.err);
-        ok = __all_sync(0xffffffffu, got);
+        const uint32_t i = kExGroups * k + wg;   // the unit's index in the block's sequence
+        const int slot = i % kExYStages, b = i % kExAcc;
+        bool got = mbar_wait_suspend(&sm.full_y[slot], (i / kExYStages) & 1, p.timeout_ns, p.err);
+        got = got && mbar_wait_suspend(&sm.acc_full[b], (i / kExAcc) & 1, p.timeout_ns, p.err);
+        if (!__all_sync(0xffffffffu, got)) break;
         if (i < 8 && et == 0) tstamp(p, 1, 17 + i);
-        if (ok) {
-            tc::fence_after_sync();
-            const ExYMeta &mt = sm.ymeta[slot];
-            const int m = mt.m, W = mt.W, w_eff = mt.w_eff, n_pad = mt.n_pad;
-            __nv_bfloat16 *ys = reinterpret_cast<__nv_bfloat16 *>(sm.ystage[slot]);
-            const uint32_t tbase = sm.tmem_base + ((uint32_t)(qw * 32) << 16) + b * kExAccCols;
-            const int nq = (w_eff + 127) >> 7;
+        tc::fence_after_sync();
+        const ExYMeta &mt = sm.ymeta[slot];
+        const int m = mt.m, W = mt.W, w_eff = mt.w_eff, n_pad = mt.n_pad;
+        __nv_bfloat16 *ys = reinterpret_cast<__nv_bfloat16 *>(sm.ystage[slot]);
+        const uint32_t tbase = sm.tmem_base + ((uint32_t)(qw * 32) << 16) + b * kExAccCols;
+        const int nq = (w_eff + 127) >> 7;
+        for (int j0 = 0; j0 < n_pad; j0 += 32) {
+            const int nrow = min(32, m - j0);
+            float f[32];   // the rows' factors (the same for every thread)
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(&mt.f[(j0 + h) & (kTileRows - 4)]);
+                f[h] = v.x; f[h + 1] = v.y; f[h + 2] = v.z; f[h + 3] = v.w;
+            }
             for (int q = 0; q < nq; ++q) {
                 const int c = q * 128 + qw * 32 + lane;
-                const bool live = c < w_eff;
-                __nv_bfloat16 *yc = ys + c;
-                for (int j0 = 0; j0 < n_pad; j0 += 32) {
-                    float v[32];
-                    // the second half re-reads the first when only 16 rows remain (stays inside the
-                    // accumulator)
-                    const uint32_t ta = tbase + q * n_pad + j0;
-                    tc::tmem_ld16x2(ta, j0 + 16 < n_pad ? ta + 16 : ta, v);
-                    const int nrow = min(32, m - j0);
-                    if (live) {
-#pragma unroll 4
-                        for (int h = 0; h < 32; h += 8) {
-                            if (h < nrow) {
-                                float yv[8];
+                float v[32];
+                // the second half re-reads the first when only 16 rows remain (stays inside the accumulator)
+                const uint32_t ta = tbase + q * n_pad + j0;
+                tc::tmem_ld16x2(ta, j0 + 16 < n_pad ? ta + 16 : ta, v);
+                if (c < w_eff) {
+                    __nv_bfloat16 *yc = ys + j0 * W + c;
 #pragma unroll
-                                for (int jj = 0; jj < 8; ++jj)
-                                    yv[jj] = h + jj < nrow ? __bfloat162float(yc[(j0 + h + jj) * W]) : 0.f;
+                    for (int h = 0; h < 32; h += 8) {
+                        if (h < nrow) {
+                            float yv[8];
 #pragma unroll
-                                for (int jj = 0; jj < 8; ++jj)
-                                    if (h + jj < nrow)
-                                        yc[(j0 + h + jj) * W] =
-                                            __float2bfloat16_rn(fmaf(mt.f[j0 + h + jj], v[h + jj], yv[jj]));
-                            }
+                            for (int jj = 0; jj < 8; ++jj) yv[jj] = h + jj < nrow ? __bfloat162float(yc[(h + jj) * W]) : 0.f;
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj)
+                                if (h + jj < nrow) yc[(h + jj) * W] = __float2bfloat16_rn(fmaf(f[h + jj], v[h + jj], yv[jj]));
                         }
                     }
                 }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
-            bar_sync(bar, kExEpi);   // every column of the unit updated
-            const int col = mt.col;
-            const unsigned char *yb = sm.ystage[slot];
-            for_chunks(et, m, w_eff >> 3, [&](int row, int c) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(yb + row * W * 2 + c * 16);
-                *reinterpret_cast<uint4 *>(p.y + (int64_t)mt.row[row] * p.ldy + col + c * 8) = v;
-            });
-            if (k == 0 && et == 0) tstamp(p, 1, 5 + wg);
         }
-        w.next();
-        if (w.valid(p)) w.next();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+        bar_sync(bar, kExEpi);   // every column of the unit updated
+        const int col = mt.col, cpr = w_eff >> 3;
+        const unsigned char *yb = sm.ystage[slot];
+        auto store = [&](int row, int c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(yb + row * W * 2 + c * 16);
+            *reinterpret_cast<uint4 *>(p.y + (int64_t)mt.row[row] * p.ldy + col + c * 8) = v;
+        };
+        if ((cpr & (cpr - 1)) == 0) {
+            const int sh = __ffs(cpr) - 1;
+            for (int q = et; q < (m << sh); q += kExEpi) store(q >> sh, q & (cpr - 1));
+        } else {
+            for (int q = et; q < m * cpr; q += kExEpi) {
+                const int row = q / cpr;
+                store(row, q - row * cpr);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty_y[slot]);   // this warp is done with the slot
+        if (k == 0 && et == 0) tstamp(p, 1, 5 + wg);
+        for (int g = 0; g < kExGroups && w.valid(p); ++g) w.next();
     }
-    tc::cp_async_wait<0>();
     if (et == 0) tstamp(p, 1, 7 + wg);
 }
 
@@ -1019,7 +1027,11 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
         tstamp(p, 1, 0);
         for (int s = 0; s < kExBStages; ++s) {
             mbar_init(&sm.full_b[s], 1);
-            mbar_init(&sm.empty_b[s], 1);
+            mbar_init(&sm.empty_b[s], 1);       // the MMA issuer's commit
+        }
+        for (int s = 0; s < kExYStages; ++s) {
+            mbar_init(&sm.full_y[s], 32);       // the y producer's 32 lanes, each once its pieces landed
+            mbar_init(&sm.empty_y[s], 4);       // the 4 warps of an epilogue group
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.s_full[s], 1);
@@ -1041,13 +1053,15 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     const int2 b0 = __ldcg(p.ex_start + blockIdx.x), b1 = __ldcg(p.ex_start + blockIdx.x + 1);
     if (threadIdx.x == 0) tstamp(p, 1, 1);
     if (warp == 0) {
-        if (lane == 0) expand_produce(p, sm, b0, b1);
+        if (lane == 0) expand_produce_b(p, sm, b0, b1);
     } else if (warp == 1) {
         if (lane == 0) expand_load_s(p, sm, b0, b1);
     } else if (warp == 2) {
         if (lane == 0) expand_mma(p, sm, b0, b1);
+    } else if (warp == 3) {
+        expand_produce_y(p, sm, b0, b1);
     } else {
-        expand_epilogue(p, sm, b0, b1, warp >= 7 ? 1 : 0);
+        expand_epilogue(p, sm, b0, b1, (warp - 4) >> 2);
     }
     __syncwarp();
     tc::fence_before_sync();

@@ -170,6 +170,12 @@ __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, bool
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// One arrival on the mbarrier once every cp.async this thread issued so far has landed (the arrival is
+// counted in the barrier's expected count: no increment).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 // make this thread's generic-proxy shared-memory writes visible to the tensor core
