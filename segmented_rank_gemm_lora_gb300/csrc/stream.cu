@@ -56,13 +56,15 @@ namespace lora {
 constexpr int kPlanItems = 3;                   // shrink chunks per block the plan aims for
 constexpr int kPartialPerRow = 8192;            // fp32 partials per row of a tile, at most (bounds the K-chunk from below)
 constexpr int kTileRows = 64;                   // rows of a tile, at most
-constexpr int kShWarps = 8;                     // MMA warps of the shrink; one more warp streams A
-constexpr int kShThreads = 32 * (kShWarps + 1);
-constexpr int kShAStages = 5;
-constexpr int kShABytes = 16 * 1024;            // A columns of one stage, at most
-constexpr int kShXBytes = 56 * 1024;            // x rows of one chunk, at most
-constexpr int kExGroups = 3;                    // epilogue warpgroups (units dealt round-robin)
-constexpr int kExThreads = 128 + 128 * kExGroups;   // B producer, S loader, MMA issuer, y producer, epilogue groups
+constexpr int kShWarps = 8;                     // MMA warps of the shrink
+constexpr int kShProd = 128;                    // producer threads (the four warps after the MMA warps)
+constexpr int kShThreads = 32 * kShWarps + kShProd;
+constexpr int kShStages = 6;
+constexpr int kShStageBytes = 32 * 1024;        // A columns and x rows of one stage, at most
+constexpr int kExGroups = 2;                    // epilogue warpgroups (units dealt round-robin)
+constexpr int kExYProd = 128;                   // y producer threads: warps 4-7
+constexpr int kExThreads = 128 + kExYProd + 128 * kExGroups;   // B producer, S loader, MMA issuer, a spare warp,
+                                                               // y producers, epilogue groups
 constexpr int kExEpi = 128;                     // threads of one epilogue warpgroup
 constexpr int kExBStages = 5;
 constexpr int kExBBytes = 16 * 1024;            // B columns of one unit, at most
@@ -199,17 +201,15 @@ __device__ __forceinline__ GroupPlan group_plan(const StreamParams &p, int4 gr, 
     g.rem = g.count - g.base * g.ntl;
     const int m_max = g.base + (g.rem > 0 ? 1 : 0);
     const int K = p.K;
-    // shrink: the x rows of one chunk fill at most one x buffer (xcap columns); a stage of A (ks columns) at
-    // most one A stage; the chunk (the same cut for every tile of the group) is about `target` bytes, and
-    // gives no more than kPartialPerRow partial floats per row where the x buffer allows it
-    const int xcap = ((kShXBytes / 2) / m_max - 8) / 16 * 16;
-    const int ks = min(min(512, (kShABytes / 2) / g.R), xcap) / 16 * 16;
+    // shrink: a stage (ks columns of A and of the tile's x rows, rows padded by 8 columns) fills at most one
+    // ring stage; the chunk (the same cut for every tile of the group) is about `target` bytes, and gives no
+    // more than kPartialPerRow partial floats per row
+    const int ks = min(512, (kShStageBytes / 2 - 8 * m_max) / (g.R + m_max)) / 16 * 16;
     const int k_all = (K + ks - 1) / ks * ks;
-    const int kcap = min(k_all, xcap / ks * ks);
-    const int kc_min = min(((K * g.R + kPartialPerRow - 1) / kPartialPerRow + ks - 1) / ks * ks, kcap);   // K R < 2^29
+    const int kc_min = min(((K * g.R + kPartialPerRow - 1) / kPartialPerRow + ks - 1) / ks * ks, k_all);   // K R < 2^29
     const float want = fminf(target / (2.f * (g.R + m_max)), (float)k_all);
     int kc = (int)ceilf(want / ks) * ks;
-    kc = min(max(kc, max(ks, kc_min)), kcap);
+    kc = min(max(kc, max(ks, kc_min)), k_all);
     g.ks = ks;
     g.kc = kc;
     g.n_kc = (K + kc - 1) / kc;
@@ -402,15 +402,38 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
 // ===========================================================================
 // shrink
 // ===========================================================================
+// A group of gs threads (gt: this thread's index in it) copies P 16-byte pieces of each of m rows into
+// shared memory, as cp.async: row r's pieces are read from src(r) and land at dst + r * stride.  With
+// P <= gs a thread keeps one piece column and steps over rows (gs / P rows per step); otherwise the group
+// walks the pieces of one row at a time.  The iterations are independent, so the source-row lookups of
+// several rows are in flight together.  One warp issuing alone leaves the gather far below the memory's
+// rate, hence groups of several warps.
+template <class Src>
+__device__ __forceinline__ void group_gather(unsigned char *dst, int stride, int m, int P, int gt, int gs, Src src)
+{
+    if (P <= gs) {
+        const int rpi = gs / P, rsub = gt / P, c = gt - rsub * P;
+        if (rsub < rpi) {
+#pragma unroll 4
+            for (int r = rsub; r < m; r += rpi) tc::cp_async16(dst + r * stride + c * 16, src(r) + c * 8, true);
+        }
+    } else {
+        for (int r = 0; r < m; ++r) {
+            const __nv_bfloat16 *g = src(r);
+#pragma unroll 2
+            for (int c = gt; c < P; c += gs) tc::cp_async16(dst + r * stride + c * 16, g + c * 8, true);
+        }
+    }
+}
+
 struct __align__(128) ShrinkSmem {
     union {
-        struct {
-            unsigned char a[kShAStages][kShABytes];   // A columns of one stage: [ks/8][R][8]
-            unsigned char x[2][kShXBytes];            // x rows of one chunk: [m][kc + 8]
-        } buf;
-        PlanSmem plan;                                // block 0, before the streams start
+        // stage: A columns [ks/8][R][8], then the tile's x rows [m][ks + 8]
+        unsigned char stage[kShStages][kShStageBytes];
+        PlanSmem plan;   // block 0, before the streams start
     };
-    uint64_t full[kShAStages], empty[kShAStages];
+    uint64_t full[kShStages], empty[kShStages];
+    int32_t xsrc[2][kTileRows];   // source rows of the producers' tiles, by tile parity
     int32_t flag;
 };
 
@@ -465,45 +488,62 @@ struct ChunkWalk {
     }
 };
 
-// Warp 8, one thread: the A columns of every stage of this block's chunks (one bulk copy each) into the
-// A ring.
+// Warps 8-11 (kShProd threads): every stage of this block's chunks into the ring.  Thread 0 of the group
+// copies the stage's A columns (one bulk copy); the group gathers the same K columns of the tile's x rows
+// as 16-byte cp.async pieces.  The stage's full barrier completes once the bulk copy's bytes and every
+// producer thread's pieces have landed.  One barrier per stage keeps the four warps in step (and lets them
+// leave together when a wait runs out); the tile's source rows are double-buffered by tile parity, so a
+// warp may write the next tile's rows while another still gathers the last stage of the previous tile.
 __device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1)
 {
+    const int gt = threadIdx.x - 32 * kShWarps, lane = threadIdx.x & 31;
     uint32_t s = 0;
-    bool ok = true;
-    for (ChunkWalk w(b0, b1); ok && w.valid(p); w.next()) {
+    int cur = -1, par = 1;
+    for (ChunkWalk w(b0, b1); w.valid(p); w.next()) {
         const TileRec &tr = w.tr;
+        bool fresh = false;
+        if (w.t != cur) {
+            cur = w.t;
+            par ^= 1;
+            fresh = true;
+        }
         const unsigned char *ablk =
             reinterpret_cast<const unsigned char *>(__ldg(p.a_ptr + tr.a * p.E_A + (p.E_A == 1 ? 0 : tr.e)));
         const int k0 = w.j * tr.kc, kend = min(k0 + tr.kc, p.K);
+        const int xoff = tr.R * tr.ks * 2, xstride = (tr.ks + 8) * 2;
+        bool ok = true;
         for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
-            const int slot = s % kShAStages;
-            if (s >= kShAStages &&
-                !(ok = mbar_wait_suspend(&sm.empty[slot], ((s / kShAStages) - 1) & 1, p.timeout_ns, p.err)))
-                break;
-            const uint32_t bytes = (uint32_t)tr.R * min(tr.ks, kend - kb) * 2;
-            mbar_arrive_expect_tx(&sm.full[slot], bytes);
-            bulk_g2s(sm.buf.a[slot], ablk + (size_t)(kb / 8) * tr.R * 16, bytes, &sm.full[slot]);
-            if (s < 8) tstamp(p, 0, 12 + s);
+            const int slot = s % kShStages;
+            bool got = true;
+            if (s >= kShStages) {
+                if (lane == 0) got = mbar_wait_suspend(&sm.empty[slot], ((s / kShStages) - 1) & 1, p.timeout_ns, p.err);
+                got = __shfl_sync(0xffffffffu, got, 0);
+            }
+            if (fresh) {
+                for (int r = gt; r < tr.m; r += kShProd) sm.xsrc[par][r] = __ldcg(p.rows + tr.row0 + r) / p.src_div;
+                fresh = false;
+            }
+            if (!(ok = bar_and(2, kShProd, got))) break;
+            const int kk = min(tr.ks, kend - kb);
+            if (gt == 0) {
+                const uint32_t bytes = (uint32_t)tr.R * kk * 2;
+                mbar_arrive_expect_tx(&sm.full[slot], bytes);
+                bulk_g2s(sm.stage[slot], ablk + (size_t)(kb / 8) * tr.R * 16, bytes, &sm.full[slot]);
+                if (s < 8) tstamp(p, 0, 12 + s);
+            }
+            const __nv_bfloat16 *xk = p.x + kb;
+            const int64_t ldx = p.ldx;
+            const int32_t *xs = sm.xsrc[par];
+            group_gather(sm.stage[slot] + xoff, xstride, tr.m, kk >> 3, gt, kShProd,
+                         [&](int r) { return xk + (int64_t)xs[r] * ldx; });
+            tc::cp_async_arrive_noinc(&sm.full[slot]);
         }
+        if (!ok) break;
     }
-    for (uint32_t q = s > kShAStages ? s - kShAStages : 0; q < s; ++q)
-        mbar_wait_suspend(&sm.full[q % kShAStages], (q / kShAStages) & 1, p.timeout_ns, p.err);
-}
-
-// x rows of one chunk into x buffer xb: thread tid takes row tid / 4 (its source row xr) and every fourth
-// 16-byte piece of the chunk's columns.  Commits one cp.async group either way.
-__device__ __forceinline__ void shrink_issue_x(const StreamParams &p, ShrinkSmem &sm, const TileRec &tr, int j, int xr,
-                                               int xb, bool live)
-{
-    const int tid = threadIdx.x, row = tid >> 2;
-    if (live && row < tr.m) {
-        const int k0 = j * tr.kc, kw = min(tr.kc, p.K - k0), cpr = kw >> 3;
-        unsigned char *dst = sm.buf.x[xb] + row * (tr.kc + 8) * 2;
-        const __nv_bfloat16 *src = p.x + (int64_t)xr * p.ldx + k0;
-        for (int c = tid & 3; c < cpr; c += 4) tc::cp_async16(dst + c * 16, src + c * 8, true);
-    }
-    tc::cp_async_commit();
+    if (gt == 0)
+        for (uint32_t q = s > kShStages ? s - kShStages : 0; q < s; ++q)
+            mbar_wait_suspend(&sm.full[q % kShStages], (q / kShStages) & 1, p.timeout_ns, p.err);
+    tc::cp_async_wait_all();
 }
 
 // One chunk of one tile on the eight MMA warps: the fp32 partial X_rows A_chunk^T in registers, then to the
@@ -511,8 +551,7 @@ __device__ __forceinline__ void shrink_issue_x(const StreamParams &p, ShrinkSmem
 // blocks mi0, mi0 + wm, ... (MM of them).  Each output element accumulates its K steps in order, one
 // m16n8k16 per 16 K, so its sum depends on the chunk cut alone.
 template <int MM, int MN>
-__device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &sm, const TileRec &tr, int j, int xb,
-                                             uint32_t &s)
+__device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &sm, const TileRec &tr, int j, uint32_t &s)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ntc = tr.R >> 3, mtc = (tr.m + 15) >> 4;
@@ -522,22 +561,21 @@ __device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &
     float acc[MM * MN][4];
 #pragma unroll
     for (int i = 0; i < MM * MN; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    const int xstride = (tr.kc + 8) * 2;
-    const uint32_t x_s = smem_u32(sm.buf.x[xb]);
-    uint32_t xrow[MM];
+    const int xstride = (tr.ks + 8) * 2;
+    uint32_t xrow[MM];   // offsets in a stage of this lane's ldmatrix rows of x
 #pragma unroll
     for (int mi = 0; mi < MM; ++mi) {
         const int row = min((mi0 + mi * wm) * 16 + (lane & 15), tr.m - 1);
-        xrow[mi] = x_s + row * xstride;
+        xrow[mi] = tr.R * tr.ks * 2 + row * xstride;
     }
     const int k0 = j * tr.kc, kend = min(k0 + tr.kc, p.K);
     for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
-        const int slot = s % kShAStages;
-        const int kk = min(tr.ks, kend - kb), koff = (kb - k0) * 2;
-        if (!mbar_wait_suspend(&sm.full[slot], (s / kShAStages) & 1, p.timeout_ns, p.err)) return false;
+        const int slot = s % kShStages;
+        const int kk = min(tr.ks, kend - kb);
+        if (!mbar_wait_suspend(&sm.full[slot], (s / kShStages) & 1, p.timeout_ns, p.err)) return false;
         if (s < 8 && lane == 0 && warp == 0) tstamp(p, 0, 20 + s);
         const int steps = kk >> 4;
-        const uint32_t a_s = smem_u32(sm.buf.a[slot]);
+        const uint32_t a_s = smem_u32(sm.stage[slot]);
         if (active) {
             const uint32_t arow = a_s + ((lane >> 3) & 1) * tr.R * 16 + (lane & 7) * 16;
 #pragma unroll 2
@@ -552,7 +590,7 @@ __device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &
                 for (int mi = 0; mi < MM; ++mi) {
                     if (mi0 + mi * wm < mtc) {
                         uint32_t a0, a1, a2, a3;
-                        ldsm_x4(xrow[mi] + koff + (2 * st + (lane >> 4)) * 16, a0, a1, a2, a3);
+                        ldsm_x4(a_s + xrow[mi] + (2 * st + (lane >> 4)) * 16, a0, a1, a2, a3);
 #pragma unroll
                         for (int ni = 0; ni < MN; ++ni)
                             if (ni0 + ni * wn < ntc) mma16816(acc[mi * MN + ni], a0, a1, a2, a3, b[ni][0], b[ni][1]);
@@ -570,7 +608,7 @@ __device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &
                 for (int mi = 0; mi < MM; ++mi) {
                     if (mi0 + mi * wm < mtc) {
                         uint32_t a0, a1;
-                        ldsm_x2(xrow[mi] + koff + (2 * steps) * 16, a0, a1);
+                        ldsm_x2(a_s + xrow[mi] + (2 * steps) * 16, a0, a1);
 #pragma unroll
                         for (int ni = 0; ni < MN; ++ni)
                             if (ni0 + ni * wn < ntc) mma1688(acc[mi * MN + ni], a0, a1, b[ni]);
@@ -601,43 +639,19 @@ __device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &
     return true;
 }
 
-// Warps 0-7: every chunk of this block.  The x rows of chunk q + 1 are put in flight as chunk q starts (two
-// x buffers), and the source rows of chunk q + 2 are fetched then too, so no copy waits on the row list.
+// Warps 0-7: every chunk of this block, stage by stage from the ring; each warp walks the chunks on its own.
 __device__ __forceinline__ void shrink_consume(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1)
 {
-    const int tid = threadIdx.x, row = tid >> 2;
-    ChunkWalk cw(b0, b1), xw(b0, b1), rw(b0, b1);
-    // source row of this thread's x row for the chunks at the x cursor (xr) and one past it (nr)
-    auto src_row = [&](ChunkWalk &w) -> int {
-        if (!w.valid(p) || row >= w.tr.m) return 0;
-        return __ldcg(p.rows + w.tr.row0 + row) / p.src_div;
-    };
-    int xr = src_row(rw);
-    if (rw.valid(p)) rw.next();
-    bool live = xw.valid(p);
-    shrink_issue_x(p, sm, xw.tr, xw.j, xr, 0, live);
-    if (live) xw.next();
-    xr = src_row(rw);
-    if (rw.valid(p)) rw.next();
     uint32_t s = 0;
-    bool ok = true;
-    for (int q = 0; cw.valid(p); ++q) {
-        if (!bar_and(1, kShWarps * 32, ok)) break;   // every warp is done with chunk q - 1 and its x buffer
-        live = xw.valid(p);
-        shrink_issue_x(p, sm, xw.tr, xw.j, xr, (q + 1) & 1, live);
-        if (live) xw.next();
-        xr = src_row(rw);
-        if (rw.valid(p)) rw.next();
-        tc::cp_async_wait<1>();   // this thread's x pieces of chunk q
-        bar_sync(1, kShWarps * 32);
-        const TileRec tr = cw.tr;
-        if (tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, tr, cw.j, q & 1, s);
-        else if (tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, tr, cw.j, q & 1, s);
-        else ok = shrink_chunk<4, 4>(p, sm, tr, cw.j, q & 1, s);
-        if (tid == 0 && q < 4) tstamp(p, 0, 3 + q);
-        cw.next();
+    int q = 0;
+    for (ChunkWalk cw(b0, b1); cw.valid(p); cw.next(), ++q) {
+        bool ok;
+        if (cw.tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, cw.tr, cw.j, s);
+        else if (cw.tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, cw.tr, cw.j, s);
+        else ok = shrink_chunk<4, 4>(p, sm, cw.tr, cw.j, s);
+        if (!ok) break;
+        if (threadIdx.x == 0 && q < 4) tstamp(p, 0, 3 + q);
     }
-    tc::cp_async_wait<0>();
 }
 
 // S chunk i of a tile (16 bytes of its S layout: slice block sb, rank group kg, row): the tile's partials
@@ -672,8 +686,8 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
     const int tid = threadIdx.x;
     if (tid == 0) {
         tstamp(p, 0, 0);
-        for (int s = 0; s < kShAStages; ++s) {
-            mbar_init(&sm.full[s], 1);
+        for (int s = 0; s < kShStages; ++s) {
+            mbar_init(&sm.full[s], 1 + kShProd);   // the A copy's expect-tx arrival and one per producer thread
             mbar_init(&sm.empty[s], kShWarps);
         }
         fence_mbar_init();
@@ -687,7 +701,7 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
         if (tid == 0) tstamp(p, 0, 2);
         const int2 b0 = __ldcg(p.sh_start + blockIdx.x), b1 = __ldcg(p.sh_start + blockIdx.x + 1);
         if (tid < kShWarps * 32) shrink_consume(p, sm, b0, b1);
-        else if (tid == kShWarps * 32) shrink_produce(p, sm, b0, b1);
+        else shrink_produce(p, sm, b0, b1);
         __syncwarp();
         if (tid == 0) tstamp(p, 0, 8);
     }
@@ -806,67 +820,58 @@ __device__ __forceinline__ void expand_produce_b(const StreamParams &p, ExpandSm
         mbar_wait_suspend(&sm.full_b[q % kExBStages], (q / kExBStages) & 1, p.timeout_ns, p.err);
 }
 
-// Warp 3: the y rows of every unit (16-byte cp.async pieces over the 32 lanes) into the y ring, with the
-// unit's rows and factors for the epilogue.  Each lane's pieces complete on the slot's mbarrier.
+// Warps 4-7 (kExYProd threads): for every unit, its y rows (16-byte cp.async pieces over the group) and its
+// description into the next y slot.  One barrier per unit keeps the four warps in step (and lets them leave
+// together when a wait runs out).
 __device__ __forceinline__ void expand_produce_y(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
 {
-    const int lane = threadIdx.x & 31;
+    const int gt = threadIdx.x - 128, lane = threadIdx.x & 31;
     uint32_t i = 0;
     int cur = -1;
-    int yr0 = 0, yr1 = 0;      // y rows lane and lane + 32 of the current tile
-    float yf0 = 0.f, yf1 = 0.f;
+    int yr = 0;      // y row gt of the current tile (gt < m) and its factor
+    float yf = 0.f;
     for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
         const TileRec &tr = w.tr;
         if (cur != w.t) {
             const float sc = __ldg(p.scale + tr.a);
-            yr0 = lane < tr.m ? __ldcg(p.rows + tr.row0 + lane) : 0;
-            yr1 = lane + 32 < tr.m ? __ldcg(p.rows + tr.row0 + lane + 32) : 0;
-            yf0 = p.row_weight ? sc * __ldg(p.row_weight + yr0) : sc;
-            yf1 = p.row_weight ? sc * __ldg(p.row_weight + yr1) : sc;
+            yr = gt < tr.m ? __ldcg(p.rows + tr.row0 + gt) : 0;
+            yf = p.row_weight ? sc * __ldg(p.row_weight + yr) : sc;
             cur = w.t;
         }
         int s, cb;
         unit_slice(p, tr.W, w.u, s, cb);
         const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
         const int slot = i % kExYStages;
-        if (i >= kExYStages &&
-            !mbar_wait_suspend(&sm.empty_y[slot], ((i / kExYStages) - 1) & 1, p.timeout_ns, p.err))
-            break;
+        bool got = true;
+        if (i >= kExYStages) {
+            if (lane == 0) got = mbar_wait_suspend(&sm.empty_y[slot], ((i / kExYStages) - 1) & 1, p.timeout_ns, p.err);
+            got = __shfl_sync(0xffffffffu, got, 0);
+        }
         ExYMeta &mt = sm.ymeta[slot];
         const int col = p.slice_off[s] + cb * tr.W;
-        if (lane < tr.m) {
-            mt.row[lane] = yr0;
-            mt.f[lane] = yf0;
-        }
-        if (lane + 32 < tr.m) {
-            mt.row[lane + 32] = yr1;
-            mt.f[lane + 32] = yf1;
-        }
-        if (lane == 0) {
-            mt.W = tr.W;
-            mt.m = tr.m;
-            mt.w_eff = w_eff;
-            mt.n_pad = tr.n_pad;
-            mt.col = col;
-        }
-        __syncwarp();
-        unsigned char *ys = sm.ystage[slot];
-        const int cpr = w_eff >> 3, W2 = tr.W * 2;
-        if ((cpr & (cpr - 1)) == 0) {
-            const int sh = __ffs(cpr) - 1;
-            for (int q = lane; q < (tr.m << sh); q += 32) {
-                const int row = q >> sh, c = q & (cpr - 1);
-                tc::cp_async16(ys + row * W2 + c * 16, p.y + (int64_t)mt.row[row] * p.ldy + col + c * 8, true);
+        if (got) {
+            if (gt < tr.m) {
+                mt.row[gt] = yr;
+                mt.f[gt] = yf;
             }
-        } else {
-            for (int q = lane; q < tr.m * cpr; q += 32) {
-                const int row = q / cpr, c = q - row * cpr;
-                tc::cp_async16(ys + row * W2 + c * 16, p.y + (int64_t)mt.row[row] * p.ldy + col + c * 8, true);
+            if (gt == 0) {
+                mt.W = tr.W;
+                mt.m = tr.m;
+                mt.w_eff = w_eff;
+                mt.n_pad = tr.n_pad;
+                mt.col = col;
             }
         }
-        tc::cp_async_arrive_noinc(&sm.full_y[slot]);   // once every piece of this lane has landed
+        if (!bar_and(5, kExYProd, got)) break;   // the slot is free for the whole group; its rows are written
+        const __nv_bfloat16 *yc = p.y + col;
+        const int64_t ldy = p.ldy;
+        if (i < 3 && gt == 0) tstamp(p, 1, 25 + 2 * i);
+        group_gather(sm.ystage[slot], tr.W * 2, tr.m, w_eff >> 3, gt, kExYProd,
+                     [&](int r) { return yc + (int64_t)mt.row[r] * ldy; });
+        if (i < 3 && gt == 0) tstamp(p, 1, 26 + 2 * i);
+        tc::cp_async_arrive_noinc(&sm.full_y[slot]);   // once every piece of this thread has landed
     }
-    tc::cp_async_wait<0>();
+    tc::cp_async_wait_all();
 }
 
 // Warp 1, one thread: S of every (tile, slice block) this block meets, into two buffers in rotation.
@@ -1030,7 +1035,7 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
             mbar_init(&sm.empty_b[s], 1);       // the MMA issuer's commit
         }
         for (int s = 0; s < kExYStages; ++s) {
-            mbar_init(&sm.full_y[s], 32);       // the y producer's 32 lanes, each once its pieces landed
+            mbar_init(&sm.full_y[s], kExYProd);   // every y producer thread, once its pieces landed
             mbar_init(&sm.empty_y[s], 4);       // the 4 warps of an epilogue group
         }
         for (int s = 0; s < 2; ++s) {
@@ -1058,10 +1063,10 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
         if (lane == 0) expand_load_s(p, sm, b0, b1);
     } else if (warp == 2) {
         if (lane == 0) expand_mma(p, sm, b0, b1);
-    } else if (warp == 3) {
+    } else if (warp >= 4 && warp < 8) {
         expand_produce_y(p, sm, b0, b1);
-    } else {
-        expand_epilogue(p, sm, b0, b1, (warp - 4) >> 2);
+    } else if (warp >= 8) {
+        expand_epilogue(p, sm, b0, b1, (warp - 8) >> 2);
     }
     __syncwarp();
     tc::fence_before_sync();

@@ -178,6 +178,8 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// every cp.async this thread issued, committed to a group or not, has landed
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // make this thread's generic-proxy shared-memory writes visible to the tensor core
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 

@@ -31,7 +31,7 @@ SRC = os.path.join(os.path.dirname(__file__), "..", "segmented_rank_gemm_lora_gb
 def _constants():
     text = open(SRC).read()
     out = {}
-    for name in ("kPlanItems", "kPartialPerRow", "kTileRows", "kShABytes", "kShXBytes", "kExBBytes", "kExYBytes",
+    for name in ("kPlanItems", "kPartialPerRow", "kTileRows", "kShStageBytes", "kExBBytes", "kExYBytes",
                  "kExSBytes", "kExAccCols", "kCostUnit"):
         m = re.search(r"constexpr int %s = ([0-9* ]+);" % name, text)
         assert m, name
@@ -68,10 +68,9 @@ def plan(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
         n = ntl[g]
         base, rem = divmod(cnt, n)
         m_max = base + (1 if rem else 0)
-        xcap = ((C["kShXBytes"] // 2) // m_max - 8) // 16 * 16
-        ks = min(min(512, (C["kShABytes"] // 2) // R), xcap) // 16 * 16
+        ks = min(512, (C["kShStageBytes"] // 2 - 8 * m_max) // (R + m_max)) // 16 * 16
         k_all = -(-K // ks) * ks
-        kcap = min(k_all, xcap // ks * ks)
+        kcap = k_all
         kc_min = min(-(-(-(-K * R // C["kPartialPerRow"])) // ks) * ks, kcap)
         want = min(f32(target / f32(2 * (R + m_max))), f32(k_all))
         kc = int(np.ceil(f32(want / f32(ks)))) * ks
@@ -142,7 +141,7 @@ def check(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
         assert seen == every, key
     for t in tiles:
         assert 1 <= t["m"] <= C["kTileRows"] and t["m"] <= tile_max
-        assert t["R"] * t["ks"] * 2 <= C["kShABytes"] and t["m"] * (t["kc"] + 8) * 2 <= C["kShXBytes"]
+        assert (t["R"] * t["ks"] + t["m"] * (t["ks"] + 8)) * 2 <= C["kShStageBytes"]
         assert t["W"] * t["rp"] * 2 <= C["kExBBytes"] and t["W"] * t["m"] * 2 <= C["kExYBytes"]
         assert (t["W"] // 128) * t["n_pad"] <= C["kExAccCols"]
         assert t["rp"] * t["n_pad"] * 2 <= C["kExSBytes"]
