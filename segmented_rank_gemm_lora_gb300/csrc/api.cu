@@ -485,6 +485,7 @@ static lora_status run_stream(lora_table t, const lora_workspace *ws, const WsLa
     p.partial_cap = ((int64_t)w.partial_floats * 4 - (int64_t)plan_bytes - (int64_t)s_cap) / 4;
     p.max_tiles = w.max_tiles;
     p.cnt = at<int32_t>(ws, w.sync);
+    p.ex_claim = p.plan_hdr + PL_CLAIM;   // not in the sync area: the persistent engine expects zeros there
     const int grid = stream_grid(di.sms);
     const int64_t want = g_opt_grid.load();
     p.grid_s = p.grid_e = (want > 0 && want < grid) ? (int)want : grid;

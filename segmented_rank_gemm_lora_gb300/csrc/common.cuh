@@ -108,7 +108,7 @@ size_t engine_smem_bytes(int group_capacity);
 const void *engine_kernel_ptr();
 
 // ---------------------------------------------------------------------------
-// streaming path (csrc/stream.cu): plan -> shrink -> expand, three kernels chained on the stream
+// streaming path (csrc/stream.cu): shrink (with the plan) -> expand, two kernels chained on the stream
 // ---------------------------------------------------------------------------
 // One row tile of a group, as the plan lays it out.  The tile's shrink is cut into n_kc K-chunks of kc
 // columns (the same cut for every tile of a group), each streamed in stages of ks columns; its expand is
@@ -118,12 +118,17 @@ struct TileRec {
     int32_t rp, R, n_pad, kc;       // stored rank, A-block rows (n_a * rp), rows rounded up to 16, chunk K
     int32_t n_kc, ks, W, n_units;   // chunks, stage K, expand unit width, expand units
     int32_t p_off, s_off;           // fp32 partial offset (floats), S offset (bytes)
-    int32_t sh_pos, ex_pos;         // position of the tile's first chunk / unit in the launch's cost order
+    int32_t c0, u0;                 // launch-wide index of the tile's first chunk / first unit
 };
 static_assert(sizeof(TileRec) == 64, "tile record");
 
 // Plan header slots (int32)
-enum PlanSlot { PL_TILES = 0, PL_ARRIVED = 1 };
+enum PlanSlot {
+    PL_TILES = 0,    // tiles
+    PL_UNITS = 1,    // expand units of the launch
+    PL_POOL_U = 2,   // first unit of the expand's claimed tail (units before it are split ahead of time)
+    PL_CLAIM = 3,    // units of that tail claimed so far
+};
 
 struct StreamParams {
     // weight table
@@ -147,7 +152,8 @@ struct StreamParams {
     TileRec *tiles;                  // [max_tiles]
     int2 *sh_start, *ex_start;       // [grid + 1] first (tile, item) of every block
     int2 *rd_start;                  // [grid + 1] first (tile, S chunk) each shrink block reduces
-    int32_t *cnt;                    // [max_tiles] chunks of a tile done (zeroed by the plan)
+    int32_t *cnt;                    // the shrink's grid-barrier counter (reset by the expand)
+    int32_t *ex_claim;               // plan_hdr + PL_CLAIM (reset by the shrink)
     float *partials;                 // fp32 chunk partials
     int64_t partial_cap;             // floats
     unsigned char *s_area;           // finished S, bf16, per tile [n_a][rp / 8][n_pad][8]

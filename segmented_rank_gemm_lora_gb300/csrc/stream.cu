@@ -61,16 +61,19 @@ constexpr int kShProd = 128;                    // producer threads (the four wa
 constexpr int kShThreads = 32 * kShWarps + kShProd;
 constexpr int kShStages = 6;
 constexpr int kShStageBytes = 32 * 1024;        // A columns and x rows of one stage, at most
-constexpr int kExGroups = 2;                    // epilogue warpgroups (units dealt round-robin)
+constexpr int kExGroups = 3;                    // epilogue warpgroups (units dealt round-robin)
 constexpr int kExYProd = 128;                   // y producer threads: warps 4-7
 constexpr int kExThreads = 128 + kExYProd + 128 * kExGroups;   // B producer, S loader, MMA issuer, a spare warp,
                                                                // y producers, epilogue groups
 constexpr int kExEpi = 128;                     // threads of one epilogue warpgroup
-constexpr int kExBStages = 5;
-constexpr int kExBBytes = 16 * 1024;            // B columns of one unit, at most
+constexpr int kExBStages = 3;
+constexpr int kExBBytes = 32 * 1024;            // B columns of one unit, at most
 constexpr int kExYStages = 6;
 constexpr int kExYBytes = 16 * 1024;            // y rows of one unit, at most
 constexpr int kExSBytes = 8 * 1024;             // S of one slice block: at most 64 ranks x 64 rows, bf16
+constexpr int kExQ = 16;                        // entries of the expand's unit queue
+constexpr int kExPoolDiv = 6;                   // the expand claims the last 1 / kExPoolDiv of its cost at run time
+constexpr int kExUposCap = 2048;                // tiles whose first units the expand keeps on chip for its claims
 constexpr int kExAcc = 4;                       // tensor-memory accumulators of kExAccCols columns
 constexpr int kExAccCols = 128;
 constexpr uint32_t kExTmemCols = kExAcc * kExAccCols;
@@ -87,7 +90,7 @@ __device__ __forceinline__ TileRec load_tile(const TileRec *t)
     r.a = v0.x; r.e = v0.y; r.row0 = v0.z; r.m = v0.w;
     r.rp = v1.x; r.R = v1.y; r.n_pad = v1.z; r.kc = v1.w;
     r.n_kc = v2.x; r.ks = v2.y; r.W = v2.z; r.n_units = v2.w;
-    r.p_off = v3.x; r.s_off = v3.y; r.sh_pos = v3.z; r.ex_pos = v3.w;
+    r.p_off = v3.x; r.s_off = v3.y; r.c0 = v3.z; r.u0 = v3.w;
     return r;
 }
 
@@ -233,8 +236,8 @@ __device__ __forceinline__ GroupPlan group_plan(const StreamParams &p, int4 gr, 
 __device__ __forceinline__ int chunk_cost(int kc, int R, int m) { return max(1, kc * (R + m) * 2 / kCostUnit); }
 __device__ __forceinline__ int unit_cost(int W, int rp, int m) { return max(1, W * (rp + 2 * m) * 2 / kCostUnit); }
 
-// A launch of G blocks over total cost T: block c starts at position c q + min(c, r), q = T / G, r = T % G
-// (contiguous shares that differ by at most one).
+// G blocks over a total cost T: block c starts at position c q + min(c, r), q = T / G, r = T % G
+// (contiguous shares that differ by at most one; start(G) = T).
 struct Split {
     int G, q, r;
     __device__ __forceinline__ Split(int T, int G_) : G(G_), q(T / G_), r(T - (T / G_) * G_) {}
@@ -246,8 +249,7 @@ struct Split {
 __device__ __forceinline__ int2 block_start(const Split &sp, int T, int c, int nt, const int32_t *pos,
                                             const int32_t *per, const int32_t *n)
 {
-    if (c >= sp.G) return make_int2(nt, 0);
-    const int lo = sp.start(c);
+    const int lo = sp.start(c);   // start(G) is the split's total
     if (lo >= T) return make_int2(nt, 0);
     int l = 0, h = nt;   // pos[l] <= lo < pos[h] (pos[nt] = T)
     while (h - l > 1) {
@@ -266,6 +268,7 @@ struct PlanSmem {
     int32_t pos[3][kPlanCap + 1];
     int32_t per[3][kPlanCap];
     int32_t n[3][kPlanCap];
+    int32_t u0[kPlanCap + 1];   // each tile's first unit
     int32_t nt, T[3], bad;
 };
 
@@ -302,7 +305,7 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
         const float target = fmaxf(1.f, (float)est / ((float)p.grid_s * kPlanItems));
         const bool fit = ntot <= p.max_tiles && ntot <= kPlanCap;
         // tile records: offsets of the partials and of S, positions in the three cost orders
-        int t_run = 0;
+        int t_run = 0, c_run = 0, u_run = 0;
         long long sh_run = 0, ex_run = 0, P_run = 0, S_run = 0;
         for (int g0 = 0; g0 < G; g0 += 32) {
             const int g = g0 + lane;
@@ -323,10 +326,12 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
                 }
             }
             const int it = warp_inclusive(nt_g);
+            const int c_g = nt_g * (g < G ? gp.n_kc : 0), u_g = nt_g * (g < G ? gp.n_units : 0);
+            const int ic = warp_inclusive(c_g), iu = warp_inclusive(u_g);
             const long long ish = warp_inclusive(sh_g), iex = warp_inclusive(ex_g);
             const long long iP = warp_inclusive(P_g), iS = warp_inclusive(S_g);
             if (g < G && fit) {
-                int t = t_run + it - nt_g;
+                int t = t_run + it - nt_g, c0 = c_run + ic - c_g, u0 = u_run + iu - u_g;
                 long long sh = sh_run + ish - sh_g, ex = ex_run + iex - ex_g, P = P_run + iP - P_g;
                 long long S = S_run + iS - S_g;
                 int row = gp.row_off;
@@ -348,8 +353,8 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
                     r.n_units = gp.n_units;
                     r.p_off = (int)P;
                     r.s_off = (int)S;
-                    r.sh_pos = (int)sh;
-                    r.ex_pos = (int)ex;
+                    r.c0 = c0;
+                    r.u0 = u0;
                     p.tiles[t] = r;
                     ps.pos[0][t] = (int)sh;
                     ps.per[0][t] = cs;
@@ -360,6 +365,9 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
                     ps.pos[2][t] = (int)(S / 16);
                     ps.per[2][t] = 1;
                     ps.n[2][t] = gp.R * r.n_pad / 8;
+                    ps.u0[t] = u0;
+                    c0 += gp.n_kc;
+                    u0 += gp.n_units;
                     sh += (long long)gp.n_kc * cs;
                     ex += (long long)gp.n_units * cu;
                     P += (long long)gp.n_kc * m * gp.R;
@@ -368,6 +376,8 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
                 }
             }
             t_run += __shfl_sync(0xffffffffu, it, 31);
+            c_run += __shfl_sync(0xffffffffu, ic, 31);
+            u_run += __shfl_sync(0xffffffffu, iu, 31);
             sh_run += __shfl_sync(0xffffffffu, ish, 31);
             ex_run += __shfl_sync(0xffffffffu, iex, 31);
             P_run += __shfl_sync(0xffffffffu, iP, 31);
@@ -384,19 +394,27 @@ __device__ void make_plan(const StreamParams &p, PlanSmem &ps)
             ps.T[1] = bad ? 0 : (int)ex_run;
             ps.T[2] = bad ? 0 : (int)(S_run / 16);
             for (int k = 0; k < 3; ++k) ps.pos[k][nt] = ps.T[k];
+            ps.u0[nt] = bad ? 0 : u_run;
             if (bad) atomicOr(p.err, kErrWorkspace);
             p.plan_hdr[PL_TILES] = nt;
+            p.plan_hdr[PL_UNITS] = ps.u0[nt];
         }
     }
     __syncthreads();
     const int nt = ps.nt;
-    const Split ss(ps.T[0], p.grid_s), se(ps.T[1], p.grid_e), sr(ps.T[2], p.grid_s);
+    // the expand's blocks split all but the last 1 / kExPoolDiv of its cost ahead of time and claim the
+    // units of that tail one by one (its claims look tiles up in a copy of u0 that holds kExUposCap tiles)
+    const int T_ex = nt <= kExUposCap ? ps.T[1] - ps.T[1] / kExPoolDiv : ps.T[1];
+    const Split ss(ps.T[0], p.grid_s), se(T_ex, p.grid_e), sr(ps.T[2], p.grid_s);
     for (int c = tid; c <= p.grid_s; c += blockDim.x) {
         p.sh_start[c] = block_start(ss, ps.T[0], c, nt, ps.pos[0], ps.per[0], ps.n[0]);
         p.rd_start[c] = block_start(sr, ps.T[2], c, nt, ps.pos[2], ps.per[2], ps.n[2]);
     }
-    for (int c = tid; c <= p.grid_e; c += blockDim.x)
-        p.ex_start[c] = block_start(se, ps.T[1], c, nt, ps.pos[1], ps.per[1], ps.n[1]);
+    for (int c = tid; c <= p.grid_e; c += blockDim.x) {
+        const int2 b = block_start(se, ps.T[1], c, nt, ps.pos[1], ps.per[1], ps.n[1]);
+        p.ex_start[c] = b;
+        if (c == p.grid_e) p.plan_hdr[PL_POOL_U] = ps.u0[b.x] + b.y;   // u0[nt] is the launch's unit count
+    }
 }
 
 // ===========================================================================
@@ -696,6 +714,7 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
     pdl_wait();      // the segment table of the build, and everything before it
     pdl_trigger();   // the expand may launch now; it waits for this grid before it reads anything
     if (tid == 0) tstamp(p, 0, 1);
+    if (blockIdx.x == 0 && tid == 0) *p.ex_claim = 0;   // the expand of the launch before has ended
     if (blockIdx.x == 0) make_plan(p, sm.plan);
     if (grid_barrier(p, sm, 1)) {   // the plan is out
         if (tid == 0) tstamp(p, 0, 2);
@@ -745,6 +764,12 @@ struct __align__(1024) ExpandSmem {
     uint64_t s_full[2], s_empty[2];
     uint64_t acc_full[kExAcc], acc_empty[kExAcc];
     uint64_t drain;                                  // the MMA issuer's last MMAs are done
+    int2 uq[kExQ];                                   // unit queue: (tile, unit), tile -1 ends the sequence
+    uint64_t uq_full[kExQ], uq_empty[kExQ];
+    uint64_t u0_ready;
+    int32_t u0[kExUposCap + 1];                      // first unit of every tile, then the launch's unit count
+    int32_t nt;
+    uint32_t obs_err;                                // the phase trace's own waits (never the launch's status)
     uint32_t tmem_base;
 };
 
@@ -785,113 +810,201 @@ struct UnitWalk {
     }
 };
 
-// Warp 0, one thread: the packed B columns of every unit (one bulk copy each) into the B ring, with the
-// unit's description for the MMA issuer.
-__device__ __forceinline__ void expand_produce_b(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+// The unit sequence of a block: its share of the units split ahead of time, then units of the launch's
+// tail claimed one at a time, so that blocks that ran ahead take more of the tail.  Warp 0 (the leader)
+// walks it and hands every unit on: to the y producers and the S loader through the unit queue, to the MMA
+// issuer with the unit's B columns; the y producers hand it to the epilogue with the unit's y rows.  The
+// end of the sequence travels the same ways, as tile -1.
+
+// Tile l with u0[l] <= g < u0[l + 1].
+__device__ __forceinline__ int find_tile(const int32_t *u0, int nt, int g)
+{
+    int l = 0, h = nt;
+    while (h - l > 1) {
+        const int mid = (l + h) >> 1;
+        if (u0[mid] <= g) l = mid;
+        else h = mid;
+    }
+    return l;
+}
+
+// Warp 0, one thread: the unit sequence into the unit queue, and the packed B columns of every unit (one
+// bulk copy each) into the B ring with the unit's description for the MMA issuer.
+__device__ __forceinline__ void expand_lead(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
 {
     uint32_t i = 0;
     const unsigned char *bblk = nullptr;
     int blk_t = -1;
-    for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
-        const TileRec &tr = w.tr;
-        if (blk_t != w.t) {
-            bblk = reinterpret_cast<const unsigned char *>(__ldg(p.b_ptr + tr.a * p.E_B + (p.E_B == 1 ? 0 : tr.e)));
-            blk_t = w.t;
-        }
-        int s, cb;
-        unit_slice(p, tr.W, w.u, s, cb);
-        const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
+    auto emit = [&](int t, int u, const TileRec &tr) -> bool {
+        const int q = i % kExQ;
+        if (i >= kExQ && !mbar_wait_suspend(&sm.uq_empty[q], ((i / kExQ) - 1) & 1, p.timeout_ns, p.err))
+            return false;
+        sm.uq[q] = make_int2(t, u);
+        mbar_arrive(&sm.uq_full[q]);
         const int slot = i % kExBStages;
         if (i >= kExBStages &&
             !mbar_wait_suspend(&sm.empty_b[slot], ((i / kExBStages) - 1) & 1, p.timeout_ns, p.err))
-            break;
+            return false;
+        ++i;
         ExBMeta &mt = sm.bmeta[slot];
-        mt.t = w.t;
+        mt.t = t;
+        if (t < 0) {
+            mbar_arrive(&sm.full_b[slot]);
+            return true;
+        }
+        if (blk_t != t) {
+            bblk = reinterpret_cast<const unsigned char *>(__ldg(p.b_ptr + tr.a * p.E_B + (p.E_B == 1 ? 0 : tr.e)));
+            blk_t = t;
+        }
+        int s, cb;
+        unit_slice(p, tr.W, u, s, cb);
+        const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
         mt.sb = p.n_a == 1 ? 0 : s;
         mt.n_pad = tr.n_pad;
         mt.rp = tr.rp;
         mt.w_eff = w_eff;
         const uint32_t bbytes = (uint32_t)((w_eff + 127) >> 7) * tr.rp * 256;
+        if (i - 1 >= 8 && i - 1 < 12) tstamp(p, 1, 13 + (i - 1 - 8));
+        if (i - 1 >= 13 && i - 1 < 15) tstamp(p, 1, 29 + (i - 1 - 13));
         mbar_arrive_expect_tx(&sm.full_b[slot], bbytes);
         bulk_g2s(sm.bstage[slot], bblk + (size_t)(p.slice_tile_off[s] + cb * (tr.W >> 7)) * tr.rp * 256, bbytes,
                  &sm.full_b[slot]);
+        return true;
+    };
+    bool ok = true;
+    TileRec tr{};
+    for (UnitWalk w(b0, b1); ok && w.valid(p); w.next()) ok = emit(w.t, w.u, w.tr);
+    const int U = __ldcg(p.plan_hdr + PL_UNITS), g0 = __ldcg(p.plan_hdr + PL_POOL_U);
+    if (ok && g0 < U) {
+        ok = mbar_wait_suspend(&sm.u0_ready, 0, p.timeout_ns, p.err);
+        const int nt = sm.nt;
+        int g = ok ? g0 + atomicAdd(p.ex_claim, 1) : U, cur = -1;
+        while (ok && g < U) {
+            const int gn = g0 + atomicAdd(p.ex_claim, 1);   // the next claim's round trip overlaps this unit
+            const int t = find_tile(sm.u0, nt, g);
+            if (t != cur) {
+                tr = load_tile(p.tiles + t);
+                cur = t;
+            }
+            ok = emit(t, g - sm.u0[t], tr);
+            g = gn;
+        }
     }
+    emit(-1, 0, tr);
     for (uint32_t q = i > kExBStages ? i - kExBStages : 0; q < i; ++q)
         mbar_wait_suspend(&sm.full_b[q % kExBStages], (q / kExBStages) & 1, p.timeout_ns, p.err);
 }
 
-// Warps 4-7 (kExYProd threads): for every unit, its y rows (16-byte cp.async pieces over the group) and its
-// description into the next y slot.  One barrier per unit keeps the four warps in step (and lets them leave
-// together when a wait runs out).
-__device__ __forceinline__ void expand_produce_y(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+// Warps 4-7 (kExYProd threads): for every unit of the queue, its y rows (16-byte cp.async pieces over the
+// group) and its description into the next y slot; at the end of the sequence one end mark (m = -1) per
+// epilogue group.  One barrier per unit keeps the four warps in step (and lets them leave together when a
+// wait runs out).
+__device__ __forceinline__ void expand_produce_y(const StreamParams &p, ExpandSmem &sm)
 {
     const int gt = threadIdx.x - 128, lane = threadIdx.x & 31;
     uint32_t i = 0;
     int cur = -1;
+    TileRec tr{};
     int yr = 0;      // y row gt of the current tile (gt < m) and its factor
     float yf = 0.f;
-    for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
-        const TileRec &tr = w.tr;
-        if (cur != w.t) {
-            const float sc = __ldg(p.scale + tr.a);
-            yr = gt < tr.m ? __ldcg(p.rows + tr.row0 + gt) : 0;
-            yf = p.row_weight ? sc * __ldg(p.row_weight + yr) : sc;
-            cur = w.t;
+    bool live = true;
+    for (;; ++i) {
+        const int q = i % kExQ;
+        bool got = true;
+        if (lane == 0) got = mbar_wait_suspend(&sm.uq_full[q], (i / kExQ) & 1, p.timeout_ns, p.err);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        const int2 e = sm.uq[q];
+        const bool end = !got || e.x < 0;
+        const int slot = i % kExYStages;
+        int col = 0, w_eff = 0;
+        if (!end) {
+            if (i >= kExYStages) {
+                if (lane == 0) got = mbar_wait_suspend(&sm.empty_y[slot], ((i / kExYStages) - 1) & 1, p.timeout_ns, p.err);
+                got = __shfl_sync(0xffffffffu, got, 0);
+            }
+            if (e.x != cur) {
+                tr = load_tile(p.tiles + e.x);
+                const float sc = __ldg(p.scale + tr.a);
+                yr = gt < tr.m ? __ldcg(p.rows + tr.row0 + gt) : 0;
+                yf = p.row_weight ? sc * __ldg(p.row_weight + yr) : sc;
+                cur = e.x;
+            }
+            int s, cb;
+            unit_slice(p, tr.W, e.y, s, cb);
+            w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
+            col = p.slice_off[s] + cb * tr.W;
+            if (got) {
+                ExYMeta &mt = sm.ymeta[slot];
+                if (gt < tr.m) {
+                    mt.row[gt] = yr;
+                    mt.f[gt] = yf;
+                }
+                if (gt == 0) {
+                    mt.W = tr.W;
+                    mt.m = tr.m;
+                    mt.w_eff = w_eff;
+                    mt.n_pad = tr.n_pad;
+                    mt.col = col;
+                }
+            }
         }
-        int s, cb;
-        unit_slice(p, tr.W, w.u, s, cb);
-        const int w_eff = min(tr.W, p.slice_n[s] - cb * tr.W);
+        // every thread has read the entry; the slot is free for the whole group and its rows are written
+        if (!bar_and(5, kExYProd, got)) {
+            live = false;
+            break;
+        }
+        if (gt == 0) mbar_arrive(&sm.uq_empty[q]);
+        if (end) break;
+        const __nv_bfloat16 *yc = p.y + col;
+        const int64_t ldy = p.ldy;
+        const ExYMeta &mt = sm.ymeta[slot];
+        if (i >= 8 && i < 12 && gt == 0) tstamp(p, 1, 17 + (i - 8));
+        group_gather(sm.ystage[slot], tr.W * 2, tr.m, w_eff >> 3, gt, kExYProd,
+                     [&](int r) { return yc + (int64_t)mt.row[r] * ldy; });
+        tc::cp_async_arrive_noinc(&sm.full_y[slot]);   // once every piece of this thread has landed
+    }
+    for (int k = 0; live && k < kExGroups; ++k, ++i) {   // an end mark for each epilogue group
         const int slot = i % kExYStages;
         bool got = true;
         if (i >= kExYStages) {
             if (lane == 0) got = mbar_wait_suspend(&sm.empty_y[slot], ((i / kExYStages) - 1) & 1, p.timeout_ns, p.err);
             got = __shfl_sync(0xffffffffu, got, 0);
         }
-        ExYMeta &mt = sm.ymeta[slot];
-        const int col = p.slice_off[s] + cb * tr.W;
-        if (got) {
-            if (gt < tr.m) {
-                mt.row[gt] = yr;
-                mt.f[gt] = yf;
-            }
-            if (gt == 0) {
-                mt.W = tr.W;
-                mt.m = tr.m;
-                mt.w_eff = w_eff;
-                mt.n_pad = tr.n_pad;
-                mt.col = col;
-            }
-        }
-        if (!bar_and(5, kExYProd, got)) break;   // the slot is free for the whole group; its rows are written
-        const __nv_bfloat16 *yc = p.y + col;
-        const int64_t ldy = p.ldy;
-        if (i < 3 && gt == 0) tstamp(p, 1, 25 + 2 * i);
-        group_gather(sm.ystage[slot], tr.W * 2, tr.m, w_eff >> 3, gt, kExYProd,
-                     [&](int r) { return yc + (int64_t)mt.row[r] * ldy; });
-        if (i < 3 && gt == 0) tstamp(p, 1, 26 + 2 * i);
-        tc::cp_async_arrive_noinc(&sm.full_y[slot]);   // once every piece of this thread has landed
+        if (got && gt == 0) sm.ymeta[slot].m = -1;
+        if (!bar_and(5, kExYProd, got)) break;
+        mbar_arrive(&sm.full_y[slot]);
     }
     tc::cp_async_wait_all();
 }
 
-// Warp 1, one thread: S of every (tile, slice block) this block meets, into two buffers in rotation.
-__device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+// Warp 1, one thread: S of every (tile, slice block) the unit queue meets, into two buffers in rotation.
+__device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem &sm)
 {
     tstamp(p, 1, 3);
     uint32_t k = 0;
-    int prev_t = -1, prev_sb = -1;
-    for (UnitWalk w(b0, b1); w.valid(p); w.next()) {
+    int prev_t = -1, prev_sb = -1, cur = -1;
+    TileRec tr{};
+    for (uint32_t i = 0;; ++i) {
+        const int q = i % kExQ;
+        if (!mbar_wait_suspend(&sm.uq_full[q], (i / kExQ) & 1, p.timeout_ns, p.err)) break;
+        const int2 e = sm.uq[q];
+        mbar_arrive(&sm.uq_empty[q]);
+        if (e.x < 0) break;
+        if (e.x != cur) {
+            tr = load_tile(p.tiles + e.x);
+            cur = e.x;
+        }
         int s, cb;
-        unit_slice(p, w.tr.W, w.u, s, cb);
+        unit_slice(p, tr.W, e.y, s, cb);
         const int sb = p.n_a == 1 ? 0 : s;
-        if (w.t == prev_t && sb == prev_sb) continue;
+        if (e.x == prev_t && sb == prev_sb) continue;
         const int slot = k & 1;
         if (k >= 2 && !mbar_wait_suspend(&sm.s_empty[slot], ((k >> 1) - 1) & 1, p.timeout_ns, p.err)) break;
-        const uint32_t bytes = (uint32_t)w.tr.rp * w.tr.n_pad * 2;
+        const uint32_t bytes = (uint32_t)tr.rp * tr.n_pad * 2;
         mbar_arrive_expect_tx(&sm.s_full[slot], bytes);
-        if (!p.withhold) bulk_g2s(sm.sbuf[slot], p.s_area + w.tr.s_off + (size_t)sb * bytes, bytes, &sm.s_full[slot]);
+        if (!p.withhold) bulk_g2s(sm.sbuf[slot], p.s_area + tr.s_off + (size_t)sb * bytes, bytes, &sm.s_full[slot]);
         ++k;
-        prev_t = w.t;
+        prev_t = e.x;
         prev_sb = sb;
     }
     if (!p.withhold)
@@ -901,17 +1014,19 @@ __device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem 
 
 // Warp 2, one thread: D(acc) = B_unit S^T for every unit (M = 128 output columns per B tile, N = the tile's
 // rows rounded up to 16, K = the stored rank).
-__device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1)
+__device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm)
 {
     uint32_t i = 0, k = 0;
     int prev_t = -1, prev_sb = -1;
-    for (UnitWalk w(b0, b1); w.valid(p); w.next(), ++i) {
+    for (;; ++i) {
         const int slot = i % kExBStages;
+        if (i >= 8 && i < 12) tstamp(p, 2, 8 + (i - 8));
         if (!mbar_wait_suspend(&sm.full_b[slot], (i / kExBStages) & 1, p.timeout_ns, p.err)) break;
-        if (i == 0) tstamp(p, 1, 2);
-        if (i < 8) tstamp(p, 1, 9 + i);
         const ExBMeta &mt = sm.bmeta[slot];
         const int t = mt.t, sb = mt.sb, n_pad = mt.n_pad, rp = mt.rp, w_eff = mt.w_eff;
+        if (t < 0) break;   // the end of the sequence
+        if (i == 0) tstamp(p, 1, 2);
+        if (i >= 8 && i < 12) tstamp(p, 1, 5 + (i - 8));
         if (t != prev_t || sb != prev_sb) {
             if (k > 0) tc::mma_commit(&sm.s_empty[(k - 1) & 1]);   // the previous S is free once these MMAs end
             if (!mbar_wait_suspend(&sm.s_full[k & 1], (k >> 1) & 1, p.timeout_ns, p.err)) break;
@@ -922,6 +1037,7 @@ __device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm
         }
         const int b = i % kExAcc;
         if (i >= kExAcc && !mbar_wait_suspend(&sm.acc_empty[b], ((i / kExAcc) - 1) & 1, p.timeout_ns, p.err)) break;
+        if (i >= 8 && i < 12) tstamp(p, 1, 25 + (i - 8));
         tc::fence_after_sync();
         const uint32_t idesc = tc::idesc_bf16(128, n_pad);
         const uint32_t s_addr = smem_u32(sm.sbuf[(k - 1) & 1]);
@@ -934,8 +1050,10 @@ __device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm
                 tc::mma_bf16(sm.tmem_base + b * kExAccCols + q * n_pad, ad, bd, idesc, kk > 0 ? 1u : 0u);
             }
         }
+        if (i >= 8 && i < 12) tstamp(p, 2, 0 + (i - 8));
         tc::mma_commit(&sm.acc_full[b]);
         tc::mma_commit(&sm.empty_b[slot]);   // the B columns are free once these MMAs end
+        if (i >= 8 && i < 12) tstamp(p, 2, 4 + (i - 8));
     }
     // tensor memory is freed when the block ends: every MMA issued must be done by then
     if (i > 0) {
@@ -947,33 +1065,25 @@ __device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm
 // Warpgroup wg (warps 4 + 4 wg .. 7 + 4 wg) takes units wg, wg + kExGroups, ...  Thread (quarter qw, lane)
 // owns output column 32 qw + lane of every 128-column group of a unit: it reads that column's accumulator
 // for all rows and adds it into the staged y rows; the rows then leave as 16-byte stores.
-__device__ __forceinline__ void expand_epilogue(const StreamParams &p, ExpandSmem &sm, int2 b0, int2 b1, int wg)
+__device__ __forceinline__ void expand_epilogue(const StreamParams &p, ExpandSmem &sm, int wg)
 {
     const int lane = threadIdx.x & 31, qw = (threadIdx.x >> 5) & 3, et = threadIdx.x & 127;
     const int bar = 1 + wg;
-    UnitWalk w(b0, b1);
-    for (int g = 0; g < wg && w.valid(p); ++g) w.next();   // this warpgroup starts at unit wg
-    for (int k = 0; w.valid(p); ++k) {
+    for (int k = 0;; ++k) {
         const uint32_t i = kExGroups * k + wg;   // the unit's index in the block's sequence
         const int slot = i % kExYStages, b = i % kExAcc;
-        bool got = mbar_wait_suspend(&sm.full_y[slot], (i / kExYStages) & 1, p.timeout_ns, p.err);
-        got = got && mbar_wait_suspend(&sm.acc_full[b], (i / kExAcc) & 1, p.timeout_ns, p.err);
-        if (!__all_sync(0xffffffffu, got)) break;
-        if (i < 8 && et == 0) tstamp(p, 1, 17 + i);
-        tc::fence_after_sync();
+        if (!bar_and(bar, kExEpi, mbar_wait_suspend(&sm.full_y[slot], (i / kExYStages) & 1, p.timeout_ns, p.err)))
+            break;
         const ExYMeta &mt = sm.ymeta[slot];
         const int m = mt.m, W = mt.W, w_eff = mt.w_eff, n_pad = mt.n_pad;
+        if (m < 0) break;   // the end of the sequence
+        if (!bar_and(bar, kExEpi, mbar_wait_suspend(&sm.acc_full[b], (i / kExAcc) & 1, p.timeout_ns, p.err))) break;
+        tc::fence_after_sync();
         __nv_bfloat16 *ys = reinterpret_cast<__nv_bfloat16 *>(sm.ystage[slot]);
         const uint32_t tbase = sm.tmem_base + ((uint32_t)(qw * 32) << 16) + b * kExAccCols;
         const int nq = (w_eff + 127) >> 7;
         for (int j0 = 0; j0 < n_pad; j0 += 32) {
             const int nrow = min(32, m - j0);
-            float f[32];   // the rows' factors (the same for every thread)
-#pragma unroll
-            for (int h = 0; h < 32; h += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(&mt.f[(j0 + h) & (kTileRows - 4)]);
-                f[h] = v.x; f[h + 1] = v.y; f[h + 2] = v.z; f[h + 3] = v.w;
-            }
             for (int q = 0; q < nq; ++q) {
                 const int c = q * 128 + qw * 32 + lane;
                 float v[32];
@@ -985,12 +1095,16 @@ __device__ __forceinline__ void expand_epilogue(const StreamParams &p, ExpandSme
 #pragma unroll
                     for (int h = 0; h < 32; h += 8) {
                         if (h < nrow) {
+                            // the rows' factors (the same for every thread)
+                            const float4 fa = *reinterpret_cast<const float4 *>(&mt.f[(j0 + h) & (kTileRows - 8)]);
+                            const float4 fb = *reinterpret_cast<const float4 *>(&mt.f[((j0 + h) & (kTileRows - 8)) + 4]);
+                            const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
                             float yv[8];
 #pragma unroll
                             for (int jj = 0; jj < 8; ++jj) yv[jj] = h + jj < nrow ? __bfloat162float(yc[(h + jj) * W]) : 0.f;
 #pragma unroll
                             for (int jj = 0; jj < 8; ++jj)
-                                if (h + jj < nrow) yc[(h + jj) * W] = __float2bfloat16_rn(fmaf(f[h + jj], v[h + jj], yv[jj]));
+                                if (h + jj < nrow) yc[(h + jj) * W] = __float2bfloat16_rn(fmaf(f[jj], v[h + jj], yv[jj]));
                         }
                     }
                 }
@@ -1017,10 +1131,7 @@ __device__ __forceinline__ void expand_epilogue(const StreamParams &p, ExpandSme
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty_y[slot]);   // this warp is done with the slot
-        if (k == 0 && et == 0) tstamp(p, 1, 5 + wg);
-        for (int g = 0; g < kExGroups && w.valid(p); ++g) w.next();
     }
-    if (et == 0) tstamp(p, 1, 7 + wg);
 }
 
 __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_constant__ StreamParams p)
@@ -1046,6 +1157,11 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
             mbar_init(&sm.acc_full[s], 1);
             mbar_init(&sm.acc_empty[s], 4);
         }
+        for (int s = 0; s < kExQ; ++s) {
+            mbar_init(&sm.uq_full[s], 1);    // the leader
+            mbar_init(&sm.uq_empty[s], 2);   // the S loader and the y producers
+        }
+        mbar_init(&sm.u0_ready, 1);
         mbar_init(&sm.drain, 1);
         fence_mbar_init();
     }
@@ -1058,15 +1174,36 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     const int2 b0 = __ldcg(p.ex_start + blockIdx.x), b1 = __ldcg(p.ex_start + blockIdx.x + 1);
     if (threadIdx.x == 0) tstamp(p, 1, 1);
     if (warp == 0) {
-        if (lane == 0) expand_produce_b(p, sm, b0, b1);
+        if (lane == 0) expand_lead(p, sm, b0, b1);
     } else if (warp == 1) {
-        if (lane == 0) expand_load_s(p, sm, b0, b1);
+        if (lane == 0) expand_load_s(p, sm);
     } else if (warp == 2) {
-        if (lane == 0) expand_mma(p, sm, b0, b1);
-    } else if (warp >= 4 && warp < 8) {
-        expand_produce_y(p, sm, b0, b1);
-    } else if (warp >= 8) {
-        expand_epilogue(p, sm, b0, b1, (warp - 8) >> 2);
+        if (lane == 0) expand_mma(p, sm);
+    } else if (warp == 3) {
+        // the tiles' first units, for the leader's claims (none when the tiles are too many to keep)
+        const int nt = __ldcg(p.plan_hdr + PL_TILES);
+        if (nt <= kExUposCap) {
+            for (int t = lane; t < nt; t += 32) sm.u0[t] = __ldcg(&p.tiles[t].u0);
+            if (lane == 0) sm.u0[nt] = __ldcg(p.plan_hdr + PL_UNITS);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            sm.nt = nt;
+            mbar_arrive(&sm.u0_ready);
+        }
+        if (p.trace != nullptr && lane < 2) {   // phase trace: when the B (lane 0) and y (lane 1) copies of units 8-11 land
+            // phases in order: a parity wait only tells a phase from the one before
+            uint64_t *bar = lane == 0 ? sm.full_b : sm.full_y;
+            const uint32_t n = lane == 0 ? kExBStages : kExYStages;
+            for (uint32_t i = 0; i < 12; ++i) {
+                if (!mbar_wait_suspend(&bar[i % n], (i / n) & 1, 100000, &sm.obs_err)) break;
+                if (i >= 8) tstamp(p, 1, (lane == 0 ? 9 : 21) + (i - 8));
+            }
+        }
+    } else if (warp < 8) {
+        expand_produce_y(p, sm);
+    } else {
+        expand_epilogue(p, sm, (warp - 8) >> 2);
     }
     __syncwarp();
     tc::fence_before_sync();

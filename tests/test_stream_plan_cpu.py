@@ -32,7 +32,7 @@ def _constants():
     text = open(SRC).read()
     out = {}
     for name in ("kPlanItems", "kPartialPerRow", "kTileRows", "kShStageBytes", "kExBBytes", "kExYBytes",
-                 "kExSBytes", "kExAccCols", "kCostUnit"):
+                 "kExSBytes", "kExAccCols", "kCostUnit", "kExPoolDiv", "kExUposCap"):
         m = re.search(r"constexpr int %s = ([0-9* ]+);" % name, text)
         assert m, name
         out[name] = int(eval(m.group(1)))
@@ -97,13 +97,15 @@ def plan(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
     return tiles, sh_pre, ex_pre
 
 
-def block_start(pre, tiles, T, G, c, key):
-    """First (tile, item) of block c: shares of T that differ by at most one, block c starting at
-    c q + min(c, r) with q = T // G, r = T % G; the first item at or past that position."""
+def block_start(pre, tiles, T, G, c, key, T_split=None):
+    """First (tile, item) of block c: shares of T_split (T unless given) that differ by at most one, block c
+    starting at c q + min(c, r) with q = T_split // G, r = T_split % G (so block G starts at T_split); the
+    first item at or past that position."""
     nt = len(tiles)
-    q, r = divmod(T, G)
+    T_split = T if T_split is None else T_split
+    q, r = divmod(T_split, G)
     lo = c * q + min(c, r)
-    if c >= G or lo >= T:
+    if lo >= T:
         return (nt, 0)
     l = int(np.searchsorted(pre, lo, side="right")) - 1
     n = tiles[l][key]
@@ -131,14 +133,25 @@ def check(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
     rd_pre = np.concatenate([[0], np.cumsum(rd)]).astype(np.int64)
     for key, pre in (("n_kc", sh_pre), ("n_units", ex_pre), ("s_items", rd_pre)):
         T = int(pre[-1])
-        starts = [block_start(pre, tiles, T, grid, c, key) for c in range(grid + 1)]
-        assert starts[-1] == (len(tiles), 0)
+        # the expand splits all but the last 1 / kExPoolDiv of its cost ahead of time; the units from block
+        # `grid`'s start on are claimed one by one (global unit index u0[tile] + unit)
+        T_split = T - T // C["kExPoolDiv"] if key == "n_units" and len(tiles) <= C["kExUposCap"] else T
+        starts = [block_start(pre, tiles, T, grid, c, key, T_split) for c in range(grid + 1)]
+        if T_split == T:
+            assert starts[-1] == (len(tiles), 0)
         seen = []
         for c in range(grid):
             assert starts[c] <= starts[c + 1]
             seen += walk(starts[c], starts[c + 1], tiles, key)
+        pool = walk(starts[grid], (len(tiles), 0), tiles, key)
         every = [(t, j) for t in range(len(tiles)) for j in range(tiles[t][key])]
-        assert seen == every, key
+        assert seen + pool == every, key
+        if key == "n_units":
+            u0 = np.concatenate([[0], np.cumsum([t["n_units"] for t in tiles])]).astype(np.int64)
+            g0 = int(u0[starts[grid][0]]) + starts[grid][1]
+            for g in range(g0, int(u0[-1])):   # a claim's tile lookup
+                l = int(np.searchsorted(u0, g, side="right")) - 1
+                assert pool[g - g0] == (l, g - int(u0[l]))
     for t in tiles:
         assert 1 <= t["m"] <= C["kTileRows"] and t["m"] <= tile_max
         assert (t["R"] * t["ks"] + t["m"] * (t["ks"] + 8)) * 2 <= C["kShStageBytes"]
