@@ -60,6 +60,7 @@ constexpr int kShWarps = 8;                     // MMA warps of the shrink
 constexpr int kShProd = 128;                    // producer threads (the four warps after the MMA warps)
 constexpr int kShThreads = 32 * kShWarps + kShProd;
 constexpr int kShStages = 6;
+constexpr int kMyTiles = 16;                    // tiles of its own chunks a shrink block keeps on chip
 constexpr int kShStageBytes = 32 * 1024;        // A columns and x rows of one stage, at most
 constexpr int kExGroups = 3;                    // epilogue warpgroups (units dealt round-robin)
 constexpr int kExYProd = 128;                   // y producer threads: warps 4-7
@@ -244,177 +245,226 @@ struct Split {
     __device__ __forceinline__ int start(int c) const { return c * q + min(c, r); }
 };
 
-// Block c's first (tile, item): the first item at or past its start position, given the tiles' positions,
-// per-item costs and item counts in shared memory.
-__device__ __forceinline__ int2 block_start(const Split &sp, int T, int c, int nt, const int32_t *pos,
-                                            const int32_t *per, const int32_t *n)
+// Launch-wide position of a group's first item in every order the plan keeps: shrink cost, expand cost,
+// S chunks (16 bytes each; S bytes are 16 times this), tiles, chunks, units, partial floats.  Entry G holds
+// the totals.
+struct GroupPos {
+    int32_t sh, ex, rd, t, c, u, P;
+};
+enum PlanOrder { ORD_SH = 0, ORD_EX = 1, ORD_RD = 2 };
+
+// The first `rem` tiles of a group have base + 1 rows and the others base rows, so an amount per tile takes
+// one of two values (A, B) and a tile's position in any order has a closed form.
+struct TwoWay {
+    int A, B, rem;
+    __device__ __forceinline__ int before(int i) const { return min(i, rem) * A + max(0, i - rem) * B; }
+    // the tile holding offset off (0 <= off < the group's total)
+    __device__ __forceinline__ int find(int off) const { return off < rem * A ? off / A : rem + (off - rem * A) / B; }
+};
+__device__ __forceinline__ int npad16(int m) { return (m + 15) & ~15; }
+__device__ __forceinline__ TwoWay two_way(const GroupPlan &g, int order)
 {
-    const int lo = sp.start(c);   // start(G) is the split's total
-    if (lo >= T) return make_int2(nt, 0);
-    int l = 0, h = nt;   // pos[l] <= lo < pos[h] (pos[nt] = T)
-    while (h - l > 1) {
-        const int mid = (l + h) >> 1;
-        if (pos[mid] <= lo) l = mid;
-        else h = mid;
+    const int m1 = g.base + 1, m0 = g.base;
+    switch (order) {
+    case ORD_SH: return {g.n_kc * chunk_cost(g.kc, g.R, m1), g.n_kc * chunk_cost(g.kc, g.R, m0), g.rem};
+    case ORD_EX: return {g.n_units * unit_cost(g.W, g.rp, m1), g.n_units * unit_cost(g.W, g.rp, m0), g.rem};
+    default: return {g.R * npad16(m1) / 8, g.R * npad16(m0) / 8, g.rem};
     }
-    const int j = (lo - pos[l] + per[l] - 1) / per[l];
-    return j >= n[l] ? make_int2(l + 1, 0) : make_int2(l, j);
 }
 
-// Shared memory of block 0 while it plans: for the shrink chunks (0), the expand units (1) and the S chunks
-// of the reduction (2), each tile's position, per-item cost and item count.
-constexpr int kPlanCap = 4096;   // tiles whose positions fit; a larger plan fails with LORA_ERR_WORKSPACE
+// Shared memory of a block while it plans (it overlays the stage ring, which is not in use yet).
+constexpr int kPlanGroups = 4096;   // groups whose positions fit; a larger plan fails with LORA_ERR_WORKSPACE
+constexpr int kPlanKept = 512;      // groups whose plans are kept (later groups are planned again when needed)
+struct GroupKept {
+    int32_t ntl, base, rem, kc, n_kc, ks, W, n_units;
+};
 struct PlanSmem {
-    int32_t pos[3][kPlanCap + 1];
-    int32_t per[3][kPlanCap];
-    int32_t n[3][kPlanCap];
-    int32_t u0[kPlanCap + 1];   // each tile's first unit
-    int32_t nt, T[3], bad;
+    GroupPos pos[kPlanGroups + 1];
+    int4 gr[kPlanGroups];        // the group records
+    int32_t rp[kPlanGroups];     // their adapters' stored ranks
+    GroupKept kept[kPlanKept];
+    int32_t G, bad;
+    float target;
 };
 
-// Block 0 of the shrink grid: tile records (global) and the first item of every block of the shrink, of
-// its reduction and of the expand.  Warp 0 walks the groups; every thread then places blocks.
-__device__ void make_plan(const StreamParams &p, PlanSmem &ps)
+__device__ __forceinline__ int gpos_field(const GroupPos &q, int order)
 {
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (tid < 32) {
-        // the group count, the first 32 group records and the first 32 stored ranks in one round trip
-        const int G = max(0, min(__ldcg(p.num_groups), p.group_capacity));
-        const int4 gr0 = lane < p.group_capacity ? __ldcg(p.groups + lane) : make_int4(0, 0, 0, 0);
-        const int rp0 = lane < p.L ? __ldg(p.rpad + lane) : 0;
-        auto rank_of = [&](int a) {   // stored rank of adapter a (a shuffle for the first 32)
-            const int v = __shfl_sync(0xffffffffu, rp0, a & 31);
-            return a < 32 ? v : __ldg(p.rpad + a);
-        };
-        // tiles, and the shrink bytes of the whole launch
-        long long est = 0;
-        int ntot = 0;
-        for (int g0 = 0; g0 < G; g0 += 32) {
-            const int g = g0 + lane;
-            const int4 gr = g0 == 0 ? gr0 : (g < G ? __ldcg(p.groups + g) : make_int4(0, 0, 0, 0));
-            const int rp = rank_of(gr.x);
-            if (g < G) {
-                const int ntl = group_tiles(p, gr.w);
-                ntot += ntl;
-                est += (long long)p.K * 2 * ((long long)p.n_a * rp * ntl + gr.w);
+    return order == ORD_SH ? q.sh : order == ORD_EX ? q.ex : q.rd;
+}
+
+// The group holding position `lo` of an order, or tile `t` (order -1): the last g with pos[g] <= lo.
+__device__ __forceinline__ int find_group(const PlanSmem &ps, int order, int lo)
+{
+    int l = 0, h = ps.G;
+    while (h - l > 1) {
+        const int mid = (l + h) >> 1;
+        if ((order < 0 ? ps.pos[mid].t : gpos_field(ps.pos[mid], order)) <= lo) l = mid;
+        else h = mid;
+    }
+    return l;
+}
+
+__device__ __forceinline__ GroupPlan load_group_plan(const StreamParams &p, const PlanSmem &ps, int g)
+{
+    if (g >= kPlanKept) return group_plan(p, ps.gr[g], ps.rp[g], ps.target);
+    const int4 gr = ps.gr[g];
+    const GroupKept &k = ps.kept[g];
+    GroupPlan r;
+    r.a = gr.x;
+    r.e = gr.y;
+    r.row_off = gr.z;
+    r.count = gr.w;
+    r.rp = ps.rp[g];
+    r.R = p.n_a * r.rp;
+    r.ntl = k.ntl;
+    r.base = k.base;
+    r.rem = k.rem;
+    r.kc = k.kc;
+    r.n_kc = k.n_kc;
+    r.ks = k.ks;
+    r.W = k.W;
+    r.n_units = k.n_units;
+    return r;
+}
+
+// Warp 0 of every block: the group table, its plan and every group's positions.  Reads only what the
+// build wrote, so no block waits for another to plan.
+__device__ void plan_groups(const StreamParams &p, PlanSmem &ps)
+{
+    const int lane = threadIdx.x & 31;
+    // the group count, the first 32 group records and the first 32 stored ranks in one round trip
+    const int G = max(0, min(__ldcg(p.num_groups), p.group_capacity));
+    const int4 gr0 = lane < p.group_capacity ? __ldcg(p.groups + lane) : make_int4(0, 0, 0, 0);
+    const int rp0 = lane < p.L ? __ldg(p.rpad + lane) : 0;
+    auto rank_of = [&](int a) {   // stored rank of adapter a (a shuffle for the first 32)
+        const int v = __shfl_sync(0xffffffffu, rp0, a & 31);
+        return a < 32 ? v : __ldg(p.rpad + a);
+    };
+    // tiles, and the shrink bytes of the whole launch
+    long long est = 0;
+    int ntot = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+        const int g = g0 + lane;
+        const int4 gr = g0 == 0 ? gr0 : (g < G ? __ldcg(p.groups + g) : make_int4(0, 0, 0, 0));
+        const int rp = rank_of(gr.x);
+        if (g < G) {
+            const int ntl = group_tiles(p, gr.w);
+            ntot += ntl;
+            est += (long long)p.K * 2 * ((long long)p.n_a * rp * ntl + gr.w);
+            if (g < kPlanGroups) {
+                ps.gr[g] = gr;
+                ps.rp[g] = rp;
             }
         }
-        est = warp_sum(est);
-        ntot = warp_sum(ntot);
-        if (lane == 0) tstamp(p, 0, 10);
-        const float target = fmaxf(1.f, (float)est / ((float)p.grid_s * kPlanItems));
-        const bool fit = ntot <= p.max_tiles && ntot <= kPlanCap;
-        // tile records: offsets of the partials and of S, positions in the three cost orders
-        int t_run = 0, c_run = 0, u_run = 0;
-        long long sh_run = 0, ex_run = 0, P_run = 0, S_run = 0;
-        for (int g0 = 0; g0 < G; g0 += 32) {
-            const int g = g0 + lane;
-            GroupPlan gp;
-            int nt_g = 0;
-            long long sh_g = 0, ex_g = 0, P_g = 0, S_g = 0;
-            const int4 gr = g0 == 0 ? gr0 : (g < G ? __ldcg(p.groups + g) : make_int4(0, 0, 0, 0));
-            const int rp = rank_of(gr.x);
-            if (g < G) {
-                gp = group_plan(p, gr, rp, target);
-                nt_g = gp.ntl;
-                for (int i = 0; i < gp.ntl; ++i) {
-                    const int m = gp.base + (i < gp.rem ? 1 : 0);
-                    sh_g += (long long)gp.n_kc * chunk_cost(gp.kc, gp.R, m);
-                    ex_g += (long long)gp.n_units * unit_cost(gp.W, gp.rp, m);
-                    P_g += (long long)gp.n_kc * m * gp.R;
-                    S_g += gp.R * ((m + 15) & ~15) * 2;
-                }
-            }
-            const int it = warp_inclusive(nt_g);
-            const int c_g = nt_g * (g < G ? gp.n_kc : 0), u_g = nt_g * (g < G ? gp.n_units : 0);
-            const int ic = warp_inclusive(c_g), iu = warp_inclusive(u_g);
-            const long long ish = warp_inclusive(sh_g), iex = warp_inclusive(ex_g);
-            const long long iP = warp_inclusive(P_g), iS = warp_inclusive(S_g);
-            if (g < G && fit) {
-                int t = t_run + it - nt_g, c0 = c_run + ic - c_g, u0 = u_run + iu - u_g;
-                long long sh = sh_run + ish - sh_g, ex = ex_run + iex - ex_g, P = P_run + iP - P_g;
-                long long S = S_run + iS - S_g;
-                int row = gp.row_off;
-                for (int i = 0; i < gp.ntl; ++i, ++t) {
-                    const int m = gp.base + (i < gp.rem ? 1 : 0);
-                    const int cs = chunk_cost(gp.kc, gp.R, m), cu = unit_cost(gp.W, gp.rp, m);
-                    TileRec r;
-                    r.a = gp.a;
-                    r.e = gp.e;
-                    r.row0 = row;
-                    r.m = m;
-                    r.rp = gp.rp;
-                    r.R = gp.R;
-                    r.n_pad = (m + 15) & ~15;
-                    r.kc = gp.kc;
-                    r.n_kc = gp.n_kc;
-                    r.ks = gp.ks;
-                    r.W = gp.W;
-                    r.n_units = gp.n_units;
-                    r.p_off = (int)P;
-                    r.s_off = (int)S;
-                    r.c0 = c0;
-                    r.u0 = u0;
-                    p.tiles[t] = r;
-                    ps.pos[0][t] = (int)sh;
-                    ps.per[0][t] = cs;
-                    ps.n[0][t] = gp.n_kc;
-                    ps.pos[1][t] = (int)ex;
-                    ps.per[1][t] = cu;
-                    ps.n[1][t] = gp.n_units;
-                    ps.pos[2][t] = (int)(S / 16);
-                    ps.per[2][t] = 1;
-                    ps.n[2][t] = gp.R * r.n_pad / 8;
-                    ps.u0[t] = u0;
-                    c0 += gp.n_kc;
-                    u0 += gp.n_units;
-                    sh += (long long)gp.n_kc * cs;
-                    ex += (long long)gp.n_units * cu;
-                    P += (long long)gp.n_kc * m * gp.R;
-                    S += gp.R * r.n_pad * 2;
-                    row += m;
-                }
-            }
-            t_run += __shfl_sync(0xffffffffu, it, 31);
-            c_run += __shfl_sync(0xffffffffu, ic, 31);
-            u_run += __shfl_sync(0xffffffffu, iu, 31);
-            sh_run += __shfl_sync(0xffffffffu, ish, 31);
-            ex_run += __shfl_sync(0xffffffffu, iex, 31);
-            P_run += __shfl_sync(0xffffffffu, iP, 31);
-            S_run += __shfl_sync(0xffffffffu, iS, 31);
+    }
+    est = warp_sum(est);
+    ntot = warp_sum(ntot);
+    if (lane == 0) tstamp(p, 0, 10);
+    const float target = fmaxf(1.f, (float)est / ((float)p.grid_s * kPlanItems));
+    bool bad = G > kPlanGroups || ntot > p.max_tiles;
+    // every group's positions: exclusive prefix sums over the groups, 32 at a time
+    long long run[7] = {0, 0, 0, 0, 0, 0, 0};
+    for (int g0 = 0; !bad && g0 < G; g0 += 32) {
+        const int g = g0 + lane;
+        long long v[7] = {0, 0, 0, 0, 0, 0, 0};
+        if (g < G) {
+            const GroupPlan gp = group_plan(p, ps.gr[g], ps.rp[g], target);
+            if (g < kPlanKept) ps.kept[g] = {gp.ntl, gp.base, gp.rem, gp.kc, gp.n_kc, gp.ks, gp.W, gp.n_units};
+            v[0] = two_way(gp, ORD_SH).before(gp.ntl);
+            v[1] = two_way(gp, ORD_EX).before(gp.ntl);
+            v[2] = two_way(gp, ORD_RD).before(gp.ntl);
+            v[3] = gp.ntl;
+            v[4] = (long long)gp.ntl * gp.n_kc;
+            v[5] = (long long)gp.ntl * gp.n_units;
+            v[6] = (long long)gp.n_kc * gp.R * gp.count;
         }
-        if (lane == 0) tstamp(p, 0, 11);
-        const bool bad = !fit || P_run > p.partial_cap || S_run > p.s_cap || sh_run >= (1ll << 31) ||
-                         ex_run >= (1ll << 31) || S_run >= (1ll << 31);
-        if (lane == 0) {
-            const int nt = bad ? 0 : t_run;
-            ps.nt = nt;
-            ps.bad = bad;
-            ps.T[0] = bad ? 0 : (int)sh_run;
-            ps.T[1] = bad ? 0 : (int)ex_run;
-            ps.T[2] = bad ? 0 : (int)(S_run / 16);
-            for (int k = 0; k < 3; ++k) ps.pos[k][nt] = ps.T[k];
-            ps.u0[nt] = bad ? 0 : u_run;
-            if (bad) atomicOr(p.err, kErrWorkspace);
-            p.plan_hdr[PL_TILES] = nt;
-            p.plan_hdr[PL_UNITS] = ps.u0[nt];
+        long long incl[7];
+#pragma unroll
+        for (int k = 0; k < 7; ++k) incl[k] = warp_inclusive(v[k]);
+        if (g < G) {
+            GroupPos &q = ps.pos[g];
+            q.sh = (int)(run[0] + incl[0] - v[0]);
+            q.ex = (int)(run[1] + incl[1] - v[1]);
+            q.rd = (int)(run[2] + incl[2] - v[2]);
+            q.t = (int)(run[3] + incl[3] - v[3]);
+            q.c = (int)(run[4] + incl[4] - v[4]);
+            q.u = (int)(run[5] + incl[5] - v[5]);
+            q.P = (int)(run[6] + incl[6] - v[6]);
         }
+#pragma unroll
+        for (int k = 0; k < 7; ++k) run[k] += __shfl_sync(0xffffffffu, incl[k], 31);
     }
-    __syncthreads();
-    const int nt = ps.nt;
-    // the expand's blocks split all but the last 1 / kExPoolDiv of its cost ahead of time and claim the
-    // units of that tail one by one (its claims look tiles up in a copy of u0 that holds kExUposCap tiles)
-    const int T_ex = nt <= kExUposCap ? ps.T[1] - ps.T[1] / kExPoolDiv : ps.T[1];
-    const Split ss(ps.T[0], p.grid_s), se(T_ex, p.grid_e), sr(ps.T[2], p.grid_s);
-    for (int c = tid; c <= p.grid_s; c += blockDim.x) {
-        p.sh_start[c] = block_start(ss, ps.T[0], c, nt, ps.pos[0], ps.per[0], ps.n[0]);
-        p.rd_start[c] = block_start(sr, ps.T[2], c, nt, ps.pos[2], ps.per[2], ps.n[2]);
+    bad = bad || run[6] > p.partial_cap || run[2] * 16 > p.s_cap || run[2] * 16 >= (1ll << 31);
+#pragma unroll
+    for (int k = 0; k < 7; ++k) bad = bad || run[k] >= (1ll << 31);
+    if (lane == 0) {
+        GroupPos &q = ps.pos[bad ? 0 : G];
+        q.sh = bad ? 0 : (int)run[0];
+        q.ex = bad ? 0 : (int)run[1];
+        q.rd = bad ? 0 : (int)run[2];
+        q.t = bad ? 0 : (int)run[3];
+        q.c = bad ? 0 : (int)run[4];
+        q.u = bad ? 0 : (int)run[5];
+        q.P = bad ? 0 : (int)run[6];
+        ps.G = bad ? 0 : G;
+        ps.bad = bad;
+        ps.target = target;
+        tstamp(p, 0, 11);
     }
-    for (int c = tid; c <= p.grid_e; c += blockDim.x) {
-        const int2 b = block_start(se, ps.T[1], c, nt, ps.pos[1], ps.per[1], ps.n[1]);
-        p.ex_start[c] = b;
-        if (c == p.grid_e) p.plan_hdr[PL_POOL_U] = ps.u0[b.x] + b.y;   // u0[nt] is the launch's unit count
+}
+
+// The record of tile t (t < the launch's tiles).
+__device__ TileRec plan_tile(const StreamParams &p, const PlanSmem &ps, int t)
+{
+    const int g = find_group(ps, -1, t);
+    const GroupPos &q = ps.pos[g];
+    const GroupPlan gp = load_group_plan(p, ps, g);
+    const int i = t - q.t, m = gp.base + (i < gp.rem ? 1 : 0);
+    TileRec r;
+    r.a = gp.a;
+    r.e = gp.e;
+    r.row0 = gp.row_off + i * gp.base + min(i, gp.rem);
+    r.m = m;
+    r.rp = gp.rp;
+    r.R = gp.R;
+    r.n_pad = npad16(m);
+    r.kc = gp.kc;
+    r.n_kc = gp.n_kc;
+    r.ks = gp.ks;
+    r.W = gp.W;
+    r.n_units = gp.n_units;
+    r.p_off = q.P + TwoWay{gp.n_kc * gp.R * (gp.base + 1), gp.n_kc * gp.R * gp.base, gp.rem}.before(i);
+    r.s_off = 16 * (q.rd + two_way(gp, ORD_RD).before(i));
+    r.c0 = q.c + i * gp.n_kc;
+    r.u0 = q.u + i * gp.n_units;
+    return r;
+}
+
+// The first (tile, item) at or past position lo of an order (the launch's end when lo is past the last).
+__device__ int2 plan_start(const StreamParams &p, const PlanSmem &ps, int order, int lo)
+{
+    const GroupPos &end = ps.pos[ps.G];
+    if (lo >= gpos_field(end, order)) return make_int2(end.t, 0);
+    const int g = find_group(ps, order, lo);
+    const GroupPos &q = ps.pos[g];
+    const GroupPlan gp = load_group_plan(p, ps, g);
+    const TwoWay tw = two_way(gp, order);
+    const int off = lo - gpos_field(q, order);
+    const int i = tw.find(off), m = gp.base + (i < gp.rem ? 1 : 0);
+    int per, n;
+    if (order == ORD_SH) {
+        per = chunk_cost(gp.kc, gp.R, m);
+        n = gp.n_kc;
+    } else if (order == ORD_EX) {
+        per = unit_cost(gp.W, gp.rp, m);
+        n = gp.n_units;
+    } else {
+        per = 1;
+        n = gp.R * npad16(m) / 8;
     }
+    const int j = (off - tw.before(i) + per - 1) / per;
+    const int t = q.t + i;
+    return j >= n ? make_int2(t + 1, 0) : make_int2(t, j);
 }
 
 // ===========================================================================
@@ -448,10 +498,13 @@ struct __align__(128) ShrinkSmem {
     union {
         // stage: A columns [ks/8][R][8], then the tile's x rows [m][ks + 8]
         unsigned char stage[kShStages][kShStageBytes];
-        PlanSmem plan;   // block 0, before the streams start
+        PlanSmem plan;   // while the block plans, before the streams start
     };
     uint64_t full[kShStages], empty[kShStages];
     int32_t xsrc[2][kTileRows];   // source rows of the producers' tiles, by tile parity
+    TileRec mytile[kMyTiles];     // records of the tiles of this block's chunks (when they are few enough)
+    int2 smeta[kShStages];        // the (tile, chunk) of every stage; tile -1 ends the sequence
+    int2 range[2];                // this block's first and end (tile, chunk)
     int32_t flag;
 };
 
@@ -486,13 +539,16 @@ __device__ __forceinline__ bool grid_barrier(const StreamParams &p, ShrinkSmem &
 struct ChunkWalk {
     int t, j, cur;
     int2 end;
+    const TileRec *mine;   // the block's own records, tile b0.x first (null: read the launch's records)
+    int t_base;
     TileRec tr;
-    __device__ __forceinline__ ChunkWalk(int2 b0, int2 b1) : t(b0.x), j(b0.y), cur(-1), end(b1) {}
+    __device__ __forceinline__ ChunkWalk(int2 b0, int2 b1, const TileRec *mine_)
+        : t(b0.x), j(b0.y), cur(-1), end(b1), mine(mine_), t_base(b0.x) {}
     __device__ __forceinline__ bool valid(const StreamParams &p)
     {
         if (!before(t, j, end)) return false;
         if (t != cur) {
-            tr = load_tile(p.tiles + t);
+            tr = mine ? mine[t - t_base] : load_tile(p.tiles + t);
             cur = t;
         }
         return true;
@@ -506,45 +562,53 @@ struct ChunkWalk {
     }
 };
 
-// Warps 8-11 (kShProd threads): every stage of this block's chunks into the ring.  Thread 0 of the group
-// copies the stage's A columns (one bulk copy); the group gathers the same K columns of the tile's x rows
-// as 16-byte cp.async pieces.  The stage's full barrier completes once the bulk copy's bytes and every
-// producer thread's pieces have landed.  One barrier per stage keeps the four warps in step (and lets them
-// leave together when a wait runs out); the tile's source rows are double-buffered by tile parity, so a
-// warp may write the next tile's rows while another still gathers the last stage of the previous tile.
-__device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1)
+// Warps 8-11 (kShProd threads): the block's chunks, stage by stage, into the ring, then an end mark.  Thread
+// 0 of the group copies a stage's A columns (one bulk copy) and writes its (tile, chunk); the group gathers
+// the same K columns of the tile's x rows as 16-byte cp.async pieces.  The stage's full barrier completes
+// once the bulk copy's bytes and every producer thread's pieces have landed.  One barrier per stage keeps
+// the four warps in step (and lets them leave together when a wait runs out); the tile's source rows are
+// double-buffered by tile parity, so a warp may write the next tile's rows while another still gathers the
+// last stage of the previous tile.
+__device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1,
+                                               const TileRec *mine)
 {
     const int gt = threadIdx.x - 32 * kShWarps, lane = threadIdx.x & 31;
     uint32_t s = 0;
     int cur = -1, par = 1;
-    for (ChunkWalk w(b0, b1); w.valid(p); w.next()) {
-        const TileRec &tr = w.tr;
+    // the next free stage for every producer thread (false: a wait ran out, and the group stops)
+    auto next_slot = [&]() -> bool {
+        bool got = true;
+        if (s >= kShStages) {
+            if (lane == 0)
+                got = mbar_wait_suspend(&sm.empty[s % kShStages], ((s / kShStages) - 1) & 1, p.timeout_ns, p.err);
+            got = __shfl_sync(0xffffffffu, got, 0);
+        }
+        return got;
+    };
+    // every stage of chunk j of tile t
+    auto stage_chunk = [&](int t, int j, const TileRec &tr) -> bool {
         bool fresh = false;
-        if (w.t != cur) {
-            cur = w.t;
+        if (t != cur) {
+            cur = t;
             par ^= 1;
             fresh = true;
         }
         const unsigned char *ablk =
             reinterpret_cast<const unsigned char *>(__ldg(p.a_ptr + tr.a * p.E_A + (p.E_A == 1 ? 0 : tr.e)));
-        const int k0 = w.j * tr.kc, kend = min(k0 + tr.kc, p.K);
+        const int k0 = j * tr.kc, kend = min(k0 + tr.kc, p.K);
         const int xoff = tr.R * tr.ks * 2, xstride = (tr.ks + 8) * 2;
-        bool ok = true;
         for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
             const int slot = s % kShStages;
-            bool got = true;
-            if (s >= kShStages) {
-                if (lane == 0) got = mbar_wait_suspend(&sm.empty[slot], ((s / kShStages) - 1) & 1, p.timeout_ns, p.err);
-                got = __shfl_sync(0xffffffffu, got, 0);
-            }
+            const bool got = next_slot();
             if (fresh) {
                 for (int r = gt; r < tr.m; r += kShProd) sm.xsrc[par][r] = __ldcg(p.rows + tr.row0 + r) / p.src_div;
                 fresh = false;
             }
-            if (!(ok = bar_and(2, kShProd, got))) break;
+            if (!bar_and(2, kShProd, got)) return false;
             const int kk = min(tr.ks, kend - kb);
             if (gt == 0) {
                 const uint32_t bytes = (uint32_t)tr.R * kk * 2;
+                sm.smeta[slot] = make_int2(t, j);
                 mbar_arrive_expect_tx(&sm.full[slot], bytes);
                 bulk_g2s(sm.stage[slot], ablk + (size_t)(kb / 8) * tr.R * 16, bytes, &sm.full[slot]);
                 if (s < 8) tstamp(p, 0, 12 + s);
@@ -556,7 +620,17 @@ __device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem
                          [&](int r) { return xk + (int64_t)xs[r] * ldx; });
             tc::cp_async_arrive_noinc(&sm.full[slot]);
         }
-        if (!ok) break;
+        return true;
+    };
+    bool ok = true;
+    for (ChunkWalk w(b0, b1, mine); ok && w.valid(p); w.next()) ok = stage_chunk(w.t, w.j, w.tr);
+    // the end mark: a stage with tile -1
+    if (ok && bar_and(2, kShProd, next_slot())) {
+        if (gt == 0) sm.smeta[s % kShStages] = make_int2(-1, 0);
+        bar_sync(2, kShProd);
+        if (gt == 0) mbar_arrive(&sm.full[s % kShStages]);
+        mbar_arrive(&sm.full[s % kShStages]);
+        ++s;
     }
     if (gt == 0)
         for (uint32_t q = s > kShStages ? s - kShStages : 0; q < s; ++q)
@@ -657,16 +731,22 @@ __device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &
     return true;
 }
 
-// Warps 0-7: every chunk of this block, stage by stage from the ring; each warp walks the chunks on its own.
-__device__ __forceinline__ void shrink_consume(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1)
+// Warps 0-7: the chunks the producers announce, stage by stage from the ring, until the end mark.  A
+// chunk's tile record is the block's own copy for its share, else the launch's.
+__device__ __forceinline__ void shrink_consume(const StreamParams &p, ShrinkSmem &sm, int2 b0, const TileRec *mine,
+                                               int n_my)
 {
     uint32_t s = 0;
-    int q = 0;
-    for (ChunkWalk cw(b0, b1); cw.valid(p); cw.next(), ++q) {
+    for (int q = 0;; ++q) {
+        const int slot = s % kShStages;
+        if (!mbar_wait_suspend(&sm.full[slot], (s / kShStages) & 1, p.timeout_ns, p.err)) break;
+        const int2 e = sm.smeta[slot];
+        if (e.x < 0) break;
+        const TileRec tr = mine && e.x - b0.x < n_my ? mine[e.x - b0.x] : load_tile(p.tiles + e.x);
         bool ok;
-        if (cw.tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, cw.tr, cw.j, s);
-        else if (cw.tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, cw.tr, cw.j, s);
-        else ok = shrink_chunk<4, 4>(p, sm, cw.tr, cw.j, s);
+        if (tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, tr, e.y, s);
+        else if (tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, tr, e.y, s);
+        else ok = shrink_chunk<4, 4>(p, sm, tr, e.y, s);
         if (!ok) break;
         if (threadIdx.x == 0 && q < 4) tstamp(p, 0, 3 + q);
     }
@@ -715,12 +795,75 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
     pdl_trigger();   // the expand may launch now; it waits for this grid before it reads anything
     if (tid == 0) tstamp(p, 0, 1);
     if (blockIdx.x == 0 && tid == 0) *p.ex_claim = 0;   // the expand of the launch before has ended
-    if (blockIdx.x == 0) make_plan(p, sm.plan);
-    if (grid_barrier(p, sm, 1)) {   // the plan is out
-        if (tid == 0) tstamp(p, 0, 2);
-        const int2 b0 = __ldcg(p.sh_start + blockIdx.x), b1 = __ldcg(p.sh_start + blockIdx.x + 1);
-        if (tid < kShWarps * 32) shrink_consume(p, sm, b0, b1);
-        else shrink_produce(p, sm, b0, b1);
+    if (tid < 32) plan_groups(p, sm.plan);
+    __syncthreads();
+    const PlanSmem &ps = sm.plan;
+    const GroupPos &tot = ps.pos[ps.G];
+    const int G = p.grid_s, c = blockIdx.x, nt = tot.t;
+    // this block's chunks (threads 0 and 32), then the records of their tiles (warp 0); the other warps write
+    // this block's share of the launch's plan, read after the shrink (S reduction, expand): the records of
+    // tiles c, c + G, ..., the first (tile, S chunk) this block reduces and the first unit of expand block c
+    const Split ss(tot.sh, G);
+    if (tid == 0) sm.range[0] = plan_start(p, ps, ORD_SH, ss.start(c));
+    if (tid == 32) sm.range[1] = plan_start(p, ps, ORD_SH, ss.start(c + 1));
+    if (tid >= 64)
+        for (int t = c + G * (tid - 64); t < nt; t += G * (blockDim.x - 64)) p.tiles[t] = plan_tile(p, ps, t);
+    if (tid == 64) {
+        const Split sr(tot.rd, G);
+        p.rd_start[c] = plan_start(p, ps, ORD_RD, sr.start(c));
+        if (c == G - 1) p.rd_start[G] = plan_start(p, ps, ORD_RD, tot.rd);
+    }
+    if (tid == 96) {
+        // the expand splits all but the last 1 / kExPoolDiv of its cost ahead of time and claims the units
+        // of that tail one by one (its claims look tiles up in a copy of u0 that holds kExUposCap tiles)
+        const Split se(nt <= kExUposCap ? tot.ex - tot.ex / kExPoolDiv : tot.ex, p.grid_e);
+        p.ex_start[c] = plan_start(p, ps, ORD_EX, se.start(c));
+        if (c == G - 1) {
+            const int2 b = plan_start(p, ps, ORD_EX, se.start(p.grid_e));
+            p.ex_start[p.grid_e] = b;
+            p.plan_hdr[PL_POOL_U] = (b.x < nt ? plan_tile(p, ps, b.x).u0 : tot.u) + b.y;
+        }
+    }
+    if (c == 0 && tid == 128) {
+        p.plan_hdr[PL_TILES] = nt;
+        p.plan_hdr[PL_UNITS] = tot.u;
+        if (ps.bad) atomicOr(p.err, kErrWorkspace);
+    }
+    __syncthreads();
+    const int2 b0 = sm.range[0], b1 = sm.range[1];
+    const int n_my = b1.x - b0.x + (b1.y > 0 ? 1 : 0);
+    const TileRec *mine = n_my <= kMyTiles ? sm.mytile : nullptr;
+    if (mine && tid < n_my) sm.mytile[tid] = plan_tile(p, ps, b0.x + tid);
+    __syncthreads();   // the block's records are in; the stages may overwrite the plan now
+    if (tid == 0) {
+        // this block's share of the launch's plan is out: its first arrival on the grid counter (thread 0 would
+        // wait for its first stage anyway)
+        tstamp(p, 0, 2);
+        __threadfence();
+        atomicAdd(p.cnt, 1);
+        // a block with more tiles than it keeps reads the launch's records, once every block has written its share
+        sm.flag = 1;
+        if (!mine) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_gpu(p.cnt) < G) {
+                if (globaltimer() - t0 > p.timeout_ns) {
+                    atomicOr(p.err, kErrTimeout);
+                    sm.flag = 0;
+                    break;
+                }
+                nanosleep_ns(32);
+            }
+            __threadfence();
+        }
+    }
+    bool go = true;
+    if (!mine) {   // block-uniform
+        __syncthreads();
+        go = sm.flag != 0;
+    }
+    if (go) {
+        if (tid < kShWarps * 32) shrink_consume(p, sm, b0, mine, n_my);
+        else shrink_produce(p, sm, b0, b1, mine);
         __syncwarp();
         if (tid == 0) tstamp(p, 0, 8);
     }
@@ -769,7 +912,6 @@ struct __align__(1024) ExpandSmem {
     uint64_t u0_ready;
     int32_t u0[kExUposCap + 1];                      // first unit of every tile, then the launch's unit count
     int32_t nt;
-    uint32_t obs_err;                                // the phase trace's own waits (never the launch's status)
     uint32_t tmem_base;
 };
 
@@ -865,7 +1007,6 @@ __device__ __forceinline__ void expand_lead(const StreamParams &p, ExpandSmem &s
         mt.w_eff = w_eff;
         const uint32_t bbytes = (uint32_t)((w_eff + 127) >> 7) * tr.rp * 256;
         if (i - 1 >= 8 && i - 1 < 12) tstamp(p, 1, 13 + (i - 1 - 8));
-        if (i - 1 >= 13 && i - 1 < 15) tstamp(p, 1, 29 + (i - 1 - 13));
         mbar_arrive_expect_tx(&sm.full_b[slot], bbytes);
         bulk_g2s(sm.bstage[slot], bblk + (size_t)(p.slice_tile_off[s] + cb * (tr.W >> 7)) * tr.rp * 256, bbytes,
                  &sm.full_b[slot]);
@@ -1020,7 +1161,6 @@ __device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm
     int prev_t = -1, prev_sb = -1;
     for (;; ++i) {
         const int slot = i % kExBStages;
-        if (i >= 8 && i < 12) tstamp(p, 2, 8 + (i - 8));
         if (!mbar_wait_suspend(&sm.full_b[slot], (i / kExBStages) & 1, p.timeout_ns, p.err)) break;
         const ExBMeta &mt = sm.bmeta[slot];
         const int t = mt.t, sb = mt.sb, n_pad = mt.n_pad, rp = mt.rp, w_eff = mt.w_eff;
@@ -1050,10 +1190,8 @@ __device__ __forceinline__ void expand_mma(const StreamParams &p, ExpandSmem &sm
                 tc::mma_bf16(sm.tmem_base + b * kExAccCols + q * n_pad, ad, bd, idesc, kk > 0 ? 1u : 0u);
             }
         }
-        if (i >= 8 && i < 12) tstamp(p, 2, 0 + (i - 8));
         tc::mma_commit(&sm.acc_full[b]);
         tc::mma_commit(&sm.empty_b[slot]);   // the B columns are free once these MMAs end
-        if (i >= 8 && i < 12) tstamp(p, 2, 4 + (i - 8));
     }
     // tensor memory is freed when the block ends: every MMA issued must be done by then
     if (i > 0) {
@@ -1170,7 +1308,7 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     __syncthreads();
     tc::fence_after_sync();
     pdl_wait();   // the plan, S and everything else of the shrink grid
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.cnt = 0;   // the shrink's grid barrier counter, for the next launch
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.cnt = 0;   // the shrink's grid counter, for the next launch
     const int2 b0 = __ldcg(p.ex_start + blockIdx.x), b1 = __ldcg(p.ex_start + blockIdx.x + 1);
     if (threadIdx.x == 0) tstamp(p, 1, 1);
     if (warp == 0) {
@@ -1190,15 +1328,6 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
         if (lane == 0) {
             sm.nt = nt;
             mbar_arrive(&sm.u0_ready);
-        }
-        if (p.trace != nullptr && lane < 2) {   // phase trace: when the B (lane 0) and y (lane 1) copies of units 8-11 land
-            // phases in order: a parity wait only tells a phase from the one before
-            uint64_t *bar = lane == 0 ? sm.full_b : sm.full_y;
-            const uint32_t n = lane == 0 ? kExBStages : kExYStages;
-            for (uint32_t i = 0; i < 12; ++i) {
-                if (!mbar_wait_suspend(&bar[i % n], (i / n) & 1, 100000, &sm.obs_err)) break;
-                if (i >= 8) tstamp(p, 1, (lane == 0 ? 9 : 21) + (i - 8));
-            }
         }
     } else if (warp < 8) {
         expand_produce_y(p, sm);

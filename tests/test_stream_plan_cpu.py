@@ -134,8 +134,10 @@ def check(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
     for key, pre in (("n_kc", sh_pre), ("n_units", ex_pre), ("s_items", rd_pre)):
         T = int(pre[-1])
         # the expand splits all but the last 1 / kExPoolDiv of its cost ahead of time; the units from block
-        # `grid`'s start on are claimed one by one (global unit index u0[tile] + unit)
-        T_split = T - T // C["kExPoolDiv"] if key == "n_units" and len(tiles) <= C["kExUposCap"] else T
+        # `grid`'s start on are claimed one by one (launch-wide index u0[tile] + unit)
+        T_split = T
+        if key == "n_units" and len(tiles) <= C["kExUposCap"]:
+            T_split = T - T // C["kExPoolDiv"]
         starts = [block_start(pre, tiles, T, grid, c, key, T_split) for c in range(grid + 1)]
         if T_split == T:
             assert starts[-1] == (len(tiles), 0)
@@ -147,7 +149,7 @@ def check(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
         every = [(t, j) for t in range(len(tiles)) for j in range(tiles[t][key])]
         assert seen + pool == every, key
         if key == "n_units":
-            u0 = np.concatenate([[0], np.cumsum([t["n_units"] for t in tiles])]).astype(np.int64)
+            u0 = np.concatenate([[0], np.cumsum([t[key] for t in tiles])]).astype(np.int64)
             g0 = int(u0[starts[grid][0]]) + starts[grid][1]
             for g in range(g0, int(u0[-1])):   # a claim's tile lookup
                 l = int(np.searchsorted(u0, g, side="right")) - 1
