@@ -317,13 +317,15 @@ lora_status lora_set_trace(void *d_trace, size_t bytes);
  * receives pre-made buffers), who can still pass their inputs and outputs.
  *
  * Every byte of scratch (segment table, hand-off partials and counters) is a
- * fixed array in this library, about 8.4 MiB, that each GPU which loads the
- * library holds until the process exits.  Limits: M <= 4096 tokens, and
- * R * (M * (ceil(K / kc) + 1) + 64 * min(M, L)) <= 2^21 partial floats, where
- * R is the table's largest A block (n_a * stored rank) and kc = clamp(floor(
- * 20480 / R) rounded down to a multiple of 64, 64, 448), the smallest K-chunk
- * the engine falls back to; larger calls return LORA_ERR_WORKSPACE before
- * launching anything.  Same argument rules as lora_apply (dense tables only).
+ * fixed array in this library, about 32.2 MiB, that each GPU which loads the
+ * library holds until the process exits.  Limits, checked before anything is
+ * launched: the table's adapters L + 1 <= 16000 (the segment build's key
+ * limit, else LORA_ERR_UNSUPPORTED); M <= 4096 tokens, and
+ * M * R * (ceil(K / 64) + 1) + 64 * R * min(M, L) <= 2^23 partial floats,
+ * where R is the table's largest A block (n_a * stored rank) and 64 the
+ * shortest K-chunk the engine cuts (else LORA_ERR_WORKSPACE).  Same argument
+ * rules as lora_apply (dense tables only).  The delta runs on the persistent
+ * engine (the streaming path of lora_apply needs the workspace's plan area).
  *
  * The first call on a device looks the array up (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  All

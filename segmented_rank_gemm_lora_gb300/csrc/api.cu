@@ -312,8 +312,8 @@ bool lora::ws_layout(int32_t max_M, int32_t L, int32_t topk, int32_t E, int32_t 
 {
     if (max_M < 1 || L < 1 || block_m < 0) return false;
     if (block_m > 0 && (topk < 1 || E < 1)) return false;
-    if (L + 1 > 16000) return false;
-    if (block_m > 0 && (int64_t)L * E + 1 > 16000) return false;
+    if (L + 1 > kMaxBuildKeys) return false;
+    if (block_m > 0 && (int64_t)L * E + 1 > kMaxBuildKeys) return false;
     WsLayout w{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -427,6 +427,18 @@ extern "C" lora_status lora_build_segments(const lora_workspace *ws, const int32
 
 // The streaming path (plan -> shrink -> expand) over the groups of the last build on `ws`.  Its plan, tile
 // records, S and fp32 partials live in the workspace's scratch area, its tile counters in the sync area.
+// The persistent engine's small-tile K-chunk when a block's share of the launch's A bytes is a staging
+// slot or more: the largest chunk of a 16-row tile (A chunk <= 40 KB, x rows <= 15 KB), in multiples of
+// 64 columns.  With smaller shares its chunks shrink, down to kEngineMinKc columns.
+constexpr int64_t kEngineMinKc = 64;
+static int64_t engine_small_kc(int64_t R)
+{
+    return std::max<int64_t>(kEngineMinKc, std::min<int64_t>(448, (20480 / R) / 64 * 64));
+}
+// Fp32 scratch the engine needs per row of small-tile work at A-block rows R, depth K and K-chunk kc: the
+// chunks' partials and the row's finished S.
+static int64_t engine_partials_per_row(int64_t R, int64_t K, int64_t kc) { return R * (ceil_div(K, kc) + 1); }
+
 static lora_status run_stream(lora_table t, const lora_workspace *ws, const WsLayout &w, bool moe, int32_t src_div,
                               const void *x, int64_t ldx, void *y, int64_t ldy, const float *row_weight,
                               int32_t tile_max, lora_stream_t stream)
@@ -510,14 +522,11 @@ static lora_status run_engine(lora_table t, const lora_workspace *ws, const WsLa
         if (!fused_ids && (path == 3 || (path == 0 && (moe || ws->max_M > 32))))
             return run_stream(t, ws, w, moe, src_div, x, ldx, y, ldy, row_weight, path == 3 ? 16 : 128, stream);
     }
-    // scratch needed per row of work at this table's largest A block, at the largest K-chunk of a
-    // 16-row small tile (x rows <= 15 KB, A chunk <= 40 KB), plus the row's finished S
-    {
-        const int64_t R = t->max_R;
-        int64_t kc = (20480 / R) / 64 * 64;
-        kc = std::max<int64_t>(64, std::min<int64_t>(448, kc));
-        if ((ceil_div(t->K, kc) + 1) * R > kPartialFloatsPerRow) return LORA_ERR_UNSUPPORTED;
-    }
+    // scratch per row of work at the K-chunk the engine's small tiles take whenever a block's share of A is
+    // a staging slot or more; with smaller shares the engine may cut shorter chunks, finds the scratch
+    // short and reports LORA_ERR_WORKSPACE through the status word
+    if (engine_partials_per_row(t->max_R, t->K, engine_small_kc(t->max_R)) > kPartialFloatsPerRow)
+        return LORA_ERR_UNSUPPORTED;
     DeviceInfo di;
     lora_status st = device_info(&di);
     if (st != LORA_OK) return st;
@@ -755,7 +764,7 @@ namespace {
 
 constexpr int32_t kStaticMaxM = 4096;                        // tokens per call
 constexpr int32_t kStaticMaxTiles = kStaticMaxM / kBgmvRows + kStaticMaxM;
-constexpr int64_t kStaticPartialFloats = 2 * 1024 * 1024;   // 8 MiB of hand-off partials
+constexpr int64_t kStaticPartialFloats = 8 * 1024 * 1024;   // 32 MiB of hand-off partials
 constexpr size_t kStaticHeader = 0;
 constexpr size_t kStaticPerm = 256;
 constexpr size_t kStaticSegments = kStaticPerm + (size_t)kStaticMaxM * 4;
@@ -795,17 +804,17 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
 {
     if (!valid_table(t) || M < 0 || (M > 0 && (!d_ids || !d_x || !d_y))) return LORA_ERR_INVALID_ARG;
     if (t->E_A != 1 || t->E_B != 1) return LORA_ERR_INVALID_ARG;
+    if (t->L + 1 > kMaxBuildKeys) return LORA_ERR_UNSUPPORTED;   // the segment build's key limit
     if (M > 0 && (ldx < t->K || ldy < t->N || ldx % 8 || ldy % 8 || !aligned16(d_x) || !aligned16(d_y)))
         return LORA_ERR_INVALID_ARG;
     if (M > kStaticMaxM) return LORA_ERR_WORKSPACE;
-    // the hand-off scratch of M rows at this table's largest A block must fit the fixed array even at
-    // the largest K-chunks the engine picks when scratch is short (16-row tiles: x rows <= 15 KB,
-    // A chunk <= 40 KB), plus the finished S of every tile
+    // the hand-off scratch of M rows at this table's largest A block must fit the fixed array at the
+    // shortest K-chunk the engine can cut (this entry point has no status word to report a shortfall),
+    // plus the S padding of up to one 64-row tile per group
     {
         const int64_t R = t->max_R;
-        int64_t kc = (20480 / R) / 64 * 64;
-        kc = std::max<int64_t>(64, std::min<int64_t>(448, kc));
-        const int64_t need = R * ((int64_t)M * (ceil_div(t->K, kc) + 1) + 64 * std::min<int64_t>(M, t->L));
+        const int64_t need = (int64_t)M * engine_partials_per_row(R, t->K, kEngineMinKc) +
+                             R * 64 * std::min<int64_t>(M, t->L);
         if (need > kStaticPartialFloats) return LORA_ERR_WORKSPACE;
     }
     unsigned char *base = nullptr;
@@ -839,6 +848,13 @@ extern "C" lora_status lora_apply_static_scratch(lora_table t, const int32_t *d_
     }
     p.m_ptr = header + H_M;
     p.m_mult = 1;
+    p.y_mult = 1;
+    if (M > 0 && t->N >= 128) {   // output tiles move as 2-D boxes only inside rows the build produced
+        st = encode_2d(d_y, std::max<int32_t>(M, 128), t->N, ldy, 128, &p.y_map_ld);
+        if (st == LORA_OK) st = encode_2d(d_y, std::max<int32_t>(M, 128), t->N, ldy, 32, &p.y_map_st);
+        if (st != LORA_OK) return st;
+        p.y_rows = M;
+    }
     p.a_ptr = t->d_a_ptr;
     p.b_ptr = t->d_b_ptr;
     p.rpad = t->d_rpad;

@@ -18,6 +18,9 @@ constexpr int kMaxRank = 64;           // largest true rank
 constexpr int kMaxSlices = 4;
 constexpr int kNTile = 128;            // B is stored in tiles of 128 output rows
 constexpr int kBgmvRows = 16;          // rows of one small tile
+// Keys the segment build sorts by, at most: adapters + 1 (the "none" key), or adapters x experts + 1.  The
+// block-wide build keeps three counters per key in its shared memory, which holds a little over 17000.
+constexpr int kMaxBuildKeys = 16000;
 constexpr int kEngineThreads = 256;
 constexpr int kHeaderInts = 16;
 constexpr int kTraceSlots = 32;        // uint64 phase stamps per thread block (lora_set_trace)
