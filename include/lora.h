@@ -198,11 +198,15 @@ lora_status lora_build_segments(const lora_workspace *ws, const int32_t *d_lora_
                                 const int32_t *d_topk_ids, const uint8_t *d_adapter_enabled, lora_stream_t stream);
 
 /*
- * Fused shrink -> expand -> add for every segment in one launch
- * ("vLLM-Ascend dynamic LoRA fused operator", section 2.3: per segment
- * X_seg A_i^T, then times B_i^T, added to the base rows, all segments in one
- * operator instance; section 4.2: the rank-sized intermediate accumulates in
- * fp32).  Reads the segment table of the last lora_build_segments on `ws`.
+ * Fused shrink -> expand -> add for every segment ("vLLM-Ascend dynamic LoRA
+ * fused operator", section 2.3: per segment X_seg A_i^T, then times B_i^T,
+ * added to the base rows, all segments in one operator instance; section 4.2:
+ * the rank-sized intermediate accumulates in fp32).  Reads the segment table
+ * of the last lora_build_segments on `ws`.  Workspaces of at most 32 tokens
+ * take one launch of the persistent engine (small tiles, the shrink-to-expand
+ * hand-off in L2); larger ones take the streaming path: a shrink kernel and an
+ * expand kernel chained with programmatic dependent launch (64-row tiles,
+ * tcgen05 expand).  LORA_OPT_PATH overrides the choice.
  *   d_x : bf16 [M][ldx] device, the layer input (K columns used).
  *   d_y : bf16 [M][ldy] device, in: the base output y_base, out: y (N columns).
  *         Rows of tokens without an adapter are not touched.
@@ -258,25 +262,33 @@ const char *lora_status_string(lora_status status);
 
 /*
  * Process-wide tuning knobs (not thread-safe against concurrent calls).
- *   LORA_OPT_PATH            : 0 auto (groups of at most LORA_OPT_TC_MIN_ROWS
- *                              rows on small 16-row tiles with warp-level MMAs,
- *                              the rest on 128-row tcgen05 tiles), 1 every group
- *                              on small tiles, 2 every group on 128-row tiles.
- *   LORA_OPT_TC_MIN_ROWS     : groups with more rows take 128-row tcgen05 tiles
+ *   LORA_OPT_PATH            : 0 auto: dense workspaces of at most 32 tokens
+ *                              on the persistent engine (groups of at most
+ *                              LORA_OPT_TC_MIN_ROWS rows on small 16-row tiles
+ *                              with warp-level MMAs, the rest on 128-row
+ *                              tcgen05 tiles), larger ones and every MoE delta
+ *                              on the streaming path (64-row tiles); 1 the
+ *                              engine, every group on small tiles; 2 the
+ *                              engine, every group on 128-row tiles; 3 the
+ *                              streaming path on 16-row tiles.
+ *   LORA_OPT_TC_MIN_ROWS     : engine groups with more rows take 128-row tiles
  *                              (default 32; groups whose A block has more than
  *                              128 rows, n_a * stored rank, switch at half).
  *   LORA_OPT_WAIT_TIMEOUT_NS : limit of every in-kernel wait (default 1 s).
- *   LORA_OPT_GRID_CTAS       : persistent grid size (0 = one wave over all SMs).
+ *   LORA_OPT_GRID_CTAS       : grid size of the engine and of both streaming
+ *                              kernels (0 = one block per SM).
  *   LORA_OPT_TEST_WITHHOLD_HANDOFF : test hook; nonzero makes the next launches
- *                              skip publishing shrink results so the waits of
- *                              the expand work run out (checks the timeout path).
+ *                              skip the shrink-to-expand hand-off (the engine
+ *                              does not publish its partials, the streaming
+ *                              expand never loads S), so the waits of the
+ *                              expand work run out (checks the timeout path).
  *   LORA_OPT_PDL             : 1 (default) launches the one-warp segment
- *                              build (dense, at most 32 tokens) with
- *                              programmatic stream serialization, and the
- *                              engine too when its workspace holds at most 32
- *                              tokens (dense): such a kernel may be scheduled
- *                              while the kernel before it on the stream
- *                              finishes, and waits on the device
+ *                              build (dense, at most 32 tokens), the engine
+ *                              when its workspace holds at most 32 tokens
+ *                              (dense) and both streaming kernels with
+ *                              programmatic stream serialization: such a kernel
+ *                              may be scheduled while the kernel before it on
+ *                              the stream finishes, and waits on the device
  *                              (griddepcontrol) before it reads anything; 0
  *                              launches every kernel in plain stream order.
  * Returns LORA_ERR_INVALID_ARG for an unknown option or value.
@@ -294,16 +306,25 @@ int64_t lora_get_option(int32_t option);
 
 /*
  * Phase tracing (off by default).  With a non-NULL device buffer, every later
- * lora_apply / lora_moe_delta launch writes, per thread block, 32 uint64
- * %globaltimer stamps (ns, 0 = phase not reached): 0 entry, 24 group
- * records loaded, 25 launch plan made, 1 work list ready, 2 first shrink item
- * started, 3..10 its pipeline stages issued (small tiles: 3 = operands
- * landed, 30 = partial computed), 11 its MMAs done, 12 its partial stored,
- * 13 it was published, 29 shrink items done, 26 first finish item started,
- * 27 its tile's partials all in, 28 its S stored, 14 first expand item's
- * tile ready, 15 its S in place, 16..23 the first four expand units
- * (operands landed, output written), 31 exit.  Blocks past bytes/256 are not
- * traced.  Pass NULL to switch tracing off.  Process-wide.
+ * lora_apply / lora_moe_delta launch writes uint64 %globaltimer stamps (ns,
+ * 0 = phase not reached).  Persistent engine: 32 per thread block, 0 entry,
+ * 24 group records loaded, 25 launch plan made, 1 work list ready, 2 first
+ * shrink item started, 3..10 its pipeline stages issued (small tiles: 3 =
+ * operands landed, 30 = partial computed), 11 its MMAs done, 12 its partial
+ * stored, 13 it was published, 29 shrink items done, 26 first finish item
+ * started, 27 its tile's partials all in, 28 its S stored, 14 first expand
+ * item's tile ready, 15 its S in place, 16..23 the first four expand units
+ * (operands landed, output written), 31 exit; blocks past bytes/256 are not
+ * traced.  Streaming path: [kernel][block][32] with kernel 0 the shrink and 1
+ * the expand, over bytes/768 blocks.  Shrink: 0 entry, 1 past its wait on
+ * the kernel before, 10 and 11 the plan's two passes over the groups done,
+ * 2 the block's share planned, 12..19 its first eight stages issued, 20..27
+ * the same stages landed, 3..6 its first four chunks done, 8 all its chunks
+ * done, 9 every block's partials in, 31 exit.  Expand: 0 entry, 1 past its
+ * wait on the shrink, 3 S loader started, 4 first S in place, 2 first MMA,
+ * 5..8 the MMA issuer found the B of units 8..11 landed, 25..28 and their
+ * accumulators free, 13..16 those units' B copies issued, 17..20 their y
+ * gathers issued, 31 exit.  Pass NULL to switch tracing off.  Process-wide.
  */
 lora_status lora_set_trace(void *d_trace, size_t bytes);
 

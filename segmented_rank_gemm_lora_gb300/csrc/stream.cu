@@ -9,40 +9,45 @@
 // pieces are accumulated; section 4.2: the rank-sized intermediate S
 // accumulates in fp32.
 //
-// GB300 form.  Every byte the delta needs crosses HBM once, so the kernels
-// are built to keep the memory system busy rather than the tensor cores.
-// Contiguous runs (packed A and B, S) move as bulk copies; gathered rows of
-// x and y move as 16-byte cp.async pieces from several warps, because the
-// bulk-copy engine spends a fixed time per copy and rows of a few hundred
-// bytes would leave it far below the memory's bandwidth.
-//   plan    one warp.  Cuts every group (an adapter segment, or an
+// GB300 form.  Every byte the delta needs crosses HBM once (B once per row
+// tile), so the kernels are built to keep the memory system busy rather than
+// the tensor cores.  Contiguous runs (packed A and B, S) move as bulk copies;
+// gathered rows of x and y move as 16-byte cp.async pieces from groups of four
+// warps, because one warp alone issues them far below the memory's rate and
+// the bulk-copy engine spends a fixed time per copy.
+//   plan    every block of the shrink, from the group table alone (no block
+//           waits for another): cuts every group (an adapter segment, or an
 //           (adapter, expert) group of the MoE variant) into row tiles of at
 //           most 64 rows, every tile's shrink into K-chunks (the same cut for
 //           all tiles of a group) and its expand into units of W output
-//           columns of one slice, and gives every block of the next two
-//           launches a contiguous run of that work of about equal bytes.
-//   shrink  one block per SM, eight warps, launched cooperatively.  An
-//           eight-stage ring: each stage is the chunk's next K columns of A
-//           (one bulk copy) and of the tile's x rows (cp.async pieces); the
-//           warps multiply them with m16n8k16 MMAs (the tile's rows as M, its
-//           rank columns as N) into fp32 registers, and each chunk's partial
-//           goes to L2 scratch.  Once every block has stored its partials (one
-//           grid-wide arrival count), the blocks split the sums of the partials
-//           in K order among themselves and store S as bf16 in the operand
-//           layout the expand reads.
-//   expand  one block per SM, warp-specialised.  Warp 0 streams the packed B
-//           columns of every unit into a five-stage ring; warp 1 waits for
-//           the shrink grid and then loads S; warp 2 issues tcgen05 MMAs
-//           D = B_unit S^T (the unit's output columns as the 128-row M
-//           operand, the tile's rows as N) into a tensor-memory accumulator,
-//           four of them in rotation; two warpgroups (warps 3-6 and 7-10) take
-//           alternate units: each gathers its units' y rows two units ahead,
-//           reads the accumulator, adds scale * D into the staged rows and
-//           stores them.  The hand-offs are mbarriers; no block ever
-//           waits on another block.
-// The expand may start before the shrink ends: everything it reads before its
-// wait on the shrink grid (plan, row list, B, y_base) was written by work
-// that had completed before the shrink passed its own wait.
+//           columns of one slice; a group's tiles differ by at most one row,
+//           so every tile's positions have a closed form.  Each block takes a
+//           contiguous run of chunks of about equal bytes, keeps the records
+//           of their tiles, and writes its share of the launch's records.
+//   shrink  one block per SM, launched cooperatively.  Warps 8-11 fill a
+//           six-stage ring: each stage is the chunk's next K columns of A
+//           (one bulk copy) and of the tile's x rows (cp.async pieces), with
+//           the stage's (tile, chunk); warps 0-7 multiply them with m16n8k16
+//           MMAs (the tile's rows as M, its rank columns as N) into fp32
+//           registers, and each chunk's partial goes to L2 scratch.  Once
+//           every block has stored its partials (a grid-wide arrival count),
+//           the blocks split the sums of the partials in K order among
+//           themselves and store S as bf16 in the operand layout the expand
+//           reads.
+//   expand  one block per SM, warp-specialised.  Warp 0 (the leader) walks
+//           the block's units (its share, then units of the launch's tail
+//           claimed one at a time) and hands each to the other roles through
+//           a shared-memory queue while it streams the unit's packed B columns
+//           into a three-stage ring; warp 1 loads S per (tile, slice block);
+//           warp 2 issues tcgen05 MMAs D = B_unit S^T (the unit's output
+//           columns as the 128-row M operand, the tile's rows as N) into one
+//           of four tensor-memory accumulators; warps 4-7 gather the unit's y
+//           rows into a six-slot ring; three epilogue warpgroups take units in
+//           rotation: each reads its accumulator, adds scale * D into the
+//           staged rows and stores them.  The hand-offs are mbarriers; a
+//           block waits on another only through the tail's claim counter.
+// The expand may start before the shrink ends: it waits for the shrink grid
+// before it reads anything the shrink writes.
 //
 // Summation orders depend only on a group's sizes (its K-chunk cut, the MMA
 // shapes), never on timing, on which block ran a piece, or on which rows

@@ -67,8 +67,9 @@ def check_close(got, ref, what=""):
 
 
 class forced_path:
-    """Context manager: LORA_OPT_PATH = path inside the block (0 the streaming path, 3 the streaming path
-    on 16-row tiles, 1 the persistent engine on small tiles, 2 the persistent engine on 128-row tiles)."""
+    """Context manager: LORA_OPT_PATH = path inside the block (0 automatic: the persistent engine for dense
+    workspaces of at most 32 tokens, else the streaming path; 1 the persistent engine on small tiles, 2 the
+    persistent engine on 128-row tiles, 3 the streaming path on 16-row tiles)."""
 
     def __init__(self, path):
         self.path = path
