@@ -320,9 +320,10 @@ int64_t lora_get_option(int32_t option);
  * the kernel before, 10 and 11 the plan's two passes over the groups done,
  * 2 the block's share planned, 12..19 its first eight stages issued, 20..27
  * the same stages landed, 3..6 its first four chunks done, 8 all its chunks
- * done, 9 every block's partials in, 31 exit.  Expand: 0 entry, 1 past its
- * wait on the shrink, 3 S loader started, 4 first S in place, 2 first MMA,
- * 5..8 the MMA issuer found the B of units 8..11 landed, 25..28 and their
+ * done, 31 exit.  Expand: 0 entry, 1 the launch's tile records out, 29 the
+ * shrink grid ended (the block's S sums start), 30 its S sums out, 3 every
+ * block's S sums out (S loader starts), 4 first S in place, 2 the MMA issuer
+ * found the first B landed, 5..8 the B of units 8..11 landed, 25..28 and their
  * accumulators free, 13..16 those units' B copies issued, 17..20 their y
  * gathers issued, 31 exit.  Pass NULL to switch tracing off.  Process-wide.
  */

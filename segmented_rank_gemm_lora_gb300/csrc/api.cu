@@ -488,16 +488,20 @@ static lora_status run_stream(lora_table t, const lora_workspace *ws, const WsLa
     unsigned char *area = at<unsigned char>(ws, w.partials);
     p.plan_hdr = reinterpret_cast<int32_t *>(area);
     p.tiles = reinterpret_cast<TileRec *>(area + 256);
-    p.sh_start = reinterpret_cast<int2 *>(area + 256 + (size_t)w.max_tiles * sizeof(TileRec));
-    p.ex_start = p.sh_start + (kStreamMaxGrid + 1);
+    p.ex_start = reinterpret_cast<int2 *>(area + 256 + (size_t)w.max_tiles * sizeof(TileRec));
     p.rd_start = p.ex_start + (kStreamMaxGrid + 1);
     p.s_area = area + plan_bytes;
     p.s_cap = (int64_t)s_cap;
     p.partials = reinterpret_cast<float *>(area + plan_bytes + s_cap);
     p.partial_cap = ((int64_t)w.partial_floats * 4 - (int64_t)plan_bytes - (int64_t)s_cap) / 4;
     p.max_tiles = w.max_tiles;
-    p.cnt = at<int32_t>(ws, w.sync);
-    p.ex_claim = p.plan_hdr + PL_CLAIM;   // not in the sync area: the persistent engine expects zeros there
+    // counters in the sync area, which the build zeroes and every launch leaves zeroed (as the persistent
+    // engine expects it): the shrink's arrival count, the expand's S count and its exit count
+    int32_t *sync = at<int32_t>(ws, w.sync);
+    p.cnt = sync;
+    p.done = sync + 1;
+    p.s_cnt = sync + 2;
+    p.ex_claim = p.plan_hdr + PL_CLAIM;
     const int grid = stream_grid(di.sms);
     const int64_t want = g_opt_grid.load();
     p.grid_s = p.grid_e = (want > 0 && want < grid) ? (int)want : grid;

@@ -153,9 +153,11 @@ struct StreamParams {
     // plan area (caller's workspace)
     int32_t *plan_hdr;               // [16]
     TileRec *tiles;                  // [max_tiles]
-    int2 *sh_start, *ex_start;       // [grid + 1] first (tile, item) of every block
-    int2 *rd_start;                  // [grid + 1] first (tile, S chunk) each shrink block reduces
-    int32_t *cnt;                    // the shrink's grid-barrier counter (reset by the expand)
+    int2 *ex_start;                  // [grid + 1] first (tile, unit) of every expand block
+    int2 *rd_start;                  // [grid + 1] first (tile, S chunk) of every expand block's S sums
+    int32_t *cnt;                    // shrink blocks whose share of the launch's tile records is out
+    int32_t *done;                   // expand blocks that have ended (the last one resets the counters)
+    int32_t *s_cnt;                  // expand blocks whose share of the S sums is out
     int32_t *ex_claim;               // plan_hdr + PL_CLAIM (reset by the shrink)
     float *partials;                 // fp32 chunk partials
     int64_t partial_cap;             // floats

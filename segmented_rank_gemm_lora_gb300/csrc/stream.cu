@@ -29,25 +29,27 @@
 //           (one bulk copy) and of the tile's x rows (cp.async pieces), with
 //           the stage's (tile, chunk); warps 0-7 multiply them with m16n8k16
 //           MMAs (the tile's rows as M, its rank columns as N) into fp32
-//           registers, and each chunk's partial goes to L2 scratch.  Once
-//           every block has stored its partials (a grid-wide arrival count),
-//           the blocks split the sums of the partials in K order among
-//           themselves and store S as bf16 in the operand layout the expand
-//           reads.
-//   expand  one block per SM, warp-specialised.  Warp 0 (the leader) walks
+//           registers, and each chunk's partial goes to L2 scratch.  A block
+//           leaves as soon as its chunks are done.
+//   expand  one block per SM, warp-specialised; its blocks start on the SMs
+//           that shrink blocks leave, once every shrink block has written its
+//           share of the launch's tile records.  Warp 0 (the leader) walks
 //           the block's units (its share, then units of the launch's tail
 //           claimed one at a time) and hands each to the other roles through
 //           a shared-memory queue while it streams the unit's packed B columns
-//           into a three-stage ring; warp 1 loads S per (tile, slice block);
-//           warp 2 issues tcgen05 MMAs D = B_unit S^T (the unit's output
-//           columns as the 128-row M operand, the tile's rows as N) into one
-//           of four tensor-memory accumulators; warps 4-7 gather the unit's y
-//           rows into a six-slot ring; three epilogue warpgroups take units in
-//           rotation: each reads its accumulator, adds scale * D into the
-//           staged rows and stores them.  The hand-offs are mbarriers; a
-//           block waits on another only through the tail's claim counter.
-// The expand may start before the shrink ends: it waits for the shrink grid
-// before it reads anything the shrink writes.
+//           into a three-stage ring; warps 4-7 gather the unit's y rows into a
+//           six-slot ring (neither needs the shrink).  Once the shrink grid
+//           has ended, the twelve epilogue warps of every block sum an equal
+//           run of the launch's S chunks (a tile's partials in chunk order,
+//           bf16 into the operand layout) and count their block in; warp 1
+//           then loads S per (tile, slice block); warp 2 issues tcgen05 MMAs
+//           D = B_unit S^T (the unit's output columns as the 128-row M
+//           operand, the tile's rows as N) into one of four tensor-memory
+//           accumulators; three epilogue warpgroups take units in rotation:
+//           each reads its accumulator, adds scale * D into the staged rows
+//           and stores them.  The hand-offs inside a block are mbarriers; the
+//           waits across blocks are bounded spins on counters that the last
+//           expand block to end resets for the next launch.
 //
 // Summation orders depend only on a group's sizes (its K-chunk cut, the MMA
 // shapes), never on timing, on which block ran a piece, or on which rows
@@ -98,6 +100,21 @@ __device__ __forceinline__ TileRec load_tile(const TileRec *t)
     r.n_kc = v2.x; r.ks = v2.y; r.W = v2.z; r.n_units = v2.w;
     r.p_off = v3.x; r.s_off = v3.y; r.c0 = v3.z; r.u0 = v3.w;
     return r;
+}
+
+// Bounded wait for *flag >= want (gpu-scope acquire); false (and the timeout bit) when it ran out.
+__device__ __forceinline__ bool wait_at_least(const StreamParams &p, const int32_t *flag, int want)
+{
+    if (ld_acquire_gpu(flag) >= want) return true;
+    const uint64_t t0 = globaltimer();
+    while (ld_acquire_gpu(flag) < want) {
+        if (globaltimer() - t0 > p.timeout_ns) {
+            atomicOr(p.err, kErrTimeout);
+            return false;
+        }
+        nanosleep_ns(64);
+    }
+    return true;
 }
 
 // (t, j) comes before the end marker e in the (tile, item) order
@@ -510,35 +527,8 @@ struct __align__(128) ShrinkSmem {
     TileRec mytile[kMyTiles];     // records of the tiles of this block's chunks (when they are few enough)
     int2 smeta[kShStages];        // the (tile, chunk) of every stage; tile -1 ends the sequence
     int2 range[2];                // this block's first and end (tile, chunk)
-    int32_t flag;
+    int32_t flag, last;
 };
-
-// Grid-wide barrier of the (cooperatively launched, so co-resident) shrink grid: the round-th arrival
-// of every block on a counter that the build zeroes and the expand resets.  Bounded: false when it ran out.
-__device__ __forceinline__ bool grid_barrier(const StreamParams &p, ShrinkSmem &sm, int round)
-{
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();   // release: this block's global writes before its arrival
-        atomicAdd(p.cnt, 1);
-        const int target = round * (int)gridDim.x;
-        bool in = ld_acquire_gpu(p.cnt) >= target;
-        if (!in) {
-            const uint64_t t0 = globaltimer();
-            while (!(in = ld_acquire_gpu(p.cnt) >= target)) {
-                if (globaltimer() - t0 > p.timeout_ns) {
-                    atomicOr(p.err, kErrTimeout);
-                    break;
-                }
-                nanosleep_ns(32);
-            }
-        }
-        __threadfence();
-        sm.flag = in ? 1 : 0;
-    }
-    __syncthreads();
-    return sm.flag != 0;
-}
 
 // Walks this block's chunks (tile, chunk) in order; the tile record is reloaded when the tile changes.
 struct ChunkWalk {
@@ -736,27 +726,6 @@ __device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &
     return true;
 }
 
-// Warps 0-7: the chunks the producers announce, stage by stage from the ring, until the end mark.  A
-// chunk's tile record is the block's own copy for its share, else the launch's.
-__device__ __forceinline__ void shrink_consume(const StreamParams &p, ShrinkSmem &sm, int2 b0, const TileRec *mine,
-                                               int n_my)
-{
-    uint32_t s = 0;
-    for (int q = 0;; ++q) {
-        const int slot = s % kShStages;
-        if (!mbar_wait_suspend(&sm.full[slot], (s / kShStages) & 1, p.timeout_ns, p.err)) break;
-        const int2 e = sm.smeta[slot];
-        if (e.x < 0) break;
-        const TileRec tr = mine && e.x - b0.x < n_my ? mine[e.x - b0.x] : load_tile(p.tiles + e.x);
-        bool ok;
-        if (tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, tr, e.y, s);
-        else if (tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, tr, e.y, s);
-        else ok = shrink_chunk<4, 4>(p, sm, tr, e.y, s);
-        if (!ok) break;
-        if (threadIdx.x == 0 && q < 4) tstamp(p, 0, 3 + q);
-    }
-}
-
 // S chunk i of a tile (16 bytes of its S layout: slice block sb, rank group kg, row): the tile's partials
 // of those 8 rank columns summed in chunk order, rounded once to bf16.  S is stored per slice block sb as
 // [rp / 8][n_pad][8], the operand layout the expand reads; rows past m are zero.
@@ -769,17 +738,52 @@ __device__ __forceinline__ void reduce_s_chunk(const StreamParams &p, const Tile
     if (row < tr.m) {
         const float *q = p.partials + tr.p_off + row * tr.R + sb * tr.rp + kg * 8;
         const int64_t cstride = (int64_t)tr.m * tr.R;
-        for (int c = 0; c < tr.n_kc; ++c, q += cstride) {
-            const float4 u = __ldcg(reinterpret_cast<const float4 *>(q));
-            const float4 w = __ldcg(reinterpret_cast<const float4 *>(q) + 1);
-            a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
-            a[4] += w.x; a[5] += w.y; a[6] += w.z; a[7] += w.w;
+        // the loads of eight chunks are in flight together; the sums still run in chunk order
+        for (int c0 = 0; c0 < tr.n_kc; c0 += 8, q += 8 * cstride) {
+            float4 u[8], w[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 *qc = reinterpret_cast<const float4 *>(q + c * cstride);
+                const bool in = c0 + c < tr.n_kc;
+                u[c] = in ? __ldcg(qc) : make_float4(0.f, 0.f, 0.f, 0.f);
+                w[c] = in ? __ldcg(qc + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                if (c0 + c < tr.n_kc) {
+                    a[0] += u[c].x; a[1] += u[c].y; a[2] += u[c].z; a[3] += u[c].w;
+                    a[4] += w[c].x; a[5] += w[c].y; a[6] += w[c].z; a[7] += w[c].w;
+                }
+            }
         }
     }
     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] = __float2bfloat16_rn(a[e]);
     *reinterpret_cast<uint4 *>(p.s_area + tr.s_off + (int64_t)i * 16) = *reinterpret_cast<const uint4 *>(o);
+}
+
+// Warps 0-7: the chunks the producers announce, stage by stage from the ring, until the end mark.  A
+// chunk's tile record is the block's own copy for its share, else the launch's.  The warps take every
+// decision together (bar.red), so that a wait that runs out ends them all.
+__device__ __forceinline__ void shrink_consume(const StreamParams &p, ShrinkSmem &sm, int2 b0, const TileRec *mine,
+                                               int n_my)
+{
+    constexpr int nthr = 32 * kShWarps;
+    uint32_t s = 0;
+    for (int q = 0;; ++q) {
+        const int slot = s % kShStages;
+        if (!bar_and(3, nthr, mbar_wait_suspend(&sm.full[slot], (s / kShStages) & 1, p.timeout_ns, p.err))) break;
+        const int2 e = sm.smeta[slot];
+        if (e.x < 0) break;
+        const TileRec tr = mine && e.x - b0.x < n_my ? mine[e.x - b0.x] : load_tile(p.tiles + e.x);
+        bool ok;
+        if (tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, tr, e.y, s);
+        else if (tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, tr, e.y, s);
+        else ok = shrink_chunk<4, 4>(p, sm, tr, e.y, s);
+        if (!bar_and(3, nthr, ok)) break;
+        if (threadIdx.x == 0 && q < 4) tstamp(p, 0, 3 + q);
+    }
 }
 
 __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_constant__ StreamParams p)
@@ -813,10 +817,11 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
     if (tid == 32) sm.range[1] = plan_start(p, ps, ORD_SH, ss.start(c + 1));
     if (tid >= 64)
         for (int t = c + G * (tid - 64); t < nt; t += G * (blockDim.x - 64)) p.tiles[t] = plan_tile(p, ps, t);
-    if (tid == 64) {
-        const Split sr(tot.rd, G);
+    if (tid == 64) {   // the first (tile, S chunk) of expand block c's share of the S sums
+        const Split sr(tot.rd, p.grid_e);
         p.rd_start[c] = plan_start(p, ps, ORD_RD, sr.start(c));
-        if (c == G - 1) p.rd_start[G] = plan_start(p, ps, ORD_RD, tot.rd);
+        if (c == G - 1)
+            for (int k = G; k <= p.grid_e; ++k) p.rd_start[k] = plan_start(p, ps, ORD_RD, sr.start(k));
     }
     if (tid == 96) {
         // the expand splits all but the last 1 / kExPoolDiv of its cost ahead of time and claims the units
@@ -872,18 +877,6 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
         __syncwarp();
         if (tid == 0) tstamp(p, 0, 8);
     }
-    // every block has stored its partials
-    if (!grid_barrier(p, sm, 2)) return;
-    if (tid == 0) tstamp(p, 0, 9);
-
-    // this block's share of S
-    const int2 r0 = __ldcg(p.rd_start + blockIdx.x), r1 = __ldcg(p.rd_start + blockIdx.x + 1);
-    for (int t = r0.x; t < r1.x || (t == r1.x && r1.y > 0); ++t) {
-        const TileRec tr = load_tile(p.tiles + t);
-        const int lo = t == r0.x ? r0.y : 0;
-        const int hi = t == r1.x ? r1.y : tr.R * tr.n_pad / 8;
-        for (int i = lo + tid; i < hi; i += kShThreads) reduce_s_chunk(p, tr, i);
-    }
     if (tid == 0) tstamp(p, 0, 31);
 }
 
@@ -917,6 +910,7 @@ struct __align__(1024) ExpandSmem {
     uint64_t u0_ready;
     int32_t u0[kExUposCap + 1];                      // first unit of every tile, then the launch's unit count
     int32_t nt;
+    int32_t flag;
     uint32_t tmem_base;
 };
 
@@ -1312,14 +1306,31 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    pdl_wait();   // the plan, S and everything else of the shrink grid
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.cnt = 0;   // the shrink's grid counter, for the next launch
-    const int2 b0 = __ldcg(p.ex_start + blockIdx.x), b1 = __ldcg(p.ex_start + blockIdx.x + 1);
+    // The expand starts while the shrink still runs (its blocks take the SMs that shrink blocks leave): it
+    // reads the launch's records once every shrink block has written its share (the shrink's first arrival
+    // count; the shrink grid is co-resident and never waits on this one), and only the S loader waits for
+    // the whole shrink grid.  The B and y copies need nothing the shrink writes.
+    if (threadIdx.x == 0) {
+        sm.flag = wait_at_least(p, p.cnt, p.grid_s);
+        __threadfence();
+    }
+    __syncthreads();
+    const bool go = sm.flag != 0;
+    const int2 b0 = go ? __ldcg(p.ex_start + blockIdx.x) : make_int2(0, 0);
+    const int2 b1 = go ? __ldcg(p.ex_start + blockIdx.x + 1) : make_int2(0, 0);
     if (threadIdx.x == 0) tstamp(p, 1, 1);
-    if (warp == 0) {
+    if (!go) {
+    } else if (warp == 0) {
         if (lane == 0) expand_lead(p, sm, b0, b1);
     } else if (warp == 1) {
-        if (lane == 0) expand_load_s(p, sm);
+        if (lane == 0) {
+            // S is summed by the epilogue warps of every expand block (below)
+            if (!p.withhold && wait_at_least(p, p.s_cnt, (int)gridDim.x)) {
+                __threadfence();
+                tc::fence_proxy_async_global();   // S was written by threads; the bulk copies read it
+            }
+            expand_load_s(p, sm);
+        }
     } else if (warp == 2) {
         if (lane == 0) expand_mma(p, sm);
     } else if (warp == 3) {
@@ -1337,6 +1348,28 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     } else if (warp < 8) {
         expand_produce_y(p, sm);
     } else {
+        // warps 8-19, idle until the first accumulator: once the shrink grid has ended, this block's equal
+        // run of the launch's S chunks (each the sum of a tile's partials in chunk order, eight chunks' loads
+        // in flight), then the block's arrival on the count the S loaders wait for
+        constexpr int nthr = 128 * kExGroups;
+        const int et = threadIdx.x - 256;
+        // (the share's range and its first tile record are the shrink plan's, out since the block started)
+        const int2 r0 = __ldcg(p.rd_start + blockIdx.x), r1 = __ldcg(p.rd_start + blockIdx.x + 1);
+        const TileRec tr0 = load_tile(p.tiles + min(r0.x, max(__ldcg(p.plan_hdr + PL_TILES) - 1, 0)));
+        pdl_wait();
+        if (et == 0) tstamp(p, 1, 29);
+        for (int t = r0.x; t < r1.x || (t == r1.x && r1.y > 0); ++t) {
+            const TileRec tr = t == r0.x ? tr0 : load_tile(p.tiles + t);
+            const int lo = t == r0.x ? r0.y : 0;
+            const int hi = t == r1.x ? r1.y : tr.R * tr.n_pad / 8;
+            for (int i = lo + et; i < hi; i += nthr) reduce_s_chunk(p, tr, i);
+        }
+        bar_sync(4, nthr);
+        if (et == 0) {
+            __threadfence();
+            atomicAdd(p.s_cnt, 1);
+            tstamp(p, 1, 30);
+        }
         expand_epilogue(p, sm, (warp - 8) >> 2);
     }
     __syncwarp();
@@ -1345,6 +1378,20 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     if (warp == 2) {
         tc::fence_after_sync();
         tc::tmem_dealloc(sm.tmem_base, kExTmemCols);
+    }
+    // the last block out resets the launch's counters for the next launch (the shrink grid has ended: every
+    // block waits for it here, most already did for their S sums)
+    if (threadIdx.x == 0) {
+        pdl_wait();
+        __threadfence();
+        sm.flag = atomicAdd(p.done, 1) == (int)gridDim.x - 1;
+        __threadfence();
+    }
+    __syncthreads();
+    if (sm.flag && threadIdx.x == 0) {
+        *p.cnt = 0;
+        *p.s_cnt = 0;
+        *p.done = 0;
     }
     if (threadIdx.x == 0) tstamp(p, 1, 31);
 }

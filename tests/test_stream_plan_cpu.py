@@ -127,11 +127,7 @@ def walk(start, end, tiles, key):
 
 def check(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
     tiles, sh_pre, ex_pre = plan(groups, ranks, K, slice_n, n_a, grid, tile_max)
-    for t in tiles:
-        t["s_items"] = t["R"] * t["n_pad"] // 8
-    rd = [t["s_items"] for t in tiles]
-    rd_pre = np.concatenate([[0], np.cumsum(rd)]).astype(np.int64)
-    for key, pre in (("n_kc", sh_pre), ("n_units", ex_pre), ("s_items", rd_pre)):
+    for key, pre in (("n_kc", sh_pre), ("n_units", ex_pre)):
         T = int(pre[-1])
         # the expand splits all but the last 1 / kExPoolDiv of its cost ahead of time; the units from block
         # `grid`'s start on are claimed one by one (launch-wide index u0[tile] + unit)
