@@ -57,6 +57,8 @@ def _load():
             lib.oracle_lora_apply.restype = ctypes.c_int
             lib.oracle_lora_apply.argtypes = [_I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                               _P, _I64, _P, _I64, _P]
+            lib.oracle_matmul_bt.restype = None
+            lib.oracle_matmul_bt.argtypes = [_I32, _I32, _I32, _P, _I64, _P, _I64, _P]
             lib.oracle_build_segments.restype = ctypes.c_int
             lib.oracle_build_segments.argtypes = [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]
             lib.oracle_moe_align.restype = ctypes.c_int
@@ -109,6 +111,29 @@ def lora_apply(ids, x, y_base, A: Sequence[np.ndarray], B: Sequence[np.ndarray],
     bad = lib.oracle_lora_apply(M, K, len(slice_n), _ptr(slice_n), n_a, len(ranks), _ptr(ranks), _ptr(scales),
                                 pa, pb, _ptr(ids), _ptr(en), _ptr(x), K, _ptr(y_base), N, _ptr(out))
     return out, int(bad)
+
+
+def matmul_bt(x, W):
+    """Base projection x W^T (float64 [M, N]) of bf16 bits x [M, K] and W [N, K]."""
+    lib = _load()
+    x = _c(x, np.uint16)
+    W = _c(W, np.uint16)
+    M, K = x.shape
+    N = W.shape[0]
+    assert W.shape == (N, K)
+    out = np.empty((M, N), np.float64)
+    lib.oracle_matmul_bt(M, N, K, _ptr(x), K, _ptr(W), K, _ptr(out))
+    return out
+
+
+def lora_linear(ids, x, W, A: Sequence[np.ndarray], B: Sequence[np.ndarray], ranks, scales, slice_n,
+                n_a: Optional[int] = None):
+    """A LoRA linear layer ("vLLM-Ascend dynamic LoRA fused operator", section 3.3): the base projection
+    x W^T plus every token's LoRA delta, as float64 [M, N]; returns (y, bad_id_count)."""
+    M = np.asarray(x).shape[0]
+    N = int(np.sum(slice_n))
+    delta, bad = lora_apply(ids, x, np.zeros((M, N), np.uint16), A, B, ranks, scales, slice_n, n_a)
+    return matmul_bt(x, W) + delta, bad
 
 
 def build_segments(ids, L: int, enabled=None):

@@ -21,6 +21,8 @@
  *        reduce), LoRAInfo weight shapes, moe_lora_align_block_size.
  *   [P5] "[SGLang] LoRA Layers: QKV, Gate/Up" (secrett2633 blog): stacked
  *        projections, A = (n*r, in), B = (sum of slice widths, r).
+ *   [P1] 3.3 the LoRA linear layer: the base matmul of the layer's input with
+ *        its weight, plus the LoRA delta (issued beside it or fused with it).
  *
  * Readings taken where the pages are silent:
  *   - a per-adapter scale multiplies the expand result (1.0 reproduces [P1]);
@@ -41,6 +43,22 @@ static double bf(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * Base projection of a LoRA linear layer, [P1] 3.3: out[t][n] = sum_k x[t,k] * W[n,k]
+ * (x: bf16 [M][ldx], W: bf16 [N][ldw], both K columns used; out: double [M][N]).
+ */
+void oracle_matmul_bt(int32_t M, int32_t N, int32_t K, const uint16_t *x, int64_t ldx, const uint16_t *W,
+                      int64_t ldw, double *out)
+{
+    for (int32_t t = 0; t < M; ++t) {
+        for (int32_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < K; ++k) acc += bf(x[(int64_t)t * ldx + k]) * bf(W[(int64_t)n * ldw + k]);
+            out[(int64_t)t * N + n] = acc;
+        }
+    }
 }
 
 /*
