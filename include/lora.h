@@ -253,6 +253,30 @@ lora_status lora_moe_delta(lora_table table, int32_t stage, const lora_workspace
                            int64_t ld_in, void *d_cache, int64_t ld_cache, const float *d_topk_weights,
                            lora_stream_t stream);
 
+/*
+ * A LoRA linear layer in one kernel ("vLLM-Ascend dynamic LoRA fused
+ * operator", section 3.3: the custom linear layer runs the base matmul and
+ * the LoRA operator, merged into one fused operator):
+ *   y[t] = x[t] W^T + scale_i (x[t] A_i^T) B_i^T   for tokens with adapter i,
+ *   y[t] = x[t] W^T                                 for tokens without one,
+ * over the segment table of the last lora_build_segments on `ws` (dense).
+ *   d_x : bf16 [M][ldx] device, the layer input (K columns used).
+ *   d_w : bf16 [N][ldw] device, the base weight (row n = output column n, K
+ *         columns used; N = the table's sum of slice widths).
+ *   d_y : bf16 [M][ldy] device, out: y (N columns).  It is written, not read:
+ *         no base output is needed.  Rows of tokens past the last build's M
+ *         are not touched.
+ * The base product and S = x A_i^T accumulate in fp32 in one pass over x; S
+ * is scaled and rounded once to bf16, and S B_i^T is added to the fp32
+ * accumulator before the one rounding of y to bf16.
+ * ldx, ldw >= K and ldy >= N, all multiples of 8; d_x, d_w and d_y 16-byte
+ * aligned.  Errors (synchronous): LORA_ERR_INVALID_ARG (also a MoE table or
+ * table L != ws->L), LORA_ERR_UNSUPPORTED (more than 65535 token tiles).
+ * Device-side: LORA_ERR_TIMEOUT via lora_get_status.
+ */
+lora_status lora_linear(lora_table table, const lora_workspace *ws, const void *d_x, int64_t ldx, const void *d_w,
+                        int64_t ldw, void *d_y, int64_t ldy, lora_stream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace's sticky device error
  * word, and return the most severe error seen since the last call (LORA_OK if
  * none). */

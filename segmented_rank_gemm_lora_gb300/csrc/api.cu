@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "linear.h"
 
 using namespace lora;
 
@@ -29,6 +30,7 @@ std::atomic<int64_t> g_trace_bytes{0};
 struct DeviceInfo {
     int sms = 0;
     int engine_blocks_per_sm = 0;
+    int max_dyn_smem = 0;               // opt-in shared memory per block
     bool attr_done = false;
 };
 std::mutex g_dev_mu;
@@ -100,6 +102,15 @@ lora_status device_info(DeviceInfo *out)
                                                           kEngineThreads, smem) != cudaSuccess)
             return LORA_ERR_CUDA;
         if (d.engine_blocks_per_sm < 1) return LORA_ERR_UNSUPPORTED;
+        int optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, linear_kernel_ptr()) != cudaSuccess)
+            return LORA_ERR_CUDA;
+        d.max_dyn_smem = optin - (int)fa.sharedSizeBytes;   // what the fused linear kernel may take
+        if (cudaFuncSetAttribute(linear_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_dyn_smem) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
         d.attr_done = true;
     }
     *out = d;
@@ -672,6 +683,61 @@ extern "C" lora_status lora_moe_delta(lora_table t, int32_t stage, const lora_wo
     const int32_t src_div = stage == LORA_MOE_GATE_UP ? ws->topk : 1;
     const int64_t in_rows = stage == LORA_MOE_GATE_UP ? (int64_t)ws->max_M : (int64_t)ws->max_M * ws->topk;
     return run_engine(t, ws, w, true, src_div, d_in, ld_in, in_rows, d_cache, ld_cache, d_topk_weights, stream);
+}
+
+extern "C" lora_status lora_linear(lora_table t, const lora_workspace *ws, const void *d_x, int64_t ldx, const void *d_w,
+                                   int64_t ldw, void *d_y, int64_t ldy, lora_stream_t stream)
+{
+    if (!valid_table(t) || !d_x || !d_w || !d_y) return LORA_ERR_INVALID_ARG;
+    WsLayout w;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    if (ws->L != t->L || t->E_A != 1 || t->E_B != 1) return LORA_ERR_INVALID_ARG;
+    if (ldx < t->K || ldw < t->K || ldy < t->N || ldx % 8 || ldw % 8 || ldy % 8 || !aligned16(d_x) ||
+        !aligned16(d_w) || !aligned16(d_y))
+        return LORA_ERR_INVALID_ARG;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != LORA_OK) return st;
+    // token tiles: every segment cut into 128-row tiles, then the tokens without an adapter
+    const int64_t row_tiles = ceil_div(ws->max_M, kLinearRows) + w.seg_capacity + 1;
+    if (row_tiles > 65535 || t->b_tiles < 1) return LORA_ERR_UNSUPPORTED;
+    const int stage = linear_stage_bytes(t->max_R);
+    const int budget = di.max_dyn_smem - kLinearBTileBytes - 1024;   // the B tile and the stages' alignment
+    const int stages = std::min(4, budget / stage);
+    if (stages < 2) return LORA_ERR_UNSUPPORTED;
+    LinearParams p{};
+    st = encode_2d(d_w, t->N, t->K, ldw, kLinearCols, &p.w_map);
+    if (st != LORA_OK) return st;
+    p.x = static_cast<const __nv_bfloat16 *>(d_x);
+    p.ldx = ldx;
+    p.y = static_cast<__nv_bfloat16 *>(d_y);
+    p.ldy = ldy;
+    p.a_ptr = t->d_a_ptr;
+    p.b_ptr = t->d_b_ptr;
+    p.rpad = t->d_rpad;
+    p.scale = t->d_scale;
+    p.L = t->L;
+    p.K = t->K;
+    p.n_a = t->n_a;
+    p.n_slices = t->n_slices;
+    p.tiles = t->b_tiles;
+    for (int s = 0; s < kMaxSlices; ++s) {
+        p.slice_n[s] = t->slice_n[s];
+        p.slice_off[s] = t->slice_off[s];
+        p.slice_tile_off[s] = t->slice_tile_off[s];
+    }
+    int32_t *header = at<int32_t>(ws, w.header);
+    p.header = header;
+    p.perm = at<int32_t>(ws, w.perm);
+    p.segments = at<int4>(ws, w.segments);
+    p.stages = stages;
+    p.stage_bytes = stage;
+    p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
+    p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
+    const size_t smem = (size_t)stages * stage + kLinearBTileBytes + 1024;
+    return cuda_status(launch_linear(p, dim3((unsigned)t->b_tiles, (unsigned)row_tiles), smem,
+                                     reinterpret_cast<cudaStream_t>(stream), g_opt_pdl.load() != 0));
 }
 
 extern "C" lora_status lora_get_status(const lora_workspace *ws, lora_stream_t stream)

@@ -29,7 +29,7 @@ LORA_OPT_PATH, LORA_OPT_TC_MIN_ROWS, LORA_OPT_WAIT_TIMEOUT_NS, LORA_OPT_GRID_CTA
 EXPORTED = ["lora_pack_weights", "lora_table_destroy", "lora_table_info", "lora_table_stored_rank",
             "lora_workspace_bytes", "lora_workspace_layout", "lora_build_segments", "lora_apply",
             "lora_moe_delta", "lora_get_status", "lora_status_string", "lora_set_option", "lora_get_option",
-            "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch", "lora_build_and_apply"]
+            "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch", "lora_build_and_apply", "lora_linear"]
 
 
 class LoraError(RuntimeError):
@@ -101,6 +101,7 @@ def load(build_if_missing: bool = False):
         "lora_set_trace": (_c_i32, [P, _c_sz]),
         "lora_apply_static_scratch": (_c_i32, [P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
         "lora_build_and_apply": (_c_i32, [P, P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
+        "lora_linear": (_c_i32, [P, P, P, _c_i64, P, _c_i64, P, _c_i64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -299,6 +300,19 @@ def lora_moe_delta(table: Table, stage: int, ws: Workspace, inp: torch.Tensor, c
         w = topk_weights.data_ptr()
     _check(load().lora_moe_delta(table.handle, int(stage), ws.ref, inp.data_ptr(), inp.stride(0), cache.data_ptr(),
                                  cache.stride(0), w, _stream(stream)), "lora_moe_delta")
+
+
+def lora_linear(table: Table, ws: Workspace, x: torch.Tensor, W: torch.Tensor, y: torch.Tensor, stream=None):
+    """y (bf16 [M, N]) = x W^T + per-token LoRA delta of x (bf16 [M, K]), in one kernel; W bf16 [N, K]."""
+    _bf16_dev(x, "x")
+    _bf16_dev(W, "W")
+    _bf16_dev(y, "y")
+    if x.stride(1) != 1 or W.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("x, W and y need unit column stride")
+    if ws.built_M is not None and (x.shape[0] < ws.built_M or y.shape[0] < ws.built_M):
+        raise ValueError("x and y need the %d rows of the last lora_build_segments" % ws.built_M)
+    _check(load().lora_linear(table.handle, ws.ref, x.data_ptr(), x.stride(0), W.data_ptr(), W.stride(0),
+                              y.data_ptr(), y.stride(0), _stream(stream)), "lora_linear")
 
 
 def lora_get_status(ws: Workspace, stream=None) -> int:
