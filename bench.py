@@ -568,6 +568,117 @@ def measure(config, K, W, args, torch, lora, dev, world, e2e_steps, clocks=None)
     return out
 
 
+LINEAR_WORKLOAD = ("linear_prefill: the prefill batch through lora_linear (base projection x W^T with a random "
+                   "bf16 W [4096][4096] and the LoRA delta in one kernel, y written, not read)")
+
+
+def measure_linear(K, W, args, torch, lora, dev, e2e_steps):
+    """The fused LoRA linear layer (lora_linear) on the prefill batch: K timed steps (build + linear) as
+    CUDA-graph replays over rotating input sets (x, W, ids, table) larger than L2, the linear kernel alone,
+    the same layer as a cuBLAS projection (torch.matmul) followed by lora_apply for comparison, and the
+    end-to-end leg (x and ids in from pinned memory, y out)."""
+    sets = []
+    R = 7
+    for j in range(R):
+        p = make_problem("prefill", 1000 + j, base="zero")
+        g = torch.Generator(device=dev).manual_seed(77 + j)
+        s = {"p": p,
+             "table": lora.lora_pack_weights([_to_dev(a, torch, dev) for a in p.A], [_to_dev(b, torch, dev) for b in p.B],
+                                             p.ranks, p.scales, p.K, p.slice_n, p.n_a),
+             "ws": lora.Workspace(p.M, p.L, device=dev),
+             "ids": torch.from_numpy(p.ids).to(dev), "x": _to_dev(p.x, torch, dev),
+             "W": (torch.randn(p.N, p.K, device=dev, generator=g) / p.K ** 0.5).to(torch.bfloat16),
+             "y": torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)}
+        sets.append(s)
+    torch.cuda.synchronize()
+
+    def step(s, build=True, fused=True):
+        if build:
+            lora.lora_build_segments(s["ws"], s["ids"])
+        if fused:
+            lora.lora_linear(s["table"], s["ws"], s["x"], s["W"], s["y"])
+        else:
+            torch.matmul(s["x"], s["W"].t(), out=s["y"])
+            lora.lora_apply(s["table"], s["ws"], s["x"], s["y"])
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):   # eager runs of both forms first (cuBLAS sets up outside any capture)
+        for s in sets:
+            step(s, fused=False)
+            step(s)
+    torch.cuda.synchronize()
+    for s in sets:
+        if lora.lora_get_status(s["ws"]) != lora.LORA_OK:
+            raise RuntimeError("linear: device status")
+
+    def graph(build, fused):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in sets:
+                step(s, build, fused)
+        return g
+
+    def timed(g, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, W // R + 1)):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * R)
+
+    reps = max(1, K // R)
+    step_ms = timed(graph(True, True), reps)
+    kernel_ms = timed(graph(False, True), reps)
+    unfused_ms = timed(graph(False, False), reps)
+    p = sets[0]["p"]
+    _, lflops = dense_algorithmic(p)
+    flops = 2.0 * p.M * p.N * p.K + lflops
+    active = sorted(set(int(i) for i in p.ids if 0 <= i < p.L))
+    # the active adapters' A and B, x and W read once, y written once, the ids
+    nbytes = sum(2 * (p.A[i].size + p.B[i].size) for i in active) + 2 * (p.M * p.K + p.N * p.K + p.M * p.N) + 4 * p.M
+    _, tc_peak, src = peaks()
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                "traffic": None, "kernel": "linear_kernel", "kernel_ms": kernel_ms, "algorithmic_bytes": nbytes,
+                "algorithmic_flops": flops, "peak_source": src + " (burst)",
+                "unfused_ms": unfused_ms, "unfused": "torch.matmul (cuBLAS) x W^T, then lora_apply on y"}
+    # end to end: x and ids in from pinned memory, build + linear, y out; one step after another
+    hx = [s["x"].cpu().pin_memory() for s in sets]
+    hi = [s["ids"].cpu().pin_memory() for s in sets]
+    hy = [torch.empty_like(s["y"], device="cpu", pin_memory=True) for s in sets]
+    n = max(1, e2e_steps)
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            s = sets[i % R]
+            s["x"].copy_(hx[i % R], non_blocking=True)
+            s["ids"].copy_(hi[i % R], non_blocking=True)
+            step(s)
+            hy[i % R].copy_(s["y"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n
+    tokens = p.M
+    out = {"value": tokens / (step_ms / 1e3), "unit": "tokens/s", "ms_per_step": step_ms, "steps": reps * R,
+           "kernel_ms": kernel_ms, "roofline": roofline,
+           "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "steps": n,
+                   "h2d_bytes_per_step": hx[0].numel() * 2 + hi[0].numel() * 4, "d2h_bytes_per_step": hy[0].numel() * 2,
+                   "path": "public API calls with host-resident x and ids, one step after another on one stream"},
+           "gpu_launches": 2 * reps * R, "workload": LINEAR_WORKLOAD}
+    for s in sets:
+        s["table"].destroy()
+    del sets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 WORKLOADS = ("decode", "prefill", "stacked_qkv", "stacked_gate_up", "stacked_down", "moe")
 
 
@@ -593,6 +704,8 @@ def run_ours(args, world, rank, local):
             per[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "kernel_ms", "roofline", "e2e",
                                             "gpu_launches")}
             per[name]["workload"] = CONFIGS[name]
+        per["linear_prefill"] = measure_linear(max(49, min(K, args.workload_steps)), W, args, torch, lora, dev,
+                                               min(args.workload_steps, 20))
 
     cpu = cpu_baseline(args.config, args.cpu_seconds) if (rank == 0 and world == 1 and args.cpu_seconds > 0) else None
     if rank == 0:

@@ -701,13 +701,20 @@ extern "C" lora_status lora_linear(lora_table t, const lora_workspace *ws, const
     if (st != LORA_OK) return st;
     // token tiles: every segment cut into 128-row tiles, then the tokens without an adapter
     const int64_t row_tiles = ceil_div(ws->max_M, kLinearRows) + w.seg_capacity + 1;
-    if (row_tiles > 65535 || t->b_tiles < 1) return LORA_ERR_UNSUPPORTED;
+    int32_t ctile_off[kMaxSlices] = {0};
+    int64_t col_tiles = 0;
+    for (int s = 0; s < t->n_slices; ++s) {
+        ctile_off[s] = (int32_t)col_tiles;
+        col_tiles += ceil_div(t->slice_n[s], kLinearCols);
+    }
+    if (row_tiles > 65535 || col_tiles < 1 || col_tiles > INT32_MAX) return LORA_ERR_UNSUPPORTED;
     const int stage = linear_stage_bytes(t->max_R);
     const int budget = di.max_dyn_smem - kLinearBTileBytes - 1024;   // the B tile and the stages' alignment
-    const int stages = std::min(4, budget / stage);
+    const int stages = std::min(kLinearMaxStages, budget / stage);
     if (stages < 2) return LORA_ERR_UNSUPPORTED;
     LinearParams p{};
     st = encode_2d(d_w, t->N, t->K, ldw, kLinearCols, &p.w_map);
+    if (st == LORA_OK) st = encode_2d(d_x, std::max<int64_t>(ws->max_M, kLinearRows), t->K, ldx, kLinearRows, &p.x_map);
     if (st != LORA_OK) return st;
     p.x = static_cast<const __nv_bfloat16 *>(d_x);
     p.ldx = ldx;
@@ -721,11 +728,12 @@ extern "C" lora_status lora_linear(lora_table t, const lora_workspace *ws, const
     p.K = t->K;
     p.n_a = t->n_a;
     p.n_slices = t->n_slices;
-    p.tiles = t->b_tiles;
+    p.tiles = (int32_t)col_tiles;
     for (int s = 0; s < kMaxSlices; ++s) {
         p.slice_n[s] = t->slice_n[s];
         p.slice_off[s] = t->slice_off[s];
         p.slice_tile_off[s] = t->slice_tile_off[s];
+        p.slice_ctile_off[s] = ctile_off[s];
     }
     int32_t *header = at<int32_t>(ws, w.header);
     p.header = header;
@@ -736,7 +744,7 @@ extern "C" lora_status lora_linear(lora_table t, const lora_workspace *ws, const
     p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
     p.timeout_ns = (uint64_t)g_opt_timeout_ns.load();
     const size_t smem = (size_t)stages * stage + kLinearBTileBytes + 1024;
-    return cuda_status(launch_linear(p, dim3((unsigned)t->b_tiles, (unsigned)row_tiles), smem,
+    return cuda_status(launch_linear(p, dim3((unsigned)col_tiles, (unsigned)row_tiles), smem,
                                      reinterpret_cast<cudaStream_t>(stream), g_opt_pdl.load() != 0));
 }
 

@@ -8,18 +8,20 @@
 //
 // One CTA per (token tile, output tile): a token tile is up to 128 tokens of
 // one segment (or of the tokens without an adapter), taken through the
-// segment table's permutation; an output tile is 128 columns of one slice.
+// segment table's permutation; an output tile is up to 256 columns of one
+// slice (two of the table's 128-column B tiles).
 // The K loop streams, through a ring of stages,
 //   x: the tile's rows gathered with 16-byte cp.async into the no-swizzle
 //      K-major layout ([8][128][8] per 64-column stage);
-//   W: one 2-D TMA box (64 K x 128 rows, 128-byte swizzle);
+//   W: one 2-D TMA box (64 K x 256 rows, 128-byte swizzle);
 //   A: for a segment's tile, the adapter's packed A chunk ([8][R][8], one
 //      bulk copy of a contiguous run);
 // and one thread issues tcgen05 MMAs into two tensor-memory accumulators,
-// D = x W^T (128 x 128) and S = x A^T (128 x R): x is read once for both.
+// D = x W^T (128 x 256) and S = x A^T (128 x R): x is read once for both.
 // After the loop the epilogue warps read S, scale it, round it once to bf16
 // and store it to shared memory as an MMA operand; one more pass of MMAs adds
-// S_slice B_tile^T to D; D is rounded to bf16 and written to y once (the
+// S_slice B^T to D (one MMA pass per B tile); D is rounded to bf16 and
+// written to y once (the
 // layer's output replaces y: no base output is read).
 #include "linear.h"
 #include "tc.cuh"
@@ -30,11 +32,11 @@ namespace {
 
 constexpr int kT = kLinearThreads;
 constexpr int kXBytes = kLinearRows * kLinearK * 2;   // x stage: [8][128][8] bf16
-constexpr int kWBytes = kLinearCols * kLinearK * 2;   // W stage: 128 rows x 128 B, swizzled
-constexpr uint32_t kTmemCols = 512;                   // D: columns [0, 128); S: [128, 128 + R)
-constexpr int kMaxStages = 4;
-static_assert(kLinearRows == 128 && kLinearCols == 128 && kLinearK == 64, "tile shape");
-static_assert(kLinearBTileBytes == kMaxRank * kLinearCols * 2, "B tile [rp/8][128][8] at the largest stored rank");
+constexpr int kWBytes = kLinearCols * kLinearK * 2;   // W stage: 256 rows x 128 B, swizzled
+constexpr uint32_t kTmemCols = 512;                   // D: columns [0, 256); S: [256, 256 + R)
+constexpr int kMaxStages = kLinearMaxStages;
+static_assert(kLinearRows == 128 && kLinearCols == 2 * kLinearBCols && kLinearK == 64, "tile shape");
+static_assert(kLinearBTileBytes == 2 * kMaxRank * kLinearBCols * 2, "two B tiles [rp/8][128][8] at the largest rank");
 
 struct LinSmem {
     uint64_t full[kMaxStages], empty[kMaxStages];
@@ -42,7 +44,7 @@ struct LinSmem {
     uint64_t a_blk, b_blk;
     float sc;
     uint32_t tmem;
-    int32_t adapter, slot0, rows, rp;
+    int32_t adapter, slot0, rows, rp, xtma;
     int32_t rowsrc[kLinearRows];
 };
 
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
     unsigned char *const dsm = dsm_raw + ((1024u - (smem_u32(dsm_raw) & 1023u)) & 1023u);
     unsigned char *const bst = dsm + p.stages * p.stage_bytes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = blockIdx.x;    // output tile
+    const int j = blockIdx.x;    // output tile (256 columns)
     const int rt = blockIdx.y;   // token tile
     pdl_wait();   // the segment table and x may come from the kernels before
     pdl_trigger();
@@ -104,6 +106,14 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
     const int rows = sm.rows;
     if (rows <= 0) return;
     if (tid < rows) sm.rowsrc[tid] = p.perm[sm.slot0 + tid];
+    {
+        // x moves as TMA boxes when the box's 128 rows are the tile's rows in order (or rows past a short
+        // tile's end, whose products are not stored) and lie inside the last build's tokens
+        const int r0 = p.perm[sm.slot0];
+        const bool run = tid >= rows || p.perm[sm.slot0 + tid] == r0 + tid;
+        const int all = __syncthreads_and(run);
+        if (tid == 0) sm.xtma = all && r0 + kLinearRows <= p.header[H_M];
+    }
     if (tid == 0) {
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&sm.full[i], 1 + 128);   // the TMA issuer's expect_tx, then one arrival per x gatherer
@@ -127,11 +137,13 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
     tc::fence_after_sync();
     const uint32_t tmem = sm.tmem;
     const int rp = sm.rp, R = p.n_a * rp;
-    const bool lora = rp > 0;
+    const bool lora = rp > 0, xtma = sm.xtma != 0;
     int s = 0;
-    while (s + 1 < p.n_slices && j >= p.slice_tile_off[s + 1]) ++s;
-    const int lt = j - p.slice_tile_off[s];
+    while (s + 1 < p.n_slices && j >= p.slice_ctile_off[s + 1]) ++s;
+    const int lt = j - p.slice_ctile_off[s];
     const int col0 = p.slice_off[s] + lt * kLinearCols, width = min(kLinearCols, p.slice_n[s] - lt * kLinearCols);
+    const int jb = p.slice_tile_off[s] + 2 * lt;              // the tile's first B tile
+    const int nb = width > kLinearBCols ? 2 : 1;              // and its B tiles
     const int nK = (p.K + kLinearK - 1) / kLinearK;
     const int S = p.stages;
 
@@ -141,9 +153,9 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
         const __nv_bfloat16 *xrow = p.x + (int64_t)(t < rows ? sm.rowsrc[t] : sm.rowsrc[0]) * p.ldx;
         const unsigned char *ablk = reinterpret_cast<const unsigned char *>(sm.a_blk);
         if (t == 0 && lora) {
-            mbar_arrive_expect_tx(&sm.bbar, (uint32_t)(rp * 256));
-            bulk_g2s(bst, reinterpret_cast<const unsigned char *>(sm.b_blk) + (int64_t)j * rp * 256, (uint32_t)(rp * 256),
-                     &sm.bbar);
+            const uint32_t bbytes = (uint32_t)(nb * rp * 256);
+            mbar_arrive_expect_tx(&sm.bbar, bbytes);
+            bulk_g2s(bst, reinterpret_cast<const unsigned char *>(sm.b_blk) + (int64_t)jb * rp * 256, bbytes, &sm.bbar);
         }
         for (int kb = 0; kb < nK; ++kb) {
             const int st = kb % S;
@@ -152,12 +164,16 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
             const int k0 = kb * kLinearK, kk = min(kLinearK, p.K - k0);
             if (t == 0) {
                 const uint32_t abytes = lora ? (uint32_t)((kk >> 3) * R * 16) : 0u;
-                mbar_arrive_expect_tx(&sm.full[st], (uint32_t)kWBytes + abytes);
+                mbar_arrive_expect_tx(&sm.full[st], (uint32_t)kWBytes + abytes + (xtma ? (uint32_t)kXBytes : 0u));
                 tc::tma_tile2d(sb + kXBytes, &p.w_map, k0, col0, &sm.full[st]);
+                if (xtma) tc::tma_tile2d(sb, &p.x_map, k0, sm.rowsrc[0], &sm.full[st]);
                 if (lora) bulk_g2s(sb + kXBytes + kWBytes, ablk + (int64_t)(k0 >> 3) * R * 16, abytes, &sm.full[st]);
             }
+            if (!xtma) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) tc::cp_async16(sb + (c * kLinearRows + t) * 16, xrow + k0 + c * 8, t < rows && c * 8 < kk);
+                for (int c = 0; c < 8; ++c)
+                    tc::cp_async16(sb + (c * kLinearRows + t) * 16, xrow + k0 + c * 8, t < rows && c * 8 < kk);
+            }
             // a last K step of 8 columns: the A rows of its other 8 columns are zero
             if (lora && (kk & 8))
                 for (int i = t; i < R; i += 128)
@@ -176,7 +192,8 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
             const uint32_t xs = smem_u32(dsm + st * p.stage_bytes), ws = xs + kXBytes, as = ws + kWBytes;
             const int nks = (min(kLinearK, p.K - kb * kLinearK) + 15) >> 4;
             for (int ks = 0; ks < nks; ++ks) {
-                const uint64_t xd = tc::smem_desc(xs + ks * 2 * kLinearRows * 16, kLinearRows * 16, 128);
+                const uint64_t xd = xtma ? tc::smem_desc_sw128(xs + ks * 32)
+                                         : tc::smem_desc(xs + ks * 2 * kLinearRows * 16, kLinearRows * 16, 128);
                 const uint32_t accum = (kb | ks) != 0;
                 tc::mma_bf16(tmem, xd, tc::smem_desc_sw128(ws + ks * 32), id_d, accum);
                 if (lora) tc::mma_bf16(tmem + kLinearCols, xd, tc::smem_desc(as + ks * 2 * R * 16, R * 16, 128), id_s, accum);
@@ -219,17 +236,19 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
                 tc::fence_after_sync();
                 const int scol = p.n_a == 1 ? 0 : s * rp;
                 const uint32_t ss = smem_u32(dsm) + (scol >> 3) * kLinearRows * 16, bs = smem_u32(bst);
-                const uint32_t id_d = tc::idesc_bf16(kLinearRows, kLinearCols);
-                for (int ks = 0; ks < (rp >> 4); ++ks)
-                    tc::mma_bf16(tmem, tc::smem_desc(ss + ks * 2 * kLinearRows * 16, kLinearRows * 16, 128),
-                                 tc::smem_desc(bs + ks * 2 * kLinearCols * 16, kLinearCols * 16, 128), id_d, 1u);
+                const uint32_t id_b = tc::idesc_bf16(kLinearRows, kLinearBCols);
+                for (int b = 0; b < nb; ++b)
+                    for (int ks = 0; ks < (rp >> 4); ++ks)
+                        tc::mma_bf16(tmem + b * kLinearBCols, tc::smem_desc(ss + ks * 2 * kLinearRows * 16, kLinearRows * 16, 128),
+                                     tc::smem_desc(bs + b * rp * 256 + ks * 2 * kLinearBCols * 16, kLinearBCols * 16, 128),
+                                     id_b, 1u);
                 tc::mma_commit(&sm.fin);
             }
             __syncwarp();
             wait_bar(&sm.fin, 0, p);
             tc::fence_after_sync();
         }
-        // D row t -> bf16 -> y (128 columns of one slice, `width` of them inside it)
+        // D row t -> bf16 -> y (256 columns of one slice, `width` of them inside it)
         __nv_bfloat16 *yrow = t < rows ? p.y + (int64_t)sm.rowsrc[t] * p.ldy + col0 : nullptr;
         for (int c0 = 0; c0 < kLinearCols; c0 += 32) {
             float v[32];

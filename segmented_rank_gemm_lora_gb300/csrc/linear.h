@@ -7,14 +7,18 @@ namespace lora {
 
 constexpr int kLinearThreads = 256;
 constexpr int kLinearRows = 128;        // tokens of one tile (MMA M)
-constexpr int kLinearCols = 128;        // output columns of one tile (MMA N of the base product)
+constexpr int kLinearCols = 256;        // output columns of one tile (MMA N of the base product)
+constexpr int kLinearBCols = 128;       // output columns of one packed B tile (two per output tile)
 constexpr int kLinearK = 64;            // K columns of one pipeline stage
-constexpr int kLinearBTileBytes = 16384;  // one B tile (stored rank 64 at most) after the stages
-// stage bytes at A blocks of R rows at most: x [8][128][8] + W (128 rows x 128 B) + A [8][R][8], 1 KB aligned
+constexpr int kLinearBTileBytes = 2 * 16384;  // the output tile's B tiles (stored rank 64 at most) after the stages
+// stage bytes at A blocks of R rows at most: x [8][128][8] + W (256 rows x 128 B) + A [8][R][8], 1 KB aligned
 inline int linear_stage_bytes(int R) { return ((kLinearRows + kLinearCols + R) * kLinearK * 2 + 1023) / 1024 * 1024; }
+constexpr int kLinearMaxStages = 6;
 
 struct LinearParams {
-    CUtensorMap w_map;                  // W bf16 [N][K] (row stride ldw): box 64 columns x 128 rows, 128-byte swizzle
+    CUtensorMap w_map;                  // W bf16 [N][K] (row stride ldw): box 64 columns x 256 rows, 128-byte swizzle
+    CUtensorMap x_map;                  // x bf16 [max_M][K] (row stride ldx): box 64 columns x 128 rows; tiles whose 128
+                                        // rows are one run of consecutive rows inside the last build's M load through it
     const __nv_bfloat16 *x;  int64_t ldx;
     __nv_bfloat16 *y;        int64_t ldy;
     // weight table (dense)
@@ -22,8 +26,9 @@ struct LinearParams {
     const int32_t *rpad;                // [L] stored rank
     const float *scale;                 // [L]
     int32_t L, K, n_a, n_slices;
-    int32_t tiles;                      // 128-column output tiles (the B tiles of one block)
-    int32_t slice_n[kMaxSlices], slice_off[kMaxSlices], slice_tile_off[kMaxSlices];
+    int32_t tiles;                      // 256-column output tiles over all slices
+    int32_t slice_n[kMaxSlices], slice_off[kMaxSlices], slice_tile_off[kMaxSlices];   // (B tiles: 128 columns)
+    int32_t slice_ctile_off[kMaxSlices];   // first 256-column output tile of each slice
     // segment table of the last build
     const int32_t *header, *perm;
     const int4 *segments;
