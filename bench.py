@@ -190,11 +190,15 @@ def barrier(world: int):
 # ---------------------------------------------------------------------------
 # traffic recorded by ncu for the current engine source (null if stale)
 # ---------------------------------------------------------------------------
-def engine_source_sha() -> str:
-    """Hash of the kernels' code (every csrc source) with comments and blank space taken out, so that an
-    edit of the comments alone does not retire the traffic counters taken on the same code."""
+ENGINE_SOURCES = ("engine.cu", "stream.cu", "segments.cu", "common.cuh", "tc.cuh")
+LINEAR_SOURCES = ("linear.cu", "linear.h", "common.cuh", "tc.cuh")
+
+
+def engine_source_sha(names=ENGINE_SOURCES) -> str:
+    """Hash of the kernels' code (the named csrc sources) with comments and blank space taken out, so that
+    an edit of the comments alone does not retire the traffic counters taken on the same code."""
     h = hashlib.sha256()
-    for name in ("engine.cu", "stream.cu", "segments.cu", "common.cuh", "tc.cuh"):
+    for name in names:
         with open(os.path.join(ROOT, "segmented_rank_gemm_lora_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -212,7 +216,8 @@ def recorded_traffic(config: str):
     except ValueError:
         return None
     entry = rec.get(config)
-    if not entry or entry.get("engine_sha") != engine_source_sha():
+    sha = engine_source_sha(LINEAR_SOURCES if config == "linear_prefill" else ENGINE_SOURCES)
+    if not entry or entry.get("engine_sha") != sha:
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -644,7 +649,7 @@ def measure_linear(K, W, args, torch, lora, dev, e2e_steps):
     _, tc_peak, src = peaks()
     achieved = flops / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
-                "traffic": None, "kernel": "linear_kernel", "kernel_ms": kernel_ms, "algorithmic_bytes": nbytes,
+                "traffic": recorded_traffic("linear_prefill"), "kernel": "linear_kernel", "kernel_ms": kernel_ms, "algorithmic_bytes": nbytes,
                 "algorithmic_flops": flops, "peak_source": src + " (burst)",
                 "unfused_ms": unfused_ms, "unfused": "torch.matmul (cuBLAS) x W^T, then lora_apply on y"}
     # end to end: x and ids in from pinned memory, build + linear, y out; one step after another
@@ -831,10 +836,21 @@ def main():
     ap.add_argument("--workload-steps", type=int, default=1000,
                     help="timed steps of each per_workload entry (the headline workload uses --steps)")
     ap.add_argument("--no-per-workload", dest="per_workload", action="store_false")
+    ap.add_argument("--linear-only", action="store_true",
+                    help="measure only the fused LoRA linear layer (the per_workload linear_prefill entry) and "
+                         "print it as one JSON line (for profiling that kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_env()
+    if args.linear_only:
+        import torch
+        from segmented_rank_gemm_lora_gb300 import lora
+        torch.cuda.set_device(local)
+        lora.load()
+        r = measure_linear(args.steps, args.warmup, args, torch, lora, torch.device("cuda", local), args.e2e_steps)
+        print(json.dumps(r), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
