@@ -57,6 +57,8 @@ def _load():
             lib.oracle_lora_apply.restype = ctypes.c_int
             lib.oracle_lora_apply.argtypes = [_I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                               _P, _I64, _P, _I64, _P]
+            lib.oracle_embedding_apply.restype = ctypes.c_int
+            lib.oracle_embedding_apply.argtypes = [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I64, _P]
             lib.oracle_matmul_bt.restype = None
             lib.oracle_matmul_bt.argtypes = [_I32, _I32, _I32, _P, _I64, _P, _I64, _P]
             lib.oracle_build_segments.restype = ctypes.c_int
@@ -134,6 +136,28 @@ def lora_linear(ids, x, W, A: Sequence[np.ndarray], B: Sequence[np.ndarray], ran
     N = int(np.sum(slice_n))
     delta, bad = lora_apply(ids, x, np.zeros((M, N), np.uint16), A, B, ranks, scales, slice_n, n_a)
     return matmul_bt(x, W) + delta, bad
+
+
+def embedding_apply(ids, vocab, y_base, A: Sequence[np.ndarray], B: Sequence[np.ndarray], ranks, scales):
+    """Embedding LoRA ("[SGLang] LoRA Layers", VocabParallelEmbeddingWithLoRA): y = y_base + scale_i * B_i
+    A_i[:, vocab[t]] per token (float64 [M, N]); returns (y, bad_count).  A[i]: bf16 bits [r_i, V];
+    B[i]: [N, r_i]; y_base: bf16 bits [M, N]."""
+    lib = _load()
+    ids = _c(ids, np.int32)
+    vocab = _c(vocab, np.int32)
+    y_base = _c(y_base, np.uint16)
+    M, N = y_base.shape
+    ranks = _c(ranks, np.int32)
+    scales = _c(scales, np.float64)
+    V = A[0].shape[1]
+    for i, r in enumerate(ranks):
+        assert A[i].shape == (r, V) and B[i].shape == (N, r)
+    pa, ka = _ptr_array(A)
+    pb, kb = _ptr_array(B)
+    out = np.empty((M, N), np.float64)
+    bad = lib.oracle_embedding_apply(M, V, N, len(ranks), _ptr(ranks), _ptr(scales), pa, pb, _ptr(ids), _ptr(vocab),
+                                     _ptr(y_base), N, _ptr(out))
+    return out, int(bad)
 
 
 def build_segments(ids, L: int, enabled=None):

@@ -23,6 +23,8 @@
  *        projections, A = (n*r, in), B = (sum of slice widths, r).
  *   [P1] 3.3 the LoRA linear layer: the base matmul of the layer's input with
  *        its weight, plus the LoRA delta (issued beside it or fused with it).
+ *   [P5] "VocabParallelEmbeddingWithLoRA": embedding LoRA, A used as an
+ *        embedding lookup (rank, vocab) and B as a plain matmul (embed_dim, rank).
  *
  * Readings taken where the pages are silent:
  *   - a per-adapter scale multiplies the expand result (1.0 reproduces [P1]);
@@ -43,6 +45,37 @@ static double bf(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * Embedding LoRA, [P5] "VocabParallelEmbeddingWithLoRA": for every token t with adapter
+ * i = ids[t] in [0, L) and vocabulary id v = vocab[t] in [0, V):
+ *   S[j]      = A_i[j, v]                                  (j < r = rank[i]: the lookup)
+ *   y[t, n]   = y_base[t, n] + scale[i] * sum_j S[j] * B_i[n, j]
+ * A[i]: bf16 [rank[i]][V] row-major; B[i]: bf16 [N][rank[i]].  Tokens with ids[t] == -1, an
+ * out-of-range adapter id or an out-of-range vocabulary id copy y_base.  Returns the number of
+ * out-of-range adapter or vocabulary ids.
+ */
+int oracle_embedding_apply(int32_t M, int32_t V, int32_t N, int32_t L, const int32_t *rank, const double *scale,
+                           const uint16_t *const *A, const uint16_t *const *B, const int32_t *ids,
+                           const int32_t *vocab, const uint16_t *y_base, int64_t ldy, double *y_out)
+{
+    int bad = 0;
+    for (int32_t t = 0; t < M; ++t) {
+        for (int32_t n = 0; n < N; ++n) y_out[(int64_t)t * N + n] = bf(y_base[(int64_t)t * ldy + n]);
+        const int32_t i = ids[t];
+        if (i == -1) continue;
+        if (i < -1 || i >= L) { ++bad; continue; }
+        const int32_t v = vocab[t];
+        if (v < 0 || v >= V) { ++bad; continue; }
+        const int32_t r = rank[i];
+        for (int32_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int32_t j = 0; j < r; ++j) acc += bf(A[i][(int64_t)j * V + v]) * bf(B[i][(int64_t)n * r + j]);
+            y_out[(int64_t)t * N + n] += scale[i] * acc;
+        }
+    }
+    return bad;
 }
 
 /*
