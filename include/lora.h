@@ -277,6 +277,28 @@ lora_status lora_moe_delta(lora_table table, int32_t stage, const lora_workspace
 lora_status lora_linear(lora_table table, const lora_workspace *ws, const void *d_x, int64_t ldx, const void *d_w,
                         int64_t ldw, void *d_y, int64_t ldy, lora_stream_t stream);
 
+/*
+ * Embedding LoRA ("[SGLang] LoRA Layers", VocabParallelEmbeddingWithLoRA: the
+ * LoRA A matrix acts as an embedding lookup over the vocabulary and B as a
+ * plain matmul added to the base embedding), over the segment table of the
+ * last lora_build_segments on `ws` (adapter per token):
+ *   y[t] += scale_i * B_i A_i[:, vocab[t]]
+ * `table`: packed with K = the vocabulary size V (a multiple of 8; A_i given as
+ * [r_i][V]), one A block for all slices (n_a = 1), N = the embedding width.
+ *   d_vocab : int32 [M] device, the tokens' vocabulary ids.
+ *   d_y     : bf16 [M][ldy] device, in: the base embedding rows, out: + delta.
+ *             Rows of tokens without an adapter are not touched.
+ * Vocabulary ids outside [0, V) leave the row unchanged and raise
+ * LORA_ERR_BAD_ADAPTER_ID through lora_get_status.  The LM-head LoRA of the
+ * same page (hidden @ A^T @ B^T added to the logits, B cut by vocabulary for
+ * a tensor-parallel shard) is lora_apply with a table of K = the hidden size
+ * and N = the vocabulary (or the shard's rows of B).
+ * ldy >= N, a multiple of 8; d_y 16-byte aligned.  Errors (synchronous):
+ * LORA_ERR_INVALID_ARG (also n_a != 1 or a MoE table), LORA_ERR_UNSUPPORTED.
+ */
+lora_status lora_embedding_apply(lora_table table, const lora_workspace *ws, const int32_t *d_vocab, void *d_y,
+                                 int64_t ldy, lora_stream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace's sticky device error
  * word, and return the most severe error seen since the last call (LORA_OK if
  * none). */

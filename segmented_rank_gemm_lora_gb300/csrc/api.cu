@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "linear.h"
+#include "embedding.h"
 
 using namespace lora;
 
@@ -746,6 +747,42 @@ extern "C" lora_status lora_linear(lora_table t, const lora_workspace *ws, const
     const size_t smem = (size_t)stages * stage + kLinearBTileBytes + 1024;
     return cuda_status(launch_linear(p, dim3((unsigned)col_tiles, (unsigned)row_tiles), smem,
                                      reinterpret_cast<cudaStream_t>(stream), g_opt_pdl.load() != 0));
+}
+
+extern "C" lora_status lora_embedding_apply(lora_table t, const lora_workspace *ws, const int32_t *d_vocab, void *d_y,
+                                            int64_t ldy, lora_stream_t stream)
+{
+    if (!valid_table(t) || !d_vocab || !d_y) return LORA_ERR_INVALID_ARG;
+    WsLayout w;
+    lora_status st = check_ws(ws, &w);
+    if (st != LORA_OK) return st;
+    if (ws->L != t->L || t->E_A != 1 || t->E_B != 1 || t->n_a != 1) return LORA_ERR_INVALID_ARG;
+    if (ldy < t->N || ldy % 8 || !aligned16(d_y)) return LORA_ERR_INVALID_ARG;
+    const int64_t row_tiles = ceil_div(ws->max_M, kEmbedRows) + w.seg_capacity + 1;
+    if (row_tiles > 65535) return LORA_ERR_UNSUPPORTED;
+    EmbedParams p{};
+    p.a_ptr = t->d_a_ptr;
+    p.b_ptr = t->d_b_ptr;
+    p.rpad = t->d_rpad;
+    p.scale = t->d_scale;
+    p.L = t->L;
+    p.V = t->K;
+    p.n_slices = t->n_slices;
+    for (int s = 0; s < kMaxSlices; ++s) {
+        p.slice_n[s] = t->slice_n[s];
+        p.slice_off[s] = t->slice_off[s];
+        p.slice_tile_off[s] = t->slice_tile_off[s];
+    }
+    int32_t *header = at<int32_t>(ws, w.header);
+    p.header = header;
+    p.perm = at<int32_t>(ws, w.perm);
+    p.segments = at<int4>(ws, w.segments);
+    p.vocab = d_vocab;
+    p.y = static_cast<__nv_bfloat16 *>(d_y);
+    p.ldy = ldy;
+    p.err = reinterpret_cast<uint32_t *>(header + H_ERR);
+    return cuda_status(launch_embedding(p, dim3((unsigned)t->b_tiles, (unsigned)row_tiles),
+                                        reinterpret_cast<cudaStream_t>(stream), g_opt_pdl.load() != 0));
 }
 
 extern "C" lora_status lora_get_status(const lora_workspace *ws, lora_stream_t stream)

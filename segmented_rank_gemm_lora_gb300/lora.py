@@ -29,7 +29,8 @@ LORA_OPT_PATH, LORA_OPT_TC_MIN_ROWS, LORA_OPT_WAIT_TIMEOUT_NS, LORA_OPT_GRID_CTA
 EXPORTED = ["lora_pack_weights", "lora_table_destroy", "lora_table_info", "lora_table_stored_rank",
             "lora_workspace_bytes", "lora_workspace_layout", "lora_build_segments", "lora_apply",
             "lora_moe_delta", "lora_get_status", "lora_status_string", "lora_set_option", "lora_get_option",
-            "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch", "lora_build_and_apply", "lora_linear"]
+            "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch", "lora_build_and_apply", "lora_linear",
+            "lora_embedding_apply"]
 
 
 class LoraError(RuntimeError):
@@ -102,6 +103,7 @@ def load(build_if_missing: bool = False):
         "lora_apply_static_scratch": (_c_i32, [P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
         "lora_build_and_apply": (_c_i32, [P, P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
         "lora_linear": (_c_i32, [P, P, P, _c_i64, P, _c_i64, P, _c_i64, P]),
+        "lora_embedding_apply": (_c_i32, [P, P, P, P, _c_i64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -313,6 +315,19 @@ def lora_linear(table: Table, ws: Workspace, x: torch.Tensor, W: torch.Tensor, y
         raise ValueError("x and y need the %d rows of the last lora_build_segments" % ws.built_M)
     _check(load().lora_linear(table.handle, ws.ref, x.data_ptr(), x.stride(0), W.data_ptr(), W.stride(0),
                               y.data_ptr(), y.stride(0), _stream(stream)), "lora_linear")
+
+
+def lora_embedding_apply(table: Table, ws: Workspace, vocab: torch.Tensor, y: torch.Tensor, stream=None):
+    """y (bf16 [M, N], the base embedding rows) += scale_i * B_i A_i[:, vocab[t]] per token (embedding LoRA)."""
+    if vocab.dtype != torch.int32 or not vocab.is_cuda or not vocab.is_contiguous():
+        raise TypeError("vocab must be a contiguous CUDA int32 tensor")
+    _bf16_dev(y, "y")
+    if y.stride(1) != 1:
+        raise ValueError("y needs unit column stride")
+    if ws.built_M is not None and (vocab.numel() < ws.built_M or y.shape[0] < ws.built_M):
+        raise ValueError("vocab and y need the %d rows of the last lora_build_segments" % ws.built_M)
+    _check(load().lora_embedding_apply(table.handle, ws.ref, vocab.data_ptr(), y.data_ptr(), y.stride(0),
+                                       _stream(stream)), "lora_embedding_apply")
 
 
 def lora_get_status(ws: Workspace, stream=None) -> int:
