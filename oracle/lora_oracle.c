@@ -64,8 +64,10 @@ int oracle_embedding_apply(int32_t M, int32_t V, int32_t N, int32_t L, const int
     for (int32_t t = 0; t < M; ++t) {
         for (int32_t n = 0; n < N; ++n) y_out[(int64_t)t * N + n] = bf(y_base[(int64_t)t * ldy + n]);
         const int32_t i = ids[t];
-        if (i == -1) continue;
-        if (i < -1 || i >= L) { ++bad; continue; }
+        if (i < 0 || i >= L) {   /* -1: no adapter; anything else out of range is counted */
+            if (i != -1) ++bad;
+            continue;
+        }
         const int32_t v = vocab[t];
         if (v < 0 || v >= V) { ++bad; continue; }
         const int32_t r = rank[i];
