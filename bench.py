@@ -684,6 +684,109 @@ def measure_linear(K, W, args, torch, lora, dev, e2e_steps):
     return out
 
 
+EMBED_WORKLOAD = ("embedding_decode: 32 tokens, 20 adapters (ranks cycling 16/32/64, 10% ids -1) over a 32768-entry "
+                  "vocabulary, embedding width 4096, through lora_embedding_apply")
+
+
+def measure_embedding(K, W, args, torch, lora, dev):
+    """Embedding LoRA on a decode batch: K timed steps (build + lora_embedding_apply) as CUDA-graph replays over
+    rotating input sets larger than L2, and the kernel alone; HBM roofline over the bytes the method moves."""
+    from segmented_rank_gemm_lora_gb300 import synth
+    V, N, R = 32768, 4096, 5
+    sets = []
+    for j in range(R):
+        rng = np.random.default_rng(2000 + j)
+        ids = synth.ids_decode(2000 + j)
+        ranks = synth.cycle_ranks(20)
+        A = [torch.randn(r, V, device=dev).to(torch.bfloat16) for r in ranks]
+        B = [(torch.randn(N, r, device=dev) / r ** 0.5).to(torch.bfloat16) for r in ranks]
+        s = {"ids": torch.from_numpy(ids).to(dev), "ids_np": ids, "ranks": ranks,
+             "vocab": torch.from_numpy(rng.integers(0, V, len(ids)).astype(np.int32)).to(dev),
+             "y": (torch.randn(len(ids), N, device=dev) * 4).to(torch.bfloat16),
+             "table": lora.lora_pack_weights(A, B, ranks, [2.0] * len(ranks), V, [N], 1),
+             "ws": lora.Workspace(len(ids), len(ranks), device=dev)}
+        del A, B
+        sets.append(s)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s, build=True):
+        if build:
+            lora.lora_build_segments(s["ws"], s["ids"])
+        lora.lora_embedding_apply(s["table"], s["ws"], s["vocab"], s["y"])
+
+    with torch.cuda.stream(stream):
+        for s in sets:
+            step(s)
+    torch.cuda.synchronize()
+    for s in sets:
+        if lora.lora_get_status(s["ws"]) != lora.LORA_OK:
+            raise RuntimeError("embedding: device status")
+
+    def timed(build, reps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in sets:
+                step(s, build)
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, W // R + 1)):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * R)
+
+    reps = max(1, K // R)
+    step_ms = timed(True, reps)
+    kernel_ms = timed(False, reps)
+    ids, ranks = sets[0]["ids_np"], sets[0]["ranks"]
+    active = sorted(set(int(i) for i in ids if i >= 0))
+    Ma = int((ids >= 0).sum())
+    # B once per active adapter, each token's A column (r values), y read and written, ids and vocabulary ids
+    nbytes = sum(2 * N * ranks[i] for i in active) + sum(2 * ranks[int(i)] for i in ids if i >= 0) + Ma * 4 * N \
+        + 8 * len(ids)
+    hbm, _, src = peaks()
+    achieved = nbytes / (kernel_ms / 1e3) / 1e9
+    # end to end: ids, vocabulary ids and the base rows in from pinned memory, build + apply, rows out
+    hi = [s["ids"].cpu().pin_memory() for s in sets]
+    hv = [s["vocab"].cpu().pin_memory() for s in sets]
+    hy = [s["y"].cpu().pin_memory() for s in sets]
+    ho = [torch.empty_like(s["y"], device="cpu", pin_memory=True) for s in sets]
+    n = 50
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            s = sets[i % R]
+            s["ids"].copy_(hi[i % R], non_blocking=True)
+            s["vocab"].copy_(hv[i % R], non_blocking=True)
+            s["y"].copy_(hy[i % R], non_blocking=True)
+            step(s)
+            ho[i % R].copy_(s["y"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n
+    e2e = {"value": len(ids) / (e2e_ms / 1e3), "unit": "tokens/s", "steps": n,
+           "h2d_bytes_per_step": hi[0].numel() * 4 + hv[0].numel() * 4 + hy[0].numel() * 2,
+           "d2h_bytes_per_step": ho[0].numel() * 2,
+           "path": "public API calls with host-resident ids, vocabulary ids and base rows, one step after another"}
+    out = {"value": len(ids) / (step_ms / 1e3), "unit": "tokens/s", "ms_per_step": step_ms, "steps": reps * R,
+           "kernel_ms": kernel_ms,
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                        "traffic": None, "kernel": "embedding_kernel", "kernel_ms": kernel_ms,
+                        "algorithmic_bytes": nbytes, "peak_source": src + " (burst)"},
+           "e2e": e2e, "gpu_launches": 2 * reps * R, "workload": EMBED_WORKLOAD}
+    for s in sets:
+        s["table"].destroy()
+    del sets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 WORKLOADS = ("decode", "prefill", "stacked_qkv", "stacked_gate_up", "stacked_down", "moe")
 
 
@@ -711,6 +814,7 @@ def run_ours(args, world, rank, local):
             per[name]["workload"] = CONFIGS[name]
         per["linear_prefill"] = measure_linear(max(49, min(K, args.workload_steps)), W, args, torch, lora, dev,
                                                min(args.workload_steps, 20))
+        per["embedding_decode"] = measure_embedding(max(50, min(K, args.workload_steps)), W, args, torch, lora, dev)
 
     cpu = cpu_baseline(args.config, args.cpu_seconds) if (rank == 0 and world == 1 and args.cpu_seconds > 0) else None
     if rank == 0:
