@@ -111,6 +111,27 @@ typedef struct {
 lora_status lora_pack_weights(const lora_adapter_desc *adapters, int32_t L, const lora_proj_shape *shape,
                               lora_stream_t stream, lora_table *out);
 
+/*
+ * Hot-swap one adapter of a live table ("vLLM-Ascend dynamic LoRA fused
+ * operator", section 3.1: a fixed-size device pool per rank group, blocks
+ * taken on load and returned whole on unload instead of frequent allocation;
+ * section 4.3: replacing an adapter while steps run needs a version lock or a
+ * double buffer).  The new weights (any rank 1..64; `adapter` as in
+ * lora_pack_weights, same K, slices and expert counts as the table) are packed
+ * on `stream` into a free block of the pool of their stored rank, then the
+ * adapter's lookup entries are rewritten on `stream`: launches enqueued on
+ * `stream` before this call read the old adapter, launches after it the new
+ * one, and none reads a mix.  The replaced block returns to the pool once
+ * `stream` has passed the new entries.  A pool with no free block of that
+ * rank grows by one chunk of 4 blocks (a device allocation: not during stream
+ * capture).  Work on other streams that uses the table must be ordered with
+ * `stream` by the caller.  Not thread-safe against other calls on the same
+ * table.  Errors: LORA_ERR_INVALID_ARG (index outside [0, L), rank outside
+ * 1..64, NULL pointers), LORA_ERR_OOM, LORA_ERR_CUDA.
+ */
+lora_status lora_table_set_adapter(lora_table table, int32_t index, const lora_adapter_desc *adapter,
+                                   lora_stream_t stream);
+
 /* Free a table.  The caller must ensure no enqueued work still uses it. */
 lora_status lora_table_destroy(lora_table table);
 
@@ -118,7 +139,7 @@ lora_status lora_table_destroy(lora_table table);
 typedef struct {
     int32_t L, K, N, n_slices, n_a, E_A, E_B;
     int32_t num_rank_groups;      /* distinct stored ranks */
-    int64_t device_bytes;         /* bytes of packed A and B */
+    int64_t device_bytes;         /* bytes of packed A and B, pool blocks included */
     int32_t stored_rank_of_max;   /* stored rank of the largest adapter */
 } lora_table_info_t;
 lora_status lora_table_info(lora_table table, lora_table_info_t *info);

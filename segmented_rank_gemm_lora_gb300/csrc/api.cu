@@ -11,6 +11,7 @@
 #include "common.cuh"
 #include "linear.h"
 #include "embedding.h"
+#include "table_entry.h"
 
 using namespace lora;
 
@@ -136,6 +137,18 @@ struct lora_table_s {
     int32_t *d_rpad = nullptr;
     float *d_scale = nullptr;
     int32_t max_R = 0;
+    // the pool of adapter blocks per stored rank ("vLLM-Ascend dynamic LoRA fused operator", section 3.1):
+    // an adapter's A blocks (E_A of them, contiguous) and B blocks (E_B), taken whole and returned whole
+    struct Slot {
+        char *a, *b;
+    };
+    std::map<int32_t, std::vector<Slot>> free_slots;               // stored rank -> free blocks
+    struct Retiring {
+        cudaEvent_t done;                                          // recorded after the entries were replaced
+        int32_t rp;
+        Slot slot;
+    };
+    std::vector<Retiring> retiring;                                // replaced blocks still readable by queued work
     uint32_t magic = 0x4c6f5241u;
 };
 
@@ -149,6 +162,7 @@ extern "C" int32_t lora_rank_padded(int32_t rank)
 
 static void free_table(lora_table t)
 {
+    for (auto &r : t->retiring) cudaEventDestroy(r.done);
     for (void *m : t->group_mem) cudaFree(m);
     cudaFree(t->d_a_ptr);
     cudaFree(t->d_b_ptr);
@@ -285,6 +299,97 @@ extern "C" lora_status lora_pack_weights(const lora_adapter_desc *adapters, int3
     return LORA_OK;
 }
 
+// Bytes of one adapter's A region (E_A blocks) and B region (E_B blocks) at stored rank rp, as the pack lays them.
+static int64_t slot_a_bytes(lora_table t, int32_t rp) { return t->E_A * round_up((int64_t)t->K * t->n_a * rp * 2, 256); }
+static int64_t slot_b_bytes(lora_table t, int32_t rp)
+{
+    return t->E_B * round_up((int64_t)t->b_tiles * kNTile * rp * 2, 256);
+}
+
+constexpr int kPoolChunkSlots = 4;   // blocks a new pool chunk of one stored rank holds
+
+extern "C" lora_status lora_table_set_adapter(lora_table t, int32_t index, const lora_adapter_desc *adapter,
+                                              lora_stream_t stream)
+{
+    if (!valid_table(t) || !adapter || index < 0 || index >= t->L) return LORA_ERR_INVALID_ARG;
+    const int32_t rp = lora_rank_padded(adapter->rank);
+    if (rp < 0 || !adapter->A || !adapter->B) return LORA_ERR_INVALID_ARG;
+    if (t->E_A > kMaxEntryBlocks || t->E_B > kMaxEntryBlocks) return LORA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // blocks whose replacement every earlier launch has passed go back to the pool
+    for (size_t i = 0; i < t->retiring.size();) {
+        const cudaError_t q = cudaEventQuery(t->retiring[i].done);
+        if (q == cudaSuccess) {
+            t->free_slots[t->retiring[i].rp].push_back(t->retiring[i].slot);
+            cudaEventDestroy(t->retiring[i].done);
+            t->retiring.erase(t->retiring.begin() + (long)i);
+        } else {
+            if (q != cudaErrorNotReady) return LORA_ERR_CUDA;
+            ++i;
+        }
+    }
+    std::vector<lora_table_s::Slot> &pool = t->free_slots[rp];
+    const int64_t abytes = slot_a_bytes(t, rp), bbytes = slot_b_bytes(t, rp);
+    if (pool.empty()) {
+        // a new chunk of blocks of this stored rank (the pool grows by whole chunks, never per adapter)
+        void *mem = nullptr;
+        if (cudaMalloc(&mem, (size_t)(kPoolChunkSlots * (abytes + bbytes))) != cudaSuccess) {
+            cudaGetLastError();
+            return LORA_ERR_OOM;
+        }
+        t->group_mem.push_back(mem);
+        t->device_bytes += kPoolChunkSlots * (abytes + bbytes);
+        char *base = static_cast<char *>(mem);
+        for (int i = kPoolChunkSlots - 1; i >= 0; --i)
+            pool.push_back({base + i * (abytes + bbytes), base + i * (abytes + bbytes) + abytes});
+    }
+    const lora_table_s::Slot slot = pool.back();
+    // the new weights into the free block (the adapter's current block stays intact for queued launches)
+    const int32_t r = adapter->rank;
+    const auto *A = static_cast<const __nv_bfloat16 *>(adapter->A);
+    const auto *B = static_cast<const __nv_bfloat16 *>(adapter->B);
+    const int64_t a_block = abytes / t->E_A, b_block = bbytes / t->E_B;
+    lora_status st = LORA_OK;
+    for (int e = 0; e < t->E_A && st == LORA_OK; ++e)
+        st = cuda_status(launch_pack_a(A + (int64_t)e * t->n_a * r * t->K,
+                                       reinterpret_cast<__nv_bfloat16 *>(slot.a + e * a_block), t->K, t->n_a, r, rp, s));
+    for (int e = 0; e < t->E_B && st == LORA_OK; ++e)
+        st = cuda_status(launch_pack_b(B + (int64_t)e * t->N * r, reinterpret_cast<__nv_bfloat16 *>(slot.b + e * b_block),
+                                       r, rp, t->n_slices, t->slice_n, s));
+    if (st != LORA_OK) return st;
+    pool.pop_back();
+    // then the lookup entries, in stream order
+    TableEntry e{};
+    e.index = index;
+    e.E_A = t->E_A;
+    e.E_B = t->E_B;
+    e.rpad = rp;
+    e.scale = adapter->scale;
+    for (int i = 0; i < t->E_A; ++i) e.a[i] = reinterpret_cast<uint64_t>(slot.a + i * a_block);
+    for (int i = 0; i < t->E_B; ++i) e.b[i] = reinterpret_cast<uint64_t>(slot.b + i * b_block);
+    st = cuda_status(launch_set_entry(e, t->d_a_ptr, t->d_b_ptr, t->d_rpad, t->d_scale, s));
+    if (st != LORA_OK) return st;
+    // the replaced block retires once the stream has passed the new entries
+    lora_table_s::Retiring ret{};
+    ret.rp = t->rpad[index];
+    ret.slot = {reinterpret_cast<char *>(t->a_ptr[(size_t)index * t->E_A]),
+                reinterpret_cast<char *>(t->b_ptr[(size_t)index * t->E_B])};
+    if (cudaEventCreateWithFlags(&ret.done, cudaEventDisableTiming) != cudaSuccess) return LORA_ERR_CUDA;
+    if (cudaEventRecord(ret.done, s) != cudaSuccess) {
+        cudaEventDestroy(ret.done);
+        return LORA_ERR_CUDA;
+    }
+    t->retiring.push_back(ret);
+    // host copies of the entries
+    t->rank[index] = r;
+    t->rpad[index] = rp;
+    t->scale[index] = adapter->scale;
+    for (int i = 0; i < t->E_A; ++i) t->a_ptr[(size_t)index * t->E_A + i] = e.a[i];
+    for (int i = 0; i < t->E_B; ++i) t->b_ptr[(size_t)index * t->E_B + i] = e.b[i];
+    t->max_R = std::max(t->max_R, t->n_a * rp);
+    return LORA_OK;
+}
+
 extern "C" lora_status lora_table_destroy(lora_table table)
 {
     if (!valid_table(table)) return LORA_ERR_INVALID_ARG;
@@ -302,7 +407,9 @@ extern "C" lora_status lora_table_info(lora_table t, lora_table_info_t *info)
     info->n_a = t->n_a;
     info->E_A = t->E_A;
     info->E_B = t->E_B;
-    info->num_rank_groups = (int32_t)t->group_mem.size();
+    std::vector<int32_t> stored(t->rpad);
+    std::sort(stored.begin(), stored.end());
+    info->num_rank_groups = (int32_t)(std::unique(stored.begin(), stored.end()) - stored.begin());
     info->device_bytes = t->device_bytes;
     int32_t best = 0, best_rank = -1;
     for (int i = 0; i < t->L; ++i)

@@ -30,7 +30,7 @@ EXPORTED = ["lora_pack_weights", "lora_table_destroy", "lora_table_info", "lora_
             "lora_workspace_bytes", "lora_workspace_layout", "lora_build_segments", "lora_apply",
             "lora_moe_delta", "lora_get_status", "lora_status_string", "lora_set_option", "lora_get_option",
             "lora_rank_padded", "lora_set_trace", "lora_apply_static_scratch", "lora_build_and_apply", "lora_linear",
-            "lora_embedding_apply"]
+            "lora_embedding_apply", "lora_table_set_adapter"]
 
 
 class LoraError(RuntimeError):
@@ -104,6 +104,7 @@ def load(build_if_missing: bool = False):
         "lora_build_and_apply": (_c_i32, [P, P, P, _c_i32, P, _c_i64, P, _c_i64, P]),
         "lora_linear": (_c_i32, [P, P, P, _c_i64, P, _c_i64, P, _c_i64, P]),
         "lora_embedding_apply": (_c_i32, [P, P, P, P, _c_i64, P]),
+        "lora_table_set_adapter": (_c_i32, [P, _c_i32, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -183,6 +184,18 @@ def lora_pack_weights(A: Sequence[torch.Tensor], B: Sequence[torch.Tensor], rank
     _check(load().lora_pack_weights(descs, L, ctypes.byref(sh), _stream(stream), ctypes.byref(h)),
            "lora_pack_weights")
     return Table(h.value, L)
+
+
+def lora_table_set_adapter(table: Table, index: int, A: torch.Tensor, B: torch.Tensor, rank: int, scale: float,
+                           stream=None):
+    """Hot-swap adapter `index` of a live table (shapes as in lora_pack_weights), in stream order."""
+    _bf16_dev(A, "A")
+    _bf16_dev(B, "B")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("adapter weights must be contiguous")
+    desc = AdapterDesc(int(rank), float(scale), A.data_ptr(), B.data_ptr())
+    _check(load().lora_table_set_adapter(table.handle, int(index), ctypes.byref(desc), _stream(stream)),
+           "lora_table_set_adapter")
 
 
 def lora_workspace_bytes(max_M: int, L: int, topk: int = 0, num_experts: int = 0, block_m: int = 0) -> int:
