@@ -216,7 +216,7 @@ def recorded_traffic(config: str):
     except ValueError:
         return None
     entry = rec.get(config)
-    sha = engine_source_sha(LINEAR_SOURCES if config == "linear_prefill" else ENGINE_SOURCES)
+    sha = engine_source_sha({"linear_prefill": LINEAR_SOURCES, "embedding_decode": EMBED_SOURCES}.get(config, ENGINE_SOURCES))
     if not entry or entry.get("engine_sha") != sha:
         return None
     return entry.get("dram_bytes_per_launch")
@@ -684,6 +684,7 @@ def measure_linear(K, W, args, torch, lora, dev, e2e_steps):
     return out
 
 
+EMBED_SOURCES = ("embedding.cu", "embedding.h", "common.cuh")
 EMBED_WORKLOAD = ("embedding_decode: 32 tokens, 20 adapters (ranks cycling 16/32/64, 10% ids -1) over a 32768-entry "
                   "vocabulary, embedding width 4096, through lora_embedding_apply")
 
@@ -776,7 +777,7 @@ def measure_embedding(K, W, args, torch, lora, dev):
     out = {"value": len(ids) / (step_ms / 1e3), "unit": "tokens/s", "ms_per_step": step_ms, "steps": reps * R,
            "kernel_ms": kernel_ms,
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                        "traffic": None, "kernel": "embedding_kernel", "kernel_ms": kernel_ms,
+                        "traffic": recorded_traffic("embedding_decode"), "kernel": "embedding_kernel", "kernel_ms": kernel_ms,
                         "algorithmic_bytes": nbytes, "peak_source": src + " (burst)"},
            "e2e": e2e, "gpu_launches": 2 * reps * R, "workload": EMBED_WORKLOAD}
     for s in sets:
@@ -943,16 +944,21 @@ def main():
     ap.add_argument("--linear-only", action="store_true",
                     help="measure only the fused LoRA linear layer (the per_workload linear_prefill entry) and "
                          "print it as one JSON line (for profiling that kernel)")
+    ap.add_argument("--embedding-only", action="store_true",
+                    help="measure only the embedding LoRA (the per_workload embedding_decode entry) and print it "
+                         "as one JSON line (for profiling that kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_env()
-    if args.linear_only:
+    if args.linear_only or args.embedding_only:
         import torch
         from segmented_rank_gemm_lora_gb300 import lora
         torch.cuda.set_device(local)
         lora.load()
-        r = measure_linear(args.steps, args.warmup, args, torch, lora, torch.device("cuda", local), args.e2e_steps)
+        dev = torch.device("cuda", local)
+        r = (measure_linear(args.steps, args.warmup, args, torch, lora, dev, args.e2e_steps) if args.linear_only
+             else measure_embedding(args.steps, args.warmup, args, torch, lora, dev))
         print(json.dumps(r), flush=True)
         return
     if args.impl == "reference":
