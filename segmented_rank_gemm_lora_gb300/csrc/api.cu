@@ -614,12 +614,15 @@ static lora_status run_stream(lora_table t, const lora_workspace *ws, const WsLa
     p.partials = reinterpret_cast<float *>(area + plan_bytes + s_cap);
     p.partial_cap = ((int64_t)w.partial_floats * 4 - (int64_t)plan_bytes - (int64_t)s_cap) / 4;
     p.max_tiles = w.max_tiles;
-    // counters in the sync area, which the build zeroes and every launch leaves zeroed (as the persistent
-    // engine expects it): the shrink's arrival count, the expand's S count and its exit count
+    // counters in the sync area (4 max_tiles ints), which the build zeroes and every launch leaves zeroed (as
+    // the persistent engine expects it): the shrink's arrival count, the expand's exit count, then two counts
+    // per tile (K-chunks done, S chunks summed)
+    if (4 + 2 * (int64_t)w.max_tiles > 4 * (int64_t)w.max_tiles) return LORA_ERR_WORKSPACE;
     int32_t *sync = at<int32_t>(ws, w.sync);
     p.cnt = sync;
     p.done = sync + 1;
-    p.s_cnt = sync + 2;
+    p.tile_cnt = sync + 4;
+    p.s_done = p.tile_cnt + w.max_tiles;
     p.ex_claim = p.plan_hdr + PL_CLAIM;
     const int grid = stream_grid(di.sms);
     const int64_t want = g_opt_grid.load();

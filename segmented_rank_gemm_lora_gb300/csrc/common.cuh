@@ -157,7 +157,8 @@ struct StreamParams {
     int2 *rd_start;                  // [grid + 1] first (tile, S chunk) of every expand block's S sums
     int32_t *cnt;                    // shrink blocks whose share of the launch's tile records is out
     int32_t *done;                   // expand blocks that have ended (the last one resets the counters)
-    int32_t *s_cnt;                  // expand blocks whose share of the S sums is out
+    int32_t *tile_cnt;               // [max_tiles] per tile: its K-chunks whose partials are out
+    int32_t *s_done;                 // [max_tiles] per tile: its S chunks summed
     int32_t *ex_claim;               // plan_hdr + PL_CLAIM (reset by the shrink)
     float *partials;                 // fp32 chunk partials
     int64_t partial_cap;             // floats

@@ -26,10 +26,12 @@
 //           of their tiles, and writes its share of the launch's records.
 //   shrink  one block per SM, launched cooperatively.  Warps 8-11 fill a
 //           six-stage ring: each stage is the chunk's next K columns of A
-//           (one bulk copy) and of the tile's x rows (cp.async pieces), with
-//           the stage's (tile, chunk); warps 0-7 multiply them with m16n8k16
-//           MMAs (the tile's rows as M, its rank columns as N) into fp32
-//           registers, and each chunk's partial goes to L2 scratch.  A block
+//           (one bulk copy) and of the tile's x rows (cp.async pieces), both
+//           in the tensor core's K-major operand layout, with the stage's
+//           (tile, chunk); one thread issues tcgen05 MMAs (the A block's rows
+//           as the 128-row M operand, the tile's rows as N) into one of two
+//           tensor-memory accumulators per chunk; warps 4-7 move each chunk's
+//           fp32 partial to L2 scratch and count it on its tile.  A block
 //           leaves as soon as its chunks are done.
 //   expand  one block per SM, warp-specialised; its blocks start on the SMs
 //           that shrink blocks leave, once every shrink block has written its
@@ -38,11 +40,12 @@
 //           claimed one at a time) and hands each to the other roles through
 //           a shared-memory queue while it streams the unit's packed B columns
 //           into a three-stage ring; warps 4-7 gather the unit's y rows into a
-//           six-slot ring (neither needs the shrink).  Once the shrink grid
-//           has ended, the twelve epilogue warps of every block sum an equal
-//           run of the launch's S chunks (a tile's partials in chunk order,
-//           bf16 into the operand layout) and count their block in; warp 1
-//           then loads S per (tile, slice block); warp 2 issues tcgen05 MMAs
+//           six-slot ring (neither needs the shrink).  The twelve epilogue
+//           warps of every block sum an equal run of the launch's S chunks
+//           (a tile's partials in chunk order, bf16 into the operand layout),
+//           each tile's once all its K-chunks are counted, and count the sums
+//           on the tile; warp 1 loads S per (tile, slice block) once all of
+//           the tile's sums are counted; warp 2 issues tcgen05 MMAs
 //           D = B_unit S^T (the unit's output columns as the 128-row M
 //           operand, the tile's rows as N) into one of four tensor-memory
 //           accumulators; three epilogue warpgroups take units in rotation:
@@ -63,9 +66,10 @@ namespace lora {
 constexpr int kPlanItems = 3;                   // shrink chunks per block the plan aims for
 constexpr int kPartialPerRow = 8192;            // fp32 partials per row of a tile, at most (bounds the K-chunk from below)
 constexpr int kTileRows = 64;                   // rows of a tile, at most
-constexpr int kShWarps = 8;                     // MMA warps of the shrink
-constexpr int kShProd = 128;                    // producer threads (the four warps after the MMA warps)
+constexpr int kShWarps = 8;                     // warps before the producers: MMA issuer, tensor-memory owner, epilogue
+constexpr int kShProd = 128;                    // producer threads (the four warps after them)
 constexpr int kShThreads = 32 * kShWarps + kShProd;
+constexpr uint32_t kShAccCols = 128;            // tensor-memory columns of one shrink accumulator (two of them)
 constexpr int kShStages = 6;
 constexpr int kMyTiles = 16;                    // tiles of its own chunks a shrink block keeps on chip
 constexpr int kShStageBytes = 32 * 1024;        // A columns and x rows of one stage, at most
@@ -139,37 +143,6 @@ __device__ __forceinline__ void bar_sync(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x1(uint32_t addr, uint32_t &r0)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x1.shared.b16 {%0}, [%1];" : "=r"(r0) : "r"(addr));
-}
-// D[16][8] += A[16][16] B[16][8] (bf16 in, fp32 accumulate), warp-wide
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// D[16][8] += A[16][8] B[8][8]
-__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0)
-{
-    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(b0));
-}
-
 // Phase stamps (lora_set_trace): kernel k (0 shrink, 1 expand), slot s of this block.
 __device__ __forceinline__ void tstamp(const StreamParams &p, int k, int s)
 {
@@ -227,10 +200,10 @@ __device__ __forceinline__ GroupPlan group_plan(const StreamParams &p, int4 gr, 
     g.rem = g.count - g.base * g.ntl;
     const int m_max = g.base + (g.rem > 0 ? 1 : 0);
     const int K = p.K;
-    // shrink: a stage (ks columns of A and of the tile's x rows, rows padded by 8 columns) fills at most one
-    // ring stage; the chunk (the same cut for every tile of the group) is about `target` bytes, and gives no
-    // more than kPartialPerRow partial floats per row
-    const int ks = min(512, (kShStageBytes / 2 - 8 * m_max) / (g.R + m_max)) / 16 * 16;
+    // shrink: a stage (ks columns of A and of the tile's x rows, both as [ks / 8][rows][8] with the x rows
+    // rounded up to 16) fills at most one ring stage; the chunk (the same cut for every tile of the group) is
+    // about `target` bytes, and gives no more than kPartialPerRow partial floats per row
+    const int ks = min(512, kShStageBytes / 2 / (g.R + ((m_max + 15) & ~15))) / 16 * 16;
     const int k_all = (K + ks - 1) / ks * ks;
     const int kc_min = min(((K * g.R + kPartialPerRow - 1) / kPartialPerRow + ks - 1) / ks * ks, k_all);   // K R < 2^29
     const float want = fminf(target / (2.f * (g.R + m_max)), (float)k_all);
@@ -497,37 +470,69 @@ __device__ int2 plan_start(const StreamParams &p, const PlanSmem &ps, int order,
 // P <= gs a thread keeps one piece column and steps over rows (gs / P rows per step); otherwise the group
 // walks the pieces of one row at a time.  The iterations are independent, so the source-row lookups of
 // several rows are in flight together.  One warp issuing alone leaves the gather far below the memory's
-// rate, hence groups of several warps.
+// rate, hence groups of several warps.  Piece c of row r lands at dst + r * rstride + c * cstride.
 template <class Src>
-__device__ __forceinline__ void group_gather(unsigned char *dst, int stride, int m, int P, int gt, int gs, Src src)
+__device__ __forceinline__ void group_gather(unsigned char *dst, int rstride, int cstride, int m, int P, int gt, int gs,
+                                             Src src)
 {
     if (P <= gs) {
         const int rpi = gs / P, rsub = gt / P, c = gt - rsub * P;
         if (rsub < rpi) {
 #pragma unroll 4
-            for (int r = rsub; r < m; r += rpi) tc::cp_async16(dst + r * stride + c * 16, src(r) + c * 8, true);
+            for (int r = rsub; r < m; r += rpi) tc::cp_async16(dst + r * rstride + c * cstride, src(r) + c * 8, true);
         }
     } else {
         for (int r = 0; r < m; ++r) {
             const __nv_bfloat16 *g = src(r);
 #pragma unroll 2
-            for (int c = gt; c < P; c += gs) tc::cp_async16(dst + r * stride + c * 16, g + c * 8, true);
+            for (int c = gt; c < P; c += gs) tc::cp_async16(dst + r * rstride + c * cstride, g + c * 8, true);
+        }
+    }
+}
+
+// The x rows of a shrink stage, [ks/8][n_pad][8]: each warp of the group takes blocks of 8 rows x 4 pieces
+// (lanes 8 q .. 8 q + 7: piece 4 b + q of rows 8 a .. 8 a + 7), so every 8 lanes fill 128 contiguous bytes of
+// shared memory and every row's 4 pieces are 64 contiguous bytes of x.
+template <class Src>
+__device__ __forceinline__ void x_gather(unsigned char *dst, int n_pad, int m, int P, int gt, Src src)
+{
+    constexpr int warps = kShProd / 32;
+    const int lane = gt & 31, w = gt >> 5, l8 = lane & 7, q = lane >> 3;
+    const int nrb = (m + 7) >> 3, npq = (P + 3) >> 2;
+    int rb = w, pq = 0;
+    while (rb >= nrb && pq < npq) {
+        rb -= nrb;
+        ++pq;
+    }
+    for (; pq < npq;) {
+        const int r = rb * 8 + l8, c = pq * 4 + q;
+        if (r < m && c < P) tc::cp_async16(dst + (c * n_pad + r) * 16, src(r) + c * 8, true);
+        rb += warps;
+        while (rb >= nrb && pq < npq) {
+            rb -= nrb;
+            ++pq;
         }
     }
 }
 
 struct __align__(128) ShrinkSmem {
     union {
-        // stage: A columns [ks/8][R][8], then the tile's x rows [m][ks + 8]
+        // stage: A columns [ks/8][R][8], then the same K columns of the tile's x rows [ks/8][n_pad][8]
         unsigned char stage[kShStages][kShStageBytes];
         PlanSmem plan;   // while the block plans, before the streams start
     };
+    // an A operand of fewer than 128 (or 256) rows is read as 128 (256) rows: the rows past R, which only
+    // reach accumulator lanes nobody reads, come from the bytes after the stage's copied A columns (later
+    // A columns or the x rows, inside the stage); the pad keeps even the last stage's reads inside the block
+    unsigned char pad[2048];
     uint64_t full[kShStages], empty[kShStages];
+    uint64_t acc_full[2], acc_empty[2], drain;
+    uint32_t tmem_base;
     int32_t xsrc[2][kTileRows];   // source rows of the producers' tiles, by tile parity
     TileRec mytile[kMyTiles];     // records of the tiles of this block's chunks (when they are few enough)
     int2 smeta[kShStages];        // the (tile, chunk) of every stage; tile -1 ends the sequence
     int2 range[2];                // this block's first and end (tile, chunk)
-    int32_t flag, last;
+    int32_t flag;
 };
 
 // Walks this block's chunks (tile, chunk) in order; the tile record is reloaded when the tile changes.
@@ -559,8 +564,10 @@ struct ChunkWalk {
 
 // Warps 8-11 (kShProd threads): the block's chunks, stage by stage, into the ring, then an end mark.  Thread
 // 0 of the group copies a stage's A columns (one bulk copy) and writes its (tile, chunk); the group gathers
-// the same K columns of the tile's x rows as 16-byte cp.async pieces.  The stage's full barrier completes
-// once the bulk copy's bytes and every producer thread's pieces have landed.  One barrier per stage keeps
+// the same K columns of the tile's x rows as 16-byte cp.async pieces into the operand layout
+// [ks/8][n_pad][8].  A stage whose K columns end with a group of 8 gets zeros for the other 8 columns of
+// its last K=16 step (A and x).  The stage's full barrier completes once the bulk copy's bytes and every
+// producer thread's pieces have landed.  One barrier per stage keeps
 // the four warps in step (and lets them leave together when a wait runs out); the tile's source rows are
 // double-buffered by tile parity, so a warp may write the next tile's rows while another still gathers the
 // last stage of the previous tile.
@@ -591,28 +598,32 @@ __device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem
         const unsigned char *ablk =
             reinterpret_cast<const unsigned char *>(__ldg(p.a_ptr + tr.a * p.E_A + (p.E_A == 1 ? 0 : tr.e)));
         const int k0 = j * tr.kc, kend = min(k0 + tr.kc, p.K);
-        const int xoff = tr.R * tr.ks * 2, xstride = (tr.ks + 8) * 2;
+        const int xoff = tr.R * tr.ks * 2;
         for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
             const int slot = s % kShStages;
             const bool got = next_slot();
-            if (fresh) {
-                for (int r = gt; r < tr.m; r += kShProd) sm.xsrc[par][r] = __ldcg(p.rows + tr.row0 + r) / p.src_div;
-                fresh = false;
-            }
-            if (!bar_and(2, kShProd, got)) return false;
             const int kk = min(tr.ks, kend - kb);
-            if (gt == 0) {
+            if (gt == 0 && got) {   // the A copy needs nothing the group writes: it leaves first
                 const uint32_t bytes = (uint32_t)tr.R * kk * 2;
                 sm.smeta[slot] = make_int2(t, j);
                 mbar_arrive_expect_tx(&sm.full[slot], bytes);
                 bulk_g2s(sm.stage[slot], ablk + (size_t)(kb / 8) * tr.R * 16, bytes, &sm.full[slot]);
                 if (s < 8) tstamp(p, 0, 12 + s);
             }
+            if (fresh) {
+                for (int r = gt; r < tr.m; r += kShProd) sm.xsrc[par][r] = __ldcg(p.rows + tr.row0 + r) / p.src_div;
+                fresh = false;
+            }
+            if (!bar_and(2, kShProd, got)) return false;
             const __nv_bfloat16 *xk = p.x + kb;
             const int64_t ldx = p.ldx;
             const int32_t *xs = sm.xsrc[par];
-            group_gather(sm.stage[slot] + xoff, xstride, tr.m, kk >> 3, gt, kShProd,
-                         [&](int r) { return xk + (int64_t)xs[r] * ldx; });
+            unsigned char *xd = sm.stage[slot] + xoff;
+            x_gather(xd, tr.n_pad, tr.m, kk >> 3, gt, [&](int r) { return xk + (int64_t)xs[r] * ldx; });
+            if (kk & 8) {   // zero-filling copies (no bytes read)
+                for (int i = gt; i < tr.R; i += kShProd) tc::cp_async16(sm.stage[slot] + ((kk >> 3) * tr.R + i) * 16, xk, false);
+                for (int i = gt; i < tr.n_pad; i += kShProd) tc::cp_async16(xd + ((kk >> 3) * tr.n_pad + i) * 16, xk, false);
+            }
             tc::cp_async_arrive_noinc(&sm.full[slot]);
         }
         return true;
@@ -633,156 +644,132 @@ __device__ __forceinline__ void shrink_produce(const StreamParams &p, ShrinkSmem
     tc::cp_async_wait_all();
 }
 
-// One chunk of one tile on the eight MMA warps: the fp32 partial X_rows A_chunk^T in registers, then to the
-// tile's partial slot.  Warp (ni0, mi0) owns 8-column blocks ni0, ni0 + wn, ... (MN of them) and 16-row
-// blocks mi0, mi0 + wm, ... (MM of them).  Each output element accumulates its K steps in order, one
-// m16n8k16 per 16 K, so its sum depends on the chunk cut alone.
-template <int MM, int MN>
-__device__ __forceinline__ bool shrink_chunk(const StreamParams &p, ShrinkSmem &sm, const TileRec &tr, int j, uint32_t &s)
+// Half h & 1 of S chunk h >> 1 of a tile (S chunk i: 16 bytes of its S layout, slice block sb, rank group kg,
+// row; a half: 4 of those rank columns): the tile's partials of those columns summed in chunk order, rounded
+// once to bf16.  S is stored per slice block sb as [rp / 8][n_pad][8], the operand layout the expand reads;
+// rows past m are zero.
+__device__ __forceinline__ void reduce_s_half(const StreamParams &p, const TileRec &tr, int h)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int ntc = tr.R >> 3, mtc = (tr.m + 15) >> 4;
-    const int wn = ntc >= 8 ? 8 : ntc, wm = 8 / wn;
-    const bool active = warp < wn * wm;
-    const int ni0 = warp % wn, mi0 = warp / wn;
-    float acc[MM * MN][4];
-#pragma unroll
-    for (int i = 0; i < MM * MN; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    const int xstride = (tr.ks + 8) * 2;
-    uint32_t xrow[MM];   // offsets in a stage of this lane's ldmatrix rows of x
-#pragma unroll
-    for (int mi = 0; mi < MM; ++mi) {
-        const int row = min((mi0 + mi * wm) * 16 + (lane & 15), tr.m - 1);
-        xrow[mi] = tr.R * tr.ks * 2 + row * xstride;
-    }
-    const int k0 = j * tr.kc, kend = min(k0 + tr.kc, p.K);
-    for (int kb = k0; kb < kend; kb += tr.ks, ++s) {
-        const int slot = s % kShStages;
-        const int kk = min(tr.ks, kend - kb);
-        if (!mbar_wait_suspend(&sm.full[slot], (s / kShStages) & 1, p.timeout_ns, p.err)) return false;
-        if (s < 8 && lane == 0 && warp == 0) tstamp(p, 0, 20 + s);
-        const int steps = kk >> 4;
-        const uint32_t a_s = smem_u32(sm.stage[slot]);
-        if (active) {
-            const uint32_t arow = a_s + ((lane >> 3) & 1) * tr.R * 16 + (lane & 7) * 16;
-#pragma unroll 2
-            for (int st = 0; st < steps; ++st) {
-                uint32_t b[MN][2];
-#pragma unroll
-                for (int ni = 0; ni < MN; ++ni) {
-                    const int nt = ni0 + ni * wn;
-                    if (nt < ntc) ldsm_x2(arow + (2 * st * tr.R + nt * 8) * 16, b[ni][0], b[ni][1]);
-                }
-#pragma unroll
-                for (int mi = 0; mi < MM; ++mi) {
-                    if (mi0 + mi * wm < mtc) {
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4(a_s + xrow[mi] + (2 * st + (lane >> 4)) * 16, a0, a1, a2, a3);
-#pragma unroll
-                        for (int ni = 0; ni < MN; ++ni)
-                            if (ni0 + ni * wn < ntc) mma16816(acc[mi * MN + ni], a0, a1, a2, a3, b[ni][0], b[ni][1]);
-                    }
-                }
-            }
-            if (kk & 8) {   // a last K-group of 8
-                uint32_t b[MN];
-#pragma unroll
-                for (int ni = 0; ni < MN; ++ni) {
-                    const int nt = ni0 + ni * wn;
-                    if (nt < ntc) ldsm_x1(a_s + ((2 * steps) * tr.R + nt * 8 + (lane & 7)) * 16, b[ni]);
-                }
-#pragma unroll
-                for (int mi = 0; mi < MM; ++mi) {
-                    if (mi0 + mi * wm < mtc) {
-                        uint32_t a0, a1;
-                        ldsm_x2(a_s + xrow[mi] + (2 * steps) * 16, a0, a1);
-#pragma unroll
-                        for (int ni = 0; ni < MN; ++ni)
-                            if (ni0 + ni * wn < ntc) mma1688(acc[mi * MN + ni], a0, a1, b[ni]);
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
-    }
-    if (active) {
-        float *dst = p.partials + tr.p_off + (int64_t)j * tr.m * tr.R;
-#pragma unroll
-        for (int mi = 0; mi < MM; ++mi) {
-#pragma unroll
-            for (int ni = 0; ni < MN; ++ni) {
-                const int mt = mi0 + mi * wm, nt = ni0 + ni * wn;
-                if (mt < mtc && nt < ntc) {
-                    const int row = mt * 16 + (lane >> 2), col = nt * 8 + (lane & 3) * 2;
-                    const float *c = acc[mi * MN + ni];
-                    if (row < tr.m) *reinterpret_cast<float2 *>(dst + row * tr.R + col) = make_float2(c[0], c[1]);
-                    if (row + 8 < tr.m)
-                        *reinterpret_cast<float2 *>(dst + (row + 8) * tr.R + col) = make_float2(c[2], c[3]);
-                }
-            }
-        }
-    }
-    return true;
-}
-
-// S chunk i of a tile (16 bytes of its S layout: slice block sb, rank group kg, row): the tile's partials
-// of those 8 rank columns summed in chunk order, rounded once to bf16.  S is stored per slice block sb as
-// [rp / 8][n_pad][8], the operand layout the expand reads; rows past m are zero.
-__device__ __forceinline__ void reduce_s_chunk(const StreamParams &p, const TileRec &tr, int i)
-{
+    constexpr int kBatch = 16;   // chunks whose loads are in flight together
+    const int i = h >> 1, half = h & 1;
     const int per_sb = (tr.rp >> 3) * tr.n_pad;
     const int sb = i / per_sb, rem = i - sb * per_sb;
     const int kg = rem / tr.n_pad, row = rem - kg * tr.n_pad;
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
     if (row < tr.m) {
-        const float *q = p.partials + tr.p_off + row * tr.R + sb * tr.rp + kg * 8;
+        const float *q = p.partials + tr.p_off + row * tr.R + sb * tr.rp + kg * 8 + half * 4;
         const int64_t cstride = (int64_t)tr.m * tr.R;
-        // the loads of eight chunks are in flight together; the sums still run in chunk order
-        for (int c0 = 0; c0 < tr.n_kc; c0 += 8, q += 8 * cstride) {
-            float4 u[8], w[8];
+        for (int c0 = 0; c0 < tr.n_kc; c0 += kBatch, q += kBatch * cstride) {
+            float4 u[kBatch];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 *qc = reinterpret_cast<const float4 *>(q + c * cstride);
-                const bool in = c0 + c < tr.n_kc;
-                u[c] = in ? __ldcg(qc) : make_float4(0.f, 0.f, 0.f, 0.f);
-                w[c] = in ? __ldcg(qc + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            for (int c = 0; c < kBatch; ++c)
+                u[c] = c0 + c < tr.n_kc ? __ldcg(reinterpret_cast<const float4 *>(q + c * cstride))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < kBatch; ++c) {
                 if (c0 + c < tr.n_kc) {
                     a[0] += u[c].x; a[1] += u[c].y; a[2] += u[c].z; a[3] += u[c].w;
-                    a[4] += w[c].x; a[5] += w[c].y; a[6] += w[c].z; a[7] += w[c].w;
                 }
             }
         }
     }
-    __align__(16) __nv_bfloat16 o[8];
+    __align__(8) __nv_bfloat16 o[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = __float2bfloat16_rn(a[e]);
-    *reinterpret_cast<uint4 *>(p.s_area + tr.s_off + (int64_t)i * 16) = *reinterpret_cast<const uint4 *>(o);
+    for (int e = 0; e < 4; ++e) o[e] = __float2bfloat16_rn(a[e]);
+    *reinterpret_cast<uint2 *>(p.s_area + tr.s_off + (int64_t)i * 16 + half * 8) = *reinterpret_cast<const uint2 *>(o);
 }
 
-// Warps 0-7: the chunks the producers announce, stage by stage from the ring, until the end mark.  A
-// chunk's tile record is the block's own copy for its share, else the launch's.  The warps take every
-// decision together (bar.red), so that a wait that runs out ends them all.
-__device__ __forceinline__ void shrink_consume(const StreamParams &p, ShrinkSmem &sm, int2 b0, const TileRec *mine,
-                                               int n_my)
+// Warp 0, one thread: the stages the producers announce, until the end mark.  Each chunk accumulates into
+// one of two tensor-memory accumulators (in turn): D[r][n] = sum over the chunk's K columns of A[r][k] x[n][k],
+// the A block's rows as the 128-row M operand (two blocks of 128 rows when R > 128) and the tile's rows,
+// rounded up to 16, as N.  A stage is released by the commit after its MMAs; a chunk's accumulator goes to
+// the epilogue with the commit after its last stage.  Within a chunk the MMAs run in K order, so a
+// partial's sums depend on the chunk cut alone.
+__device__ __forceinline__ void shrink_mma(const StreamParams &p, ShrinkSmem &sm, int2 b0, const TileRec *mine,
+                                           int n_my)
 {
-    constexpr int nthr = 32 * kShWarps;
     uint32_t s = 0;
-    for (int q = 0;; ++q) {
+    int ci = -1, cur_t = -1, cur_j = -1, kb = 0, kend = 0;
+    TileRec tr{};
+    for (;; ++s) {
         const int slot = s % kShStages;
-        if (!bar_and(3, nthr, mbar_wait_suspend(&sm.full[slot], (s / kShStages) & 1, p.timeout_ns, p.err))) break;
+        if (!mbar_wait_suspend(&sm.full[slot], (s / kShStages) & 1, p.timeout_ns, p.err)) break;
         const int2 e = sm.smeta[slot];
-        if (e.x < 0) break;
-        const TileRec tr = mine && e.x - b0.x < n_my ? mine[e.x - b0.x] : load_tile(p.tiles + e.x);
-        bool ok;
-        if (tr.R <= 64) ok = shrink_chunk<4, 1>(p, sm, tr, e.y, s);
-        else if (tr.R <= 128) ok = shrink_chunk<4, 2>(p, sm, tr, e.y, s);
-        else ok = shrink_chunk<4, 4>(p, sm, tr, e.y, s);
-        if (!bar_and(3, nthr, ok)) break;
-        if (threadIdx.x == 0 && q < 4) tstamp(p, 0, 3 + q);
+        if (e.x != cur_t || e.y != cur_j) {   // a chunk ends here (or the sequence does)
+            if (ci >= 0) tc::mma_commit(&sm.acc_full[ci & 1]);
+            if (e.x < 0) break;
+            ++ci;
+            if (ci >= 2 && !mbar_wait_suspend(&sm.acc_empty[ci & 1], ((ci >> 1) - 1) & 1, p.timeout_ns, p.err)) break;
+            if (e.x != cur_t) tr = mine && e.x - b0.x < n_my ? mine[e.x - b0.x] : load_tile(p.tiles + e.x);
+            cur_t = e.x;
+            cur_j = e.y;
+            kb = e.y * tr.kc;
+            kend = min(kb + tr.kc, p.K);
+        }
+        tc::fence_proxy_async_smem();   // the producers' cp.async pieces, seen through the barrier, to the tensor core
+        tc::fence_after_sync();
+        const int nk = (min(tr.ks, kend - kb) + 15) >> 4;
+        const uint32_t a_s = smem_u32(sm.stage[slot]), x_s = a_s + tr.R * tr.ks * 2;
+        const uint32_t idesc = tc::idesc_bf16(128, tr.n_pad);
+        const uint32_t d = sm.tmem_base + (ci & 1) * kShAccCols;
+        // descriptors advance by their start-address field (16-byte units; stays below 2^14 in shared memory)
+        uint64_t ad = tc::smem_desc(a_s, tr.R * 16, 128), xd = tc::smem_desc(x_s, tr.n_pad * 16, 128);
+        const uint64_t astep = (uint64_t)(tr.R * 2), xstep = (uint64_t)(tr.n_pad * 2);
+        uint32_t acc = kb == cur_j * tr.kc ? 0u : 1u;   // the chunk's first K step starts the accumulator
+        if (tr.R <= 128) {
+            for (int k = 0; k < nk; ++k, ad += astep, xd += xstep, acc = 1u) tc::mma_bf16(d, ad, xd, idesc, acc);
+        } else {   // two 128-row blocks of A, 128 rows (2048 bytes, 128 units) apart
+            for (int k = 0; k < nk; ++k, ad += astep, xd += xstep, acc = 1u) {
+                tc::mma_bf16(d, ad, xd, idesc, acc);
+                tc::mma_bf16(d + tr.n_pad, ad + 128, xd, idesc, acc);
+            }
+        }
+        kb += min(tr.ks, kend - kb);
+        tc::mma_commit(&sm.empty[slot]);   // the stage is free once these MMAs are done
+        if (s < 8) tstamp(p, 0, 20 + s);
+    }
+    // every MMA issued is done before the tensor memory is freed
+    if (s > 0) {
+        tc::mma_commit(&sm.drain);
+        mbar_wait_suspend(&sm.drain, 0, p.timeout_ns, p.err);
+    }
+}
+
+// Warps 4-7: every chunk's accumulator, in the block's chunk order, to the tile's partial slot [m][R] (fp32):
+// thread (quarter q, lane) reads tensor-memory lane 32 q + lane of each 128-row block (A row r) for the
+// tile's rows; then the chunk counts on its tile (the expand sums a tile's S once all its chunks are counted).
+__device__ __forceinline__ void shrink_epilogue(const StreamParams &p, ShrinkSmem &sm, int2 b0, int2 b1,
+                                                const TileRec *mine)
+{
+    const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, et = threadIdx.x - 128;
+    int ci = 0;
+    for (ChunkWalk w(b0, b1, mine); w.valid(p); w.next(), ++ci) {
+        const int b = ci & 1;
+        if (!bar_and(3, 128, mbar_wait_suspend(&sm.acc_full[b], (ci >> 1) & 1, p.timeout_ns, p.err))) break;
+        tc::fence_after_sync();
+        const TileRec &tr = w.tr;
+        float *dst = p.partials + tr.p_off + (int64_t)w.j * tr.m * tr.R;
+        for (int mb = 0; mb * 128 < tr.R; ++mb) {
+            const int r = mb * 128 + q * 32 + lane;
+            const uint32_t ta = sm.tmem_base + ((uint32_t)(q * 32) << 16) + b * kShAccCols + mb * tr.n_pad;
+            for (int n0 = 0; n0 < tr.n_pad; n0 += 16) {
+                float v[16];
+                tc::tmem_ld16(ta + n0, v);
+                if (r < tr.R) {
+#pragma unroll
+                    for (int n = 0; n < 16; ++n)
+                        if (n0 + n < tr.m) dst[(n0 + n) * tr.R + r] = v[n];
+                }
+            }
+        }
+        tc::fence_before_sync();
+        bar_sync(3, 128);   // the partial is out of the accumulator and stored
+        if (et == 0) {
+            mbar_arrive(&sm.acc_empty[b]);
+            if (ci < 4) tstamp(p, 0, 3 + ci);
+            __threadfence();   // every thread's stores (ordered by the barrier) before the count
+            atomicAdd(p.tile_cnt + w.t, 1);
+        }
     }
 }
 
@@ -795,8 +782,13 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
         tstamp(p, 0, 0);
         for (int s = 0; s < kShStages; ++s) {
             mbar_init(&sm.full[s], 1 + kShProd);   // the A copy's expect-tx arrival and one per producer thread
-            mbar_init(&sm.empty[s], kShWarps);
+            mbar_init(&sm.empty[s], 1);            // the MMA issuer's commit
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.acc_full[b], 1);         // the MMA issuer's commit
+            mbar_init(&sm.acc_empty[b], 1);        // the epilogue
+        }
+        mbar_init(&sm.drain, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -805,13 +797,16 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
     if (tid == 0) tstamp(p, 0, 1);
     if (blockIdx.x == 0 && tid == 0) *p.ex_claim = 0;   // the expand of the launch before has ended
     if (tid < 32) plan_groups(p, sm.plan);
+    else if (tid < 64) tc::tmem_alloc(&sm.tmem_base, 2 * kShAccCols);
+    tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
     const PlanSmem &ps = sm.plan;
     const GroupPos &tot = ps.pos[ps.G];
     const int G = p.grid_s, c = blockIdx.x, nt = tot.t;
     // this block's chunks (threads 0 and 32), then the records of their tiles (warp 0); the other warps write
-    // this block's share of the launch's plan, read after the shrink (S reduction, expand): the records of
-    // tiles c, c + G, ..., the first (tile, S chunk) this block reduces and the first unit of expand block c
+    // this block's share of the launch's plan, read by the expand: the records of tiles c, c + G, ..., the
+    // first (tile, S chunk) of expand block c's S sums and the first unit of expand block c
     const Split ss(tot.sh, G);
     if (tid == 0) sm.range[0] = plan_start(p, ps, ORD_SH, ss.start(c));
     if (tid == 32) sm.range[1] = plan_start(p, ps, ORD_SH, ss.start(c + 1));
@@ -871,11 +866,23 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
         __syncthreads();
         go = sm.flag != 0;
     }
+    const int warp = tid >> 5;
     if (go) {
-        if (tid < kShWarps * 32) shrink_consume(p, sm, b0, mine, n_my);
-        else shrink_produce(p, sm, b0, b1, mine);
+        if (warp == 0) {
+            if (tid == 0) shrink_mma(p, sm, b0, mine, n_my);
+        } else if (warp >= 4 && warp < kShWarps) {
+            shrink_epilogue(p, sm, b0, b1, mine);
+        } else if (warp >= kShWarps) {
+            shrink_produce(p, sm, b0, b1, mine);
+        }
         __syncwarp();
-        if (tid == 0) tstamp(p, 0, 8);
+        if (tid == 128) tstamp(p, 0, 8);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(sm.tmem_base, 2 * kShAccCols);
     }
     if (tid == 0) tstamp(p, 0, 31);
 }
@@ -910,7 +917,7 @@ struct __align__(1024) ExpandSmem {
     uint64_t u0_ready;
     int32_t u0[kExUposCap + 1];                      // first unit of every tile, then the launch's unit count
     int32_t nt;
-    int32_t flag;
+    int32_t flag, rd_ok;
     uint32_t tmem_base;
 };
 
@@ -1099,7 +1106,7 @@ __device__ __forceinline__ void expand_produce_y(const StreamParams &p, ExpandSm
         const int64_t ldy = p.ldy;
         const ExYMeta &mt = sm.ymeta[slot];
         if (i >= 8 && i < 12 && gt == 0) tstamp(p, 1, 17 + (i - 8));
-        group_gather(sm.ystage[slot], tr.W * 2, tr.m, w_eff >> 3, gt, kExYProd,
+        group_gather(sm.ystage[slot], tr.W * 2, 16, tr.m, w_eff >> 3, gt, kExYProd,
                      [&](int r) { return yc + (int64_t)mt.row[r] * ldy; });
         tc::cp_async_arrive_noinc(&sm.full_y[slot]);   // once every piece of this thread has landed
     }
@@ -1117,12 +1124,12 @@ __device__ __forceinline__ void expand_produce_y(const StreamParams &p, ExpandSm
     tc::cp_async_wait_all();
 }
 
-// Warp 1, one thread: S of every (tile, slice block) the unit queue meets, into two buffers in rotation.
+// Warp 1, one thread: S of every (tile, slice block) the unit queue meets, into two buffers in rotation, each
+// tile's once every S chunk of the tile is summed.
 __device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem &sm)
 {
-    tstamp(p, 1, 3);
     uint32_t k = 0;
-    int prev_t = -1, prev_sb = -1, cur = -1;
+    int prev_t = -1, prev_sb = -1, cur = -1, ready = -1;
     TileRec tr{};
     for (uint32_t i = 0;; ++i) {
         const int q = i % kExQ;
@@ -1138,8 +1145,15 @@ __device__ __forceinline__ void expand_load_s(const StreamParams &p, ExpandSmem 
         unit_slice(p, tr.W, e.y, s, cb);
         const int sb = p.n_a == 1 ? 0 : s;
         if (e.x == prev_t && sb == prev_sb) continue;
+        if (e.x != ready && !p.withhold) {
+            if (!wait_at_least(p, p.s_done + e.x, tr.R * tr.n_pad / 8)) break;
+            __threadfence();
+            tc::fence_proxy_async_global();   // S was written by threads; the bulk copies read it
+            ready = e.x;
+        }
         const int slot = k & 1;
         if (k >= 2 && !mbar_wait_suspend(&sm.s_empty[slot], ((k >> 1) - 1) & 1, p.timeout_ns, p.err)) break;
+        if (k == 0) tstamp(p, 1, 3);
         const uint32_t bytes = (uint32_t)tr.rp * tr.n_pad * 2;
         mbar_arrive_expect_tx(&sm.s_full[slot], bytes);
         if (!p.withhold) bulk_g2s(sm.sbuf[slot], p.s_area + tr.s_off + (size_t)sb * bytes, bytes, &sm.s_full[slot]);
@@ -1308,8 +1322,8 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     tc::fence_after_sync();
     // The expand starts while the shrink still runs (its blocks take the SMs that shrink blocks leave): it
     // reads the launch's records once every shrink block has written its share (the shrink's first arrival
-    // count; the shrink grid is co-resident and never waits on this one), and only the S loader waits for
-    // the whole shrink grid.  The B and y copies need nothing the shrink writes.
+    // count; the shrink grid is co-resident and never waits on this one), and the S loader waits for each
+    // tile's S on its own.  The B and y copies need nothing the shrink writes.
     if (threadIdx.x == 0) {
         sm.flag = wait_at_least(p, p.cnt, p.grid_s);
         __threadfence();
@@ -1323,14 +1337,7 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     } else if (warp == 0) {
         if (lane == 0) expand_lead(p, sm, b0, b1);
     } else if (warp == 1) {
-        if (lane == 0) {
-            // S is summed by the epilogue warps of every expand block (below)
-            if (!p.withhold && wait_at_least(p, p.s_cnt, (int)gridDim.x)) {
-                __threadfence();
-                tc::fence_proxy_async_global();   // S was written by threads; the bulk copies read it
-            }
-            expand_load_s(p, sm);
-        }
+        if (lane == 0) expand_load_s(p, sm);
     } else if (warp == 2) {
         if (lane == 0) expand_mma(p, sm);
     } else if (warp == 3) {
@@ -1348,27 +1355,30 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
     } else if (warp < 8) {
         expand_produce_y(p, sm);
     } else {
-        // warps 8-19, idle until the first accumulator: once the shrink grid has ended, this block's equal
-        // run of the launch's S chunks (each the sum of a tile's partials in chunk order, eight chunks' loads
-        // in flight), then the block's arrival on the count the S loaders wait for
+        // warps 8-19, idle until the first accumulator: this block's equal run of the launch's S chunks (each
+        // the sum of a tile's partials in chunk order, in two halves), each tile's once all its K-chunks are
+        // counted, then the sums counted on the tile (what the S loaders wait for)
         constexpr int nthr = 128 * kExGroups;
         const int et = threadIdx.x - 256;
-        // (the share's range and its first tile record are the shrink plan's, out since the block started)
         const int2 r0 = __ldcg(p.rd_start + blockIdx.x), r1 = __ldcg(p.rd_start + blockIdx.x + 1);
-        const TileRec tr0 = load_tile(p.tiles + min(r0.x, max(__ldcg(p.plan_hdr + PL_TILES) - 1, 0)));
-        pdl_wait();
-        if (et == 0) tstamp(p, 1, 29);
         for (int t = r0.x; t < r1.x || (t == r1.x && r1.y > 0); ++t) {
-            const TileRec tr = t == r0.x ? tr0 : load_tile(p.tiles + t);
+            const TileRec tr = load_tile(p.tiles + t);
             const int lo = t == r0.x ? r0.y : 0;
             const int hi = t == r1.x ? r1.y : tr.R * tr.n_pad / 8;
-            for (int i = lo + et; i < hi; i += nthr) reduce_s_chunk(p, tr, i);
-        }
-        bar_sync(4, nthr);
-        if (et == 0) {
-            __threadfence();
-            atomicAdd(p.s_cnt, 1);
-            tstamp(p, 1, 30);
+            if (et == 0) {
+                sm.rd_ok = wait_at_least(p, p.tile_cnt + t, tr.n_kc);
+                __threadfence();
+                if (t == r0.x) tstamp(p, 1, 29);
+            }
+            bar_sync(4, nthr);
+            if (!sm.rd_ok) break;   // block-uniform
+            for (int h = 2 * lo + et; h < 2 * hi; h += nthr) reduce_s_half(p, tr, h);
+            bar_sync(4, nthr);
+            if (et == 0) {
+                __threadfence();
+                atomicAdd(p.s_done + t, hi - lo);
+                tstamp(p, 1, 30);
+            }
         }
         expand_epilogue(p, sm, (warp - 8) >> 2);
     }
@@ -1380,7 +1390,7 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
         tc::tmem_dealloc(sm.tmem_base, kExTmemCols);
     }
     // the last block out resets the launch's counters for the next launch (the shrink grid has ended: every
-    // block waits for it here, most already did for their S sums)
+    // block waits for it here)
     if (threadIdx.x == 0) {
         pdl_wait();
         __threadfence();
@@ -1388,10 +1398,13 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
         __threadfence();
     }
     __syncthreads();
-    if (sm.flag && threadIdx.x == 0) {
-        *p.cnt = 0;
-        *p.s_cnt = 0;
-        *p.done = 0;
+    if (sm.flag) {
+        const int nt = min(__ldcg(p.plan_hdr + PL_TILES), p.max_tiles);
+        for (int t = threadIdx.x; t < nt; t += blockDim.x) p.tile_cnt[t] = p.s_done[t] = 0;
+        if (threadIdx.x == 0) {
+            *p.cnt = 0;
+            *p.done = 0;
+        }
     }
     if (threadIdx.x == 0) tstamp(p, 1, 31);
 }
@@ -1401,7 +1414,7 @@ __global__ void __launch_bounds__(kExThreads, 1) expand_kernel(const __grid_cons
 // ===========================================================================
 size_t stream_plan_bytes(int32_t max_tiles)
 {
-    const size_t a = 256 + (size_t)max_tiles * sizeof(TileRec) + 3 * ((size_t)kStreamMaxGrid + 1) * 8;
+    const size_t a = 256 + (size_t)max_tiles * sizeof(TileRec) + 2 * ((size_t)kStreamMaxGrid + 1) * 8;
     return (a + 255) / 256 * 256;
 }
 

@@ -68,7 +68,7 @@ def plan(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
         n = ntl[g]
         base, rem = divmod(cnt, n)
         m_max = base + (1 if rem else 0)
-        ks = min(512, (C["kShStageBytes"] // 2 - 8 * m_max) // (R + m_max)) // 16 * 16
+        ks = min(512, C["kShStageBytes"] // 2 // (R + (m_max + 15) // 16 * 16)) // 16 * 16
         k_all = -(-K // ks) * ks
         kcap = k_all
         kc_min = min(-(-(-(-K * R // C["kPartialPerRow"])) // ks) * ks, kcap)
@@ -152,7 +152,7 @@ def check(groups, ranks, K, slice_n, n_a, grid, tile_max=128):
                 assert pool[g - g0] == (l, g - int(u0[l]))
     for t in tiles:
         assert 1 <= t["m"] <= C["kTileRows"] and t["m"] <= tile_max
-        assert (t["R"] * t["ks"] + t["m"] * (t["ks"] + 8)) * 2 <= C["kShStageBytes"]
+        assert (t["R"] + t["n_pad"]) * t["ks"] * 2 <= C["kShStageBytes"]
         assert t["W"] * t["rp"] * 2 <= C["kExBBytes"] and t["W"] * t["m"] * 2 <= C["kExYBytes"]
         assert (t["W"] // 128) * t["n_pad"] <= C["kExAccCols"]
         assert t["rp"] * t["n_pad"] * 2 <= C["kExSBytes"]
