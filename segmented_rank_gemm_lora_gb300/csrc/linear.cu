@@ -188,7 +188,9 @@ __global__ void __launch_bounds__(kT, 1) linear_kernel(const __grid_constant__ L
         for (int kb = 0; kb < nK; ++kb) {
             const int st = kb % S;
             wait_bar(&sm.full[st], (kb / S) & 1, p);
-            tc::fence_proxy_async_smem();   // the producers' cp.async pieces, seen through the barrier, to the tensor core
+            // the producers' cp.async pieces (gathered x rows, a zeroed K tail), seen through the barrier, to the
+            // tensor core; a stage of TMA and bulk copies alone needs no proxy fence
+            if (!xtma || (lora && ((p.K - kb * kLinearK) & 8) && p.K - kb * kLinearK < kLinearK)) tc::fence_proxy_async_smem();
             tc::fence_after_sync();
             const uint32_t xs = smem_u32(dsm + st * p.stage_bytes), ws = xs + kXBytes, as = ws + kWBytes;
             const int nks = (min(kLinearK, p.K - kb * kLinearK) + 15) >> 4;
