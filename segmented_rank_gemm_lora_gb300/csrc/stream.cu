@@ -793,7 +793,6 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
     }
     __syncthreads();
     pdl_wait();      // the segment table of the build, and everything before it
-    pdl_trigger();   // the expand may launch now; it waits for this grid before it reads anything
     if (tid == 0) tstamp(p, 0, 1);
     if (blockIdx.x == 0 && tid == 0) *p.ex_claim = 0;   // the expand of the launch before has ended
     if (tid < 32) plan_groups(p, sm.plan);
@@ -801,6 +800,10 @@ __global__ void __launch_bounds__(kShThreads, 1) shrink_kernel(const __grid_cons
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    // the expand may launch now; it waits for this grid's records before it reads anything.  This block holds
+    // its tensor memory already, so an expand block (which takes all of an SM's tensor memory) never gets it
+    // first on a shared SM and then waits on this block's chunks
+    pdl_trigger();
     const PlanSmem &ps = sm.plan;
     const GroupPos &tot = ps.pos[ps.G];
     const int G = p.grid_s, c = blockIdx.x, nt = tot.t;
