@@ -227,7 +227,7 @@ lora_status lora_build_segments(const lora_workspace *ws, const int32_t *d_lora_
  * take one launch of the persistent engine (small tiles, the shrink-to-expand
  * hand-off in L2); larger ones take the streaming path: a shrink kernel and an
  * expand kernel chained with programmatic dependent launch (64-row tiles,
- * tcgen05 expand).  LORA_OPT_PATH overrides the choice.
+ * tcgen05 shrink and expand).  LORA_OPT_PATH overrides the choice.
  *   d_x : bf16 [M][ldx] device, the layer input (K columns used).
  *   d_y : bf16 [M][ldy] device, in: the base output y_base, out: y (N columns).
  *         Rows of tokens without an adapter are not touched.
